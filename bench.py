@@ -1,0 +1,391 @@
+"""Benchmark of the NVFP4 MegaMoE routed-expert forward.
+
+One step = one megamoe_forward (route -> amax -> quantise -> L1 grouped GEMM
+with SiLU*up -> requantise -> L2 grouped GEMM -> combine) over one batch of
+the MegaMoE decode workload (384 experts, top-6, d 7168, I 2048, 8 tokens,
+NVFP4 weights resident in HBM).  Prints one JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config decode]
+                  [--impl ours|reference]
+
+--impl reference times the CPU oracle (the float64 reference of the method)
+on a bounded sample of the same workload.  Under torchrun every rank runs its
+own replica (the path has no exchange step); rank 0 prints.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "routed tokens/s and NVFP4 TFLOP/s per MoE layer fwd; % HBM / FP4 roofline"
+UNIT = "routed tokens/s"
+KERNELS_PER_STEP = 7  # route, amax, quant, L1 GEMM, requant, L2 GEMM, combine
+
+
+def _dist():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines: list[str] = []
+        self._t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self._t = threading.Thread(target=self._read, daemon=True)
+        self._t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        if self._t:
+            self._t.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def _profile_traffic(kernel_src: str, name: str):
+    """DRAM bytes per launch from a committed ncu summary, if the kernel source
+    is unchanged since the capture (else None)."""
+    path = os.path.join(ROOT, "profiles", name)
+    try:
+        with open(path) as f:
+            prof = json.load(f)
+        with open(kernel_src, "rb") as f:
+            h = hashlib.sha256(f.read()).hexdigest()[:16]
+        if prof.get("source_sha256_16") != h:
+            return None
+        return prof.get("dram_bytes_per_launch")
+    except Exception:
+        return None
+
+
+# --------------------------------------------------------------------------
+# the oracle leg (cpu_baseline and --impl reference)
+# --------------------------------------------------------------------------
+def oracle_sample(cfg, x, ids, w, experts_src, tokens: int):
+    """Time the CPU oracle's forward on the first `tokens` tokens."""
+    import numpy as np
+
+    import oracle
+    from nvfp4_block_scaled_topk_gb300 import inputs
+
+    xs = x[:tokens].float().cpu().numpy()
+    ids_s = ids[:tokens].cpu().numpy()
+    ws = w[:tokens].cpu().numpy()
+    ex = inputs.ExpertSet(cfg, experts_src)
+    t0 = time.perf_counter()
+    out = oracle.forward(xs, ids_s, ws, ex, pad=32)
+    dt = time.perf_counter() - t0
+    assert np.all(np.isfinite(out))
+    return dt
+
+
+def _cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def run_reference(args):
+    import torch
+
+    from nvfp4_block_scaled_topk_gb300 import inputs
+
+    rank, world, _ = _dist()
+    if rank != 0:
+        return
+    cfg = inputs.CONFIGS[args.config]
+    x = inputs.make_activations(cfg)
+    ids, w = inputs.make_routing(cfg)
+    tokens = max(1, min(cfg.T, args.ref_tokens))
+    times = []
+    for i in range(args.warmup + args.steps):
+        dt = oracle_sample(cfg, x, ids, w, None, tokens)
+        if i >= args.warmup:
+            times.append(dt)
+    total = sum(times)
+    value = tokens * len(times) / total
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / len(times),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": f"{cfg.name}: E={cfg.E} top-{cfg.k} d={cfg.d} I={cfg.I} "
+                               f"T={cfg.T} (oracle on the first {tokens} tokens per step)",
+                   "global_batch": cfg.T, "parallelism": "replicas"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": _cores(), "kind": "oracle",
+                         "sample": f"first {tokens} of {cfg.T} tokens of the {cfg.name} batch, "
+                                   "weights of the experts they touch, full forward"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------------
+# our arm
+# --------------------------------------------------------------------------
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    from nvfp4_block_scaled_topk_gb300 import build, inputs, megamoe
+
+    rank, world, local = _dist()
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    build.build()
+    megamoe.load()
+
+    cfg = inputs.CONFIGS[args.config]
+    raw = inputs.make_all_experts(cfg, device=dev)
+    weights = megamoe.Weights.prepare(raw)
+    x = inputs.make_activations(cfg, device=dev)
+    ids, w = inputs.make_routing(cfg, device=dev)
+    fwd = megamoe.Forward(weights, cfg.T, cfg.k, pad=32)
+    stream = torch.cuda.current_stream()
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+
+            dist.barrier()
+
+    # ---- device-timed steps (inputs resident in HBM)
+    for _ in range(max(3, args.warmup)):
+        fwd(x, ids, w)
+    torch.cuda.synchronize()
+    bits = fwd.read_status()
+    if bits:
+        raise RuntimeError(f"device status {bits:#x}")
+    v = fwd.intermediates()
+    counts = v["counts"].cpu().numpy()
+    active = int((counts > 0).sum())
+    valid_slots = int(counts.sum())
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    barrier()
+    torch.cuda.synchronize()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        fwd(x, ids, w)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    ms = ev0.elapsed_time(ev1) / args.steps
+
+    # ---- dominant kernel (L1 grouped GEMM) timed alone on the forward's own
+    # intermediates, CUDA events on the launching stream
+    l1_out = torch.empty_like(v["h"])
+    l1_amax = torch.empty(1, dtype=torch.float32, device=dev)
+    tile_n = 32 if cfg.slots / cfg.E <= 32 else (64 if cfg.slots / cfg.E <= 96 else 128)
+
+    def l1():
+        megamoe.grouped_gemm(v["xq_codes"], v["xq_sf"], v["gs_x"], weights.w13_codes,
+                             weights.w13_scales, weights.w13_gs, v["offsets"],
+                             v["padded_offsets"], megamoe.EPI_SILU_MUL, tile_n=tile_n,
+                             out=l1_out, out_amax=l1_amax)
+
+    def l2():
+        megamoe.grouped_gemm(v["hq_codes"], v["hq_sf"], v["gs_h"], weights.w2_codes,
+                             weights.w2_scales, weights.w2_gs.view(-1, 1), v["offsets"],
+                             v["padded_offsets"], megamoe.EPI_F32, tile_n=tile_n,
+                             out=v["y"], out_amax=None)
+
+    def timed(fn, n):
+        for _ in range(3):
+            fn()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(n):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / n
+
+    l1_ms = timed(l1, max(args.steps, 10))
+    l2_ms = timed(l2, max(args.steps, 10))
+    clk = clocks.stop()
+
+    # ---- end to end through the public call, host buffers, copies inside
+    x_h = x.cpu().pin_memory()
+    ids_h = ids.cpu().pin_memory()
+    w_h = w.cpu().pin_memory()
+    out_h = torch.empty(cfg.T, cfg.d, dtype=torch.bfloat16).pin_memory()
+    x_d = torch.empty_like(x)
+    ids_d = torch.empty_like(ids)
+    w_d = torch.empty_like(w)
+
+    def e2e_step():
+        x_d.copy_(x_h, non_blocking=True)
+        ids_d.copy_(ids_h, non_blocking=True)
+        w_d.copy_(w_h, non_blocking=True)
+        o = fwd(x_d, ids_d, w_d)
+        out_h.copy_(o, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    barrier()
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = a.elapsed_time(b) / args.steps
+    h2d = x_h.numel() * 2 + ids_h.numel() * 4 + w_h.numel() * 4
+    d2h = out_h.numel() * 2
+
+    # ---- max over ranks
+    if world > 1:
+        import torch.distributed as dist
+
+        t = torch.tensor([ms, e2e_ms, l1_ms, l2_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms, e2e_ms, l1_ms, l2_ms = t.tolist()
+
+    hbm_gbs, bf16_tf, peak_kind = _peaks()
+    tokens_total = cfg.T * world
+    value = tokens_total / (ms * 1e-3)
+    flops = inputs.algorithmic_flops(cfg, valid_slots)
+    alg_bytes = inputs.algorithmic_bytes(cfg, active)
+    w_el = cfg.d * cfg.I * (0.5 + 1.0 / 16)
+    l1_bytes = active * 2 * w_el + valid_slots * cfg.d * (0.5 + 1 / 16) + valid_slots * cfg.I * 2
+    l1_gbs = l1_bytes / (l1_ms * 1e-3) / 1e9
+    traffic = _profile_traffic(os.path.join(ROOT, "nvfp4_block_scaled_topk_gb300", "csrc",
+                                            "gemm.cu"), f"l1_gemm_{cfg.name}.json")
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        tokens = max(1, min(cfg.T, args.ref_tokens))
+        dt = oracle_sample(cfg, x, ids, w, raw, tokens)
+        cpu = {"value": tokens / dt, "unit": UNIT, "cores": _cores(), "kind": "oracle",
+               "sample": f"first {tokens} of {cfg.T} tokens of the {cfg.name} batch, weights of "
+                         "the experts they touch, full float64 forward"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "nvfp4 (e2m1 x e4m3 scales, fp32 acc)",
+            "data": "synthetic",
+            "config": {"workload": f"{cfg.name}: MegaMoE decode, E={cfg.E} top-{cfg.k} d={cfg.d} "
+                                   f"I={cfg.I} T={cfg.T}, NVFP4 weights resident",
+                       "global_batch": cfg.T * world, "parallelism": f"replicas x{world}",
+                       "l2": "inputs larger than L2 (≈1.1 GB of expert weights read per step)",
+                       "active_experts": active, "valid_slots": valid_slots},
+            "tflops": flops / (ms * 1e-3) / 1e12,
+            "hbm_gbs": alg_bytes / (ms * 1e-3) / 1e9,
+            "hbm_frac_of_measured": alg_bytes / (ms * 1e-3) / 1e9 / hbm_gbs,
+            "stage_ms": {"l1_gemm": l1_ms, "l2_gemm": l2_ms},
+            "roofline": {"bound": "hbm", "achieved": l1_gbs, "peak": hbm_gbs, "unit": "GB/s",
+                         "frac": l1_gbs / hbm_gbs, "traffic": traffic,
+                         "kernel": "k_grouped_gemm (L1 gate+up, SiLU*up epilogue)",
+                         "peak_source": peak_kind},
+            "cpu_baseline": cpu,
+            "e2e": {"value": tokens_total / (e2e_ms * 1e-3), "unit": UNIT,
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": KERNELS_PER_STEP * args.steps,
+            "clocks": clk,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", default="decode")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--ref-tokens", type=int, default=2)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,272 @@
+/*
+ * megamoe.h -- C ABI of the GB300 (sm_103a) NVFP4 MegaMoE routed-expert forward.
+ *
+ * What it computes (sources are the titles and sections of the pages the
+ * method is taken from):
+ *   "CURRENT_BUG.md -- DeepSeek-V4 Blackwell NVFP4"
+ *     - "Architecture: DeepSeek-V4 MegaMoE": 384 experts with top-6 routing
+ *       and a persistent grouped GEMM whose groups are the experts;
+ *     - "What's Been Verified": the MoE is the L1 gate+up GEMM and the L2 down
+ *       GEMM, both NVFP4;
+ *     - "Test Plan -- Finding the NaN", Phase 1: the runner takes
+ *       hidden_states, topk_ids, topk_weights and variable per-expert token
+ *       counts padded to 128 rows, quantises the activations to NVFP4, and
+ *       runs L1 GEMM -> SiLU -> L2 GEMM; Phase 2: zero-token experts and the
+ *       expert_offsets / padded_expert_offsets arrays.
+ *   "Current Bug: vLLM produces NaN from layer 0"
+ *     - "What we've tried" item 1 and "Key evidence": the activation global
+ *       scale must come from the measured amax, never from a stored
+ *       input_scale.
+ *
+ * NVFP4 here: E2M1 element codes (two per byte, even element in the low
+ * nibble), one unsigned E4M3 block scale per 16 elements along K, one FP32
+ * global scale gs per tensor.  An element decodes to
+ * e2m1(code) * e4m3(scale) / gs.  Activations are encoded with
+ * gs = 2688 / amax (448 * 6), and with the float32 steps
+ * s = (amax_b * gs) / 6, s8 = e4m3_rne_satfinite(s), enc = gs / decode(s8),
+ * code = e2m1_rne_satfinite(x * enc), each a correctly rounded operation.
+ *
+ * Conventions for every entry point:
+ *   - All pointers are DEVICE pointers unless a parameter says "host".  The
+ *     caller owns every buffer (workspace included); the library never
+ *     allocates or frees memory and never synchronises on the compute path.
+ *   - All work is enqueued asynchronously on `stream` (a cudaStream_t; NULL is
+ *     the legacy default stream).
+ *   - Argument and shape errors are returned synchronously, before anything
+ *     is enqueued.  A failed launch returns MEGAMOE_ERR_CUDA.  Problems only
+ *     the device can see (an expert id >= E, a non-finite input, a spin-wait
+ *     that ran out) set bits in a device status word and never trap; read it
+ *     with megamoe_read_status.
+ *   - Matrices are row-major.  "Atom layout" (MEGAMOE_SCALES_MMA) stores block
+ *     scales in 512-byte atoms of 128 rows x 4 blocks: atom (a, c) covers rows
+ *     128a..128a+127 and blocks 4c..4c+3 and holds row 128a + 32j + i, block
+ *     4c + b at byte 16i + 4j + b; atoms are ordered [a][c].  This is the
+ *     layout the tensor cores read block scales in.
+ */
+#ifndef MEGAMOE_H
+#define MEGAMOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* megamoe_stream_t; /* == cudaStream_t */
+
+typedef enum megamoe_status {
+  MEGAMOE_OK = 0,
+  MEGAMOE_ERR_INVALID_ARG = 1,       /* null pointer, negative size, bad enum */
+  MEGAMOE_ERR_UNSUPPORTED_SHAPE = 2, /* shape outside the supported set      */
+  MEGAMOE_ERR_WORKSPACE_TOO_SMALL = 3,
+  MEGAMOE_ERR_CUDA = 4,              /* a CUDA runtime/driver call failed     */
+  MEGAMOE_ERR_DEVICE_STATUS = 5      /* megamoe_read_status found bits set    */
+} megamoe_status;
+
+/* Bits of the device status word. */
+#define MEGAMOE_DEV_BAD_EXPERT_ID 0x1u /* a topk id >= E was seen (slot skipped) */
+#define MEGAMOE_DEV_NONFINITE 0x2u     /* the amax of an input was not finite    */
+#define MEGAMOE_DEV_TIMEOUT 0x4u       /* a bounded device wait gave up          */
+
+/* Scale layouts. */
+#define MEGAMOE_SCALES_ROWMAJOR 0 /* [rows, K/16] bytes                         */
+#define MEGAMOE_SCALES_MMA 1      /* atom layout, ceil(rows/128)+1 row-groups    */
+
+/* Grouped-GEMM epilogues. */
+#define MEGAMOE_EPI_F32 0      /* out[r, n] = fp32 accumulator * alpha            */
+#define MEGAMOE_EPI_SILU_MUL 1 /* out[r, i] = bf16(silu(gate) * up), amax of it   */
+
+/* Limits. */
+#define MEGAMOE_MAX_EXPERTS 1024
+#define MEGAMOE_MAX_TOPK 16
+
+/*
+ * NVFP4 expert weights.  Expert e of W13 is [2I, d]: rows 0..I-1 are the gate
+ * projection, rows I..2I-1 the up projection ("What's Been Verified": L1
+ * gate+up).  W2 is [d, I] per expert (L2 down).
+ *   w13_codes   [E, 2I, d/2]            E2M1 codes
+ *   w13_scales  atom layout of [E*2I, d/16] (from megamoe_swizzle_scales)
+ *   w13_gs      [E, 2] float            global scales (gate, up)
+ *   w2_codes    [E, d, I/2]
+ *   w2_scales   atom layout of [E*d, I/16]
+ *   w2_gs       [E] float
+ * Supported: 1 <= E <= 1024, d and I multiples of 256.
+ */
+typedef struct megamoe_weights {
+  int32_t num_experts;
+  int32_t hidden;       /* d */
+  int32_t intermediate; /* I */
+  const uint8_t* w13_codes;
+  const uint8_t* w13_scales;
+  const float* w13_gs;
+  const uint8_t* w2_codes;
+  const uint8_t* w2_scales;
+  const float* w2_gs;
+} megamoe_weights;
+
+/* Human-readable name of a status code (static storage). */
+const char* megamoe_status_string(megamoe_status s);
+
+/*
+ * Largest number of padded rows routing can produce:
+ * T*k + min(E, T*k) * (pad - 1).  Host-only, no device work.
+ */
+int64_t megamoe_max_padded_rows(int T, int k, int E, int pad);
+
+/*
+ * megamoe_route_permute -- bucket the (token, slot) pairs by expert.
+ * ("Test Plan -- Finding the NaN", Phase 1: variable token counts per expert
+ * padded to 128; Phase 2: zero-token experts, expert_offsets and
+ * padded_expert_offsets.)
+ *
+ * Slot s = t*k + j is routed to expert topk_ids[t*k + j].  Slots are grouped
+ * by expert with a stable counting sort (ascending s inside an expert).
+ *   topk_ids        [T, k] int32; ids < 0 are skipped; ids >= E are skipped and
+ *                   set MEGAMOE_DEV_BAD_EXPERT_ID in *status
+ *   counts          [E]    valid slots per expert (out)
+ *   offsets         [E+1]  exclusive prefix sum of counts (out)
+ *   padded_offsets  [E+1]  exclusive prefix sum of counts rounded up to pad;
+ *                          a zero count stays zero (out)
+ *   row_src         [row_capacity] flat slot held by each padded row, -1 for
+ *                   padding and for every row >= padded_offsets[E] (out)
+ *   slot_dst        [T*k]  padded row of each slot, -1 if skipped (out)
+ *   status          device uint32 status word (bits are OR-ed in; may be NULL)
+ * Requires 1 <= E <= 1024, 1 <= k <= 16, pad >= 1, T >= 0 and
+ * row_capacity >= megamoe_max_padded_rows(T, k, E, pad).  One thread block.
+ */
+megamoe_status megamoe_route_permute(const int32_t* topk_ids, int T, int k, int E, int pad,
+                                     int32_t* counts, int32_t* offsets,
+                                     int32_t* padded_offsets, int32_t* row_src,
+                                     int64_t row_capacity, int32_t* slot_dst,
+                                     uint32_t* status, megamoe_stream_t stream);
+
+/*
+ * megamoe_quantize_nvfp4 -- bf16 activations -> NVFP4
+ * ("Test Plan -- Finding the NaN", Phase 1 item 4: quantize_activation_nvfp4;
+ * global scale from the measured amax per "Current Bug: vLLM produces NaN
+ * from layer 0", "What we've tried" item 1).
+ *
+ *   x          [rows, K] bf16 with row stride ld (elements), ld >= K
+ *   amax_in    if non-NULL, the amax to use (device float, e.g. the amax the
+ *              L1 epilogue measured); if NULL the amax of x over all rows is
+ *              measured here (one extra read of x)
+ *   amax_out   device float: the amax used (out; may be NULL if amax_in given)
+ *   gs_out     device float: gs = 2688 / amax, or 1 if amax == 0 (out)
+ *   codes      [out_rows, K/2] (out), scales in `scale_layout` (out)
+ * Row mapping:
+ *   slot_dst == NULL: out row r is x row r (out_rows == rows).
+ *   slot_dst != NULL: x row t is written to out rows slot_dst[t*k + j],
+ *                     j = 0..k-1, skipping -1 (the routed gather).
+ *   row_src != NULL:  out rows with row_src[r] < 0 are written as zero codes
+ *                     and zero scales instead (padding rows).
+ *   live_rows != NULL: device int32; out rows >= *live_rows are not touched.
+ * Requires K a multiple of 64, rows >= 0, out_rows >= 0.
+ */
+megamoe_status megamoe_quantize_nvfp4(const uint16_t* x, int64_t rows, int K, int64_t ld,
+                                      const int32_t* slot_dst, int k, const int32_t* row_src,
+                                      const int32_t* live_rows, int64_t out_rows,
+                                      const float* amax_in, float* amax_out, float* gs_out,
+                                      uint8_t* codes, uint8_t* scales, int scale_layout,
+                                      uint32_t* status, megamoe_stream_t stream);
+
+/*
+ * megamoe_swizzle_scales -- one-time weight preparation: row-major block
+ * scales [rows, K/16] -> atom layout (see the file comment).  Rows are padded
+ * to a multiple of 128 with zero bytes; dst holds ceil(rows/128)*128*K/16
+ * bytes.  Requires K a multiple of 64.
+ */
+megamoe_status megamoe_swizzle_scales(const uint8_t* src, int64_t rows, int K, uint8_t* dst,
+                                      megamoe_stream_t stream);
+
+/*
+ * megamoe_grouped_gemm -- one persistent grouped block-scaled GEMM over all
+ * experts ("Architecture: DeepSeek-V4 MegaMoE": one problem per expert,
+ * persistent tile scheduling across groups, token tile chosen from the
+ * expected tokens per expert).  On tcgen05 tensor cores with TMEM
+ * accumulators and TMA loads.
+ *
+ * For every expert e and every valid row r of e
+ * (padded_offsets[e] <= r < padded_offsets[e] + offsets[e+1] - offsets[e]):
+ *   acc[r, n] = sum_K dequant(act)[r, :] . dequant(w_e)[n, :]   (fp32 accumulate)
+ *   act_codes   [act_rows, K/2]; act_scales atom layout (ceil(act_rows/128)+1
+ *               row-groups); act_gs device float (one global scale)
+ *   w_codes     [E, N, K/2]; w_scales atom layout of [E*N, K/16]
+ *   w_gs        [E, G] float: G = 1 for MEGAMOE_EPI_F32; G = 2 (gate, up) for
+ *               MEGAMOE_EPI_SILU_MUL
+ *   offsets, padded_offsets  [E+1] int32 as produced by megamoe_route_permute
+ *               with a pad that is a multiple of 32
+ * Epilogues:
+ *   MEGAMOE_EPI_F32:      out float [act_rows, ld_out], out[r, n] = acc * alpha,
+ *                         alpha = 1 / (act_gs * w_gs[e]).
+ *   MEGAMOE_EPI_SILU_MUL: N = 2I; out bf16 [act_rows, ld_out],
+ *                         out[r, i] = bf16(silu(acc[r, i] * alpha_gate) *
+ *                                          (acc[r, I + i] * alpha_up)),
+ *                         out_amax (device float, zeroed here) = max |out| over
+ *                         valid rows.
+ * Padding rows of `out` are not written.  tile_n selects the token tile
+ * (32, 64 or 128; 0 = choose from the expected tokens per expert,
+ * expected_tokens = rows the caller expects per active expert, may be 0).
+ * Requires N a multiple of 128 (256 for SILU_MUL), K a multiple of 256,
+ * 1 <= E <= 1024, 16-byte aligned pointers, ld_out >= output width.
+ */
+megamoe_status megamoe_grouped_gemm(const uint8_t* act_codes, const uint8_t* act_scales,
+                                    const float* act_gs, int64_t act_rows,
+                                    const uint8_t* w_codes, const uint8_t* w_scales,
+                                    const float* w_gs, int E, int N, int K,
+                                    const int32_t* offsets, const int32_t* padded_offsets,
+                                    int epilogue, void* out, int64_t ld_out, float* out_amax,
+                                    int tile_n, double expected_tokens, uint32_t* status,
+                                    megamoe_stream_t stream);
+
+/*
+ * megamoe_combine -- top-k weighted combine (topk_weights input of "Test Plan
+ * -- Finding the NaN", Phase 1):
+ *   out[t, :] = bf16( sum_{j=0..k-1, slot_dst[t*k+j] >= 0}
+ *                     topk_weights[t*k+j] * y[slot_dst[t*k+j], :] )
+ * summed in fp32 in ascending j.  y is float [*, ld_y]; out bf16 [T, d].
+ * Requires d a multiple of 4, ld_y a multiple of 4.
+ */
+megamoe_status megamoe_combine(const float* y, int64_t ld_y, const int32_t* slot_dst,
+                               const float* topk_weights, int T, int k, int d, uint16_t* out,
+                               megamoe_stream_t stream);
+
+/*
+ * Workspace bytes megamoe_forward needs for these sizes (host-only).
+ */
+size_t megamoe_workspace_size(int T, int k, int E, int d, int I, int pad);
+
+/*
+ * megamoe_forward -- the whole routed-expert forward on one stream:
+ * route -> amax(x) -> quantise x into routed rows -> L1 grouped GEMM with
+ * SiLU(gate)*up and amax(h) in its epilogue -> requantise h -> L2 grouped
+ * GEMM -> top-k weighted combine.
+ *   x             [T, d] bf16 hidden_states
+ *   topk_ids      [T, k] int32 (ids < 0 skipped)
+ *   topk_weights  [T, k] float (used as given)
+ *   pad           rows per expert are padded to a multiple of pad; must be a
+ *                 multiple of 32 (32, 64, 128, ...)
+ *   out           [T, d] bf16 (out)
+ *   ws, ws_bytes  workspace, at least megamoe_workspace_size(...) bytes,
+ *                 256-byte aligned; its first 4 bytes are the device status
+ *                 word, cleared at the start of every call.
+ * Requires the weight shapes above, 1 <= k <= 16, T >= 0.
+ */
+megamoe_status megamoe_forward(const megamoe_weights* w, const uint16_t* x,
+                               const int32_t* topk_ids, const float* topk_weights, int T, int k,
+                               int pad, uint16_t* out, void* ws, size_t ws_bytes,
+                               megamoe_stream_t stream);
+
+/*
+ * megamoe_read_status -- synchronise `stream`, copy the device status word at
+ * `status` (for megamoe_forward: the first 4 bytes of ws) into *bits (host),
+ * and return MEGAMOE_ERR_DEVICE_STATUS if any bit is set, else MEGAMOE_OK.
+ */
+megamoe_status megamoe_read_status(const uint32_t* status, uint32_t* bits,
+                                   megamoe_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MEGAMOE_H */

@@ -1,0 +1,330 @@
+// C ABI of the MegaMoE library: argument checks, workspace layout and the
+// forward orchestration.  No allocation, no synchronisation on the compute
+// path; every launch goes to the caller's stream.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <algorithm>
+
+#include "../../include/megamoe.h"
+#include "kernels.h"
+
+using namespace megamoe;
+
+namespace {
+
+inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+inline size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+inline megamoe_status cuda_status(cudaError_t e) {
+  return e == cudaSuccess ? MEGAMOE_OK : MEGAMOE_ERR_CUDA;
+}
+
+// Byte size of an atom-layout scale buffer for `rows` rows (one spare row-group
+// so a token tile that starts near the end can read a whole second group).
+inline size_t sf_atom_bytes(int64_t rows, int K) {
+  return static_cast<size_t>((rows + 127) / 128 + 1) * 128 * (K / 16);
+}
+
+// Workspace of megamoe_forward, every region 256-byte aligned.
+struct Workspace {
+  uint32_t* status;
+  float* amax_x;
+  float* gs_x;
+  float* amax_h;
+  float* gs_h;
+  int32_t* counts;
+  int32_t* offsets;
+  int32_t* padded_offsets;
+  int32_t* slot_dst;
+  int32_t* row_src;
+  uint8_t* xq_codes;
+  uint8_t* xq_sf;
+  uint16_t* h;
+  uint8_t* hq_codes;
+  uint8_t* hq_sf;
+  float* y;
+  int64_t rows;  // padded-row capacity
+  size_t bytes;
+};
+
+Workspace carve(void* base, int T, int k, int E, int d, int I, int pad) {
+  Workspace w{};
+  const int64_t rows = megamoe_max_padded_rows(T, k, E, pad);
+  w.rows = rows;
+  size_t off = 0;
+  auto take = [&](size_t bytes) -> uint8_t* {
+    uint8_t* p = base ? static_cast<uint8_t*>(base) + off : nullptr;
+    off = round_up(off + bytes, 256);
+    return p;
+  };
+  uint8_t* hdr = take(256);
+  if (hdr) {
+    w.status = reinterpret_cast<uint32_t*>(hdr);
+    w.amax_x = reinterpret_cast<float*>(hdr + 4);
+    w.gs_x = reinterpret_cast<float*>(hdr + 8);
+    w.amax_h = reinterpret_cast<float*>(hdr + 12);
+    w.gs_h = reinterpret_cast<float*>(hdr + 16);
+  }
+  w.counts = reinterpret_cast<int32_t*>(take(4 * static_cast<size_t>(E)));
+  w.offsets = reinterpret_cast<int32_t*>(take(4 * static_cast<size_t>(E + 1)));
+  w.padded_offsets = reinterpret_cast<int32_t*>(take(4 * static_cast<size_t>(E + 1)));
+  w.slot_dst = reinterpret_cast<int32_t*>(take(4 * static_cast<size_t>(T) * k));
+  w.row_src = reinterpret_cast<int32_t*>(take(4 * static_cast<size_t>(rows)));
+  w.xq_codes = take(static_cast<size_t>(rows) * (d / 2));
+  w.xq_sf = take(sf_atom_bytes(rows, d));
+  w.h = reinterpret_cast<uint16_t*>(take(static_cast<size_t>(rows) * I * 2));
+  w.hq_codes = take(static_cast<size_t>(rows) * (I / 2));
+  w.hq_sf = take(sf_atom_bytes(rows, I));
+  w.y = reinterpret_cast<float*>(take(static_cast<size_t>(rows) * d * 4));
+  w.bytes = off;
+  return w;
+}
+
+megamoe_status check_route_args(int T, int k, int E, int pad) {
+  if (T < 0 || k < 1 || E < 1 || pad < 1) return MEGAMOE_ERR_INVALID_ARG;
+  if (E > MEGAMOE_MAX_EXPERTS || k > MEGAMOE_MAX_TOPK) return MEGAMOE_ERR_UNSUPPORTED_SHAPE;
+  if (static_cast<int64_t>(T) * k > (int64_t{1} << 30)) return MEGAMOE_ERR_UNSUPPORTED_SHAPE;
+  return MEGAMOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* megamoe_status_string(megamoe_status s) {
+  switch (s) {
+    case MEGAMOE_OK: return "ok";
+    case MEGAMOE_ERR_INVALID_ARG: return "invalid argument";
+    case MEGAMOE_ERR_UNSUPPORTED_SHAPE: return "unsupported shape";
+    case MEGAMOE_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case MEGAMOE_ERR_CUDA: return "CUDA error";
+    case MEGAMOE_ERR_DEVICE_STATUS: return "device reported an error";
+  }
+  return "unknown status";
+}
+
+int64_t megamoe_max_padded_rows(int T, int k, int E, int pad) {
+  if (T < 0 || k < 1 || E < 1 || pad < 1) return 0;
+  const int64_t slots = static_cast<int64_t>(T) * k;
+  return slots + std::min<int64_t>(E, slots) * (pad - 1);
+}
+
+megamoe_status megamoe_route_permute(const int32_t* topk_ids, int T, int k, int E, int pad,
+                                     int32_t* counts, int32_t* offsets, int32_t* padded_offsets,
+                                     int32_t* row_src, int64_t row_capacity, int32_t* slot_dst,
+                                     uint32_t* status, megamoe_stream_t stream) {
+  megamoe_status st = check_route_args(T, k, E, pad);
+  if (st != MEGAMOE_OK) return st;
+  if (!counts || !offsets || !padded_offsets || (T > 0 && (!topk_ids || !slot_dst)))
+    return MEGAMOE_ERR_INVALID_ARG;
+  const int64_t need = megamoe_max_padded_rows(T, k, E, pad);
+  if (row_capacity < need || (row_capacity > 0 && !row_src)) return MEGAMOE_ERR_INVALID_ARG;
+  return cuda_status(launch_route(topk_ids, T * k, E, pad, counts, offsets, padded_offsets,
+                                  row_src, row_capacity, slot_dst, status,
+                                  reinterpret_cast<cudaStream_t>(stream)));
+}
+
+megamoe_status megamoe_quantize_nvfp4(const uint16_t* x, int64_t rows, int K, int64_t ld,
+                                      const int32_t* slot_dst, int k, const int32_t* row_src,
+                                      const int32_t* live_rows, int64_t out_rows,
+                                      const float* amax_in, float* amax_out, float* gs_out,
+                                      uint8_t* codes, uint8_t* scales, int scale_layout,
+                                      uint32_t* status, megamoe_stream_t stream) {
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (rows < 0 || out_rows < 0 || K <= 0 || ld < K) return MEGAMOE_ERR_INVALID_ARG;
+  if (scale_layout != MEGAMOE_SCALES_ROWMAJOR && scale_layout != MEGAMOE_SCALES_MMA)
+    return MEGAMOE_ERR_INVALID_ARG;
+  if (K % 64 != 0 || ld % 8 != 0) return MEGAMOE_ERR_UNSUPPORTED_SHAPE;
+  if (!gs_out || (!amax_in && !amax_out)) return MEGAMOE_ERR_INVALID_ARG;
+  if (slot_dst) {
+    if (k < 1 || k > MEGAMOE_MAX_TOPK) return MEGAMOE_ERR_INVALID_ARG;
+  } else if (rows < out_rows) {
+    return MEGAMOE_ERR_INVALID_ARG;
+  }
+  if ((rows > 0 && !x) || (out_rows > 0 && (!codes || !scales))) return MEGAMOE_ERR_INVALID_ARG;
+  if (x && !aligned(x, 16)) return MEGAMOE_ERR_UNSUPPORTED_SHAPE;
+  if ((codes && !aligned(codes, 16)) || (scales && !aligned(scales, 4)))
+    return MEGAMOE_ERR_UNSUPPORTED_SHAPE;
+  const float* amax = amax_in;
+  if (!amax_in) {
+    cudaError_t e = launch_amax(x, rows, K, ld, amax_out, status, s);
+    if (e != cudaSuccess) return MEGAMOE_ERR_CUDA;
+    amax = amax_out;
+  } else if (amax_out && amax_out != amax_in) {
+    if (cudaMemcpyAsync(amax_out, amax_in, sizeof(float), cudaMemcpyDeviceToDevice, s) !=
+        cudaSuccess)
+      return MEGAMOE_ERR_CUDA;
+  }
+  return cuda_status(launch_quant(x, rows, K, ld, slot_dst, k, row_src, live_rows, out_rows, amax,
+                                  gs_out, codes, scales, scale_layout, s));
+}
+
+megamoe_status megamoe_swizzle_scales(const uint8_t* src, int64_t rows, int K, uint8_t* dst,
+                                      megamoe_stream_t stream) {
+  if (rows < 0 || K <= 0) return MEGAMOE_ERR_INVALID_ARG;
+  if (K % 64 != 0) return MEGAMOE_ERR_UNSUPPORTED_SHAPE;
+  if (rows > 0 && (!src || !dst)) return MEGAMOE_ERR_INVALID_ARG;
+  if (rows > 0 && (!aligned(src, 4) || !aligned(dst, 4))) return MEGAMOE_ERR_UNSUPPORTED_SHAPE;
+  return cuda_status(launch_swizzle(src, rows, K, dst, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+megamoe_status megamoe_grouped_gemm(const uint8_t* act_codes, const uint8_t* act_scales,
+                                    const float* act_gs, int64_t act_rows, const uint8_t* w_codes,
+                                    const uint8_t* w_scales, const float* w_gs, int E, int N,
+                                    int K, const int32_t* offsets, const int32_t* padded_offsets,
+                                    int epilogue, void* out, int64_t ld_out, float* out_amax,
+                                    int tile_n, double expected_tokens, uint32_t* status,
+                                    megamoe_stream_t stream) {
+  if (act_rows < 0 || E < 1 || N <= 0 || K <= 0) return MEGAMOE_ERR_INVALID_ARG;
+  if (epilogue != MEGAMOE_EPI_F32 && epilogue != MEGAMOE_EPI_SILU_MUL)
+    return MEGAMOE_ERR_INVALID_ARG;
+  if (E > MEGAMOE_MAX_EXPERTS || K % 256 != 0 || N % (epilogue == MEGAMOE_EPI_F32 ? 128 : 256))
+    return MEGAMOE_ERR_UNSUPPORTED_SHAPE;
+  if (static_cast<int64_t>(E) * N >= (int64_t{1} << 31) || act_rows >= (int64_t{1} << 31))
+    return MEGAMOE_ERR_UNSUPPORTED_SHAPE;
+  if (tile_n != 0 && tile_n != 32 && tile_n != 64 && tile_n != 128) return MEGAMOE_ERR_INVALID_ARG;
+  const int width = epilogue == MEGAMOE_EPI_F32 ? N : N / 2;
+  if (ld_out < width) return MEGAMOE_ERR_INVALID_ARG;
+  if (!w_codes || !w_scales || !w_gs || !offsets || !padded_offsets ||
+      (act_rows > 0 && (!act_codes || !act_scales || !act_gs || !out)))
+    return MEGAMOE_ERR_INVALID_ARG;
+  if (epilogue == MEGAMOE_EPI_SILU_MUL && !out_amax) return MEGAMOE_ERR_INVALID_ARG;
+  if (!aligned(w_codes, 16) || !aligned(w_scales, 16) || (act_codes && !aligned(act_codes, 16)) ||
+      (act_scales && !aligned(act_scales, 16)))
+    return MEGAMOE_ERR_UNSUPPORTED_SHAPE;
+  GemmLaunch g{};
+  g.act_codes = act_codes;
+  g.act_scales = act_scales;
+  g.act_gs = act_gs;
+  g.act_rows = act_rows;
+  g.w_codes = w_codes;
+  g.w_scales = w_scales;
+  g.w_gs = w_gs;
+  g.E = E;
+  g.N = N;
+  g.K = K;
+  g.offsets = offsets;
+  g.padded_offsets = padded_offsets;
+  g.epilogue = epilogue;
+  g.out = out;
+  g.ld_out = ld_out;
+  g.out_amax = out_amax;
+  g.tile_n = tile_n ? tile_n : pick_tile_n(expected_tokens);
+  g.status = status;
+  return cuda_status(launch_grouped_gemm(g, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+megamoe_status megamoe_combine(const float* y, int64_t ld_y, const int32_t* slot_dst,
+                               const float* topk_weights, int T, int k, int d, uint16_t* out,
+                               megamoe_stream_t stream) {
+  if (T < 0 || k < 1 || k > MEGAMOE_MAX_TOPK || d <= 0 || ld_y < d) return MEGAMOE_ERR_INVALID_ARG;
+  if (d % 4 != 0 || ld_y % 4 != 0) return MEGAMOE_ERR_UNSUPPORTED_SHAPE;
+  if (T > 0 && (!y || !slot_dst || !topk_weights || !out)) return MEGAMOE_ERR_INVALID_ARG;
+  if (T > 0 && (!aligned(y, 16) || !aligned(out, 8))) return MEGAMOE_ERR_UNSUPPORTED_SHAPE;
+  return cuda_status(
+      launch_combine(y, ld_y, slot_dst, topk_weights, T, k, d, out,
+                     reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t megamoe_workspace_size(int T, int k, int E, int d, int I, int pad) {
+  if (T < 0 || k < 1 || E < 1 || d <= 0 || I <= 0 || pad < 1) return 0;
+  return carve(nullptr, T, k, E, d, I, pad).bytes;
+}
+
+megamoe_status megamoe_forward(const megamoe_weights* w, const uint16_t* x,
+                               const int32_t* topk_ids, const float* topk_weights, int T, int k,
+                               int pad, uint16_t* out, void* ws, size_t ws_bytes,
+                               megamoe_stream_t stream) {
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (!w) return MEGAMOE_ERR_INVALID_ARG;
+  const int E = w->num_experts, d = w->hidden, I = w->intermediate;
+  megamoe_status st = check_route_args(T, k, E, pad);
+  if (st != MEGAMOE_OK) return st;
+  if (d <= 0 || I <= 0) return MEGAMOE_ERR_INVALID_ARG;
+  if (d % 256 != 0 || I % 256 != 0 || pad % 32 != 0) return MEGAMOE_ERR_UNSUPPORTED_SHAPE;
+  if (!w->w13_codes || !w->w13_scales || !w->w13_gs || !w->w2_codes || !w->w2_scales ||
+      !w->w2_gs || !ws)
+    return MEGAMOE_ERR_INVALID_ARG;
+  if (T > 0 && (!x || !topk_ids || !topk_weights || !out)) return MEGAMOE_ERR_INVALID_ARG;
+  if (!aligned(ws, 256)) return MEGAMOE_ERR_INVALID_ARG;
+  if ((x && !aligned(x, 16)) || (out && !aligned(out, 8)) || !aligned(w->w13_codes, 16) ||
+      !aligned(w->w2_codes, 16) || !aligned(w->w13_scales, 16) || !aligned(w->w2_scales, 16))
+    return MEGAMOE_ERR_UNSUPPORTED_SHAPE;
+  Workspace wk = carve(ws, T, k, E, d, I, pad);
+  if (ws_bytes < wk.bytes) return MEGAMOE_ERR_WORKSPACE_TOO_SMALL;
+
+  if (cudaMemsetAsync(wk.status, 0, 256, s) != cudaSuccess) return MEGAMOE_ERR_CUDA;
+  if (T == 0) return MEGAMOE_OK;
+  const double expected = static_cast<double>(T) * k / E;
+  const int tile_n = pick_tile_n(expected);
+
+  cudaError_t e;
+  // 1. route
+  e = launch_route(topk_ids, T * k, E, pad, wk.counts, wk.offsets, wk.padded_offsets, wk.row_src,
+                   wk.rows, wk.slot_dst, wk.status, s);
+  if (e != cudaSuccess) return MEGAMOE_ERR_CUDA;
+  // 2-3. amax of x, then quantise x into its routed rows (padding rows zeroed)
+  e = launch_amax(x, T, d, d, wk.amax_x, wk.status, s);
+  if (e != cudaSuccess) return MEGAMOE_ERR_CUDA;
+  e = launch_quant(x, T, d, d, wk.slot_dst, k, wk.row_src, wk.padded_offsets + E, wk.rows,
+                   wk.amax_x, wk.gs_x, wk.xq_codes, wk.xq_sf, MEGAMOE_SCALES_MMA, s);
+  if (e != cudaSuccess) return MEGAMOE_ERR_CUDA;
+  // 4. L1 gate+up grouped GEMM, SiLU(gate)*up -> bf16 h, amax(h)
+  GemmLaunch g{};
+  g.act_codes = wk.xq_codes;
+  g.act_scales = wk.xq_sf;
+  g.act_gs = wk.gs_x;
+  g.act_rows = wk.rows;
+  g.w_codes = w->w13_codes;
+  g.w_scales = w->w13_scales;
+  g.w_gs = w->w13_gs;
+  g.E = E;
+  g.N = 2 * I;
+  g.K = d;
+  g.offsets = wk.offsets;
+  g.padded_offsets = wk.padded_offsets;
+  g.epilogue = MEGAMOE_EPI_SILU_MUL;
+  g.out = wk.h;
+  g.ld_out = I;
+  g.out_amax = wk.amax_h;
+  g.tile_n = tile_n;
+  g.status = wk.status;
+  e = launch_grouped_gemm(g, s);
+  if (e != cudaSuccess) return MEGAMOE_ERR_CUDA;
+  // 5. requantise h with gs from amax(h)
+  e = launch_quant(wk.h, wk.rows, I, I, nullptr, 1, wk.row_src, wk.padded_offsets + E, wk.rows,
+                   wk.amax_h, wk.gs_h, wk.hq_codes, wk.hq_sf, MEGAMOE_SCALES_MMA, s);
+  if (e != cudaSuccess) return MEGAMOE_ERR_CUDA;
+  // 6. L2 down grouped GEMM -> fp32 y
+  g.act_codes = wk.hq_codes;
+  g.act_scales = wk.hq_sf;
+  g.act_gs = wk.gs_h;
+  g.w_codes = w->w2_codes;
+  g.w_scales = w->w2_scales;
+  g.w_gs = w->w2_gs;
+  g.N = d;
+  g.K = I;
+  g.epilogue = MEGAMOE_EPI_F32;
+  g.out = wk.y;
+  g.ld_out = d;
+  g.out_amax = nullptr;
+  e = launch_grouped_gemm(g, s);
+  if (e != cudaSuccess) return MEGAMOE_ERR_CUDA;
+  // 7. top-k weighted combine
+  e = launch_combine(wk.y, d, wk.slot_dst, topk_weights, T, k, d, out, s);
+  return cuda_status(e);
+}
+
+megamoe_status megamoe_read_status(const uint32_t* status, uint32_t* bits,
+                                   megamoe_stream_t stream) {
+  if (!status || !bits) return MEGAMOE_ERR_INVALID_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MEGAMOE_ERR_CUDA;
+  if (cudaMemcpy(bits, status, sizeof(uint32_t), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return MEGAMOE_ERR_CUDA;
+  return *bits ? MEGAMOE_ERR_DEVICE_STATUS : MEGAMOE_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,460 @@
+// Persistent grouped block-scaled NVFP4 GEMM on tcgen05 tensor cores.
+//
+// "CURRENT_BUG.md -- DeepSeek-V4 Blackwell NVFP4", "Architecture: DeepSeek-V4
+// MegaMoE": one GEMM problem per expert, persistent tile scheduling across the
+// experts, a token tile chosen from the expected tokens per expert (small for
+// decode, large for prefill); "What's Been Verified": L1 gate+up and L2 down.
+//
+// Shape of one tile (weights on the MMA's M side, tokens on N):
+//   D[128 output features, BN tokens] = W_e[features, K] x A[tokens, K]^T
+// with E2M1 operands and one E4M3 scale per 16 elements of each operand,
+// accumulated in fp32 in tensor memory (tcgen05.mma kind::mxf4nvf4,
+// scale_vec::4X, M = 128, K = 64 per instruction).  For the L1 GEMM a tile
+// holds the gate AND the up accumulators of the same 128 features (two MMAs
+// per K step into two TMEM ranges), so SiLU(gate) * up is a per-lane epilogue.
+//
+// Roles (192 threads, one CTA per SM, grid = number of SMs):
+//   warp 0      TMA producer: weight tiles and token tiles (128-byte swizzle)
+//               plus their block-scale atoms (bulk copies) into a STAGES-deep
+//               shared-memory ring;
+//   warp 1      TMEM allocator; one lane issues tcgen05.cp (scales -> TMEM)
+//               and tcgen05.mma, and commits stage-free / accumulator-ready;
+//   warps 2..5  epilogue: tcgen05.ld of their 32-lane quarter, alpha scaling,
+//               SiLU * up -> bf16 + amax (L1) or fp32 (L2), masked stores.
+// Every expert's weights live in one [E*N, K/2] tensor, so one tensor map
+// serves all experts: the expert is a row coordinate, not a new descriptor.
+// Tiles are numbered expert-major, weight-tile-major, token-tile-minor, so CTAs
+// working on the same expert's weight tile run together and share it in L2.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace megamoe {
+
+constexpr int kGemmThreads = 192;
+
+struct GemmArgs {
+  const uint8_t* w_sf;  // atom layout [E*N/128][K/64][512]
+  const uint8_t* a_sf;  // atom layout [ceil(rows/128)+1][K/64][512]
+  const float* w_gs;    // [E][G]
+  const float* a_gs;    // device scalar
+  const int32_t* offsets;
+  const int32_t* padded_offsets;
+  void* out;
+  int64_t ld_out;
+  float* out_amax;
+  uint32_t* status;
+  int E, N, K;
+};
+
+template <int BN, int EPI, int STAGES>
+struct GemmCfg {
+  static constexpr int G = EPI == MEGAMOE_EPI_SILU_MUL ? 2 : 1;
+  static constexpr int A_TILE = 128 * 128;  // one weight matrix, 128 rows x 128 bytes
+  static constexpr int B_TILE = BN * 128;
+  static constexpr int SFW = 2048;  // 4 atoms of 512 bytes (one per 64-element slice)
+  static constexpr int SFA = 4096;  // two row-groups of 4 atoms
+  static constexpr int OFF_A = 0;
+  static constexpr int OFF_B = G * A_TILE;
+  static constexpr int OFF_SFW = OFF_B + B_TILE;
+  static constexpr int OFF_SFA = OFF_SFW + G * SFW;
+  static constexpr int STAGE = (OFF_SFA + SFA + 1023) / 1024 * 1024;
+  static constexpr uint32_t TX = G * A_TILE + B_TILE + G * SFW + SFA;
+  static constexpr int ACC_COLS = G * BN;
+  static constexpr int SF_COLS = 16 * G + 32;  // per stage: weight scales + token scales
+  static constexpr int SF_COL0 = ACC_COLS;
+  static constexpr int BAR_OFF = STAGES * STAGE;
+  static constexpr int TOFF_OFF = BAR_OFF + 256;
+  static constexpr int SMEM = 1024 + TOFF_OFF + 4 * (MEGAMOE_MAX_EXPERTS + 1);
+  static constexpr uint32_t IDESC = idesc_nvf4(128, BN);
+  static_assert(SF_COL0 + STAGES * SF_COLS <= 512, "tensor memory budget");
+  static_assert(SMEM <= 232448, "shared memory budget");
+  static_assert((2 * STAGES + 3) * 8 + 8 <= 256, "barrier area");
+};
+
+struct TileInfo {
+  int e, mt, nt, count, poff;
+};
+
+template <int BN>
+__device__ __forceinline__ TileInfo decode_tile(int tile, const int* s_toff, int E,
+                                                const int32_t* offsets,
+                                                const int32_t* padded_offsets) {
+  int lo = 0, hi = E - 1;
+  while (lo < hi) {  // largest e with s_toff[e] <= tile; it always owns tiles
+    const int mid = (lo + hi + 1) >> 1;
+    if (s_toff[mid] <= tile) lo = mid;
+    else hi = mid - 1;
+  }
+  TileInfo t;
+  t.e = lo;
+  t.count = __ldg(offsets + lo + 1) - __ldg(offsets + lo);
+  t.poff = __ldg(padded_offsets + lo);
+  const int ntiles = (t.count + BN - 1) / BN;
+  const int local = tile - s_toff[lo];
+  t.mt = local / ntiles;
+  t.nt = local - t.mt * ntiles;
+  return t;
+}
+
+// s_toff[e] = first tile of expert e, s_toff[E] = total tiles.  All threads.
+template <int BN>
+__device__ void build_tile_offsets(const int32_t* offsets, int E, int MT, int* s_toff,
+                                   int* s_scan) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int per = (E + kGemmThreads - 1) / kGemmThreads;
+  const int e0 = tid * per, e1 = min(E, e0 + per);
+  int sum = 0;
+  for (int e = e0; e < e1; ++e) {
+    const int cnt = __ldg(offsets + e + 1) - __ldg(offsets + e);
+    const int t = cnt > 0 ? (cnt + BN - 1) / BN * MT : 0;
+    s_toff[e] = t;
+    sum += t;
+  }
+  int x = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) s_scan[warp] = x;
+  __syncthreads();
+  int base = x - sum;
+  for (int w = 0; w < warp; ++w) base += s_scan[w];
+  for (int e = e0; e < e1; ++e) {
+    const int t = s_toff[e];
+    s_toff[e] = base;
+    base += t;
+  }
+  if (tid == kGemmThreads - 1) s_toff[E] = base;
+  __syncthreads();
+}
+
+// Waits that ignore the abort flag (used only while unwinding).
+__device__ __forceinline__ void mbar_drain(uint64_t* bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer() - t0 > kWaitTimeoutNs) break;
+  }
+}
+
+template <int BN, int EPI, int STAGES>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    k_grouped_gemm(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_a,
+                   const GemmArgs p) {
+  using C = GemmCfg<BN, EPI, STAGES>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
+  uint64_t* empty = full + STAGES;
+  uint64_t* acc_full = empty + STAGES;
+  uint64_t* acc_empty = acc_full + 1;
+  uint64_t* drain = acc_empty + 1;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+  int* s_toff = reinterpret_cast<int*>(smem + C::TOFF_OFF);
+  __shared__ int s_scan[kGemmThreads / 32];
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int E = p.E, N = p.N, K = p.K;
+  const int MT = (C::G == 2 ? N / 2 : N) / 128;
+  const int KT = K / 256;
+  const int slices = K / 64;
+
+  build_tile_offsets<BN>(p.offsets, E, MT, s_toff, s_scan);
+  const int total = s_toff[E];
+  if (static_cast<int>(blockIdx.x) >= total) return;  // uniform: no work for this CTA
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(acc_full, 1);
+    mbar_init(acc_empty, 4);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_holder, 512);
+    tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tensormap(&tm_w);
+    prefetch_tensormap(&tm_a);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ producer
+      const uint64_t pol_w = policy_evict_first();
+      const uint64_t pol_a = policy_evict_last();
+      int stage = 0;
+      uint32_t phase = 0;
+      int issued_parity[STAGES];
+      for (int s = 0; s < STAGES; ++s) issued_parity[s] = -1;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+        const TileInfo ti = decode_tile<BN>(tile, s_toff, E, p.offsets, p.padded_offsets);
+        const int w_row0 = ti.e * N + ti.mt * 128;
+        const int w_row1 = ti.e * N + N / 2 + ti.mt * 128;  // up rows (L1 only)
+        const int a_row0 = ti.poff + ti.nt * BN;
+        const int64_t atom0 = a_row0 >> 7;
+        for (int kt = 0; kt < KT; ++kt) {
+          if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          uint8_t* sb = smem + stage * C::STAGE;
+          mbar_arrive_expect_tx(&full[stage], C::TX);
+          tma_load_2d(sb + C::OFF_A, &tm_w, &full[stage], kt * 128, w_row0, pol_w);
+          bulk_load(sb + C::OFF_SFW,
+                    p.w_sf + (static_cast<int64_t>(w_row0 >> 7) * slices + 4 * kt) * 512, C::SFW,
+                    &full[stage], pol_w);
+          if (C::G == 2) {
+            tma_load_2d(sb + C::OFF_A + C::A_TILE, &tm_w, &full[stage], kt * 128, w_row1, pol_w);
+            bulk_load(sb + C::OFF_SFW + C::SFW,
+                      p.w_sf + (static_cast<int64_t>(w_row1 >> 7) * slices + 4 * kt) * 512,
+                      C::SFW, &full[stage], pol_w);
+          }
+          tma_load_2d(sb + C::OFF_B, &tm_a, &full[stage], kt * 128, a_row0, pol_a);
+          bulk_load(sb + C::OFF_SFA, p.a_sf + (atom0 * slices + 4 * kt) * 512, 2048, &full[stage],
+                    pol_a);
+          bulk_load(sb + C::OFF_SFA + 2048, p.a_sf + ((atom0 + 1) * slices + 4 * kt) * 512, 2048,
+                    &full[stage], pol_a);
+          issued_parity[stage] = static_cast<int>(phase);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {  // unwinding: let every copy already in flight land first
+        for (int s = 0; s < STAGES; ++s)
+          if (issued_parity[s] >= 0) mbar_drain(&full[s], static_cast<uint32_t>(issued_parity[s]));
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ MMA issuer
+      int stage = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+        const TileInfo ti = decode_tile<BN>(tile, s_toff, E, p.offsets, p.padded_offsets);
+        const uint32_t sfb_shift = static_cast<uint32_t>(((ti.poff + ti.nt * BN) & 127) >> 5);
+        if (!mbar_wait(acc_empty, acc_phase ^ 1u, abort_flag, p.status)) break;
+        tc_fence_after();
+        for (int kt = 0; kt < KT; ++kt) {
+          if (!mbar_wait(&full[stage], phase, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint8_t* sb = smem + stage * C::STAGE;
+          const uint32_t sf_col = tmem + C::SF_COL0 + stage * C::SF_COLS;
+          const uint32_t sfa_col = sf_col + 16 * C::G;
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+#pragma unroll
+            for (int g = 0; g < C::G; ++g)
+              tmem_cp_32x128b_x4(sf_col + 16 * g + 4 * c,
+                                 sdesc_sf(smem_u32(sb + C::OFF_SFW + g * C::SFW + c * 512)));
+            tmem_cp_32x128b_x4(sfa_col + 8 * c, sdesc_sf(smem_u32(sb + C::OFF_SFA + c * 512)));
+            tmem_cp_32x128b_x4(sfa_col + 8 * c + 4,
+                               sdesc_sf(smem_u32(sb + C::OFF_SFA + 2048 + c * 512)));
+          }
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const uint64_t bdesc = sdesc_sw128(smem_u32(sb + C::OFF_B) + 32 * c);
+#pragma unroll
+            for (int g = 0; g < C::G; ++g) {
+              const uint64_t adesc = sdesc_sw128(smem_u32(sb + C::OFF_A + g * C::A_TILE) + 32 * c);
+              mma_nvf4(tmem + g * BN, adesc, bdesc, C::IDESC, sf_col + 16 * g + 4 * c,
+                       sfa_col + 8 * c + sfb_shift, (kt | c) != 0 ? 1u : 0u);
+            }
+          }
+          tc_commit(&empty[stage]);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        tc_commit(acc_full);
+        acc_phase ^= 1u;
+      }
+      // every MMA issued so far must finish before tensor memory is released
+      tc_commit(drain);
+      mbar_drain(drain, 0);
+    }
+    __syncwarp();
+  } else {
+    // -------------------------------------------------------------- epilogue
+    const int q = warp & 3;  // the TMEM lane quarter this warp may access
+    const float a_gs = __ldg(p.a_gs);
+    uint32_t acc_phase = 0;
+    float amax = 0.f;
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+      const TileInfo ti = decode_tile<BN>(tile, s_toff, E, p.offsets, p.padded_offsets);
+      const int m_valid = min(BN, ti.count - ti.nt * BN);
+      const int64_t row0 = ti.poff + static_cast<int64_t>(ti.nt) * BN;
+      const int f = ti.mt * 128 + q * 32 + lane;
+      float alpha0, alpha1 = 0.f;
+      if (C::G == 2) {
+        alpha0 = 1.0f / (a_gs * __ldg(p.w_gs + 2 * ti.e));
+        alpha1 = 1.0f / (a_gs * __ldg(p.w_gs + 2 * ti.e + 1));
+      } else {
+        alpha0 = 1.0f / (a_gs * __ldg(p.w_gs + ti.e));
+      }
+      if (!mbar_wait(acc_full, acc_phase, abort_flag, p.status)) break;
+      tc_fence_after();
+      const uint32_t lane_base = tmem + (static_cast<uint32_t>(q * 32) << 16);
+      for (int n0 = 0; n0 < m_valid; n0 += 16) {
+        uint32_t g[16];
+        tmem_ld_32x32b_x16(lane_base + n0, g);
+        if (C::G == 2) {
+          uint32_t u[16];
+          tmem_ld_32x32b_x16(lane_base + BN + n0, u);
+          tmem_ld_wait();
+          __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            if (n0 + j < m_valid) {
+              const float gv = __uint_as_float(g[j]) * alpha0;
+              const float uv = __uint_as_float(u[j]) * alpha1;
+              const float h = gv / (1.0f + expf(-gv)) * uv;
+              const __nv_bfloat16 hb = __float2bfloat16_rn(h);
+              amax = fmaxf(amax, fabsf(__bfloat162float(hb)));
+              out[(row0 + n0 + j) * p.ld_out + f] = hb;
+            }
+          }
+        } else {
+          tmem_ld_wait();
+          float* out = reinterpret_cast<float*>(p.out);
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            if (n0 + j < m_valid) out[(row0 + n0 + j) * p.ld_out + f] = __uint_as_float(g[j]) * alpha0;
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acc_empty);
+      acc_phase ^= 1u;
+    }
+    if (C::G == 2) {
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+      if (lane == 0 && amax > 0.f)
+        atomicMax(reinterpret_cast<unsigned int*>(p.out_amax), __float_as_uint(amax));
+    }
+  }
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+// 2-D map over a [rows, row_bytes] byte matrix, boxes of box_rows x 128 bytes
+// in the 128-byte swizzle the MMA descriptors expect.
+static bool make_codes_map(CUtensorMap* map, const void* base, uint64_t rows, uint64_t row_bytes,
+                           uint32_t box_rows) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {row_bytes, rows};
+  cuuint64_t strides[1] = {row_bytes};
+  cuuint32_t box[2] = {128, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+static int num_sms() {
+  int dev = 0, n = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  return n > 0 ? n : 1;
+}
+
+template <int BN, int EPI, int STAGES>
+static cudaError_t launch_cfg(const CUtensorMap& tm_w, const CUtensorMap& tm_a, const GemmArgs& a,
+                              cudaStream_t stream) {
+  using C = GemmCfg<BN, EPI, STAGES>;
+  auto kern = k_grouped_gemm<BN, EPI, STAGES>;
+  cudaError_t err =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  if (err != cudaSuccess) return err;
+  kern<<<num_sms(), kGemmThreads, C::SMEM, stream>>>(tm_w, tm_a, a);
+  return cudaGetLastError();
+}
+
+int pick_tile_n(double expected) {
+  if (expected <= 32.0) return 32;
+  if (expected <= 96.0) return 64;
+  return 128;
+}
+
+cudaError_t launch_grouped_gemm(const GemmLaunch& g, cudaStream_t stream) {
+  if (g.act_rows == 0 || g.E == 0) return cudaSuccess;
+  const int bn = g.tile_n;
+  CUtensorMap tm_w, tm_a;
+  if (!make_codes_map(&tm_w, g.w_codes, static_cast<uint64_t>(g.E) * g.N, g.K / 2, 128) ||
+      !make_codes_map(&tm_a, g.act_codes, static_cast<uint64_t>(g.act_rows), g.K / 2, bn))
+    return cudaErrorInvalidValue;
+  GemmArgs a{g.w_scales, g.act_scales, g.w_gs,   g.act_gs, g.offsets, g.padded_offsets,
+             g.out,      g.ld_out,     g.out_amax, g.status, g.E,       g.N,
+             g.K};
+  if (g.epilogue == MEGAMOE_EPI_SILU_MUL) {
+    if (g.out_amax) {
+      cudaError_t err = cudaMemsetAsync(g.out_amax, 0, sizeof(float), stream);
+      if (err != cudaSuccess) return err;
+    }
+    switch (bn) {
+      case 32: return launch_cfg<32, MEGAMOE_EPI_SILU_MUL, 5>(tm_w, tm_a, a, stream);
+      case 64: return launch_cfg<64, MEGAMOE_EPI_SILU_MUL, 4>(tm_w, tm_a, a, stream);
+      case 128: return launch_cfg<128, MEGAMOE_EPI_SILU_MUL, 3>(tm_w, tm_a, a, stream);
+    }
+  } else {
+    switch (bn) {
+      case 32: return launch_cfg<32, MEGAMOE_EPI_F32, 8>(tm_w, tm_a, a, stream);
+      case 64: return launch_cfg<64, MEGAMOE_EPI_F32, 7>(tm_w, tm_a, a, stream);
+      case 128: return launch_cfg<128, MEGAMOE_EPI_F32, 5>(tm_w, tm_a, a, stream);
+    }
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace megamoe

@@ -1,0 +1,220 @@
+// NVFP4 activation quantisation with a global scale from the measured amax
+// ("CURRENT_BUG.md -- DeepSeek-V4 Blackwell NVFP4", "Test Plan -- Finding the
+// NaN", Phase 1 item 4: quantize_activation_nvfp4; "Current Bug: vLLM
+// produces NaN from layer 0", "What we've tried" item 1 and "Key evidence":
+// the global scale comes from the measured amax, never a stored input_scale).
+//
+// k_amax    one streaming read of the bf16 tensor with 128-bit loads; the
+//           |x| maximum is taken on the bf16 bit patterns with packed 16-bit
+//           integer max (monotone for finite values), reduced with warp
+//           shuffles and one atomicMax per block.
+// k_quant   one thread per (row, 64-element slice): 128 bytes of bf16 in
+//           (8 x 128-bit loads), 32 bytes of E2M1 codes and one 32-bit word of
+//           four E4M3 block scales out.  The routed gather is fused: a token
+//           row is encoded once and written to each of its k expert rows.
+// k_swizzle row-major block scales -> the tensor-core atom layout (weights,
+//           once, off the hot path).
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace megamoe {
+
+__global__ void __launch_bounds__(256) k_amax(const uint16_t* __restrict__ x, int64_t rows, int K,
+                                              int64_t ld, float* amax, uint32_t* status) {
+  const int vecs = K / 8;
+  const int64_t total = rows * vecs;
+  uint32_t m2 = 0;  // two packed |bf16| maxima
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t r = i / vecs;
+    const int v = static_cast<int>(i - r * vecs);
+    const uint4 q = __ldg(reinterpret_cast<const uint4*>(x + r * ld) + v);
+    m2 = __vmaxu2(m2, q.x & 0x7FFF7FFFu);
+    m2 = __vmaxu2(m2, q.y & 0x7FFF7FFFu);
+    m2 = __vmaxu2(m2, q.z & 0x7FFF7FFFu);
+    m2 = __vmaxu2(m2, q.w & 0x7FFF7FFFu);
+  }
+  uint32_t m = max(m2 & 0xFFFFu, m2 >> 16);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+  __shared__ uint32_t red[8];
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int w = 1; w < (blockDim.x >> 5); ++w) m = max(m, red[w]);
+    if (m >= 0x7F80u) {  // Inf or NaN
+      set_status(status, MEGAMOE_DEV_NONFINITE);
+      m = 0x7F7Fu;  // keep the scale finite; the result is flagged anyway
+    }
+    atomicMax(reinterpret_cast<unsigned int*>(amax), m << 16);
+  }
+}
+
+struct QuantArgs {
+  const uint16_t* x;
+  int64_t rows_in;
+  int K;
+  int64_t ld;
+  const int32_t* slot_dst;
+  int k;
+  const int32_t* row_src;
+  const int32_t* live_rows;
+  int64_t out_rows;
+  const float* amax;
+  float* gs_out;
+  uint8_t* codes;
+  uint8_t* scales;
+  int scale_layout;
+};
+
+__device__ __forceinline__ float bf16_bits_to_float(uint32_t h) { return __uint_as_float(h << 16); }
+
+// Encode 64 consecutive bf16 values (eight 128-bit words) into 8 code words
+// (32 bytes) and one word of four scale bytes.
+__device__ __forceinline__ void encode_slice(const uint4 (&v)[8], float gs, uint32_t (&codes)[8],
+                                             uint32_t& sword) {
+  sword = 0;
+#pragma unroll
+  for (int b = 0; b < 4; ++b) {  // 16-element block b = words 2b, 2b+1
+    float xv[16];
+#pragma unroll
+    for (int w = 0; w < 2; ++w) {
+      const uint4 q = v[2 * b + w];
+      const uint32_t u[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        xv[8 * w + 2 * j] = bf16_bits_to_float(u[j] & 0xFFFFu);
+        xv[8 * w + 2 * j + 1] = bf16_bits_to_float(u[j] >> 16);
+      }
+    }
+    float amax_b = 0.f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) amax_b = fmaxf(amax_b, fabsf(xv[i]));
+    const float s = __fdiv_rn(__fmul_rn(amax_b, gs), 6.0f);
+    const uint32_t s8 = e4m3_code(s);
+    const float sd = e4m3_value(s8);
+    sword |= s8 << (8 * b);
+    uint32_t c0 = 0, c1 = 0;
+    if (sd > 0.f) {
+      const float enc = __fdiv_rn(gs, sd);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) c0 |= e2m1_code(__fmul_rn(xv[i], enc)) << (4 * i);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) c1 |= e2m1_code(__fmul_rn(xv[8 + i], enc)) << (4 * i);
+    }
+    codes[2 * b] = c0;
+    codes[2 * b + 1] = c1;
+  }
+}
+
+__device__ __forceinline__ void store_slice(const QuantArgs& a, int64_t out_row, int slice,
+                                            const uint32_t (&c)[8], uint32_t sword) {
+  uint4* dst = reinterpret_cast<uint4*>(a.codes + out_row * (a.K / 2) + 32 * slice);
+  dst[0] = make_uint4(c[0], c[1], c[2], c[3]);
+  dst[1] = make_uint4(c[4], c[5], c[6], c[7]);
+  const int slices = a.K / 64;
+  const int64_t so = a.scale_layout == MEGAMOE_SCALES_MMA
+                         ? sf_atom_offset(out_row, slice, slices)
+                         : out_row * (a.K / 16) + 4 * slice;
+  *reinterpret_cast<uint32_t*>(a.scales + so) = sword;
+}
+
+// Tasks: with slot_dst, [0, rows_in*S) are token rows (scattered to their
+// routed rows) and [rows_in*S, (rows_in+out_rows)*S) zero the padding rows;
+// without slot_dst, [0, out_rows*S) map out row r <- x row r (padding rows
+// zeroed).  S = K/64 slices per row.
+__global__ void __launch_bounds__(256) k_quant(const QuantArgs a) {
+  const int S = a.K / 64;
+  const float amax = *a.amax;
+  const float gs = amax == 0.f ? 1.f : __fdiv_rn(2688.0f, amax);
+  if (blockIdx.x == 0 && threadIdx.x == 0 && a.gs_out) *a.gs_out = gs;
+  const int64_t live = a.live_rows ? static_cast<int64_t>(*a.live_rows) : a.out_rows;
+  const int64_t token_tasks = a.slot_dst ? a.rows_in * S : 0;
+  const int64_t total = token_tasks + a.out_rows * S;
+  for (int64_t t = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; t < total;
+       t += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const bool token_task = t < token_tasks;
+    const int64_t u = token_task ? t : t - token_tasks;
+    const int64_t row = u / S;
+    const int slice = static_cast<int>(u - row * S);
+    if (!token_task) {
+      if (row >= live) continue;
+      const bool pad_row = a.row_src && a.row_src[row] < 0;
+      if (a.slot_dst && !pad_row) continue;  // written by its token task
+      if (pad_row) {
+        const uint32_t z[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+        store_slice(a, row, slice, z, 0u);
+        continue;
+      }
+    }
+    const uint4* src = reinterpret_cast<const uint4*>(a.x + row * a.ld) + 8 * slice;
+    uint4 v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = __ldg(src + i);
+    uint32_t c[8], sword;
+    encode_slice(v, gs, c, sword);
+    if (token_task) {
+      for (int j = 0; j < a.k; ++j) {
+        const int dst = a.slot_dst[row * a.k + j];
+        if (dst >= 0 && dst < live) store_slice(a, dst, slice, c, sword);
+      }
+    } else {
+      store_slice(a, row, slice, c, sword);
+    }
+  }
+}
+
+__global__ void __launch_bounds__(256) k_swizzle(const uint8_t* __restrict__ src, int64_t rows,
+                                                 int K, uint8_t* __restrict__ dst) {
+  const int S = K / 64;
+  const int64_t rows_pad = (rows + 127) / 128 * 128;
+  const int64_t total = rows_pad * S;
+  for (int64_t t = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; t < total;
+       t += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t r = t / S;
+    const int c = static_cast<int>(t - r * S);
+    const uint32_t w =
+        r < rows ? *reinterpret_cast<const uint32_t*>(src + r * (K / 16) + 4 * c) : 0u;
+    *reinterpret_cast<uint32_t*>(dst + sf_atom_offset(r, c, S)) = w;
+  }
+}
+
+static int grid_for(int64_t tasks, int threads) {
+  int64_t b = (tasks + threads - 1) / threads;
+  const int64_t cap = 152 * 32;
+  if (b > cap) b = cap;
+  if (b < 1) b = 1;
+  return static_cast<int>(b);
+}
+
+cudaError_t launch_amax(const uint16_t* x, int64_t rows, int K, int64_t ld, float* amax,
+                        uint32_t* status, cudaStream_t stream) {
+  cudaError_t err = cudaMemsetAsync(amax, 0, sizeof(float), stream);
+  if (err != cudaSuccess || rows == 0) return err;
+  k_amax<<<grid_for(rows * (K / 8), 256), 256, 0, stream>>>(x, rows, K, ld, amax, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quant(const uint16_t* x, int64_t rows_in, int K, int64_t ld,
+                         const int32_t* slot_dst, int k, const int32_t* row_src,
+                         const int32_t* live_rows, int64_t out_rows, const float* amax,
+                         float* gs_out, uint8_t* codes, uint8_t* scales, int scale_layout,
+                         cudaStream_t stream) {
+  QuantArgs a{x, rows_in, K, ld, slot_dst, k, row_src, live_rows, out_rows, amax,
+              gs_out, codes, scales, scale_layout};
+  const int64_t tasks = ((slot_dst ? rows_in : 0) + out_rows) * (K / 64);
+  k_quant<<<grid_for(tasks, 256), 256, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_swizzle(const uint8_t* src, int64_t rows, int K, uint8_t* dst,
+                           cudaStream_t stream) {
+  const int64_t tasks = (rows + 127) / 128 * 128 * (K / 64);
+  if (tasks == 0) return cudaSuccess;
+  k_swizzle<<<grid_for(tasks, 256), 256, 0, stream>>>(src, rows, K, dst);
+  return cudaGetLastError();
+}
+
+}  // namespace megamoe

@@ -1,0 +1,158 @@
+// Token bucketing: per-expert counts, expert_offsets, padded_expert_offsets
+// and the stable permutation ("CURRENT_BUG.md -- DeepSeek-V4 Blackwell NVFP4",
+// "Test Plan -- Finding the NaN", Phase 1: variable token counts per expert
+// padded to 128; Phase 2: zero-token experts, expert_offsets and
+// padded_expert_offsets).
+//
+// One thread block of 32 warps.  Warp w owns a contiguous chunk of the flat
+// slots, so the order "chunk, then position inside the chunk" is the flat slot
+// order and the sort is stable without atomics deciding anything:
+//   1. per-warp histograms hist[w][e] (shared-memory atomics; counts only);
+//   2. per expert: the total, then hist[w][e] becomes the exclusive prefix over
+//      warps; a block scan over experts gives offsets and padded offsets;
+//   3. each warp walks its chunk 32 slots at a time; lanes with the same expert
+//      find each other with __match_any_sync, rank = earlier peers + the running
+//      count of that expert in this warp.
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace megamoe {
+
+constexpr int kRouteWarps = 32;
+constexpr int kRouteThreads = kRouteWarps * 32;
+
+// Exclusive scan of one value per thread over a 1024-thread block.
+__device__ __forceinline__ int block_exclusive_scan_1024(int v, int* warp_sums, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) warp_sums[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int s = warp_sums[lane];
+    int t = s;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int y = __shfl_up_sync(0xffffffffu, t, o);
+      if (lane >= o) t += y;
+    }
+    warp_sums[lane] = t - s;  // exclusive warp base
+    if (lane == 31) *total = t;
+  }
+  __syncthreads();
+  const int r = warp_sums[warp] + x - v;
+  __syncthreads();
+  return r;
+}
+
+__global__ void __launch_bounds__(kRouteThreads, 1)
+    k_route(const int32_t* __restrict__ ids, int n_slots, int E, int pad, int32_t* counts,
+            int32_t* offsets, int32_t* padded_offsets, int32_t* row_src, int64_t row_capacity,
+            int32_t* slot_dst, uint32_t* status) {
+  extern __shared__ int smem_route[];
+  int* hist = smem_route;                       // [32][E]
+  int* s_poff = hist + kRouteWarps * E;         // [E+1]
+  int* s_cnt = s_poff + (E + 1);                // [E]
+  __shared__ int warp_sums[32];
+  __shared__ int totals[2];
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  for (int i = tid; i < kRouteWarps * E; i += kRouteThreads) hist[i] = 0;
+  __syncthreads();
+
+  const int chunk = (n_slots + kRouteWarps - 1) / kRouteWarps;
+  const int s_begin = warp * chunk;
+  const int s_end = min(n_slots, s_begin + chunk);
+
+  // 1. per-warp histograms
+  bool bad = false;
+  for (int s = s_begin + lane; s < s_end; s += 32) {
+    const int e = ids[s];
+    if (e >= E) bad = true;
+    else if (e >= 0) atomicAdd(&hist[warp * E + e], 1);
+  }
+  if (__any_sync(0xffffffffu, bad) && lane == 0) set_status(status, MEGAMOE_DEV_BAD_EXPERT_ID);
+  __syncthreads();
+
+  // 2. totals, per-warp exclusive bases, offsets (E <= 1024: one expert per thread)
+  int cnt = 0, padded = 0;
+  if (tid < E) {
+    for (int w = 0; w < kRouteWarps; ++w) {
+      const int h = hist[w * E + tid];
+      hist[w * E + tid] = cnt;
+      cnt += h;
+    }
+    padded = (cnt + pad - 1) / pad * pad;
+  }
+  const int off = block_exclusive_scan_1024(cnt, warp_sums, &totals[0]);
+  const int poff = block_exclusive_scan_1024(padded, warp_sums, &totals[1]);
+  if (tid < E) {
+    counts[tid] = cnt;
+    offsets[tid] = off;
+    padded_offsets[tid] = poff;
+    s_poff[tid] = poff;
+    s_cnt[tid] = cnt;
+  }
+  if (tid == 0) {
+    offsets[E] = totals[0];
+    padded_offsets[E] = totals[1];
+    s_poff[E] = totals[1];
+  }
+  __syncthreads();
+
+  // 3. stable scatter, warp by warp over its own chunk
+  for (int base = s_begin; base < s_end; base += 32) {
+    const int s = base + lane;
+    const bool in = s < s_end;
+    int e = in ? ids[s] : -1;
+    if (e >= E) e = -1;
+    const unsigned active = __ballot_sync(0xffffffffu, in);
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    if (in) {
+      if (e >= 0) {
+        const unsigned lower = peers & ((1u << lane) - 1u);
+        const int rank = hist[warp * E + e] + __popc(lower);
+        const int row = s_poff[e] + rank;
+        row_src[row] = s;
+        slot_dst[s] = row;
+      } else {
+        slot_dst[s] = -1;
+      }
+    }
+    __syncwarp();
+    // the highest lane of each peer group advances that expert's running count
+    if (in && e >= 0 && (31 - __clz(peers & active)) == lane)
+      hist[warp * E + e] += __popc(peers & active);
+    __syncwarp();
+  }
+
+  // padding rows of every expert, then everything past the last expert
+  for (int e = tid; e < E; e += kRouteThreads) {
+    for (int r = s_poff[e] + s_cnt[e]; r < s_poff[e + 1]; ++r) row_src[r] = -1;
+  }
+  for (int64_t r = s_poff[E] + tid; r < row_capacity; r += kRouteThreads) row_src[r] = -1;
+}
+
+size_t route_smem_bytes(int E) { return sizeof(int) * (static_cast<size_t>(kRouteWarps) * E + 2 * E + 1); }
+
+cudaError_t launch_route(const int32_t* ids, int n_slots, int E, int pad, int32_t* counts,
+                         int32_t* offsets, int32_t* padded_offsets, int32_t* row_src,
+                         int64_t row_capacity, int32_t* slot_dst, uint32_t* status,
+                         cudaStream_t stream) {
+  const size_t smem = route_smem_bytes(E);
+  cudaError_t err = cudaFuncSetAttribute(k_route, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+  if (err != cudaSuccess) return err;
+  k_route<<<1, kRouteThreads, smem, stream>>>(ids, n_slots, E, pad, counts, offsets,
+                                              padded_offsets, row_src, row_capacity, slot_dst,
+                                              status);
+  return cudaGetLastError();
+}
+
+}  // namespace megamoe

@@ -1,0 +1,324 @@
+"""Thin ctypes binding over the C ABI in ``include/megamoe.h``.
+
+Argument marshalling only: torch tensors supply device pointers, torch's
+current CUDA stream is passed as the stream, and every step of the forward
+runs in the library's CUDA kernels.  There is no CPU or PyTorch fallback: if
+the library is missing, ``load()`` raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+import torch
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libmegamoe.so")
+
+OK = 0
+STATUS_NAMES = {0: "ok", 1: "invalid argument", 2: "unsupported shape",
+                3: "workspace too small", 4: "CUDA error", 5: "device reported an error"}
+DEV_BAD_EXPERT_ID = 0x1
+DEV_NONFINITE = 0x2
+DEV_TIMEOUT = 0x4
+SCALES_ROWMAJOR = 0
+SCALES_MMA = 1
+EPI_F32 = 0
+EPI_SILU_MUL = 1
+
+#: every function the header declares, with (restype, argtypes)
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_I64 = ctypes.c_int64
+_SZ = ctypes.c_size_t
+SIGNATURES = {
+    "megamoe_status_string": (ctypes.c_char_p, [_I]),
+    "megamoe_max_padded_rows": (_I64, [_I, _I, _I, _I]),
+    "megamoe_route_permute": (_I, [_P, _I, _I, _I, _I, _P, _P, _P, _P, _I64, _P, _P, _P]),
+    "megamoe_quantize_nvfp4": (_I, [_P, _I64, _I, _I64, _P, _I, _P, _P, _I64, _P, _P, _P, _P, _P,
+                                    _I, _P, _P]),
+    "megamoe_swizzle_scales": (_I, [_P, _I64, _I, _P, _P]),
+    "megamoe_grouped_gemm": (_I, [_P, _P, _P, _I64, _P, _P, _P, _I, _I, _I, _P, _P, _I, _P, _I64,
+                                  _P, _I, ctypes.c_double, _P, _P]),
+    "megamoe_combine": (_I, [_P, _I64, _P, _P, _I, _I, _I, _P, _P]),
+    "megamoe_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I]),
+    "megamoe_forward": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P, _SZ, _P]),
+    "megamoe_read_status": (_I, [_P, _P, _P]),
+}
+
+
+class MegaMoEError(RuntimeError):
+    def __init__(self, fn, code):
+        super().__init__(f"{fn}: {STATUS_NAMES.get(code, code)} ({code})")
+        self.code = code
+
+
+class CWeights(ctypes.Structure):
+    _fields_ = [("num_experts", ctypes.c_int32), ("hidden", ctypes.c_int32),
+                ("intermediate", ctypes.c_int32), ("w13_codes", _P), ("w13_scales", _P),
+                ("w13_gs", _P), ("w2_codes", _P), ("w2_scales", _P), ("w2_gs", _P)]
+
+
+_LIB = None
+
+
+def load(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load the C-ABI library (raises if it has not been built)."""
+    global _LIB
+    if _LIB is None:
+        if not os.path.exists(path):
+            raise RuntimeError(f"{path} is missing: build it with __graft_entry__.build()")
+        lib = ctypes.CDLL(path)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _LIB = lib
+    return _LIB
+
+
+def _check(fn, code):
+    if code != OK:
+        raise MegaMoEError(fn, code)
+
+
+def _p(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream():
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def _dev(t, dtype, name):
+    if not (t.is_cuda and t.dtype == dtype and t.is_contiguous()):
+        raise TypeError(f"{name} must be a contiguous CUDA {dtype} tensor")
+
+
+def max_padded_rows(T, k, E, pad):
+    return int(load().megamoe_max_padded_rows(T, k, E, pad))
+
+
+def workspace_size(T, k, E, d, I, pad):
+    return int(load().megamoe_workspace_size(T, k, E, d, I, pad))
+
+
+def status_string(code):
+    return load().megamoe_status_string(code).decode()
+
+
+# --------------------------------------------------------------------------
+# the four steps and the forward
+# --------------------------------------------------------------------------
+def route_permute(topk_ids: torch.Tensor, E: int, pad: int = 1, status=None):
+    """Bucket slots by expert; returns a dict of device int32 tensors."""
+    _dev(topk_ids, torch.int32, "topk_ids")
+    T, k = topk_ids.shape
+    dev = topk_ids.device
+    cap = max_padded_rows(T, k, E, pad)
+    r = dict(counts=torch.empty(E, dtype=torch.int32, device=dev),
+             offsets=torch.empty(E + 1, dtype=torch.int32, device=dev),
+             padded_offsets=torch.empty(E + 1, dtype=torch.int32, device=dev),
+             row_src=torch.empty(max(cap, 1), dtype=torch.int32, device=dev),
+             slot_dst=torch.empty(max(T * k, 1), dtype=torch.int32, device=dev))
+    _check("megamoe_route_permute", load().megamoe_route_permute(
+        _p(topk_ids), T, k, E, pad, _p(r["counts"]), _p(r["offsets"]), _p(r["padded_offsets"]),
+        _p(r["row_src"]), cap, _p(r["slot_dst"]), _p(status), _stream()))
+    r["row_src"] = r["row_src"][:cap]
+    r["slot_dst"] = r["slot_dst"][:T * k]
+    return r
+
+
+def sf_atom_bytes(rows, K):
+    return ((rows + 127) // 128 + 1) * 128 * (K // 16)
+
+
+def quantize_nvfp4(x: torch.Tensor, amax_in=None, slot_dst=None, k=1, row_src=None,
+                   live_rows=None, out_rows=None, scale_layout=SCALES_ROWMAJOR, status=None):
+    """bf16 [rows, K] -> (codes [out_rows, K/2] u8, scales u8, amax f32[1], gs f32[1])."""
+    _dev(x, torch.bfloat16, "x")
+    rows, K = x.shape
+    dev = x.device
+    if out_rows is None:
+        out_rows = rows
+    codes = torch.empty(max(out_rows, 1), K // 2, dtype=torch.uint8, device=dev)
+    if scale_layout == SCALES_MMA:
+        scales = torch.empty(max(sf_atom_bytes(out_rows, K), 1), dtype=torch.uint8, device=dev)
+    else:
+        scales = torch.empty(max(out_rows, 1), K // 16, dtype=torch.uint8, device=dev)
+    amax = torch.empty(1, dtype=torch.float32, device=dev)
+    gs = torch.empty(1, dtype=torch.float32, device=dev)
+    _check("megamoe_quantize_nvfp4", load().megamoe_quantize_nvfp4(
+        _p(x), rows, K, K, _p(slot_dst), k, _p(row_src), _p(live_rows), out_rows, _p(amax_in),
+        _p(amax), _p(gs), _p(codes), _p(scales), scale_layout, _p(status), _stream()))
+    if scale_layout != SCALES_MMA:
+        scales = scales[:out_rows]
+    return codes[:out_rows], scales, amax, gs
+
+
+def swizzle_scales(scales: torch.Tensor) -> torch.Tensor:
+    """Row-major [rows, K/16] E4M3 bytes -> atom layout (weight preparation)."""
+    _dev(scales, torch.uint8, "scales")
+    rows, nb = scales.shape
+    K = nb * 16
+    dst = torch.empty((rows + 127) // 128 * 128 * nb, dtype=torch.uint8, device=scales.device)
+    _check("megamoe_swizzle_scales",
+           load().megamoe_swizzle_scales(_p(scales), rows, K, _p(dst), _stream()))
+    return dst
+
+
+def grouped_gemm(act_codes, act_scales_mma, act_gs, w_codes, w_scales_mma, w_gs, offsets,
+                 padded_offsets, epilogue=EPI_F32, tile_n=0, expected_tokens=0.0, out=None,
+                 out_amax=None, status=None):
+    """Grouped block-scaled GEMM; returns (out, out_amax)."""
+    act_rows, half_k = act_codes.shape
+    E, N, _ = w_codes.shape
+    K = half_k * 2
+    dev = act_codes.device
+    width = N if epilogue == EPI_F32 else N // 2
+    if out is None:
+        dt = torch.float32 if epilogue == EPI_F32 else torch.bfloat16
+        out = torch.full((max(act_rows, 1), width), float("nan"), dtype=dt, device=dev)
+    if out_amax is None and epilogue == EPI_SILU_MUL:
+        out_amax = torch.empty(1, dtype=torch.float32, device=dev)
+    _check("megamoe_grouped_gemm", load().megamoe_grouped_gemm(
+        _p(act_codes), _p(act_scales_mma), _p(act_gs), act_rows, _p(w_codes), _p(w_scales_mma),
+        _p(w_gs), E, N, K, _p(offsets), _p(padded_offsets), epilogue, _p(out), out.shape[1],
+        _p(out_amax), tile_n, float(expected_tokens), _p(status), _stream()))
+    return out[:act_rows], out_amax
+
+
+def combine(y, slot_dst, topk_weights, out=None):
+    """bf16 [T, d] = sum_j w[t, j] * y[slot_dst[t*k+j]]."""
+    T, k = topk_weights.shape
+    d = y.shape[1]
+    if out is None:
+        out = torch.empty(T, d, dtype=torch.bfloat16, device=y.device)
+    _check("megamoe_combine", load().megamoe_combine(
+        _p(y), y.stride(0), _p(slot_dst), _p(topk_weights), T, k, d, _p(out), _stream()))
+    return out
+
+
+@dataclass
+class Weights:
+    """Device NVFP4 expert weights, prepared for the library (scales swizzled)."""
+
+    E: int
+    d: int
+    I: int
+    w13_codes: torch.Tensor
+    w13_scales: torch.Tensor  # atom layout
+    w13_gs: torch.Tensor
+    w2_codes: torch.Tensor
+    w2_scales: torch.Tensor  # atom layout
+    w2_gs: torch.Tensor
+
+    @classmethod
+    def prepare(cls, w: dict) -> "Weights":
+        """From row-major stacked weights (w13_codes [E, 2I, d/2], w13_scales
+        [E, 2I, d/16], w13_gs [E, 2], w2_codes [E, d, I/2], w2_scales
+        [E, d, I/16], w2_gs [E]) on the GPU: swizzle the block scales once."""
+        E, I2, half_d = w["w13_codes"].shape
+        d, I = half_d * 2, I2 // 2
+        s13 = swizzle_scales(w["w13_scales"].reshape(E * I2, d // 16))
+        s2 = swizzle_scales(w["w2_scales"].reshape(E * d, I // 16))
+        return cls(E, d, I, w["w13_codes"].contiguous(), s13, w["w13_gs"].contiguous(),
+                   w["w2_codes"].contiguous(), s2, w["w2_gs"].reshape(E).contiguous())
+
+    def cstruct(self) -> CWeights:
+        return CWeights(self.E, self.d, self.I, self.w13_codes.data_ptr(),
+                        self.w13_scales.data_ptr(), self.w13_gs.data_ptr(),
+                        self.w2_codes.data_ptr(), self.w2_scales.data_ptr(),
+                        self.w2_gs.data_ptr())
+
+
+class Forward:
+    """megamoe_forward with a reusable workspace for one (T, k, pad) shape."""
+
+    def __init__(self, weights: Weights, T: int, k: int, pad: int = 32, device=None):
+        self.w = weights
+        self.cw = weights.cstruct()
+        self.T, self.k, self.pad = T, k, pad
+        dev = device or weights.w13_codes.device
+        self.ws_bytes = workspace_size(T, k, weights.E, weights.d, weights.I, pad)
+        self.ws = torch.empty(self.ws_bytes + 256, dtype=torch.uint8, device=dev)
+        base = self.ws.data_ptr()
+        self.ws_off = (-base) % 256
+        self.out = torch.empty(max(T, 1), weights.d, dtype=torch.bfloat16, device=dev)
+
+    @property
+    def ws_ptr(self):
+        return ctypes.c_void_p(self.ws.data_ptr() + self.ws_off)
+
+    def status_tensor(self):
+        return self.ws[self.ws_off:self.ws_off + 4].view(torch.int32)
+
+    def __call__(self, x, topk_ids, topk_weights, out=None):
+        _dev(x, torch.bfloat16, "x")
+        _dev(topk_ids, torch.int32, "topk_ids")
+        _dev(topk_weights, torch.float32, "topk_weights")
+        out = self.out if out is None else out
+        _check("megamoe_forward", load().megamoe_forward(
+            ctypes.byref(self.cw), _p(x), _p(topk_ids), _p(topk_weights), self.T, self.k,
+            self.pad, _p(out), self.ws_ptr, self.ws_bytes, _stream()))
+        return out[:self.T]
+
+    def read_status(self) -> int:
+        bits = ctypes.c_uint32(0)
+        code = load().megamoe_read_status(self.ws_ptr, ctypes.byref(bits), _stream())
+        if code not in (OK, 5):
+            raise MegaMoEError("megamoe_read_status", code)
+        return int(bits.value)
+
+    def intermediates(self):
+        """Views into the workspace (for debugging and stage-level tests)."""
+        return _carve_views(self.ws, self.ws_off, self.T, self.k, self.w.E, self.w.d, self.w.I,
+                            self.pad)
+
+
+def _carve_views(ws, off, T, k, E, d, I, pad):
+    """Mirror of the workspace layout (every region 256-byte aligned)."""
+    rows = max_padded_rows(T, k, E, pad)
+    views = {}
+    cur = off
+
+    def take(name, nbytes):
+        nonlocal cur
+        views[name] = ws[cur:cur + nbytes]
+        cur += -(-nbytes // 256) * 256
+
+    take("hdr", 256)
+    take("counts", 4 * E)
+    take("offsets", 4 * (E + 1))
+    take("padded_offsets", 4 * (E + 1))
+    take("slot_dst", 4 * T * k)
+    take("row_src", 4 * rows)
+    take("xq_codes", rows * (d // 2))
+    take("xq_sf", sf_atom_bytes(rows, d))
+    take("h", rows * I * 2)
+    take("hq_codes", rows * (I // 2))
+    take("hq_sf", sf_atom_bytes(rows, I))
+    take("y", rows * d * 4)
+    hdr = views.pop("hdr")
+    v = {
+        "status": hdr[0:4].view(torch.int32),
+        "amax_x": hdr[4:8].view(torch.float32),
+        "gs_x": hdr[8:12].view(torch.float32),
+        "amax_h": hdr[12:16].view(torch.float32),
+        "gs_h": hdr[16:20].view(torch.float32),
+        "counts": views["counts"].view(torch.int32),
+        "offsets": views["offsets"].view(torch.int32),
+        "padded_offsets": views["padded_offsets"].view(torch.int32),
+        "slot_dst": views["slot_dst"].view(torch.int32),
+        "row_src": views["row_src"].view(torch.int32),
+        "xq_codes": views["xq_codes"].view(rows, d // 2),
+        "xq_sf": views["xq_sf"],
+        "h": views["h"].view(torch.bfloat16).view(rows, I),
+        "hq_codes": views["hq_codes"].view(rows, I // 2),
+        "hq_sf": views["hq_sf"],
+        "y": views["y"].view(torch.float32).view(rows, d),
+        "rows": rows,
+    }
+    return v

@@ -206,13 +206,31 @@ def quantize(x, amax=None):
     return pack_nibbles(codes.reshape(rows, K)), s8, gs, amax
 
 
+def _byte_tables():
+    """Value tables built from the scalar decoders: code byte -> E2M1 value of
+    its low nibble (even element) and of its high nibble (odd element); scale
+    byte -> E4M3 value."""
+    b = np.arange(256)
+    return e2m1_decode(b & 0xF), e2m1_decode(b >> 4), e4m3_decode(b)
+
+
+_LO_TABLE, _HI_TABLE, _SCALE_TABLE = _byte_tables()
+
+
 def dequantize(codes, scales, gs) -> np.ndarray:
-    """NVFP4 -> float64: e2m1(code) * e4m3(scale) / gs, element by element."""
-    c = unpack_nibbles(codes)
-    rows, K = c.shape
-    v = e2m1_decode(c).reshape(rows, K // BLOCK, BLOCK)
-    sd = e4m3_decode(scales)[..., None]
-    return (v * sd / np.float64(gs)).reshape(rows, K)
+    """NVFP4 -> float64: e2m1(code) * e4m3(scale) / gs, element by element.
+
+    Each code byte holds elements 2i (low nibble) and 2i+1 (high nibble); each
+    nibble is decoded by table lookup.
+    """
+    c = np.asarray(codes, dtype=np.uint8)
+    rows, half = c.shape
+    K = half * 2
+    v = np.empty((rows, K))
+    v[:, 0::2] = _LO_TABLE[c]
+    v[:, 1::2] = _HI_TABLE[c]
+    sd = _SCALE_TABLE[np.asarray(scales, dtype=np.uint8)][..., None]
+    return (v.reshape(rows, K // BLOCK, BLOCK) * sd / np.float64(gs)).reshape(rows, K)
 
 
 # --------------------------------------------------------------------------

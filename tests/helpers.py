@@ -1,0 +1,74 @@
+"""Shared helpers of the GPU parity tests."""
+
+import numpy as np
+import torch
+
+# Tolerance for floating-point GEMM / combine outputs against the float64 oracle:
+# relative L2 error and max |error| relative to the rms of the expected output.
+REL_L2 = 2e-3
+MAX_ABS_OF_RMS = 1e-2
+
+
+def assert_close(got, want, rel_l2=REL_L2, max_abs_of_rms=MAX_ABS_OF_RMS, what=""):
+    got = np.asarray(got, dtype=np.float64)
+    want = np.asarray(want, dtype=np.float64)
+    assert got.shape == want.shape, (what, got.shape, want.shape)
+    assert np.all(np.isfinite(got)), f"{what}: non-finite output"
+    if want.size == 0:
+        return 0.0, 0.0
+    nrm = np.linalg.norm(want)
+    err = np.linalg.norm(got - want) / nrm if nrm > 0 else np.linalg.norm(got)
+    rms = np.sqrt(np.mean(want ** 2))
+    mae = np.max(np.abs(got - want))
+    assert err <= rel_l2, f"{what}: rel-L2 {err:.3e} > {rel_l2}"
+    assert mae <= max_abs_of_rms * rms, f"{what}: max-abs {mae:.3e} > {max_abs_of_rms}*rms ({rms:.3e})"
+    return err, mae / rms if rms > 0 else 0.0
+
+
+def to_np(t):
+    return t.detach().cpu().numpy()
+
+
+def bf16_to_np(t):
+    return t.detach().float().cpu().numpy().astype(np.float64)
+
+
+class NumpyExperts:
+    """Expert set over in-memory NumPy weights (the oracle's protocol)."""
+
+    def __init__(self, ws, d, I):
+        self.ws, self.d, self.I = ws, d, I
+        self.num_experts = len(ws)
+
+    def __getitem__(self, e):
+        return self.ws[e]
+
+
+def random_experts(rng, E, d, I, oracle_q):
+    """Quantise random float weights with the oracle; returns (NumpyExperts,
+    stacked dict of torch CPU tensors in the library's row-major layout)."""
+    ws = []
+    for _ in range(E):
+        g = (rng.standard_normal((I, d)) * 0.05).astype(np.float32)
+        u = (rng.standard_normal((I, d)) * 0.05).astype(np.float32)
+        dn = (rng.standard_normal((d, I)) * 0.05).astype(np.float32)
+        gc, gsc, ggs, _ = oracle_q.quantize(g)
+        uc, usc, ugs, _ = oracle_q.quantize(u)
+        dc, dsc, dgs, _ = oracle_q.quantize(dn)
+        ws.append(dict(w13_codes=np.concatenate([gc, uc]), w13_scales=np.concatenate([gsc, usc]),
+                       w13_gs=np.array([ggs, ugs], np.float32), w2_codes=dc, w2_scales=dsc,
+                       w2_gs=np.float32(dgs)))
+    stacked = dict(
+        w13_codes=torch.from_numpy(np.stack([w["w13_codes"] for w in ws])),
+        w13_scales=torch.from_numpy(np.stack([w["w13_scales"] for w in ws])),
+        w13_gs=torch.from_numpy(np.stack([w["w13_gs"] for w in ws])),
+        w2_codes=torch.from_numpy(np.stack([w["w2_codes"] for w in ws])),
+        w2_scales=torch.from_numpy(np.stack([w["w2_scales"] for w in ws])),
+        w2_gs=torch.from_numpy(np.array([w["w2_gs"] for w in ws], np.float32)),
+    )
+    return NumpyExperts(ws, d, I), stacked
+
+
+def bf16_tensor(rng, shape, scale=1.0):
+    x = torch.from_numpy((rng.standard_normal(shape) * scale).astype(np.float32))
+    return x.to(torch.bfloat16)

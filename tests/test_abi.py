@@ -1,0 +1,97 @@
+"""The C-ABI library loads, exports what include/megamoe.h declares, and its
+host-side logic (size helpers, argument checks) behaves, all without a GPU."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import __graft_entry__
+from nvfp4_block_scaled_topk_gb300 import megamoe
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    __graft_entry__.build()
+    return megamoe.load()
+
+
+def _declared_functions():
+    src = open(os.path.join(ROOT, "include", "megamoe.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(megamoe_[a-z_0-9]+)\s*\(", src)))
+
+
+def test_header_declares_the_boundary_calls():
+    names = _declared_functions()
+    for n in ("megamoe_route_permute", "megamoe_quantize_nvfp4", "megamoe_grouped_gemm",
+              "megamoe_forward", "megamoe_workspace_size", "megamoe_read_status"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    names = _declared_functions()
+    assert names == sorted(megamoe.SIGNATURES)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(lib):
+    assert megamoe.status_string(0) == "ok"
+    assert megamoe.status_string(3) == "workspace too small"
+    assert megamoe.status_string(99) == "unknown status"
+
+
+def test_max_padded_rows(lib):
+    assert megamoe.max_padded_rows(8, 6, 384, 32) == 48 + 48 * 31
+    assert megamoe.max_padded_rows(4096, 6, 384, 32) == 24576 + 384 * 31
+    assert megamoe.max_padded_rows(0, 6, 384, 128) == 0
+    assert megamoe.max_padded_rows(1, 6, 48, 1) == 6
+    assert megamoe.max_padded_rows(-1, 6, 48, 1) == 0
+
+
+def test_workspace_size_is_aligned_and_monotone(lib):
+    a = megamoe.workspace_size(8, 6, 384, 7168, 2048, 32)
+    b = megamoe.workspace_size(16, 6, 384, 7168, 2048, 32)
+    assert a > 0 and a % 256 == 0 and b > a
+    assert megamoe.workspace_size(8, 0, 384, 7168, 2048, 32) == 0
+
+
+def test_argument_errors_return_before_any_device_work(lib):
+    P = None
+    # route: E = 0, E too large, k too large, capacity too small
+    assert lib.megamoe_route_permute(P, 1, 1, 0, 1, P, P, P, P, 0, P, P, P) == 1
+    assert lib.megamoe_route_permute(P, 1, 1, 2000, 1, P, P, P, P, 0, P, P, P) == 2
+    assert lib.megamoe_route_permute(P, 1, 17, 8, 1, P, P, P, P, 0, P, P, P) == 2
+    fake = ctypes.c_void_p(256)
+    assert lib.megamoe_route_permute(fake, 4, 2, 8, 32, fake, fake, fake, fake, 10, fake, P,
+                                     P) == 1
+    # quantise: K not a multiple of 64, bad layout, missing gs
+    assert lib.megamoe_quantize_nvfp4(fake, 4, 48, 48, P, 1, P, P, 4, P, fake, fake, fake, fake,
+                                      0, P, P) == 2
+    assert lib.megamoe_quantize_nvfp4(fake, 4, 64, 64, P, 1, P, P, 4, P, fake, fake, fake, fake,
+                                      7, P, P) == 1
+    assert lib.megamoe_quantize_nvfp4(fake, 4, 64, 64, P, 1, P, P, 4, P, fake, P, fake, fake,
+                                      0, P, P) == 1
+    # grouped GEMM: bad epilogue, K not a multiple of 256, bad tile
+    assert lib.megamoe_grouped_gemm(fake, fake, fake, 8, fake, fake, fake, 2, 256, 256, fake,
+                                    fake, 9, fake, 256, P, 0, 0.0, P, P) == 1
+    assert lib.megamoe_grouped_gemm(fake, fake, fake, 8, fake, fake, fake, 2, 256, 128, fake,
+                                    fake, 0, fake, 256, P, 0, 0.0, P, P) == 2
+    assert lib.megamoe_grouped_gemm(fake, fake, fake, 8, fake, fake, fake, 2, 256, 256, fake,
+                                    fake, 0, fake, 256, P, 48, 0.0, P, P) == 1
+    # combine: d not a multiple of 4
+    assert lib.megamoe_combine(fake, 6, fake, fake, 2, 2, 6, fake, P) == 2
+    # forward: no weights; pad not a multiple of 32; workspace too small
+    assert lib.megamoe_forward(P, fake, fake, fake, 1, 1, 32, fake, fake, 1 << 30, P) == 1
+    w = megamoe.CWeights(8, 256, 512, 256, 256, 256, 256, 256, 256)
+    assert lib.megamoe_forward(ctypes.byref(w), fake, fake, fake, 4, 2, 16, fake, fake,
+                               1 << 30, P) == 2
+    assert lib.megamoe_forward(ctypes.byref(w), fake, fake, fake, 4, 2, 32, fake, fake, 16,
+                               P) == 3
+    w_bad = megamoe.CWeights(8, 200, 512, 256, 256, 256, 256, 256, 256)
+    assert lib.megamoe_forward(ctypes.byref(w_bad), fake, fake, fake, 4, 2, 32, fake, fake,
+                               1 << 30, P) == 2

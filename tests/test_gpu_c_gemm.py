@@ -1,0 +1,120 @@
+"""megamoe_grouped_gemm (tcgen05 block-scaled NVFP4) against the oracle's
+float64 grouped GEMM on identical NVFP4 operands: the fp32 epilogue and the
+fused SiLU(gate)*up -> bf16 + amax epilogue, over every token tile, with
+ragged per-expert counts, zero-token experts and several tiles per expert."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import nvfp4 as q
+from helpers import assert_close, bf16_tensor, random_experts
+
+pytestmark = pytest.mark.gpu
+
+
+def _setup(seed, E, d, I, counts, pad=32):
+    rng = np.random.default_rng(seed)
+    ex, stacked = random_experts(rng, E, d, I, q)
+    ids = np.concatenate([np.full(c, e) for e, c in enumerate(counts)])
+    rng.shuffle(ids)
+    ids = ids.reshape(-1, 1)
+    rt = oracle.route(ids, E, pad)
+    R = int(rt.padded_offsets[-1])
+    return rng, ex, stacked, rt, R
+
+
+def _quantised_rows(rng, rt, R, K, scale):
+    """Activations already in padded-row order, quantised by the oracle."""
+    x = bf16_tensor(rng, (R, K), scale).float().numpy()
+    valid = rt.row_src >= 0
+    x[~valid] = 0
+    c, s, g, _ = q.quantize(x)
+    return x, c, s, g
+
+
+def _dev_weights(stacked, which, megamoe):
+    if which == "w13":
+        E, N, hk = stacked["w13_codes"].shape
+        codes = stacked["w13_codes"].cuda()
+        sc = megamoe.swizzle_scales(stacked["w13_scales"].reshape(E * N, hk // 8).cuda())
+        gs = stacked["w13_gs"].cuda()
+    else:
+        E, N, hk = stacked["w2_codes"].shape
+        codes = stacked["w2_codes"].cuda()
+        sc = megamoe.swizzle_scales(stacked["w2_scales"].reshape(E * N, hk // 8).cuda())
+        gs = stacked["w2_gs"].cuda()
+    return codes, sc, gs
+
+
+COUNTS = [37, 0, 1, 130, 64, 0, 5, 260]
+
+
+@pytest.mark.parametrize("tile_n", [32, 64, 128])
+def test_grouped_gemm_f32_epilogue(cuda_lib, tile_n):
+    from nvfp4_block_scaled_topk_gb300 import megamoe
+
+    E, d, I = len(COUNTS), 512, 256  # L2 shape: N = d = 512, K = I = 256
+    rng, ex, stacked, rt, R = _setup(30 + tile_n, E, d, I, COUNTS)
+    a, ac, asc, ag = _quantised_rows(rng, rt, R, I, 0.5)
+    wcodes, wsc, wgs = _dev_weights(stacked, "w2", megamoe)
+    act_sf = torch.from_numpy(np.concatenate([q.swizzle_scales(asc), np.zeros(128 * I // 16, np.uint8)]))
+    out, _ = megamoe.grouped_gemm(
+        torch.from_numpy(ac).cuda(), act_sf.cuda(), torch.tensor([ag]).cuda(), wcodes, wsc, wgs,
+        torch.from_numpy(rt.offsets.astype(np.int32)).cuda(),
+        torch.from_numpy(rt.padded_offsets.astype(np.int32)).cuda(), megamoe.EPI_F32,
+        tile_n=tile_n)
+    torch.cuda.synchronize()
+    got = out.cpu().numpy().astype(np.float64)
+    want = oracle.grouped_gemm(ac, asc, ag, ex, "w2", rt, "f32")
+    v = rt.row_src >= 0
+    err, _ = assert_close(got[v], want[v], what=f"f32 tile {tile_n}")
+    assert err < 1e-5  # identical operands: only fp32 accumulation differs
+    assert np.all(np.isnan(got[~v]))  # padding rows untouched
+
+
+@pytest.mark.parametrize("tile_n", [32, 64, 128])
+def test_grouped_gemm_silu_mul_epilogue(cuda_lib, tile_n):
+    from nvfp4_block_scaled_topk_gb300 import megamoe
+
+    E, d, I = len(COUNTS), 512, 256  # L1 shape: N = 2I = 512, K = d = 512
+    rng, ex, stacked, rt, R = _setup(40 + tile_n, E, d, I, COUNTS)
+    a, ac, asc, ag = _quantised_rows(rng, rt, R, d, 0.5)
+    wcodes, wsc, wgs = _dev_weights(stacked, "w13", megamoe)
+    act_sf = torch.from_numpy(np.concatenate([q.swizzle_scales(asc), np.zeros(128 * d // 16, np.uint8)]))
+    out, amax = megamoe.grouped_gemm(
+        torch.from_numpy(ac).cuda(), act_sf.cuda(), torch.tensor([ag]).cuda(), wcodes, wsc, wgs,
+        torch.from_numpy(rt.offsets.astype(np.int32)).cuda(),
+        torch.from_numpy(rt.padded_offsets.astype(np.int32)).cuda(), megamoe.EPI_SILU_MUL,
+        tile_n=tile_n)
+    torch.cuda.synchronize()
+    got = out.float().cpu().numpy().astype(np.float64)
+    want, want_amax = oracle.grouped_gemm(ac, asc, ag, ex, "w13", rt, "silu_mul")
+    v = rt.row_src >= 0
+    assert_close(got[v], want[v], what=f"silu tile {tile_n}")
+    # bf16 outputs: all but a few rounding-boundary cases are identical
+    assert np.mean(got[v] == want[v]) > 0.99
+    assert abs(amax.item() - float(want_amax)) <= 2 ** -7 * float(want_amax)
+
+
+def test_grouped_gemm_real_shape_one_expert_per_token(cuda_lib):
+    """d = 7168, I = 2048 (the MegaMoE expert shape) with decode-like counts."""
+    from nvfp4_block_scaled_topk_gb300 import megamoe
+
+    E, d, I = 3, 7168, 2048
+    counts = [1, 0, 3]
+    rng, ex, stacked, rt, R = _setup(50, E, d, I, counts)
+    a, ac, asc, ag = _quantised_rows(rng, rt, R, d, 0.09)
+    wcodes, wsc, wgs = _dev_weights(stacked, "w13", megamoe)
+    act_sf = torch.from_numpy(np.concatenate([q.swizzle_scales(asc), np.zeros(128 * d // 16, np.uint8)]))
+    out, amax = megamoe.grouped_gemm(
+        torch.from_numpy(ac).cuda(), act_sf.cuda(), torch.tensor([ag]).cuda(), wcodes, wsc, wgs,
+        torch.from_numpy(rt.offsets.astype(np.int32)).cuda(),
+        torch.from_numpy(rt.padded_offsets.astype(np.int32)).cuda(), megamoe.EPI_SILU_MUL,
+        tile_n=32)
+    torch.cuda.synchronize()
+    got = out.float().cpu().numpy().astype(np.float64)
+    want, _ = oracle.grouped_gemm(ac, asc, ag, ex, "w13", rt, "silu_mul")
+    v = rt.row_src >= 0
+    assert_close(got[v], want[v], what="real shape")

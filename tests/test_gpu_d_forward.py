@@ -1,0 +1,147 @@
+"""megamoe_forward end to end against the oracle's forward, on the MegaMoE
+workloads (full size where the oracle finishes in seconds, sampled stages
+and invariants otherwise), plus robustness cases: poisoned workspace,
+stress routings, skipped and out-of-range ids."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import nvfp4 as q
+from nvfp4_block_scaled_topk_gb300 import inputs, megamoe
+from helpers import assert_close, bf16_to_np, random_experts
+
+pytestmark = pytest.mark.gpu
+
+_CACHE = {}
+
+
+def _weights(cfg):
+    """All experts generated on the GPU (torch RNG) and prepared once."""
+    key = (cfg.E, cfg.d, cfg.I, cfg.seed)
+    if key not in _CACHE:
+        _CACHE.clear()
+        torch.cuda.empty_cache()
+        raw = inputs.make_all_experts(cfg, device="cuda")
+        _CACHE[key] = (raw, megamoe.Weights.prepare(raw))
+    return _CACHE[key]
+
+
+def _run(cfg, pad, x=None, ids=None, w=None, poison=False):
+    raw, weights = _weights(cfg)
+    x = inputs.make_activations(cfg) if x is None else x
+    if ids is None:
+        ids, w = inputs.make_routing(cfg)
+    fwd = megamoe.Forward(weights, x.shape[0], ids.shape[1], pad=pad)
+    if poison:
+        fwd.ws.fill_(0xFF)
+    out = fwd(x.cuda(), ids.cuda(), w.cuda())
+    bits = fwd.read_status()
+    return raw, fwd, x, ids, w, out, bits
+
+
+@pytest.mark.parametrize("name,pad", [("tiny", 32), ("tiny", 128), ("decode", 32),
+                                      ("decode1", 32), ("slice", 128), ("slice1", 128)])
+def test_forward_matches_oracle(cuda_lib, name, pad):
+    cfg = inputs.CONFIGS[name]
+    raw, fwd, x, ids, w, out, bits = _run(cfg, pad)
+    assert bits == 0
+    want = oracle.forward(x.float().numpy(), ids.numpy(), w.numpy(),
+                          inputs.ExpertSet(cfg, raw), pad=pad)
+    assert_close(bf16_to_np(out), want, what=name)
+
+
+def test_forward_prefill_shaped_mid_size(cuda_lib):
+    """Zipf-skewed routing with hot and empty experts, outliers, several
+    token tiles per expert; small enough for the full oracle."""
+    cfg = inputs.MoEConfig("prefill_mid", 64, 6, 2048, 1024, 512, "zipf", seed=77,
+                           outlier_frac=1e-3)
+    raw, fwd, x, ids, w, out, bits = _run(cfg, 32)
+    assert bits == 0
+    want = oracle.forward(x.float().numpy(), ids.numpy(), w.numpy(),
+                          inputs.ExpertSet(cfg, raw), pad=32)
+    assert_close(bf16_to_np(out), want, what="prefill_mid")
+
+
+@pytest.mark.parametrize("name", ["prefill", "large"])
+def test_forward_full_size_prefill_stages(cuda_lib, name):
+    """Full-size prefill: routing and activation quantisation bit-exact, the
+    L1 output on sampled rows against the oracle, the L1 amax bounds the
+    sample, and the output is finite."""
+    cfg = inputs.CONFIGS[name]
+    raw, fwd, x, ids, w, out, bits = _run(cfg, 32)
+    assert bits == 0
+    o = bf16_to_np(out)
+    assert np.all(np.isfinite(o)) and np.any(o != 0)
+    v = fwd.intermediates()
+    rt = oracle.route(ids.numpy(), cfg.E, 32)
+    R = int(rt.padded_offsets[-1])
+    assert np.array_equal(v["padded_offsets"].cpu().numpy(), rt.padded_offsets)
+    assert np.array_equal(v["row_src"].cpu().numpy()[:R], rt.row_src)
+    xc, xs, xg, xa = q.quantize(x.float().numpy())
+    assert np.float32(v["gs_x"].item()) == xg
+    assert np.array_equal(v["xq_codes"].cpu().numpy()[:R][rt.row_src >= 0],
+                          xc[rt.row_src[rt.row_src >= 0] // cfg.k])
+    # sampled rows of h, one or two per expert, computed by the oracle alone
+    rng = np.random.default_rng(5)
+    experts = inputs.ExpertSet(cfg, raw)
+    rows = []
+    for e in rng.choice(np.nonzero(rt.counts)[0], size=min(12, int((rt.counts > 0).sum())),
+                        replace=False):
+        r0 = int(rt.padded_offsets[e])
+        rows += [r0, r0 + int(rt.counts[e]) - 1]
+    h_gpu = v["h"].float().cpu().numpy()
+    amax_h = v["amax_h"].item()
+    for r in rows:
+        t = int(rt.row_src[r]) // cfg.k
+        e = int(np.searchsorted(rt.padded_offsets, r, side="right") - 1)
+        ew = experts[e]
+        xh = q.dequantize(xc[t:t + 1], xs[t:t + 1], xg)
+        gate = q.dequantize(ew["w13_codes"][:cfg.I], ew["w13_scales"][:cfg.I], ew["w13_gs"][0])
+        up = q.dequantize(ew["w13_codes"][cfg.I:], ew["w13_scales"][cfg.I:], ew["w13_gs"][1])
+        hw = q.bf16_round(oracle.silu(xh @ gate.T) * (xh @ up.T))[0]
+        assert_close(h_gpu[r], hw, what=f"h row {r}")
+        assert amax_h >= np.abs(hw).max()
+
+
+def test_forward_ignores_poisoned_workspace(cuda_lib):
+    cfg = inputs.CONFIGS["tiny"]
+    _, _, _, _, _, clean, b0 = _run(cfg, 32)
+    clean = clean.clone()
+    _, _, _, _, _, dirty, b1 = _run(cfg, 32, poison=True)
+    assert b0 == 0 and b1 == 0
+    assert torch.equal(clean, dirty)
+
+
+@pytest.mark.parametrize("case", ["all_one_expert", "one_nonempty", "skipped_slots",
+                                  "bad_ids", "no_tokens"])
+def test_forward_stress_routings(cuda_lib, case):
+    cfg = inputs.CONFIGS["tiny"]
+    raw, weights = _weights(cfg)
+    x = inputs.make_activations(cfg)
+    ids, w = inputs.make_routing(cfg)
+    ids = ids.clone()
+    if case == "all_one_expert":
+        ids[:] = 3
+        ids[:, 1] = 3
+    elif case == "one_nonempty":
+        ids[:] = 7
+    elif case == "skipped_slots":
+        ids[::3, 1] = -1
+        ids[5] = -1
+    elif case == "bad_ids":
+        ids[2, 0] = 8
+        ids[9, 1] = 100
+    elif case == "no_tokens":
+        x, ids, w = x[:0], ids[:0], w[:0]
+    raw, fwd, x, ids, w, out, bits = _run(cfg, 32, x=x, ids=ids, w=w)
+    if case == "bad_ids":
+        assert bits & megamoe.DEV_BAD_EXPERT_ID
+        ids_ok = torch.where(ids >= cfg.E, torch.full_like(ids, -1), ids)
+    else:
+        assert bits == 0
+        ids_ok = ids
+    want = oracle.forward(x.float().numpy(), ids_ok.numpy(), w.numpy(),
+                          inputs.ExpertSet(cfg, raw), pad=32)
+    assert_close(bf16_to_np(out), want, what=case)
