@@ -71,7 +71,7 @@ typedef enum megamoe_status {
 
 /* Scale layouts. */
 #define MEGAMOE_SCALES_ROWMAJOR 0 /* [rows, K/16] bytes                         */
-#define MEGAMOE_SCALES_MMA 1      /* atom layout, ceil(rows/128)+1 row-groups    */
+#define MEGAMOE_SCALES_MMA 1      /* atom layout, ceil(rows/128)*128 rows          */
 
 /* Grouped-GEMM epilogues. */
 #define MEGAMOE_EPI_F32 0      /* out[r, n] = fp32 accumulator * alpha            */
@@ -189,8 +189,8 @@ megamoe_status megamoe_swizzle_scales(const uint8_t* src, int64_t rows, int K, u
  * For every expert e and every valid row r of e
  * (padded_offsets[e] <= r < padded_offsets[e] + offsets[e+1] - offsets[e]):
  *   acc[r, n] = sum_K dequant(act)[r, :] . dequant(w_e)[n, :]   (fp32 accumulate)
- *   act_codes   [act_rows, K/2]; act_scales atom layout (ceil(act_rows/128)+1
- *               row-groups); act_gs device float (one global scale)
+ *   act_codes   [act_rows, K/2]; act_scales row-major [act_rows, K/16];
+ *               act_gs device float (one global scale)
  *   w_codes     [E, N, K/2]; w_scales atom layout of [E*N, K/16]
  *   w_gs        [E, G] float: G = 1 for MEGAMOE_EPI_F32; G = 2 (gate, up) for
  *               MEGAMOE_EPI_SILU_MUL

@@ -21,12 +21,6 @@ inline megamoe_status cuda_status(cudaError_t e) {
   return e == cudaSuccess ? MEGAMOE_OK : MEGAMOE_ERR_CUDA;
 }
 
-// Byte size of an atom-layout scale buffer for `rows` rows (one spare row-group
-// so a token tile that starts near the end can read a whole second group).
-inline size_t sf_atom_bytes(int64_t rows, int K) {
-  return static_cast<size_t>((rows + 127) / 128 + 1) * 128 * (K / 16);
-}
-
 // Workspace of megamoe_forward, every region 256-byte aligned.
 struct Workspace {
   uint32_t* status;
@@ -73,10 +67,10 @@ Workspace carve(void* base, int T, int k, int E, int d, int I, int pad) {
   w.slot_dst = reinterpret_cast<int32_t*>(take(4 * static_cast<size_t>(T) * k));
   w.row_src = reinterpret_cast<int32_t*>(take(4 * static_cast<size_t>(rows)));
   w.xq_codes = take(static_cast<size_t>(rows) * (d / 2));
-  w.xq_sf = take(sf_atom_bytes(rows, d));
+  w.xq_sf = take(static_cast<size_t>(rows) * (d / 16));
   w.h = reinterpret_cast<uint16_t*>(take(static_cast<size_t>(rows) * I * 2));
   w.hq_codes = take(static_cast<size_t>(rows) * (I / 2));
-  w.hq_sf = take(sf_atom_bytes(rows, I));
+  w.hq_sf = take(static_cast<size_t>(rows) * (I / 16));
   w.y = reinterpret_cast<float*>(take(static_cast<size_t>(rows) * d * 4));
   w.bytes = off;
   return w;
@@ -269,7 +263,7 @@ megamoe_status megamoe_forward(const megamoe_weights* w, const uint16_t* x,
   e = launch_amax(x, T, d, d, wk.amax_x, wk.status, s);
   if (e != cudaSuccess) return MEGAMOE_ERR_CUDA;
   e = launch_quant(x, T, d, d, wk.slot_dst, k, wk.row_src, wk.padded_offsets + E, wk.rows,
-                   wk.amax_x, wk.gs_x, wk.xq_codes, wk.xq_sf, MEGAMOE_SCALES_MMA, s);
+                   wk.amax_x, wk.gs_x, wk.xq_codes, wk.xq_sf, MEGAMOE_SCALES_ROWMAJOR, s);
   if (e != cudaSuccess) return MEGAMOE_ERR_CUDA;
   // 4. L1 gate+up grouped GEMM, SiLU(gate)*up -> bf16 h, amax(h)
   GemmLaunch g{};
@@ -295,7 +289,7 @@ megamoe_status megamoe_forward(const megamoe_weights* w, const uint16_t* x,
   if (e != cudaSuccess) return MEGAMOE_ERR_CUDA;
   // 5. requantise h with gs from amax(h)
   e = launch_quant(wk.h, wk.rows, I, I, nullptr, 1, wk.row_src, wk.padded_offsets + E, wk.rows,
-                   wk.amax_h, wk.gs_h, wk.hq_codes, wk.hq_sf, MEGAMOE_SCALES_MMA, s);
+                   wk.amax_h, wk.gs_h, wk.hq_codes, wk.hq_sf, MEGAMOE_SCALES_ROWMAJOR, s);
   if (e != cudaSuccess) return MEGAMOE_ERR_CUDA;
   // 6. L2 down grouped GEMM -> fp32 y
   g.act_codes = wk.hq_codes;

@@ -13,14 +13,17 @@
 // holds the gate AND the up accumulators of the same 128 features (two MMAs
 // per K step into two TMEM ranges), so SiLU(gate) * up is a per-lane epilogue.
 //
-// Roles (192 threads, one CTA per SM, grid = number of SMs):
-//   warp 0      TMA producer: weight tiles and token tiles (128-byte swizzle)
-//               plus their block-scale atoms (bulk copies) into a STAGES-deep
-//               shared-memory ring;
+// Roles (224 threads, one CTA per SM, grid = number of SMs):
+//   warp 0      TMA producer: weight tiles and token tiles (128-byte swizzle),
+//               the weights' block-scale atoms (bulk copies) and the token
+//               tile's row-major block scales into a STAGES-deep ring;
 //   warp 1      TMEM allocator; one lane issues tcgen05.cp (scales -> TMEM)
 //               and tcgen05.mma, and commits stage-free / accumulator-ready;
 //   warps 2..5  epilogue: tcgen05.ld of their 32-lane quarter, alpha scaling,
-//               SiLU * up -> bf16 + amax (L1) or fp32 (L2), masked stores.
+//               SiLU * up -> bf16 + amax (L1) or fp32 (L2), masked stores;
+//   warp 6      scale transposer: rewrites the token tile's row-major scales
+//               into the 32 x 16-byte atoms tcgen05.cp reads, so the tile's
+//               first row always lands in the first TMEM scale column.
 // Every expert's weights live in one [E*N, K/2] tensor, so one tensor map
 // serves all experts: the expert is a row coordinate, not a new descriptor.
 // Tiles are numbered expert-major, weight-tile-major, token-tile-minor, so CTAs
@@ -37,11 +40,11 @@
 
 namespace megamoe {
 
-constexpr int kGemmThreads = 192;
+constexpr int kGemmThreads = 224;
+constexpr int kSfWarp = 6;
 
 struct GemmArgs {
   const uint8_t* w_sf;  // atom layout [E*N/128][K/64][512]
-  const uint8_t* a_sf;  // atom layout [ceil(rows/128)+1][K/64][512]
   const float* w_gs;    // [E][G]
   const float* a_gs;    // device scalar
   const int32_t* offsets;
@@ -58,16 +61,18 @@ struct GemmCfg {
   static constexpr int G = EPI == MEGAMOE_EPI_SILU_MUL ? 2 : 1;
   static constexpr int A_TILE = 128 * 128;  // one weight matrix, 128 rows x 128 bytes
   static constexpr int B_TILE = BN * 128;
-  static constexpr int SFW = 2048;  // 4 atoms of 512 bytes (one per 64-element slice)
-  static constexpr int SFA = 4096;  // two row-groups of 4 atoms
+  static constexpr int SFW = 2048;     // 4 atoms of 512 bytes (one per 64-element slice)
+  static constexpr int SFA_RAW = BN * 16;  // token scales as loaded: BN rows x 16 bytes
+  static constexpr int SFA = 2048;     // token scales as 4 atoms of 512 bytes
   static constexpr int OFF_A = 0;
   static constexpr int OFF_B = G * A_TILE;
   static constexpr int OFF_SFW = OFF_B + B_TILE;
-  static constexpr int OFF_SFA = OFF_SFW + G * SFW;
+  static constexpr int OFF_SFA_RAW = OFF_SFW + G * SFW;
+  static constexpr int OFF_SFA = OFF_SFA_RAW + SFA_RAW;
   static constexpr int STAGE = (OFF_SFA + SFA + 1023) / 1024 * 1024;
-  static constexpr uint32_t TX = G * A_TILE + B_TILE + G * SFW + SFA;
+  static constexpr uint32_t TX = G * A_TILE + B_TILE + G * SFW + SFA_RAW;
   static constexpr int ACC_COLS = G * BN;
-  static constexpr int SF_COLS = 16 * G + 32;  // per stage: weight scales + token scales
+  static constexpr int SF_COLS = 16 * G + 16;  // per stage: weight scales + token scales
   static constexpr int SF_COL0 = ACC_COLS;
   static constexpr int BAR_OFF = STAGES * STAGE;
   static constexpr int TOFF_OFF = BAR_OFF + 256;
@@ -75,7 +80,7 @@ struct GemmCfg {
   static constexpr uint32_t IDESC = idesc_nvf4(128, BN);
   static_assert(SF_COL0 + STAGES * SF_COLS <= 512, "tensor memory budget");
   static_assert(SMEM <= 232448, "shared memory budget");
-  static_assert((2 * STAGES + 3) * 8 + 8 <= 256, "barrier area");
+  static_assert((3 * STAGES + 3) * 8 + 8 <= 256, "barrier area");
 };
 
 struct TileInfo {
@@ -147,14 +152,15 @@ __device__ __forceinline__ void mbar_drain(uint64_t* bar, uint32_t parity) {
 template <int BN, int EPI, int STAGES>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     k_grouped_gemm(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_a,
-                   const GemmArgs p) {
+                   const __grid_constant__ CUtensorMap tm_asf, const GemmArgs p) {
   using C = GemmCfg<BN, EPI, STAGES>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
   uint64_t* empty = full + STAGES;
-  uint64_t* acc_full = empty + STAGES;
+  uint64_t* sf_ready = empty + STAGES;
+  uint64_t* acc_full = sf_ready + STAGES;
   uint64_t* acc_empty = acc_full + 1;
   uint64_t* drain = acc_empty + 1;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
@@ -176,6 +182,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
+      mbar_init(&sf_ready[s], 1);
     }
     mbar_init(acc_full, 1);
     mbar_init(acc_empty, 4);
@@ -190,6 +197,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   if (warp == 0 && lane == 0) {
     prefetch_tensormap(&tm_w);
     prefetch_tensormap(&tm_a);
+    prefetch_tensormap(&tm_asf);
   }
   tc_fence_before();
   __syncthreads();
@@ -211,7 +219,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const int w_row0 = ti.e * N + ti.mt * 128;
         const int w_row1 = ti.e * N + N / 2 + ti.mt * 128;  // up rows (L1 only)
         const int a_row0 = ti.poff + ti.nt * BN;
-        const int64_t atom0 = a_row0 >> 7;
         for (int kt = 0; kt < KT; ++kt) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.status)) {
             ok = false;
@@ -230,10 +237,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                       C::SFW, &full[stage], pol_w);
           }
           tma_load_2d(sb + C::OFF_B, &tm_a, &full[stage], kt * 128, a_row0, pol_a);
-          bulk_load(sb + C::OFF_SFA, p.a_sf + (atom0 * slices + 4 * kt) * 512, 2048, &full[stage],
-                    pol_a);
-          bulk_load(sb + C::OFF_SFA + 2048, p.a_sf + ((atom0 + 1) * slices + 4 * kt) * 512, 2048,
-                    &full[stage], pol_a);
+          tma_load_2d(sb + C::OFF_SFA_RAW, &tm_asf, &full[stage], kt * 16, a_row0, pol_a);
           issued_parity[stage] = static_cast<int>(phase);
           if (++stage == STAGES) {
             stage = 0;
@@ -254,12 +258,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
-        const TileInfo ti = decode_tile<BN>(tile, s_toff, E, p.offsets, p.padded_offsets);
-        const uint32_t sfb_shift = static_cast<uint32_t>(((ti.poff + ti.nt * BN) & 127) >> 5);
         if (!mbar_wait(acc_empty, acc_phase ^ 1u, abort_flag, p.status)) break;
         tc_fence_after();
         for (int kt = 0; kt < KT; ++kt) {
-          if (!mbar_wait(&full[stage], phase, abort_flag, p.status)) {
+          if (!mbar_wait(&full[stage], phase, abort_flag, p.status) ||
+              !mbar_wait(&sf_ready[stage], phase, abort_flag, p.status)) {
             ok = false;
             break;
           }
@@ -273,9 +276,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             for (int g = 0; g < C::G; ++g)
               tmem_cp_32x128b_x4(sf_col + 16 * g + 4 * c,
                                  sdesc_sf(smem_u32(sb + C::OFF_SFW + g * C::SFW + c * 512)));
-            tmem_cp_32x128b_x4(sfa_col + 8 * c, sdesc_sf(smem_u32(sb + C::OFF_SFA + c * 512)));
-            tmem_cp_32x128b_x4(sfa_col + 8 * c + 4,
-                               sdesc_sf(smem_u32(sb + C::OFF_SFA + 2048 + c * 512)));
+            tmem_cp_32x128b_x4(sfa_col + 4 * c, sdesc_sf(smem_u32(sb + C::OFF_SFA + c * 512)));
           }
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
@@ -284,7 +285,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             for (int g = 0; g < C::G; ++g) {
               const uint64_t adesc = sdesc_sw128(smem_u32(sb + C::OFF_A + g * C::A_TILE) + 32 * c);
               mma_nvf4(tmem + g * BN, adesc, bdesc, C::IDESC, sf_col + 16 * g + 4 * c,
-                       sfa_col + 8 * c + sfb_shift, (kt | c) != 0 ? 1u : 0u);
+                       sfa_col + 4 * c, (kt | c) != 0 ? 1u : 0u);
             }
           }
           tc_commit(&empty[stage]);
@@ -302,6 +303,40 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       mbar_drain(drain, 0);
     }
     __syncwarp();
+  } else if (warp == kSfWarp) {
+    // ------------------------------------------------------ scale transposer
+    // Raw token scales: row n (0..BN-1) holds 16 bytes = 4 slices x 4 blocks.
+    // Atom of slice c: byte 16 i + 4 j + b = row 32 j + i, block 4 c + b.
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+      for (int kt = 0; kt < KT; ++kt) {
+        if (!mbar_wait(&full[stage], phase, abort_flag, p.status)) {
+          ok = false;
+          break;
+        }
+        uint8_t* sb = smem + stage * C::STAGE;
+        const uint4* raw = reinterpret_cast<const uint4*>(sb + C::OFF_SFA_RAW);
+        uint4 r[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          r[j] = (32 * j + lane < BN) ? raw[32 * j + lane] : make_uint4(0u, 0u, 0u, 0u);
+        uint4* atom = reinterpret_cast<uint4*>(sb + C::OFF_SFA);
+        atom[0 * 32 + lane] = make_uint4(r[0].x, r[1].x, r[2].x, r[3].x);
+        atom[1 * 32 + lane] = make_uint4(r[0].y, r[1].y, r[2].y, r[3].y);
+        atom[2 * 32 + lane] = make_uint4(r[0].z, r[1].z, r[2].z, r[3].z);
+        atom[3 * 32 + lane] = make_uint4(r[0].w, r[1].w, r[2].w, r[3].w);
+        // make the generic-proxy stores visible to tcgen05.cp (async proxy)
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sf_ready[stage]);
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
   } else {
     // -------------------------------------------------------------- epilogue
     const int q = warp & 3;  // the TMEM lane quarter this warp may access
@@ -409,15 +444,31 @@ static int num_sms() {
   return n > 0 ? n : 1;
 }
 
+// 2-D map over row-major block scales [rows, K/16] bytes, boxes of
+// box_rows x 16 bytes (the four 64-element slices of one 256-element K step).
+static bool make_scales_map(CUtensorMap* map, const void* base, uint64_t rows, uint64_t row_bytes,
+                            uint32_t box_rows) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {row_bytes, rows};
+  cuuint64_t strides[1] = {row_bytes};
+  cuuint32_t box[2] = {16, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 template <int BN, int EPI, int STAGES>
-static cudaError_t launch_cfg(const CUtensorMap& tm_w, const CUtensorMap& tm_a, const GemmArgs& a,
-                              cudaStream_t stream) {
+static cudaError_t launch_cfg(const CUtensorMap& tm_w, const CUtensorMap& tm_a,
+                              const CUtensorMap& tm_asf, const GemmArgs& a, cudaStream_t stream) {
   using C = GemmCfg<BN, EPI, STAGES>;
   auto kern = k_grouped_gemm<BN, EPI, STAGES>;
   cudaError_t err =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (err != cudaSuccess) return err;
-  kern<<<num_sms(), kGemmThreads, C::SMEM, stream>>>(tm_w, tm_a, a);
+  kern<<<num_sms(), kGemmThreads, C::SMEM, stream>>>(tm_w, tm_a, tm_asf, a);
   return cudaGetLastError();
 }
 
@@ -430,28 +481,28 @@ int pick_tile_n(double expected) {
 cudaError_t launch_grouped_gemm(const GemmLaunch& g, cudaStream_t stream) {
   if (g.act_rows == 0 || g.E == 0) return cudaSuccess;
   const int bn = g.tile_n;
-  CUtensorMap tm_w, tm_a;
+  CUtensorMap tm_w, tm_a, tm_asf;
   if (!make_codes_map(&tm_w, g.w_codes, static_cast<uint64_t>(g.E) * g.N, g.K / 2, 128) ||
-      !make_codes_map(&tm_a, g.act_codes, static_cast<uint64_t>(g.act_rows), g.K / 2, bn))
+      !make_codes_map(&tm_a, g.act_codes, static_cast<uint64_t>(g.act_rows), g.K / 2, bn) ||
+      !make_scales_map(&tm_asf, g.act_scales, static_cast<uint64_t>(g.act_rows), g.K / 16, bn))
     return cudaErrorInvalidValue;
-  GemmArgs a{g.w_scales, g.act_scales, g.w_gs,   g.act_gs, g.offsets, g.padded_offsets,
-             g.out,      g.ld_out,     g.out_amax, g.status, g.E,       g.N,
-             g.K};
+  GemmArgs a{g.w_scales, g.w_gs,     g.act_gs, g.offsets, g.padded_offsets, g.out,
+             g.ld_out,   g.out_amax, g.status, g.E,       g.N,              g.K};
   if (g.epilogue == MEGAMOE_EPI_SILU_MUL) {
     if (g.out_amax) {
       cudaError_t err = cudaMemsetAsync(g.out_amax, 0, sizeof(float), stream);
       if (err != cudaSuccess) return err;
     }
     switch (bn) {
-      case 32: return launch_cfg<32, MEGAMOE_EPI_SILU_MUL, 5>(tm_w, tm_a, a, stream);
-      case 64: return launch_cfg<64, MEGAMOE_EPI_SILU_MUL, 4>(tm_w, tm_a, a, stream);
-      case 128: return launch_cfg<128, MEGAMOE_EPI_SILU_MUL, 3>(tm_w, tm_a, a, stream);
+      case 32: return launch_cfg<32, MEGAMOE_EPI_SILU_MUL, 5>(tm_w, tm_a, tm_asf, a, stream);
+      case 64: return launch_cfg<64, MEGAMOE_EPI_SILU_MUL, 4>(tm_w, tm_a, tm_asf, a, stream);
+      case 128: return launch_cfg<128, MEGAMOE_EPI_SILU_MUL, 3>(tm_w, tm_a, tm_asf, a, stream);
     }
   } else {
     switch (bn) {
-      case 32: return launch_cfg<32, MEGAMOE_EPI_F32, 8>(tm_w, tm_a, a, stream);
-      case 64: return launch_cfg<64, MEGAMOE_EPI_F32, 7>(tm_w, tm_a, a, stream);
-      case 128: return launch_cfg<128, MEGAMOE_EPI_F32, 5>(tm_w, tm_a, a, stream);
+      case 32: return launch_cfg<32, MEGAMOE_EPI_F32, 8>(tm_w, tm_a, tm_asf, a, stream);
+      case 64: return launch_cfg<64, MEGAMOE_EPI_F32, 7>(tm_w, tm_a, tm_asf, a, stream);
+      case 128: return launch_cfg<128, MEGAMOE_EPI_F32, 5>(tm_w, tm_a, tm_asf, a, stream);
     }
   }
   return cudaErrorInvalidValue;

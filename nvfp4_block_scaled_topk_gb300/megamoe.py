@@ -132,7 +132,7 @@ def route_permute(topk_ids: torch.Tensor, E: int, pad: int = 1, status=None):
 
 
 def sf_atom_bytes(rows, K):
-    return ((rows + 127) // 128 + 1) * 128 * (K // 16)
+    return (rows + 127) // 128 * 128 * (K // 16)
 
 
 def quantize_nvfp4(x: torch.Tensor, amax_in=None, slot_dst=None, k=1, row_src=None,
@@ -169,7 +169,7 @@ def swizzle_scales(scales: torch.Tensor) -> torch.Tensor:
     return dst
 
 
-def grouped_gemm(act_codes, act_scales_mma, act_gs, w_codes, w_scales_mma, w_gs, offsets,
+def grouped_gemm(act_codes, act_scales, act_gs, w_codes, w_scales_mma, w_gs, offsets,
                  padded_offsets, epilogue=EPI_F32, tile_n=0, expected_tokens=0.0, out=None,
                  out_amax=None, status=None):
     """Grouped block-scaled GEMM; returns (out, out_amax)."""
@@ -184,7 +184,7 @@ def grouped_gemm(act_codes, act_scales_mma, act_gs, w_codes, w_scales_mma, w_gs,
     if out_amax is None and epilogue == EPI_SILU_MUL:
         out_amax = torch.empty(1, dtype=torch.float32, device=dev)
     _check("megamoe_grouped_gemm", load().megamoe_grouped_gemm(
-        _p(act_codes), _p(act_scales_mma), _p(act_gs), act_rows, _p(w_codes), _p(w_scales_mma),
+        _p(act_codes), _p(act_scales), _p(act_gs), act_rows, _p(w_codes), _p(w_scales_mma),
         _p(w_gs), E, N, K, _p(offsets), _p(padded_offsets), epilogue, _p(out), out.shape[1],
         _p(out_amax), tile_n, float(expected_tokens), _p(status), _stream()))
     return out[:act_rows], out_amax
@@ -296,10 +296,10 @@ def _carve_views(ws, off, T, k, E, d, I, pad):
     take("slot_dst", 4 * T * k)
     take("row_src", 4 * rows)
     take("xq_codes", rows * (d // 2))
-    take("xq_sf", sf_atom_bytes(rows, d))
+    take("xq_sf", rows * (d // 16))
     take("h", rows * I * 2)
     take("hq_codes", rows * (I // 2))
-    take("hq_sf", sf_atom_bytes(rows, I))
+    take("hq_sf", rows * (I // 16))
     take("y", rows * d * 4)
     hdr = views.pop("hdr")
     v = {
@@ -314,10 +314,10 @@ def _carve_views(ws, off, T, k, E, d, I, pad):
         "slot_dst": views["slot_dst"].view(torch.int32),
         "row_src": views["row_src"].view(torch.int32),
         "xq_codes": views["xq_codes"].view(rows, d // 2),
-        "xq_sf": views["xq_sf"],
+        "xq_sf": views["xq_sf"].view(rows, d // 16),
         "h": views["h"].view(torch.bfloat16).view(rows, I),
         "hq_codes": views["hq_codes"].view(rows, I // 2),
-        "hq_sf": views["hq_sf"],
+        "hq_sf": views["hq_sf"].view(rows, I // 16),
         "y": views["y"].view(torch.float32).view(rows, d),
         "rows": rows,
     }

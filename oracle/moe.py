@@ -156,11 +156,12 @@ def grouped_gemm(a_codes, a_scales, a_gs, experts, which, routing: Routing,
     raise ValueError(epilogue)
 
 
-def combine(y, topk_weights, slot_dst):
+def combine(y, topk_weights, slot_dst, round_bf16=True):
     """out[t] = bf16( sum_j w[t, j] * y[slot_dst[t*k + j]] ), j ascending, float64.
 
     Skipped slots (slot_dst = -1) contribute nothing; a token without a valid
-    slot gives a zero row.
+    slot gives a zero row.  With round_bf16=False the float64 sum is returned
+    before the final rounding.
     """
     w = np.asarray(topk_weights, dtype=np.float64)
     T, k = w.shape
@@ -173,7 +174,7 @@ def combine(y, topk_weights, slot_dst):
             if r >= 0:
                 acc = acc + w[t, j] * y[r]
         out[t] = acc
-    return bf16_round(out)
+    return bf16_round(out) if round_bf16 else out
 
 
 def forward(x, topk_ids, topk_weights, experts, pad: int = 1, return_intermediates=False):
@@ -209,9 +210,10 @@ def forward(x, topk_ids, topk_weights, experts, pad: int = 1, return_intermediat
     hq_codes[~valid] = 0
     hq_scales[~valid] = 0
     y = grouped_gemm(hq_codes, hq_scales, gs_h, experts, "w2", rt, "f32")
-    out = combine(y, topk_weights, rt.slot_dst)
+    out64 = combine(y, topk_weights, rt.slot_dst, round_bf16=False)
+    out = bf16_round(out64)
     if return_intermediates:
-        return out, dict(routing=rt, gs_x=gs_x, amax_x=amax_x, xq_codes=xq_codes,
+        return out, dict(routing=rt, out_f64=out64, gs_x=gs_x, amax_x=amax_x, xq_codes=xq_codes,
                          xq_scales=xq_scales, a_codes=a_codes, a_scales=a_scales,
                          h=h, amax_h=amax_h, gs_h=gs_h, hq_codes=hq_codes,
                          hq_scales=hq_scales, y=y)

@@ -25,6 +25,38 @@ def assert_close(got, want, rel_l2=REL_L2, max_abs_of_rms=MAX_ABS_OF_RMS, what="
     return err, mae / rms if rms > 0 else 0.0
 
 
+def bf16_half_ulp(v):
+    """Half a bf16 ulp at |v| (bf16 keeps 8 significant bits)."""
+    a = np.abs(np.asarray(v, dtype=np.float64))
+    e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    return np.where(a > 0, np.ldexp(1.0, (e - 8).astype(np.int64)), 0.0)
+
+
+def assert_close_bf16(got, want_f64, rel_l2=REL_L2, max_abs_of_rms=MAX_ABS_OF_RMS, what=""):
+    """A bf16 output against the oracle's value before its final bf16 rounding.
+
+    The bound of assert_close applies to |got - want| minus the half ulp that
+    rounding the exact value to bf16 may add by itself: two correct programs
+    whose sums straddle a bf16 rounding midpoint differ by one whole ulp, which
+    for outputs above ~2.6 rms is more than 1e-2 rms.
+    """
+    got = np.asarray(got, dtype=np.float64)
+    want = np.asarray(want_f64, dtype=np.float64)
+    assert got.shape == want.shape, (what, got.shape, want.shape)
+    assert np.all(np.isfinite(got)), f"{what}: non-finite output"
+    if want.size == 0:
+        return 0.0, 0.0
+    nrm = np.linalg.norm(want)
+    err = np.linalg.norm(got - want) / nrm if nrm > 0 else np.linalg.norm(got)
+    rms = np.sqrt(np.mean(want ** 2))
+    excess = np.maximum(np.abs(got - want) - bf16_half_ulp(want), 0.0)
+    mae = float(np.max(excess))
+    assert err <= rel_l2, f"{what}: rel-L2 {err:.3e} > {rel_l2}"
+    assert mae <= max_abs_of_rms * rms, \
+        f"{what}: max-abs beyond half an ulp {mae:.3e} > {max_abs_of_rms}*rms ({rms:.3e})"
+    return err, mae / rms if rms > 0 else 0.0
+
+
 def to_np(t):
     return t.detach().cpu().numpy()
 
