@@ -139,7 +139,7 @@ def oracle_sample(cfg, x, ids, w, experts_src, tokens: int):
     ws = w[:tokens].cpu().numpy()
     ex = inputs.ExpertSet(cfg, experts_src)
     t0 = time.perf_counter()
-    out = oracle.forward(xs, ids_s, ws, ex, pad=32)
+    out = oracle.forward(xs, ids_s, ws, ex, pad=cfg.pad)
     dt = time.perf_counter() - t0
     assert np.all(np.isfinite(out))
     return dt
@@ -211,7 +211,7 @@ def run_ours(args):
     weights = megamoe.Weights.prepare(raw)
     x = inputs.make_activations(cfg, device=dev)
     ids, w = inputs.make_routing(cfg, device=dev)
-    fwd = megamoe.Forward(weights, cfg.T, cfg.k, pad=32)
+    fwd = megamoe.Forward(weights, cfg.T, cfg.k, pad=cfg.pad)
     stream = torch.cuda.current_stream()
 
     def barrier():

@@ -85,10 +85,11 @@ typedef enum megamoe_status {
  * NVFP4 expert weights.  Expert e of W13 is [2I, d]: rows 0..I-1 are the gate
  * projection, rows I..2I-1 the up projection ("What's Been Verified": L1
  * gate+up).  W2 is [d, I] per expert (L2 down).
- *   w13_codes   [E, 2I, d/2]            E2M1 codes
+ *   w13_codes   tile-major layout of [E*2I, d/2] E2M1 codes (from
+ *               megamoe_pack_weight_codes)
  *   w13_scales  atom layout of [E*2I, d/16] (from megamoe_swizzle_scales)
  *   w13_gs      [E, 2] float            global scales (gate, up)
- *   w2_codes    [E, d, I/2]
+ *   w2_codes    tile-major layout of [E*d, I/2]
  *   w2_scales   atom layout of [E*d, I/16]
  *   w2_gs       [E] float
  * Supported: 1 <= E <= 1024, d and I multiples of 256.
@@ -180,6 +181,17 @@ megamoe_status megamoe_swizzle_scales(const uint8_t* src, int64_t rows, int K, u
                                       megamoe_stream_t stream);
 
 /*
+ * megamoe_pack_weight_codes -- one-time weight preparation: row-major E2M1
+ * codes [rows, K/2] -> tile-major layout: blocks of 128 rows x 128 bytes
+ * (256 elements of K), ordered [rows/128][K/256], each block row-major.  Row
+ * r, bytes 128t .. 128t+127 land at ((r/128)*(K/256) + t)*16384 + (r%128)*128.
+ * Every weight tile the grouped GEMM loads is then one contiguous 16 KB read.
+ * Requires rows a multiple of 128, K a multiple of 256, 16-byte alignment.
+ */
+megamoe_status megamoe_pack_weight_codes(const uint8_t* src, int64_t rows, int K, uint8_t* dst,
+                                         megamoe_stream_t stream);
+
+/*
  * megamoe_grouped_gemm -- one persistent grouped block-scaled GEMM over all
  * experts ("Architecture: DeepSeek-V4 MegaMoE": one problem per expert,
  * persistent tile scheduling across groups, token tile chosen from the
@@ -191,7 +203,8 @@ megamoe_status megamoe_swizzle_scales(const uint8_t* src, int64_t rows, int K, u
  *   acc[r, n] = sum_K dequant(act)[r, :] . dequant(w_e)[n, :]   (fp32 accumulate)
  *   act_codes   [act_rows, K/2]; act_scales row-major [act_rows, K/16];
  *               act_gs device float (one global scale)
- *   w_codes     [E, N, K/2]; w_scales atom layout of [E*N, K/16]
+ *   w_codes     tile-major layout of [E*N, K/2] (megamoe_pack_weight_codes);
+ *               w_scales atom layout of [E*N, K/16] (megamoe_swizzle_scales)
  *   w_gs        [E, G] float: G = 1 for MEGAMOE_EPI_F32; G = 2 (gate, up) for
  *               MEGAMOE_EPI_SILU_MUL
  *   offsets, padded_offsets  [E+1] int32 as produced by megamoe_route_permute

@@ -164,6 +164,15 @@ megamoe_status megamoe_swizzle_scales(const uint8_t* src, int64_t rows, int K, u
   return cuda_status(launch_swizzle(src, rows, K, dst, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+megamoe_status megamoe_pack_weight_codes(const uint8_t* src, int64_t rows, int K, uint8_t* dst,
+                                        megamoe_stream_t stream) {
+  if (rows < 0 || K <= 0) return MEGAMOE_ERR_INVALID_ARG;
+  if (K % 256 != 0 || rows % 128 != 0) return MEGAMOE_ERR_UNSUPPORTED_SHAPE;
+  if (rows > 0 && (!src || !dst)) return MEGAMOE_ERR_INVALID_ARG;
+  if (rows > 0 && (!aligned(src, 16) || !aligned(dst, 16))) return MEGAMOE_ERR_UNSUPPORTED_SHAPE;
+  return cuda_status(launch_pack(src, rows, K, dst, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 megamoe_status megamoe_grouped_gemm(const uint8_t* act_codes, const uint8_t* act_scales,
                                     const float* act_gs, int64_t act_rows, const uint8_t* w_codes,
                                     const uint8_t* w_scales, const float* w_gs, int E, int N,
@@ -176,7 +185,8 @@ megamoe_status megamoe_grouped_gemm(const uint8_t* act_codes, const uint8_t* act
     return MEGAMOE_ERR_INVALID_ARG;
   if (E > MEGAMOE_MAX_EXPERTS || K % 256 != 0 || N % (epilogue == MEGAMOE_EPI_F32 ? 128 : 256))
     return MEGAMOE_ERR_UNSUPPORTED_SHAPE;
-  if (static_cast<int64_t>(E) * N >= (int64_t{1} << 31) || act_rows >= (int64_t{1} << 31))
+  if (static_cast<int64_t>(E) * N * (K / 256) >= (int64_t{1} << 31) ||
+      act_rows >= (int64_t{1} << 31))
     return MEGAMOE_ERR_UNSUPPORTED_SHAPE;
   if (tile_n != 0 && tile_n != 32 && tile_n != 64 && tile_n != 128) return MEGAMOE_ERR_INVALID_ARG;
   const int width = epilogue == MEGAMOE_EPI_F32 ? N : N / 2;

@@ -24,8 +24,10 @@
 //   warp 6      scale transposer: rewrites the token tile's row-major scales
 //               into the 32 x 16-byte atoms tcgen05.cp reads, so the tile's
 //               first row always lands in the first TMEM scale column.
-// Every expert's weights live in one [E*N, K/2] tensor, so one tensor map
-// serves all experts: the expert is a row coordinate, not a new descriptor.
+// Every expert's weights live in one tensor (tile-major: blocks of 128 rows x
+// 128 bytes, [E*N/128][K/256] blocks), so one tensor map serves all experts:
+// the expert is a coordinate, not a new descriptor, and every weight box is
+// one contiguous 16 KB read.
 // Tiles are numbered expert-major, weight-tile-major, token-tile-minor, so CTAs
 // working on the same expert's weight tile run together and share it in L2.
 #include <cuda.h>
@@ -59,6 +61,9 @@ struct GemmArgs {
 template <int BN, int EPI, int STAGES>
 struct GemmCfg {
   static constexpr int G = EPI == MEGAMOE_EPI_SILU_MUL ? 2 : 1;
+  // Two accumulator slots (the MMA fills one while the epilogue drains the
+  // other) whenever tensor memory has room for them.
+  static constexpr int ACC_STAGES = (2 * G * BN + STAGES * (16 * G + 16) <= 512) ? 2 : 1;
   static constexpr int A_TILE = 128 * 128;  // one weight matrix, 128 rows x 128 bytes
   static constexpr int B_TILE = BN * 128;
   static constexpr int SFW = 2048;     // 4 atoms of 512 bytes (one per 64-element slice)
@@ -73,14 +78,14 @@ struct GemmCfg {
   static constexpr uint32_t TX = G * A_TILE + B_TILE + G * SFW + SFA_RAW;
   static constexpr int ACC_COLS = G * BN;
   static constexpr int SF_COLS = 16 * G + 16;  // per stage: weight scales + token scales
-  static constexpr int SF_COL0 = ACC_COLS;
+  static constexpr int SF_COL0 = ACC_STAGES * ACC_COLS;
   static constexpr int BAR_OFF = STAGES * STAGE;
   static constexpr int TOFF_OFF = BAR_OFF + 256;
   static constexpr int SMEM = 1024 + TOFF_OFF + 4 * (MEGAMOE_MAX_EXPERTS + 1);
   static constexpr uint32_t IDESC = idesc_nvf4(128, BN);
   static_assert(SF_COL0 + STAGES * SF_COLS <= 512, "tensor memory budget");
   static_assert(SMEM <= 232448, "shared memory budget");
-  static_assert((3 * STAGES + 3) * 8 + 8 <= 256, "barrier area");
+  static_assert((3 * STAGES + 2 * ACC_STAGES + 1) * 8 + 8 <= 256, "barrier area");
 };
 
 struct TileInfo {
@@ -160,9 +165,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
   uint64_t* empty = full + STAGES;
   uint64_t* sf_ready = empty + STAGES;
-  uint64_t* acc_full = sf_ready + STAGES;
-  uint64_t* acc_empty = acc_full + 1;
-  uint64_t* drain = acc_empty + 1;
+  uint64_t* acc_full = sf_ready + STAGES;  // [ACC_STAGES]
+  uint64_t* acc_empty = acc_full + C::ACC_STAGES;  // [ACC_STAGES]
+  uint64_t* drain = acc_empty + C::ACC_STAGES;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   int* s_toff = reinterpret_cast<int*>(smem + C::TOFF_OFF);
@@ -184,8 +189,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       mbar_init(&empty[s], 1);
       mbar_init(&sf_ready[s], 1);
     }
-    mbar_init(acc_full, 1);
-    mbar_init(acc_empty, 4);
+    for (int a = 0; a < C::ACC_STAGES; ++a) {
+      mbar_init(&acc_full[a], 1);
+      mbar_init(&acc_empty[a], 4);
+    }
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -226,12 +233,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           }
           uint8_t* sb = smem + stage * C::STAGE;
           mbar_arrive_expect_tx(&full[stage], C::TX);
-          tma_load_2d(sb + C::OFF_A, &tm_w, &full[stage], kt * 128, w_row0, pol_w);
+          tma_load_2d(sb + C::OFF_A, &tm_w, &full[stage], 0, ((w_row0 >> 7) * KT + kt) * 128,
+                      pol_w);
           bulk_load(sb + C::OFF_SFW,
                     p.w_sf + (static_cast<int64_t>(w_row0 >> 7) * slices + 4 * kt) * 512, C::SFW,
                     &full[stage], pol_w);
           if (C::G == 2) {
-            tma_load_2d(sb + C::OFF_A + C::A_TILE, &tm_w, &full[stage], kt * 128, w_row1, pol_w);
+            tma_load_2d(sb + C::OFF_A + C::A_TILE, &tm_w, &full[stage], 0,
+                        ((w_row1 >> 7) * KT + kt) * 128, pol_w);
             bulk_load(sb + C::OFF_SFW + C::SFW,
                       p.w_sf + (static_cast<int64_t>(w_row1 >> 7) * slices + 4 * kt) * 512,
                       C::SFW, &full[stage], pol_w);
@@ -254,12 +263,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   } else if (warp == 1) {
     if (lane == 0) {
       // ------------------------------------------------------------ MMA issuer
-      int stage = 0;
+      int stage = 0, acc = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
-        if (!mbar_wait(acc_empty, acc_phase ^ 1u, abort_flag, p.status)) break;
+        if (!mbar_wait(&acc_empty[acc], acc_phase ^ 1u, abort_flag, p.status)) break;
         tc_fence_after();
+        const uint32_t d_col = tmem + acc * C::ACC_COLS;
         for (int kt = 0; kt < KT; ++kt) {
           if (!mbar_wait(&full[stage], phase, abort_flag, p.status) ||
               !mbar_wait(&sf_ready[stage], phase, abort_flag, p.status)) {
@@ -284,7 +294,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 #pragma unroll
             for (int g = 0; g < C::G; ++g) {
               const uint64_t adesc = sdesc_sw128(smem_u32(sb + C::OFF_A + g * C::A_TILE) + 32 * c);
-              mma_nvf4(tmem + g * BN, adesc, bdesc, C::IDESC, sf_col + 16 * g + 4 * c,
+              mma_nvf4(d_col + g * BN, adesc, bdesc, C::IDESC, sf_col + 16 * g + 4 * c,
                        sfa_col + 4 * c, (kt | c) != 0 ? 1u : 0u);
             }
           }
@@ -295,8 +305,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           }
         }
         if (!ok) break;
-        tc_commit(acc_full);
-        acc_phase ^= 1u;
+        tc_commit(&acc_full[acc]);
+        if (++acc == C::ACC_STAGES) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
       }
       // every MMA issued so far must finish before tensor memory is released
       tc_commit(drain);
@@ -341,6 +354,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // -------------------------------------------------------------- epilogue
     const int q = warp & 3;  // the TMEM lane quarter this warp may access
     const float a_gs = __ldg(p.a_gs);
+    int acc = 0;
     uint32_t acc_phase = 0;
     float amax = 0.f;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
@@ -355,9 +369,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       } else {
         alpha0 = 1.0f / (a_gs * __ldg(p.w_gs + ti.e));
       }
-      if (!mbar_wait(acc_full, acc_phase, abort_flag, p.status)) break;
+      if (!mbar_wait(&acc_full[acc], acc_phase, abort_flag, p.status)) break;
       tc_fence_after();
-      const uint32_t lane_base = tmem + (static_cast<uint32_t>(q * 32) << 16);
+      const uint32_t lane_base =
+          tmem + acc * C::ACC_COLS + (static_cast<uint32_t>(q * 32) << 16);
       for (int n0 = 0; n0 < m_valid; n0 += 16) {
         uint32_t g[16];
         tmem_ld_32x32b_x16(lane_base + n0, g);
@@ -387,8 +402,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(acc_empty);
-      acc_phase ^= 1u;
+      if (lane == 0) mbar_arrive(&acc_empty[acc]);
+      if (++acc == C::ACC_STAGES) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
     }
     if (C::G == 2) {
 #pragma unroll
@@ -482,7 +500,8 @@ cudaError_t launch_grouped_gemm(const GemmLaunch& g, cudaStream_t stream) {
   if (g.act_rows == 0 || g.E == 0) return cudaSuccess;
   const int bn = g.tile_n;
   CUtensorMap tm_w, tm_a, tm_asf;
-  if (!make_codes_map(&tm_w, g.w_codes, static_cast<uint64_t>(g.E) * g.N, g.K / 2, 128) ||
+  if (!make_codes_map(&tm_w, g.w_codes, static_cast<uint64_t>(g.E) * g.N * (g.K / 256), 128,
+                      128) ||
       !make_codes_map(&tm_a, g.act_codes, static_cast<uint64_t>(g.act_rows), g.K / 2, bn) ||
       !make_scales_map(&tm_asf, g.act_scales, static_cast<uint64_t>(g.act_rows), g.K / 16, bn))
     return cudaErrorInvalidValue;

@@ -23,12 +23,15 @@ cudaError_t launch_quant(const uint16_t* x, int64_t rows_in, int K, int64_t ld,
 cudaError_t launch_swizzle(const uint8_t* src, int64_t rows, int K, uint8_t* dst,
                            cudaStream_t stream);
 
+cudaError_t launch_pack(const uint8_t* src, int64_t rows, int K, uint8_t* dst,
+                        cudaStream_t stream);
+
 struct GemmLaunch {
   const uint8_t* act_codes;
   const uint8_t* act_scales;  // atom layout
   const float* act_gs;
   int64_t act_rows;
-  const uint8_t* w_codes;
+  const uint8_t* w_codes;   // tile-major (k_pack)
   const uint8_t* w_scales;  // atom layout
   const float* w_gs;
   int E, N, K;

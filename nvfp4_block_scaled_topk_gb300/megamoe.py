@@ -40,6 +40,7 @@ SIGNATURES = {
     "megamoe_quantize_nvfp4": (_I, [_P, _I64, _I, _I64, _P, _I, _P, _P, _I64, _P, _P, _P, _P, _P,
                                     _I, _P, _P]),
     "megamoe_swizzle_scales": (_I, [_P, _I64, _I, _P, _P]),
+    "megamoe_pack_weight_codes": (_I, [_P, _I64, _I, _P, _P]),
     "megamoe_grouped_gemm": (_I, [_P, _P, _P, _I64, _P, _P, _P, _I, _I, _I, _P, _P, _I, _P, _I64,
                                   _P, _I, ctypes.c_double, _P, _P]),
     "megamoe_combine": (_I, [_P, _I64, _P, _P, _I, _I, _I, _P, _P]),
@@ -169,12 +170,24 @@ def swizzle_scales(scales: torch.Tensor) -> torch.Tensor:
     return dst
 
 
-def grouped_gemm(act_codes, act_scales, act_gs, w_codes, w_scales_mma, w_gs, offsets,
+def pack_weight_codes(codes: torch.Tensor) -> torch.Tensor:
+    """Row-major [rows, K/2] E2M1 codes -> tile-major layout (weight preparation)."""
+    _dev(codes, torch.uint8, "codes")
+    rows, half = codes.shape
+    dst = torch.empty_like(codes)
+    _check("megamoe_pack_weight_codes",
+           load().megamoe_pack_weight_codes(_p(codes), rows, half * 2, _p(dst), _stream()))
+    return dst
+
+
+def grouped_gemm(act_codes, act_scales, act_gs, w_codes_packed, w_scales_mma, w_gs, offsets,
                  padded_offsets, epilogue=EPI_F32, tile_n=0, expected_tokens=0.0, out=None,
                  out_amax=None, status=None):
-    """Grouped block-scaled GEMM; returns (out, out_amax)."""
+    """Grouped block-scaled GEMM; returns (out, out_amax).  ``w_codes_packed``
+    is [E, N, K/2]-shaped in the tile-major layout of pack_weight_codes."""
     act_rows, half_k = act_codes.shape
-    E, N, _ = w_codes.shape
+    E, N, _ = w_codes_packed.shape
+    w_codes = w_codes_packed
     K = half_k * 2
     dev = act_codes.device
     width = N if epilogue == EPI_F32 else N // 2
@@ -203,7 +216,8 @@ def combine(y, slot_dst, topk_weights, out=None):
 
 @dataclass
 class Weights:
-    """Device NVFP4 expert weights, prepared for the library (scales swizzled)."""
+    """Device NVFP4 expert weights, prepared for the library (codes packed
+    tile-major, scales swizzled into the atom layout)."""
 
     E: int
     d: int
@@ -224,8 +238,10 @@ class Weights:
         d, I = half_d * 2, I2 // 2
         s13 = swizzle_scales(w["w13_scales"].reshape(E * I2, d // 16))
         s2 = swizzle_scales(w["w2_scales"].reshape(E * d, I // 16))
-        return cls(E, d, I, w["w13_codes"].contiguous(), s13, w["w13_gs"].contiguous(),
-                   w["w2_codes"].contiguous(), s2, w["w2_gs"].reshape(E).contiguous())
+        c13 = pack_weight_codes(w["w13_codes"].reshape(E * I2, d // 2)).view(E, I2, d // 2)
+        c2 = pack_weight_codes(w["w2_codes"].reshape(E * d, I // 2)).view(E, d, I // 2)
+        return cls(E, d, I, c13, s13, w["w13_gs"].contiguous(), c2, s2,
+                   w["w2_gs"].reshape(E).contiguous())
 
     def cstruct(self) -> CWeights:
         return CWeights(self.E, self.d, self.I, self.w13_codes.data_ptr(),

@@ -97,7 +97,7 @@ def silu(g):
 
 
 def grouped_gemm(a_codes, a_scales, a_gs, experts, which, routing: Routing,
-                 epilogue: str = "f32"):
+                 epilogue: str = "f32", return_unrounded: bool = False):
     """One grouped block-scaled GEMM over all experts (float64 on dequantised data).
 
     Expert e multiplies its valid rows of A (the quantised activations in
@@ -113,7 +113,8 @@ def grouped_gemm(a_codes, a_scales, a_gs, experts, which, routing: Routing,
     epilogue "f32":       returns out [R_pad, N] float64 (padding rows NaN).
     epilogue "silu_mul":  ``which`` must be "w13"; returns
         (h [R_pad, I] float64 holding bf16 values, amax_h) with
-        h = bf16(silu(gate) * up), padding rows 0, amax over valid rows.
+        h = bf16(silu(gate) * up), padding rows 0, amax over valid rows;
+        with return_unrounded also silu(gate) * up before the rounding.
     """
     ahat = dequantize(a_codes, a_scales, a_gs)
     R_pad = ahat.shape[0]
@@ -142,6 +143,7 @@ def grouped_gemm(a_codes, a_scales, a_gs, experts, which, routing: Routing,
             raise ValueError("silu_mul needs the gate+up matrix")
         I = experts.I
         h = np.zeros((R_pad, I))
+        h64 = np.zeros((R_pad, I))
         amax = 0.0
         for e in range(routing.counts.size):
             m = int(routing.counts[e])
@@ -149,9 +151,13 @@ def grouped_gemm(a_codes, a_scales, a_gs, experts, which, routing: Routing,
                 continue
             r0 = int(routing.padded_offsets[e])
             v = out[r0:r0 + m]
-            hv = bf16_round(silu(v[:, :I]) * v[:, I:])
+            hu = silu(v[:, :I]) * v[:, I:]
+            hv = bf16_round(hu)
             h[r0:r0 + m] = hv
+            h64[r0:r0 + m] = hu
             amax = max(amax, float(np.max(np.abs(hv))))
+        if return_unrounded:
+            return h, np.float32(amax), h64
         return h, np.float32(amax)
     raise ValueError(epilogue)
 
@@ -205,7 +211,8 @@ def forward(x, topk_ids, topk_weights, experts, pad: int = 1, return_intermediat
     a_codes[valid] = xq_codes[rt.row_src[valid] // k]
     a_scales[valid] = xq_scales[rt.row_src[valid] // k]
 
-    h, amax_h = grouped_gemm(a_codes, a_scales, gs_x, experts, "w13", rt, "silu_mul")
+    h, amax_h, h64 = grouped_gemm(a_codes, a_scales, gs_x, experts, "w13", rt, "silu_mul",
+                                  return_unrounded=True)
     hq_codes, hq_scales, gs_h, _ = quantize(h.astype(np.float32), amax=amax_h)
     hq_codes[~valid] = 0
     hq_scales[~valid] = 0
@@ -213,7 +220,7 @@ def forward(x, topk_ids, topk_weights, experts, pad: int = 1, return_intermediat
     out64 = combine(y, topk_weights, rt.slot_dst, round_bf16=False)
     out = bf16_round(out64)
     if return_intermediates:
-        return out, dict(routing=rt, out_f64=out64, gs_x=gs_x, amax_x=amax_x, xq_codes=xq_codes,
+        return out, dict(routing=rt, out_f64=out64, h_f64=h64, gs_x=gs_x, amax_x=amax_x, xq_codes=xq_codes,
                          xq_scales=xq_scales, a_codes=a_codes, a_scales=a_scales,
                          h=h, amax_h=amax_h, gs_h=gs_h, hq_codes=hq_codes,
                          hq_scales=hq_scales, y=y)

@@ -37,12 +37,14 @@ def _quantised_rows(rng, rt, R, K, scale):
 def _dev_weights(stacked, which, megamoe):
     if which == "w13":
         E, N, hk = stacked["w13_codes"].shape
-        codes = stacked["w13_codes"].cuda()
+        codes = megamoe.pack_weight_codes(
+            stacked["w13_codes"].reshape(E * N, hk).cuda()).view(E, N, hk)
         sc = megamoe.swizzle_scales(stacked["w13_scales"].reshape(E * N, hk // 8).cuda())
         gs = stacked["w13_gs"].cuda()
     else:
         E, N, hk = stacked["w2_codes"].shape
-        codes = stacked["w2_codes"].cuda()
+        codes = megamoe.pack_weight_codes(
+            stacked["w2_codes"].reshape(E * N, hk).cuda()).view(E, N, hk)
         sc = megamoe.swizzle_scales(stacked["w2_scales"].reshape(E * N, hk // 8).cuda())
         gs = stacked["w2_gs"].cuda()
     return codes, sc, gs
@@ -121,3 +123,32 @@ def test_grouped_gemm_real_shape_one_expert_per_token(cuda_lib):
     v = rt.row_src >= 0
     h64 = oracle.silu(gu[v][:, :I]) * gu[v][:, I:]
     assert_close_bf16(got[v], h64, what="real shape")
+
+
+@pytest.mark.parametrize("T,k,d", [(64, 2, 256), (8, 6, 7168), (333, 6, 1024)])
+def test_combine_matches_oracle(cuda_lib, T, k, d):
+    from nvfp4_block_scaled_topk_gb300 import megamoe
+
+    rng = np.random.default_rng(60 + T)
+    rows = T * k + 40
+    y = (rng.standard_normal((rows, d)) * 0.03).astype(np.float32)
+    slot_dst = rng.permutation(rows)[:T * k].astype(np.int32)
+    slot_dst[rng.random(T * k) < 0.1] = -1  # skipped slots
+    w = rng.random((T, k)).astype(np.float32)
+    out = megamoe.combine(torch.from_numpy(y).cuda(), torch.from_numpy(slot_dst).cuda(),
+                          torch.from_numpy(w).cuda())
+    torch.cuda.synchronize()
+    want64 = oracle.combine(y.astype(np.float64), w, slot_dst, round_bf16=False)
+    assert_close_bf16(out.float().cpu().numpy(), want64, what="combine")
+
+
+def test_pack_weight_codes_layout(cuda_lib):
+    from nvfp4_block_scaled_topk_gb300 import megamoe
+
+    rng = np.random.default_rng(70)
+    rows, K = 384, 768
+    c = rng.integers(0, 256, (rows, K // 2), dtype=np.uint8)
+    got = megamoe.pack_weight_codes(torch.from_numpy(c).cuda()).cpu().numpy().reshape(-1)
+    # blocks of 128 rows x 128 bytes, ordered [rows/128][K/256]
+    want = c.reshape(rows // 128, 128, K // 256, 128).transpose(0, 2, 1, 3).reshape(-1)
+    assert np.array_equal(got, want)

@@ -10,7 +10,7 @@ import torch
 import oracle
 from oracle import nvfp4 as q
 from nvfp4_block_scaled_topk_gb300 import inputs, megamoe
-from helpers import assert_close, assert_close_bf16, bf16_to_np
+from helpers import assert_close, assert_close_bf16, bf16_to_np, check_forward
 
 pytestmark = pytest.mark.gpu
 
@@ -49,7 +49,7 @@ def test_forward_matches_oracle(cuda_lib, name, pad):
     assert bits == 0
     _, inter = oracle.forward(x.float().numpy(), ids.numpy(), w.numpy(),
                               inputs.ExpertSet(cfg, raw), pad=pad, return_intermediates=True)
-    assert_close_bf16(bf16_to_np(out), inter["out_f64"], what=name)
+    check_forward(cfg, fwd, out, inter, what=name)
 
 
 def test_forward_prefill_shaped_mid_size(cuda_lib):
@@ -61,7 +61,7 @@ def test_forward_prefill_shaped_mid_size(cuda_lib):
     assert bits == 0
     _, inter = oracle.forward(x.float().numpy(), ids.numpy(), w.numpy(),
                               inputs.ExpertSet(cfg, raw), pad=32, return_intermediates=True)
-    assert_close_bf16(bf16_to_np(out), inter["out_f64"], what="prefill_mid")
+    check_forward(cfg, fwd, out, inter, what="prefill_mid")
 
 
 @pytest.mark.parametrize("name", ["prefill", "large"])
@@ -144,4 +144,4 @@ def test_forward_stress_routings(cuda_lib, case):
         ids_ok = ids
     _, inter = oracle.forward(x.float().numpy(), ids_ok.numpy(), w.numpy(),
                               inputs.ExpertSet(cfg, raw), pad=32, return_intermediates=True)
-    assert_close_bf16(bf16_to_np(out), inter["out_f64"], what=case)
+    check_forward(cfg, fwd, out, inter, what=case)
