@@ -47,6 +47,7 @@ SIGNATURES = {
     "megamoe_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I]),
     "megamoe_forward": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P, _SZ, _P]),
     "megamoe_read_status": (_I, [_P, _P, _P]),
+    "megamoe_forward_static": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P, _P]),
 }
 
 
@@ -292,6 +293,23 @@ class Forward:
         """Views into the workspace (for debugging and stage-level tests)."""
         return _carve_views(self.ws, self.ws_off, self.T, self.k, self.w.E, self.w.d, self.w.I,
                             self.pad)
+
+
+def forward_static(weights: Weights, x, topk_ids, topk_weights, pad: int = 32, out=None,
+                   status_out=None):
+    """megamoe_forward_static: the forward with the library's fixed internal
+    workspace (no allocation by the library; for small batches)."""
+    _dev(x, torch.bfloat16, "x")
+    _dev(topk_ids, torch.int32, "topk_ids")
+    _dev(topk_weights, torch.float32, "topk_weights")
+    T, k = topk_ids.shape
+    if out is None:
+        out = torch.empty(max(T, 1), weights.d, dtype=torch.bfloat16, device=x.device)
+    cw = weights.cstruct()
+    _check("megamoe_forward_static", load().megamoe_forward_static(
+        ctypes.byref(cw), _p(x), _p(topk_ids), _p(topk_weights), T, k, pad, _p(out),
+        _p(status_out), _stream()))
+    return out[:T]
 
 
 def _carve_views(ws, off, T, k, E, d, I, pad):
