@@ -13,17 +13,21 @@
 // holds the gate AND the up accumulators of the same 128 features (two MMAs
 // per K step into two TMEM ranges), so SiLU(gate) * up is a per-lane epilogue.
 //
-// Roles (224 threads, one CTA per SM, grid = number of SMs):
+// Roles (320 threads, one CTA per SM, grid = number of SMs):
 //   warp 0      TMA producer: weight tiles and token tiles (128-byte swizzle),
 //               the weights' block-scale atoms (bulk copies) and the token
 //               tile's row-major block scales into a STAGES-deep ring;
-//   warp 1      TMEM allocator; one lane issues tcgen05.cp (scales -> TMEM)
-//               and tcgen05.mma, and commits stage-free / accumulator-ready;
+//   warp 1      TMEM allocator; one lane issues tcgen05.mma and commits
+//               stage-free / accumulator-ready;
 //   warps 2..5  epilogue: tcgen05.ld of their 32-lane quarter, alpha scaling,
 //               SiLU * up -> bf16 + amax (L1) or fp32 (L2), masked stores;
-//   warp 6      scale transposer: rewrites the token tile's row-major scales
-//               into the 32 x 16-byte atoms tcgen05.cp reads, so the tile's
-//               first row always lands in the first TMEM scale column.
+//   warps 6..9  scale writers: each writes the stage's weight and token block
+//               scales into its own 32-lane quarter of tensor memory with
+//               tcgen05.st (every quarter holds the same copy, the layout the
+//               block-scaled MMA reads).  Scales do not go through the tensor
+//               pipe (a tcgen05.cp costs about as much as an MMA), and the
+//               token tile's first row always lands in the first scale
+//               column whatever row the tile starts at.
 // Every expert's weights live in one tensor (tile-major: blocks of 128 rows x
 // 128 bytes, [E*N/128][K/256] blocks), so one tensor map serves all experts:
 // the expert is a coordinate, not a new descriptor, and every weight box is
@@ -42,8 +46,8 @@
 
 namespace megamoe {
 
-constexpr int kGemmThreads = 224;
-constexpr int kSfWarp = 6;
+constexpr int kGemmThreads = 320;
+constexpr int kSfWarp0 = 6;  // warps 6..9 write block scales into TMEM
 
 struct GemmArgs {
   const uint8_t* w_sf;  // atom layout [E*N/128][K/64][512]
@@ -68,13 +72,11 @@ struct GemmCfg {
   static constexpr int B_TILE = BN * 128;
   static constexpr int SFW = 2048;     // 4 atoms of 512 bytes (one per 64-element slice)
   static constexpr int SFA_RAW = BN * 16;  // token scales as loaded: BN rows x 16 bytes
-  static constexpr int SFA = 2048;     // token scales as 4 atoms of 512 bytes
   static constexpr int OFF_A = 0;
   static constexpr int OFF_B = G * A_TILE;
   static constexpr int OFF_SFW = OFF_B + B_TILE;
   static constexpr int OFF_SFA_RAW = OFF_SFW + G * SFW;
-  static constexpr int OFF_SFA = OFF_SFA_RAW + SFA_RAW;
-  static constexpr int STAGE = (OFF_SFA + SFA + 1023) / 1024 * 1024;
+  static constexpr int STAGE = (OFF_SFA_RAW + SFA_RAW + 1023) / 1024 * 1024;
   static constexpr uint32_t TX = G * A_TILE + B_TILE + G * SFW + SFA_RAW;
   static constexpr int ACC_COLS = G * BN;
   static constexpr int SF_COLS = 16 * G + 16;  // per stage: weight scales + token scales
@@ -187,7 +189,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
-      mbar_init(&sf_ready[s], 1);
+      mbar_init(&sf_ready[s], 4);
     }
     for (int a = 0; a < C::ACC_STAGES; ++a) {
       mbar_init(&acc_full[a], 1);
@@ -282,14 +284,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           const uint32_t sfa_col = sf_col + 16 * C::G;
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
-#pragma unroll
-            for (int g = 0; g < C::G; ++g)
-              tmem_cp_32x128b_x4(sf_col + 16 * g + 4 * c,
-                                 sdesc_sf(smem_u32(sb + C::OFF_SFW + g * C::SFW + c * 512)));
-            tmem_cp_32x128b_x4(sfa_col + 4 * c, sdesc_sf(smem_u32(sb + C::OFF_SFA + c * 512)));
-          }
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
             const uint64_t bdesc = sdesc_sw128(smem_u32(sb + C::OFF_B) + 32 * c);
 #pragma unroll
             for (int g = 0; g < C::G; ++g) {
@@ -316,10 +310,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       mbar_drain(drain, 0);
     }
     __syncwarp();
-  } else if (warp == kSfWarp) {
-    // ------------------------------------------------------ scale transposer
-    // Raw token scales: row n (0..BN-1) holds 16 bytes = 4 slices x 4 blocks.
-    // Atom of slice c: byte 16 i + 4 j + b = row 32 j + i, block 4 c + b.
+  } else if (warp >= kSfWarp0) {
+    // --------------------------------------------------------- scale writers
+    // Weight atom of slice c: byte 16 i + 4 j + b = row 32 j + i, block 4c + b;
+    // lane i writes word j to column (4c + j) of lane quarter*32 + i.  Token
+    // scales arrive row-major (row n: 16 bytes = 4 slices x 4 blocks) and are
+    // regrouped the same way in registers.
+    const int q = warp & 3;
+    const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
@@ -329,19 +327,28 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           ok = false;
           break;
         }
-        uint8_t* sb = smem + stage * C::STAGE;
+        const uint8_t* sb = smem + stage * C::STAGE;
+        const uint32_t sf_col = tmem + lane_off + C::SF_COL0 + stage * C::SF_COLS;
+#pragma unroll
+        for (int g = 0; g < C::G; ++g) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const uint4 a = reinterpret_cast<const uint4*>(sb + C::OFF_SFW + g * C::SFW + c * 512)[lane];
+            tmem_st_32x32b_x4(sf_col + 16 * g + 4 * c, a.x, a.y, a.z, a.w);
+          }
+        }
         const uint4* raw = reinterpret_cast<const uint4*>(sb + C::OFF_SFA_RAW);
         uint4 r[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j)
           r[j] = (32 * j + lane < BN) ? raw[32 * j + lane] : make_uint4(0u, 0u, 0u, 0u);
-        uint4* atom = reinterpret_cast<uint4*>(sb + C::OFF_SFA);
-        atom[0 * 32 + lane] = make_uint4(r[0].x, r[1].x, r[2].x, r[3].x);
-        atom[1 * 32 + lane] = make_uint4(r[0].y, r[1].y, r[2].y, r[3].y);
-        atom[2 * 32 + lane] = make_uint4(r[0].z, r[1].z, r[2].z, r[3].z);
-        atom[3 * 32 + lane] = make_uint4(r[0].w, r[1].w, r[2].w, r[3].w);
-        // make the generic-proxy stores visible to tcgen05.cp (async proxy)
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        const uint32_t sfa_col = sf_col + 16 * C::G;
+        tmem_st_32x32b_x4(sfa_col + 0, r[0].x, r[1].x, r[2].x, r[3].x);
+        tmem_st_32x32b_x4(sfa_col + 4, r[0].y, r[1].y, r[2].y, r[3].y);
+        tmem_st_32x32b_x4(sfa_col + 8, r[0].z, r[1].z, r[2].z, r[3].z);
+        tmem_st_32x32b_x4(sfa_col + 12, r[0].w, r[1].w, r[2].w, r[3].w);
+        tmem_st_wait();
+        tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&sf_ready[stage]);
         if (++stage == STAGES) {
