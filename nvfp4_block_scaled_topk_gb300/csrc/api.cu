@@ -116,7 +116,7 @@ megamoe_status megamoe_route_permute(const int32_t* topk_ids, int T, int k, int 
   const int64_t need = megamoe_max_padded_rows(T, k, E, pad);
   if (row_capacity < need || (row_capacity > 0 && !row_src)) return MEGAMOE_ERR_INVALID_ARG;
   return cuda_status(launch_route(topk_ids, T * k, E, pad, counts, offsets, padded_offsets,
-                                  row_src, row_capacity, slot_dst, status,
+                                  row_src, row_capacity, slot_dst, status, nullptr, 0,
                                   reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -143,7 +143,7 @@ megamoe_status megamoe_quantize_nvfp4(const uint16_t* x, int64_t rows, int K, in
     return MEGAMOE_ERR_UNSUPPORTED_SHAPE;
   const float* amax = amax_in;
   if (!amax_in) {
-    cudaError_t e = launch_amax(x, rows, K, ld, amax_out, status, s);
+    cudaError_t e = launch_amax(x, rows, K, ld, amax_out, status, true, s);
     if (e != cudaSuccess) return MEGAMOE_ERR_CUDA;
     amax = amax_out;
   } else if (amax_out && amax_out != amax_in) {
@@ -259,18 +259,18 @@ megamoe_status megamoe_forward(const megamoe_weights* w, const uint16_t* x,
   Workspace wk = carve(ws, T, k, E, d, I, pad);
   if (ws_bytes < wk.bytes) return MEGAMOE_ERR_WORKSPACE_TOO_SMALL;
 
-  if (cudaMemsetAsync(wk.status, 0, 256, s) != cudaSuccess) return MEGAMOE_ERR_CUDA;
-  if (T == 0) return MEGAMOE_OK;
+  if (T == 0) return cudaMemsetAsync(wk.status, 0, 256, s) == cudaSuccess ? MEGAMOE_OK
+                                                                         : MEGAMOE_ERR_CUDA;
   const double expected = static_cast<double>(T) * k / E;
   const int tile_n = pick_tile_n(expected);
 
   cudaError_t e;
-  // 1. route
+  // 1. route; its first act clears the status word and the amax accumulators
   e = launch_route(topk_ids, T * k, E, pad, wk.counts, wk.offsets, wk.padded_offsets, wk.row_src,
-                   wk.rows, wk.slot_dst, wk.status, s);
+                   wk.rows, wk.slot_dst, wk.status, wk.status, 5, s);
   if (e != cudaSuccess) return MEGAMOE_ERR_CUDA;
   // 2-3. amax of x, then quantise x into its routed rows (padding rows zeroed)
-  e = launch_amax(x, T, d, d, wk.amax_x, wk.status, s);
+  e = launch_amax(x, T, d, d, wk.amax_x, wk.status, false, s);
   if (e != cudaSuccess) return MEGAMOE_ERR_CUDA;
   e = launch_quant(x, T, d, d, wk.slot_dst, k, wk.row_src, wk.padded_offsets + E, wk.rows,
                    wk.amax_x, wk.gs_x, wk.xq_codes, wk.xq_sf, MEGAMOE_SCALES_ROWMAJOR, s);
@@ -295,6 +295,7 @@ megamoe_status megamoe_forward(const megamoe_weights* w, const uint16_t* x,
   g.out_amax = wk.amax_h;
   g.tile_n = tile_n;
   g.status = wk.status;
+  g.zero_amax = false;
   e = launch_grouped_gemm(g, s);
   if (e != cudaSuccess) return MEGAMOE_ERR_CUDA;
   // 5. requantise h with gs from amax(h)

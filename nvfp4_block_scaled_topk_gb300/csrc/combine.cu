@@ -15,6 +15,8 @@ __global__ void __launch_bounds__(256) k_combine(const float* __restrict__ y, in
                                                  const int32_t* __restrict__ slot_dst,
                                                  const float* __restrict__ w, int T, int k, int d,
                                                  uint16_t* __restrict__ out) {
+  pdl_wait();
+  pdl_trigger();
   const int vecs = d / 4;
   const int64_t total = static_cast<int64_t>(T) * vecs;
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
@@ -47,8 +49,8 @@ cudaError_t launch_combine(const float* y, int64_t ld_y, const int32_t* slot_dst
   if (tasks == 0) return cudaSuccess;
   int64_t blocks = (tasks + 255) / 256;
   if (blocks > 152 * 16) blocks = 152 * 16;
-  k_combine<<<static_cast<int>(blocks), 256, 0, stream>>>(y, ld_y, slot_dst, w, T, k, d, out);
-  return cudaGetLastError();
+  return launch_pdl(k_combine, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, y, ld_y,
+                    slot_dst, w, T, k, d, out);
 }
 
 }  // namespace megamoe

@@ -29,6 +29,14 @@ __device__ __forceinline__ uint64_t globaltimer() {
   return t;
 }
 
+// Programmatic dependent launch: wait until the preceding kernel in the stream
+// has completed and its memory is visible (call before touching global
+// memory), and let the next kernel be scheduled early (it still waits).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ void set_status(uint32_t* status, uint32_t bits) {
   if (status) atomicOr(status, bits);
 }

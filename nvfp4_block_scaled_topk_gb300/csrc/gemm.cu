@@ -181,6 +181,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const int KT = K / 256;
   const int slices = K / 64;
 
+  if (warp == 0 && lane == 0) {
+    prefetch_tensormap(&tm_w);
+    prefetch_tensormap(&tm_a);
+    prefetch_tensormap(&tm_asf);
+  }
+  pdl_wait();  // the routing offsets and activations come from earlier kernels
+  pdl_trigger();
   build_tile_offsets<BN>(p.offsets, E, MT, s_toff, s_scan);
   const int total = s_toff[E];
   if (static_cast<int>(blockIdx.x) >= total) return;  // uniform: no work for this CTA
@@ -202,11 +209,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   if (warp == 1) {
     tmem_alloc(tmem_holder, 512);
     tmem_relinquish();
-  }
-  if (warp == 0 && lane == 0) {
-    prefetch_tensormap(&tm_w);
-    prefetch_tensormap(&tm_a);
-    prefetch_tensormap(&tm_asf);
   }
   tc_fence_before();
   __syncthreads();
@@ -493,8 +495,8 @@ static cudaError_t launch_cfg(const CUtensorMap& tm_w, const CUtensorMap& tm_a,
   cudaError_t err =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (err != cudaSuccess) return err;
-  kern<<<num_sms(), kGemmThreads, C::SMEM, stream>>>(tm_w, tm_a, tm_asf, a);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(num_sms()), dim3(kGemmThreads), C::SMEM, stream, tm_w, tm_a, tm_asf,
+                    a);
 }
 
 int pick_tile_n(double expected) {
@@ -515,7 +517,7 @@ cudaError_t launch_grouped_gemm(const GemmLaunch& g, cudaStream_t stream) {
   GemmArgs a{g.w_scales, g.w_gs,     g.act_gs, g.offsets, g.padded_offsets, g.out,
              g.ld_out,   g.out_amax, g.status, g.E,       g.N,              g.K};
   if (g.epilogue == MEGAMOE_EPI_SILU_MUL) {
-    if (g.out_amax) {
+    if (g.out_amax && g.zero_amax) {
       cudaError_t err = cudaMemsetAsync(g.out_amax, 0, sizeof(float), stream);
       if (err != cudaSuccess) return err;
     }

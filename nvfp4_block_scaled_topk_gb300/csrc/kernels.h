@@ -7,14 +7,36 @@
 
 namespace megamoe {
 
+// Launch on `stream` with programmatic stream serialization: the kernel may be
+// scheduled while its predecessor finishes; every kernel of this library
+// executes griddepcontrol.wait before touching global memory.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 size_t route_smem_bytes(int E);
+// zero_words (may be null): n_zero 32-bit words cleared before anything else
+// (the forward's status word and amax accumulators).
 cudaError_t launch_route(const int32_t* ids, int n_slots, int E, int pad, int32_t* counts,
                          int32_t* offsets, int32_t* padded_offsets, int32_t* row_src,
                          int64_t row_capacity, int32_t* slot_dst, uint32_t* status,
-                         cudaStream_t stream);
+                         uint32_t* zero_words, int n_zero, cudaStream_t stream);
 
+// zero_first: clear *amax first (false when the caller already cleared it).
 cudaError_t launch_amax(const uint16_t* x, int64_t rows, int K, int64_t ld, float* amax,
-                        uint32_t* status, cudaStream_t stream);
+                        uint32_t* status, bool zero_first, cudaStream_t stream);
 cudaError_t launch_quant(const uint16_t* x, int64_t rows_in, int K, int64_t ld,
                          const int32_t* slot_dst, int k, const int32_t* row_src,
                          const int32_t* live_rows, int64_t out_rows, const float* amax,
@@ -43,6 +65,7 @@ struct GemmLaunch {
   float* out_amax;
   int tile_n;
   uint32_t* status;
+  bool zero_amax = true;  // false when the caller already cleared out_amax
 };
 // Encodes the tensor maps and launches the persistent grouped GEMM.
 cudaError_t launch_grouped_gemm(const GemmLaunch& g, cudaStream_t stream);

@@ -26,6 +26,8 @@ namespace megamoe {
 
 __global__ void __launch_bounds__(256) k_amax(const uint16_t* __restrict__ x, int64_t rows, int K,
                                               int64_t ld, float* amax, uint32_t* status) {
+  pdl_wait();
+  pdl_trigger();
   const int vecs = K / 8;
   const int64_t total = rows * vecs;
   uint32_t m2 = 0;  // two packed |bf16| maxima
@@ -129,6 +131,8 @@ __device__ __forceinline__ void store_slice(const QuantArgs& a, int64_t out_row,
 // without slot_dst, [0, out_rows*S) map out row r <- x row r (padding rows
 // zeroed).  S = K/64 slices per row.
 __global__ void __launch_bounds__(256) k_quant(const QuantArgs a) {
+  pdl_wait();
+  pdl_trigger();
   const int S = a.K / 64;
   const float amax = *a.amax;
   const float gs = amax == 0.f ? 1.f : __fdiv_rn(2688.0f, amax);
@@ -171,6 +175,8 @@ __global__ void __launch_bounds__(256) k_quant(const QuantArgs a) {
 
 __global__ void __launch_bounds__(256) k_swizzle(const uint8_t* __restrict__ src, int64_t rows,
                                                  int K, uint8_t* __restrict__ dst) {
+  pdl_wait();
+  pdl_trigger();
   const int S = K / 64;
   const int64_t rows_pad = (rows + 127) / 128 * 128;
   const int64_t total = rows_pad * S;
@@ -186,6 +192,8 @@ __global__ void __launch_bounds__(256) k_swizzle(const uint8_t* __restrict__ src
 
 __global__ void __launch_bounds__(256) k_pack(const uint8_t* __restrict__ src, int64_t rows, int K,
                                               uint8_t* __restrict__ dst) {
+  pdl_wait();
+  pdl_trigger();
   const int chunks = K / 32;  // 16-byte chunks per row
   const int KT = K / 256;     // 128-byte K blocks per row
   const int64_t total = rows * chunks;
@@ -209,11 +217,14 @@ static int grid_for(int64_t tasks, int threads) {
 }
 
 cudaError_t launch_amax(const uint16_t* x, int64_t rows, int K, int64_t ld, float* amax,
-                        uint32_t* status, cudaStream_t stream) {
-  cudaError_t err = cudaMemsetAsync(amax, 0, sizeof(float), stream);
-  if (err != cudaSuccess || rows == 0) return err;
-  k_amax<<<grid_for(rows * (K / 8), 256), 256, 0, stream>>>(x, rows, K, ld, amax, status);
-  return cudaGetLastError();
+                        uint32_t* status, bool zero_first, cudaStream_t stream) {
+  if (zero_first) {
+    cudaError_t err = cudaMemsetAsync(amax, 0, sizeof(float), stream);
+    if (err != cudaSuccess) return err;
+  }
+  if (rows == 0) return cudaSuccess;
+  return launch_pdl(k_amax, dim3(grid_for(rows * (K / 8), 256)), dim3(256), 0, stream, x, rows,
+                    K, ld, amax, status);
 }
 
 cudaError_t launch_quant(const uint16_t* x, int64_t rows_in, int K, int64_t ld,
@@ -224,24 +235,22 @@ cudaError_t launch_quant(const uint16_t* x, int64_t rows_in, int K, int64_t ld,
   QuantArgs a{x, rows_in, K, ld, slot_dst, k, row_src, live_rows, out_rows, amax,
               gs_out, codes, scales, scale_layout};
   const int64_t tasks = ((slot_dst ? rows_in : 0) + out_rows) * (K / 64);
-  k_quant<<<grid_for(tasks, 256), 256, 0, stream>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(k_quant, dim3(grid_for(tasks, 256)), dim3(256), 0, stream, a);
 }
 
 cudaError_t launch_swizzle(const uint8_t* src, int64_t rows, int K, uint8_t* dst,
                            cudaStream_t stream) {
   const int64_t tasks = (rows + 127) / 128 * 128 * (K / 64);
   if (tasks == 0) return cudaSuccess;
-  k_swizzle<<<grid_for(tasks, 256), 256, 0, stream>>>(src, rows, K, dst);
-  return cudaGetLastError();
+  return launch_pdl(k_swizzle, dim3(grid_for(tasks, 256)), dim3(256), 0, stream, src, rows, K,
+                    dst);
 }
 
 cudaError_t launch_pack(const uint8_t* src, int64_t rows, int K, uint8_t* dst,
                         cudaStream_t stream) {
   const int64_t tasks = rows * (K / 32);
   if (tasks == 0) return cudaSuccess;
-  k_pack<<<grid_for(tasks, 256), 256, 0, stream>>>(src, rows, K, dst);
-  return cudaGetLastError();
+  return launch_pdl(k_pack, dim3(grid_for(tasks, 256)), dim3(256), 0, stream, src, rows, K, dst);
 }
 
 }  // namespace megamoe

@@ -54,7 +54,7 @@ __device__ __forceinline__ int block_exclusive_scan_1024(int v, int* warp_sums, 
 __global__ void __launch_bounds__(kRouteThreads, 1)
     k_route(const int32_t* __restrict__ ids, int n_slots, int E, int pad, int32_t* counts,
             int32_t* offsets, int32_t* padded_offsets, int32_t* row_src, int64_t row_capacity,
-            int32_t* slot_dst, uint32_t* status) {
+            int32_t* slot_dst, uint32_t* status, uint32_t* zero_words, int n_zero) {
   extern __shared__ int smem_route[];
   int* hist = smem_route;                       // [32][E]
   int* s_poff = hist + kRouteWarps * E;         // [E+1]
@@ -63,6 +63,9 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
   __shared__ int totals[2];
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  pdl_wait();
+  pdl_trigger();
+  if (tid < n_zero) zero_words[tid] = 0u;
   for (int i = tid; i < kRouteWarps * E; i += kRouteThreads) hist[i] = 0;
   __syncthreads();
 
@@ -144,15 +147,14 @@ size_t route_smem_bytes(int E) { return sizeof(int) * (static_cast<size_t>(kRout
 cudaError_t launch_route(const int32_t* ids, int n_slots, int E, int pad, int32_t* counts,
                          int32_t* offsets, int32_t* padded_offsets, int32_t* row_src,
                          int64_t row_capacity, int32_t* slot_dst, uint32_t* status,
-                         cudaStream_t stream) {
+                         uint32_t* zero_words, int n_zero, cudaStream_t stream) {
   const size_t smem = route_smem_bytes(E);
   cudaError_t err = cudaFuncSetAttribute(k_route, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
   if (err != cudaSuccess) return err;
-  k_route<<<1, kRouteThreads, smem, stream>>>(ids, n_slots, E, pad, counts, offsets,
-                                              padded_offsets, row_src, row_capacity, slot_dst,
-                                              status);
-  return cudaGetLastError();
+  return launch_pdl(k_route, dim3(1), dim3(kRouteThreads), smem, stream, ids, n_slots, E, pad,
+                    counts, offsets, padded_offsets, row_src, row_capacity, slot_dst, status,
+                    zero_words, n_zero);
 }
 
 }  // namespace megamoe
