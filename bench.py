@@ -108,16 +108,22 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def _profile_traffic(kernel_src: str, name: str):
-    """DRAM bytes per launch from a committed ncu summary, if the kernel source
-    is unchanged since the capture (else None)."""
-    path = os.path.join(ROOT, "profiles", name)
+def kernel_source_hash() -> str:
+    """sha256 (16 hex digits) of the grouped-GEMM kernel sources."""
+    h = hashlib.sha256()
+    for name in ("gemm.cu", "common.cuh"):
+        with open(os.path.join(ROOT, "nvfp4_block_scaled_topk_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def _profile_traffic(name: str):
+    """DRAM bytes per launch from a committed ncu summary, if the kernel
+    sources are unchanged since the capture (else None)."""
     try:
-        with open(path) as f:
+        with open(os.path.join(ROOT, "profiles", name)) as f:
             prof = json.load(f)
-        with open(kernel_src, "rb") as f:
-            h = hashlib.sha256(f.read()).hexdigest()[:16]
-        if prof.get("source_sha256_16") != h:
+        if prof.get("source_sha256_16") != kernel_source_hash():
             return None
         return prof.get("dram_bytes_per_launch")
     except Exception:
@@ -328,8 +334,7 @@ def run_ours(args):
     w_el = cfg.d * cfg.I * (0.5 + 1.0 / 16)
     l1_bytes = active * 2 * w_el + valid_slots * cfg.d * (0.5 + 1 / 16) + valid_slots * cfg.I * 2
     l1_gbs = l1_bytes / (l1_ms * 1e-3) / 1e9
-    traffic = _profile_traffic(os.path.join(ROOT, "nvfp4_block_scaled_topk_gb300", "csrc",
-                                            "gemm.cu"), f"l1_gemm_{cfg.name}.json")
+    traffic = _profile_traffic(f"l1_gemm_{cfg.name}.json")
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
