@@ -151,6 +151,18 @@ def oracle_sample(cfg, x, ids, w, experts_src, tokens: int):
     return dt
 
 
+def max_over_ranks(values, world: int, device="cpu"):
+    """Element-wise maximum of `values` over all ranks (identity at world 1)."""
+    if world <= 1:
+        return [float(v) for v in values]
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
 def _cores():
     try:
         return len(os.sched_getaffinity(0))
@@ -319,12 +331,7 @@ def run_ours(args):
     d2h = out_h.numel() * 2
 
     # ---- max over ranks
-    if world > 1:
-        import torch.distributed as dist
-
-        t = torch.tensor([ms, e2e_ms, l1_ms, l2_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms, e2e_ms, l1_ms, l2_ms = t.tolist()
+    ms, e2e_ms, l1_ms, l2_ms = max_over_ranks([ms, e2e_ms, l1_ms, l2_ms], world, dev)
 
     hbm_gbs, bf16_tf, peak_kind = _peaks()
     tokens_total = cfg.T * world

@@ -85,11 +85,11 @@ typedef enum megamoe_status {
  * NVFP4 expert weights.  Expert e of W13 is [2I, d]: rows 0..I-1 are the gate
  * projection, rows I..2I-1 the up projection ("What's Been Verified": L1
  * gate+up).  W2 is [d, I] per expert (L2 down).
- *   w13_codes   tile-major layout of [E*2I, d/2] E2M1 codes (from
- *               megamoe_pack_weight_codes)
+ *   w13_codes   [E*2I, d/2] E2M1 codes packed by megamoe_pack_weight_codes
+ *               with half_rows = I
  *   w13_scales  atom layout of [E*2I, d/16] (from megamoe_swizzle_scales)
  *   w13_gs      [E, 2] float            global scales (gate, up)
- *   w2_codes    tile-major layout of [E*d, I/2]
+ *   w2_codes    [E*d, I/2] packed by megamoe_pack_weight_codes, half_rows = 0
  *   w2_scales   atom layout of [E*d, I/16]
  *   w2_gs       [E] float
  * Supported: 1 <= E <= 1024, d and I multiples of 256.
@@ -182,14 +182,19 @@ megamoe_status megamoe_swizzle_scales(const uint8_t* src, int64_t rows, int K, u
 
 /*
  * megamoe_pack_weight_codes -- one-time weight preparation: row-major E2M1
- * codes [rows, K/2] -> tile-major layout: blocks of 128 rows x 128 bytes
- * (256 elements of K), ordered [rows/128][K/256], each block row-major.  Row
- * r, bytes 128t .. 128t+127 land at ((r/128)*(K/256) + t)*16384 + (r%128)*128.
- * Every weight tile the grouped GEMM loads is then one contiguous 16 KB read.
- * Requires rows a multiple of 128, K a multiple of 256, 16-byte alignment.
+ * codes [rows, K/2] -> tile-major blocks of 128 rows x 128 bytes (256
+ * elements of K), each block row-major (row r%128 at byte (r%128)*128).
+ *   half_rows == 0: blocks ordered [rows/128][K/256] (the W2 layout).
+ *   half_rows == H: rows come in groups of 2H, H gate rows then H up rows (one
+ *                   expert of W13, H = I); the gate and up blocks of the same
+ *                   128 features and K step are adjacent:
+ *                   [rows/2H][H/128][K/256][gate, up] (the W13 layout).
+ * A stage of the grouped GEMM then reads one contiguous 16 KB (W2) or 32 KB
+ * (W13) block.  Requires rows a multiple of 128 (of 2H when H > 0), H a
+ * multiple of 128, K a multiple of 256, 16-byte alignment.
  */
-megamoe_status megamoe_pack_weight_codes(const uint8_t* src, int64_t rows, int K, uint8_t* dst,
-                                         megamoe_stream_t stream);
+megamoe_status megamoe_pack_weight_codes(const uint8_t* src, int64_t rows, int K, int half_rows,
+                                         uint8_t* dst, megamoe_stream_t stream);
 
 /*
  * megamoe_grouped_gemm -- one persistent grouped block-scaled GEMM over all
@@ -203,7 +208,8 @@ megamoe_status megamoe_pack_weight_codes(const uint8_t* src, int64_t rows, int K
  *   acc[r, n] = sum_K dequant(act)[r, :] . dequant(w_e)[n, :]   (fp32 accumulate)
  *   act_codes   [act_rows, K/2]; act_scales row-major [act_rows, K/16];
  *               act_gs device float (one global scale)
- *   w_codes     tile-major layout of [E*N, K/2] (megamoe_pack_weight_codes);
+ *   w_codes     [E*N, K/2] packed by megamoe_pack_weight_codes (half_rows =
+ *               N/2 for MEGAMOE_EPI_SILU_MUL, 0 for MEGAMOE_EPI_F32);
  *               w_scales atom layout of [E*N, K/16] (megamoe_swizzle_scales)
  *   w_gs        [E, G] float: G = 1 for MEGAMOE_EPI_F32; G = 2 (gate, up) for
  *               MEGAMOE_EPI_SILU_MUL
@@ -269,6 +275,17 @@ megamoe_status megamoe_forward(const megamoe_weights* w, const uint16_t* x,
                                const int32_t* topk_ids, const float* topk_weights, int T, int k,
                                int pad, uint16_t* out, void* ws, size_t ws_bytes,
                                megamoe_stream_t stream);
+
+/*
+ * megamoe_set_wait_limit_ns -- bound of every pipeline wait inside the
+ * grouped GEMM kernels launched afterwards (host setting of this library,
+ * all devices; 0 restores the default of 4 s).  A wait that runs out raises
+ * the kernel's abort flag and MEGAMOE_DEV_TIMEOUT; the kernel then lets its
+ * copies and MMAs in flight land (waiting up to 4 s), frees its tensor memory
+ * and returns, so the context stays usable.  For failure-detection tests and
+ * diagnosis; the default never fires in normal operation.
+ */
+void megamoe_set_wait_limit_ns(uint64_t ns);
 
 /*
  * megamoe_read_status -- synchronise `stream`, copy the device status word at

@@ -164,13 +164,16 @@ megamoe_status megamoe_swizzle_scales(const uint8_t* src, int64_t rows, int K, u
   return cuda_status(launch_swizzle(src, rows, K, dst, reinterpret_cast<cudaStream_t>(stream)));
 }
 
-megamoe_status megamoe_pack_weight_codes(const uint8_t* src, int64_t rows, int K, uint8_t* dst,
-                                        megamoe_stream_t stream) {
-  if (rows < 0 || K <= 0) return MEGAMOE_ERR_INVALID_ARG;
+megamoe_status megamoe_pack_weight_codes(const uint8_t* src, int64_t rows, int K, int half_rows,
+                                         uint8_t* dst, megamoe_stream_t stream) {
+  if (rows < 0 || K <= 0 || half_rows < 0) return MEGAMOE_ERR_INVALID_ARG;
   if (K % 256 != 0 || rows % 128 != 0) return MEGAMOE_ERR_UNSUPPORTED_SHAPE;
+  if (half_rows > 0 && (half_rows % 128 != 0 || rows % (2 * static_cast<int64_t>(half_rows))))
+    return MEGAMOE_ERR_UNSUPPORTED_SHAPE;
   if (rows > 0 && (!src || !dst)) return MEGAMOE_ERR_INVALID_ARG;
   if (rows > 0 && (!aligned(src, 16) || !aligned(dst, 16))) return MEGAMOE_ERR_UNSUPPORTED_SHAPE;
-  return cuda_status(launch_pack(src, rows, K, dst, reinterpret_cast<cudaStream_t>(stream)));
+  return cuda_status(
+      launch_pack(src, rows, K, half_rows, dst, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 megamoe_status megamoe_grouped_gemm(const uint8_t* act_codes, const uint8_t* act_scales,
@@ -321,6 +324,8 @@ megamoe_status megamoe_forward(const megamoe_weights* w, const uint16_t* x,
   e = launch_combine(wk.y, d, wk.slot_dst, topk_weights, T, k, d, out, s);
   return cuda_status(e);
 }
+
+void megamoe_set_wait_limit_ns(uint64_t ns) { set_wait_limit_ns(ns); }
 
 megamoe_status megamoe_read_status(const uint32_t* status, uint32_t* bits,
                                    megamoe_stream_t stream) {

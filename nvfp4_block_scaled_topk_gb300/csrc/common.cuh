@@ -76,16 +76,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Wait until the phase with parity `parity` of `bar` has completed.  Returns
-// false if the abort flag was raised or the wait ran past kWaitTimeoutNs (in
-// which case the abort flag is raised here and `status` gets the TIMEOUT bit).
+// false if the abort flag was raised or the wait ran past `limit_ns` (in which
+// case the abort flag is raised here and `status` gets the TIMEOUT bit).
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                          uint32_t* status) {
+                                          uint32_t* status, uint64_t limit_ns = kWaitTimeoutNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort_flag) return false;
-    if (globaltimer() - t0 > kWaitTimeoutNs) {
+    if (globaltimer() - t0 > limit_ns) {
       *abort_flag = 1;
       set_status(status, MEGAMOE_DEV_TIMEOUT);
       return false;

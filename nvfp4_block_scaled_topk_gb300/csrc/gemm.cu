@@ -29,9 +29,10 @@
 //               token tile's first row always lands in the first scale
 //               column whatever row the tile starts at.
 // Every expert's weights live in one tensor (tile-major: blocks of 128 rows x
-// 128 bytes, [E*N/128][K/256] blocks), so one tensor map serves all experts:
-// the expert is a coordinate, not a new descriptor, and every weight box is
-// one contiguous 16 KB read.
+// 128 bytes, [E*N/128][K/256] blocks; for L1 the gate and up blocks of the
+// same features and K step are adjacent), so one tensor map serves all
+// experts: the expert is a coordinate, not a new descriptor, and a stage's
+// weights are one contiguous 16 KB (L2) or 32 KB (L1) read.
 // Tiles are numbered expert-major, weight-tile-major, token-tile-minor, so CTAs
 // working on the same expert's weight tile run together and share it in L2.
 #include <cuda.h>
@@ -59,6 +60,7 @@ struct GemmArgs {
   int64_t ld_out;
   float* out_amax;
   uint32_t* status;
+  uint64_t wait_limit_ns;  // bound of every pipeline wait (unwinding waits use 4 s)
   int E, N, K;
 };
 
@@ -229,22 +231,24 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const TileInfo ti = decode_tile<BN>(tile, s_toff, E, p.offsets, p.padded_offsets);
         const int w_row0 = ti.e * N + ti.mt * 128;
         const int w_row1 = ti.e * N + N / 2 + ti.mt * 128;  // up rows (L1 only)
+        // first 128-row code block of this tile's K = 0 step (paired for L1)
+        const int w_blk0 = C::G == 2 ? ((ti.e * MT + ti.mt) * KT) * 2 : (w_row0 >> 7) * KT;
         const int a_row0 = ti.poff + ti.nt * BN;
         for (int kt = 0; kt < KT; ++kt) {
-          if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.status)) {
+          if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.status, p.wait_limit_ns)) {
             ok = false;
             break;
           }
           uint8_t* sb = smem + stage * C::STAGE;
           mbar_arrive_expect_tx(&full[stage], C::TX);
-          tma_load_2d(sb + C::OFF_A, &tm_w, &full[stage], 0, ((w_row0 >> 7) * KT + kt) * 128,
+          tma_load_2d(sb + C::OFF_A, &tm_w, &full[stage], 0, (w_blk0 + kt * C::G) * 128,
                       pol_w);
           bulk_load(sb + C::OFF_SFW,
                     p.w_sf + (static_cast<int64_t>(w_row0 >> 7) * slices + 4 * kt) * 512, C::SFW,
                     &full[stage], pol_w);
           if (C::G == 2) {
             tma_load_2d(sb + C::OFF_A + C::A_TILE, &tm_w, &full[stage], 0,
-                        ((w_row1 >> 7) * KT + kt) * 128, pol_w);
+                        (w_blk0 + kt * 2 + 1) * 128, pol_w);
             bulk_load(sb + C::OFF_SFW + C::SFW,
                       p.w_sf + (static_cast<int64_t>(w_row1 >> 7) * slices + 4 * kt) * 512,
                       C::SFW, &full[stage], pol_w);
@@ -271,12 +275,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
-        if (!mbar_wait(&acc_empty[acc], acc_phase ^ 1u, abort_flag, p.status)) break;
+        if (!mbar_wait(&acc_empty[acc], acc_phase ^ 1u, abort_flag, p.status, p.wait_limit_ns)) break;
         tc_fence_after();
         const uint32_t d_col = tmem + acc * C::ACC_COLS;
         for (int kt = 0; kt < KT; ++kt) {
-          if (!mbar_wait(&full[stage], phase, abort_flag, p.status) ||
-              !mbar_wait(&sf_ready[stage], phase, abort_flag, p.status)) {
+          if (!mbar_wait(&full[stage], phase, abort_flag, p.status, p.wait_limit_ns) ||
+              !mbar_wait(&sf_ready[stage], phase, abort_flag, p.status, p.wait_limit_ns)) {
             ok = false;
             break;
           }
@@ -325,7 +329,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     bool ok = true;
     for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
       for (int kt = 0; kt < KT; ++kt) {
-        if (!mbar_wait(&full[stage], phase, abort_flag, p.status)) {
+        if (!mbar_wait(&full[stage], phase, abort_flag, p.status, p.wait_limit_ns)) {
           ok = false;
           break;
         }
@@ -378,7 +382,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       } else {
         alpha0 = 1.0f / (a_gs * __ldg(p.w_gs + ti.e));
       }
-      if (!mbar_wait(&acc_full[acc], acc_phase, abort_flag, p.status)) break;
+      if (!mbar_wait(&acc_full[acc], acc_phase, abort_flag, p.status, p.wait_limit_ns)) break;
       tc_fence_after();
       const uint32_t lane_base =
           tmem + acc * C::ACC_COLS + (static_cast<uint32_t>(q * 32) << 16);
@@ -499,6 +503,11 @@ static cudaError_t launch_cfg(const CUtensorMap& tm_w, const CUtensorMap& tm_a,
                     a);
 }
 
+static uint64_t g_wait_limit_ns = kWaitTimeoutNs;
+
+void set_wait_limit_ns(uint64_t ns) { g_wait_limit_ns = ns ? ns : kWaitTimeoutNs; }
+uint64_t wait_limit_ns() { return g_wait_limit_ns; }
+
 int pick_tile_n(double expected) {
   if (expected <= 32.0) return 32;
   if (expected <= 96.0) return 64;
@@ -514,8 +523,9 @@ cudaError_t launch_grouped_gemm(const GemmLaunch& g, cudaStream_t stream) {
       !make_codes_map(&tm_a, g.act_codes, static_cast<uint64_t>(g.act_rows), g.K / 2, bn) ||
       !make_scales_map(&tm_asf, g.act_scales, static_cast<uint64_t>(g.act_rows), g.K / 16, bn))
     return cudaErrorInvalidValue;
-  GemmArgs a{g.w_scales, g.w_gs,     g.act_gs, g.offsets, g.padded_offsets, g.out,
-             g.ld_out,   g.out_amax, g.status, g.E,       g.N,              g.K};
+  GemmArgs a{g.w_scales, g.w_gs,     g.act_gs, g.offsets,         g.padded_offsets, g.out,
+             g.ld_out,   g.out_amax, g.status, wait_limit_ns(), g.E,             g.N,
+             g.K};
   if (g.epilogue == MEGAMOE_EPI_SILU_MUL) {
     if (g.out_amax && g.zero_amax) {
       cudaError_t err = cudaMemsetAsync(g.out_amax, 0, sizeof(float), stream);

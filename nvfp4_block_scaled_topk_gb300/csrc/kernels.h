@@ -45,7 +45,7 @@ cudaError_t launch_quant(const uint16_t* x, int64_t rows_in, int K, int64_t ld,
 cudaError_t launch_swizzle(const uint8_t* src, int64_t rows, int K, uint8_t* dst,
                            cudaStream_t stream);
 
-cudaError_t launch_pack(const uint8_t* src, int64_t rows, int K, uint8_t* dst,
+cudaError_t launch_pack(const uint8_t* src, int64_t rows, int K, int half_rows, uint8_t* dst,
                         cudaStream_t stream);
 
 struct GemmLaunch {
@@ -53,7 +53,7 @@ struct GemmLaunch {
   const uint8_t* act_scales;  // atom layout
   const float* act_gs;
   int64_t act_rows;
-  const uint8_t* w_codes;   // tile-major (k_pack)
+  const uint8_t* w_codes;   // tile-major (k_pack; gate/up paired for SILU_MUL)
   const uint8_t* w_scales;  // atom layout
   const float* w_gs;
   int E, N, K;
@@ -70,6 +70,9 @@ struct GemmLaunch {
 // Encodes the tensor maps and launches the persistent grouped GEMM.
 cudaError_t launch_grouped_gemm(const GemmLaunch& g, cudaStream_t stream);
 int pick_tile_n(double expected_tokens_per_expert);
+// Bound of the grouped GEMM's pipeline waits (0 restores the default 4 s).
+void set_wait_limit_ns(uint64_t ns);
+uint64_t wait_limit_ns();
 
 cudaError_t launch_combine(const float* y, int64_t ld_y, const int32_t* slot_dst,
                            const float* w, int T, int k, int d, uint16_t* out,

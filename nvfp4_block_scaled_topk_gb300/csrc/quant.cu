@@ -190,8 +190,12 @@ __global__ void __launch_bounds__(256) k_swizzle(const uint8_t* __restrict__ src
   }
 }
 
+// half_rows == 0: blocks ordered [rows/128][K/256].  half_rows == H > 0: rows
+// come in groups of 2H (gate rows then up rows of one expert) and the gate and
+// up blocks of the same 128 features and K step sit side by side:
+// [group][H/128][K/256][gate, up], so the L1 GEMM reads 32 KB contiguous.
 __global__ void __launch_bounds__(256) k_pack(const uint8_t* __restrict__ src, int64_t rows, int K,
-                                              uint8_t* __restrict__ dst) {
+                                              int half_rows, uint8_t* __restrict__ dst) {
   pdl_wait();
   pdl_trigger();
   const int chunks = K / 32;  // 16-byte chunks per row
@@ -202,7 +206,17 @@ __global__ void __launch_bounds__(256) k_pack(const uint8_t* __restrict__ src, i
     const int64_t r = t / chunks;
     const int c = static_cast<int>(t - r * chunks);
     const int kt = c >> 3;
-    const int64_t o = (((r >> 7) * KT + kt) * 128 + (r & 127)) * 128 + (c & 7) * 16;
+    int64_t block;
+    if (half_rows > 0) {
+      const int64_t group = r / (2 * half_rows);
+      const int64_t in = r - group * 2 * half_rows;
+      const int g = in >= half_rows ? 1 : 0;
+      const int64_t mt = (in - g * half_rows) >> 7;
+      block = ((group * (half_rows >> 7) + mt) * KT + kt) * 2 + g;
+    } else {
+      block = (r >> 7) * KT + kt;
+    }
+    const int64_t o = (block * 128 + (r & 127)) * 128 + (c & 7) * 16;
     *reinterpret_cast<uint4*>(dst + o) =
         __ldg(reinterpret_cast<const uint4*>(src + r * (K / 2)) + c);
   }
@@ -246,11 +260,12 @@ cudaError_t launch_swizzle(const uint8_t* src, int64_t rows, int K, uint8_t* dst
                     dst);
 }
 
-cudaError_t launch_pack(const uint8_t* src, int64_t rows, int K, uint8_t* dst,
+cudaError_t launch_pack(const uint8_t* src, int64_t rows, int K, int half_rows, uint8_t* dst,
                         cudaStream_t stream) {
   const int64_t tasks = rows * (K / 32);
   if (tasks == 0) return cudaSuccess;
-  return launch_pdl(k_pack, dim3(grid_for(tasks, 256)), dim3(256), 0, stream, src, rows, K, dst);
+  return launch_pdl(k_pack, dim3(grid_for(tasks, 256)), dim3(256), 0, stream, src, rows, K,
+                    half_rows, dst);
 }
 
 }  // namespace megamoe

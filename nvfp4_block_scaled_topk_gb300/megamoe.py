@@ -40,7 +40,7 @@ SIGNATURES = {
     "megamoe_quantize_nvfp4": (_I, [_P, _I64, _I, _I64, _P, _I, _P, _P, _I64, _P, _P, _P, _P, _P,
                                     _I, _P, _P]),
     "megamoe_swizzle_scales": (_I, [_P, _I64, _I, _P, _P]),
-    "megamoe_pack_weight_codes": (_I, [_P, _I64, _I, _P, _P]),
+    "megamoe_pack_weight_codes": (_I, [_P, _I64, _I, _I, _P, _P]),
     "megamoe_grouped_gemm": (_I, [_P, _P, _P, _I64, _P, _P, _P, _I, _I, _I, _P, _P, _I, _P, _I64,
                                   _P, _I, ctypes.c_double, _P, _P]),
     "megamoe_combine": (_I, [_P, _I64, _P, _P, _I, _I, _I, _P, _P]),
@@ -48,6 +48,7 @@ SIGNATURES = {
     "megamoe_forward": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P, _SZ, _P]),
     "megamoe_read_status": (_I, [_P, _P, _P]),
     "megamoe_forward_static": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P, _P]),
+    "megamoe_set_wait_limit_ns": (None, [ctypes.c_uint64]),
 }
 
 
@@ -105,6 +106,11 @@ def max_padded_rows(T, k, E, pad):
 
 def workspace_size(T, k, E, d, I, pad):
     return int(load().megamoe_workspace_size(T, k, E, d, I, pad))
+
+
+def set_wait_limit_ns(ns: int):
+    """Bound of the grouped GEMM's pipeline waits (0 restores 4 s)."""
+    load().megamoe_set_wait_limit_ns(int(ns))
 
 
 def status_string(code):
@@ -171,13 +177,14 @@ def swizzle_scales(scales: torch.Tensor) -> torch.Tensor:
     return dst
 
 
-def pack_weight_codes(codes: torch.Tensor) -> torch.Tensor:
-    """Row-major [rows, K/2] E2M1 codes -> tile-major layout (weight preparation)."""
+def pack_weight_codes(codes: torch.Tensor, half_rows: int = 0) -> torch.Tensor:
+    """Row-major [rows, K/2] E2M1 codes -> tile-major layout (weight preparation);
+    half_rows = I pairs the gate and up blocks of W13."""
     _dev(codes, torch.uint8, "codes")
     rows, half = codes.shape
     dst = torch.empty_like(codes)
-    _check("megamoe_pack_weight_codes",
-           load().megamoe_pack_weight_codes(_p(codes), rows, half * 2, _p(dst), _stream()))
+    _check("megamoe_pack_weight_codes", load().megamoe_pack_weight_codes(
+        _p(codes), rows, half * 2, half_rows, _p(dst), _stream()))
     return dst
 
 
@@ -239,7 +246,7 @@ class Weights:
         d, I = half_d * 2, I2 // 2
         s13 = swizzle_scales(w["w13_scales"].reshape(E * I2, d // 16))
         s2 = swizzle_scales(w["w2_scales"].reshape(E * d, I // 16))
-        c13 = pack_weight_codes(w["w13_codes"].reshape(E * I2, d // 2)).view(E, I2, d // 2)
+        c13 = pack_weight_codes(w["w13_codes"].reshape(E * I2, d // 2), I).view(E, I2, d // 2)
         c2 = pack_weight_codes(w["w2_codes"].reshape(E * d, I // 2)).view(E, d, I // 2)
         return cls(E, d, I, c13, s13, w["w13_gs"].contiguous(), c2, s2,
                    w["w2_gs"].reshape(E).contiguous())

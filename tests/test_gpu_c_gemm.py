@@ -38,7 +38,7 @@ def _dev_weights(stacked, which, megamoe):
     if which == "w13":
         E, N, hk = stacked["w13_codes"].shape
         codes = megamoe.pack_weight_codes(
-            stacked["w13_codes"].reshape(E * N, hk).cuda()).view(E, N, hk)
+            stacked["w13_codes"].reshape(E * N, hk).cuda(), N // 2).view(E, N, hk)
         sc = megamoe.swizzle_scales(stacked["w13_scales"].reshape(E * N, hk // 8).cuda())
         gs = stacked["w13_gs"].cuda()
     else:
@@ -146,9 +146,15 @@ def test_pack_weight_codes_layout(cuda_lib):
     from nvfp4_block_scaled_topk_gb300 import megamoe
 
     rng = np.random.default_rng(70)
-    rows, K = 384, 768
+    rows, K = 512, 768
     c = rng.integers(0, 256, (rows, K // 2), dtype=np.uint8)
     got = megamoe.pack_weight_codes(torch.from_numpy(c).cuda()).cpu().numpy().reshape(-1)
     # blocks of 128 rows x 128 bytes, ordered [rows/128][K/256]
     want = c.reshape(rows // 128, 128, K // 256, 128).transpose(0, 2, 1, 3).reshape(-1)
+    assert np.array_equal(got, want)
+    # gate/up pairing: groups of 2H rows, [group][H/128][K/256][gate, up]
+    H = 128
+    got = megamoe.pack_weight_codes(torch.from_numpy(c).cuda(), H).cpu().numpy().reshape(-1)
+    want = (c.reshape(rows // (2 * H), 2, H // 128, 128, K // 256, 128)
+            .transpose(0, 2, 4, 1, 3, 5).reshape(-1))
     assert np.array_equal(got, want)
