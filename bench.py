@@ -269,18 +269,18 @@ def run_ours(args):
     # intermediates, CUDA events on the launching stream
     l1_out = torch.empty_like(v["h"])
     l1_amax = torch.empty(1, dtype=torch.float32, device=dev)
-    tile_n = 32 if cfg.slots / cfg.E <= 32 else (64 if cfg.slots / cfg.E <= 96 else 128)
+    expected = cfg.slots / cfg.E  # the forward's token-tile choice (tile_n 0 = auto)
 
     def l1():
         megamoe.grouped_gemm(v["xq_codes"], v["xq_sf"], v["gs_x"], weights.w13_codes,
                              weights.w13_scales, weights.w13_gs, v["offsets"],
-                             v["padded_offsets"], megamoe.EPI_SILU_MUL, tile_n=tile_n,
+                             v["padded_offsets"], megamoe.EPI_SILU_MUL, expected_tokens=expected,
                              out=l1_out, out_amax=l1_amax)
 
     def l2():
         megamoe.grouped_gemm(v["hq_codes"], v["hq_sf"], v["gs_h"], weights.w2_codes,
                              weights.w2_scales, weights.w2_gs.view(-1, 1), v["offsets"],
-                             v["padded_offsets"], megamoe.EPI_F32, tile_n=tile_n,
+                             v["padded_offsets"], megamoe.EPI_F32, expected_tokens=expected,
                              out=v["y"], out_amax=None)
 
     def timed(fn, n):

@@ -5,6 +5,7 @@
 #include <stdint.h>
 
 #include <algorithm>
+#include <cstdlib>
 
 #include "../../include/megamoe.h"
 #include "kernels.h"
@@ -74,6 +75,17 @@ Workspace carve(void* base, int T, int k, int E, int d, int I, int pad) {
   w.y = reinterpret_cast<float*>(take(static_cast<size_t>(rows) * d * 4));
   w.bytes = off;
   return w;
+}
+
+// Token tile of the forward's grouped GEMMs: chosen from the expected tokens
+// per expert; the MEGAMOE_TILE_N environment variable (32/64/128) overrides.
+int tile_n_setting(double expected) {
+  static const int forced = [] {
+    const char* e = std::getenv("MEGAMOE_TILE_N");
+    return (e && *e) ? std::atoi(e) : 0;
+  }();
+  if (forced == 32 || forced == 64 || forced == 128) return forced;
+  return pick_tile_n(expected);
 }
 
 megamoe_status check_route_args(int T, int k, int E, int pad) {
@@ -265,7 +277,7 @@ megamoe_status megamoe_forward(const megamoe_weights* w, const uint16_t* x,
   if (T == 0) return cudaMemsetAsync(wk.status, 0, 256, s) == cudaSuccess ? MEGAMOE_OK
                                                                          : MEGAMOE_ERR_CUDA;
   const double expected = static_cast<double>(T) * k / E;
-  const int tile_n = pick_tile_n(expected);
+  const int tile_n = tile_n_setting(expected);
 
   cudaError_t e;
   // 1. route; its first act clears the status word and the amax accumulators
