@@ -280,14 +280,23 @@ megamoe_status megamoe_forward(const megamoe_weights* w, const uint16_t* x,
   const int tile_n = tile_n_setting(expected);
 
   cudaError_t e;
-  // 1. route; its first act clears the status word and the amax accumulators
-  e = launch_route(topk_ids, T * k, E, pad, wk.counts, wk.offsets, wk.padded_offsets, wk.row_src,
-                   wk.rows, wk.slot_dst, wk.status, wk.status, 5, s);
+  // 1-3. route (its first act clears the status word and the amax
+  //      accumulators), amax of x, quantise x into its routed rows.  Padding
+  //      rows are left as they are: each output column of the grouped GEMM
+  //      depends on one token row, and columns of padding rows are never
+  //      stored.  Small batches route and take the amax in one thread block.
+  if (prologue_fits(T, d)) {
+    e = launch_prologue(topk_ids, T, k, E, pad, wk.counts, wk.offsets, wk.padded_offsets,
+                        wk.row_src, wk.rows, wk.slot_dst, wk.status, wk.status, 5, x, d,
+                        wk.amax_x, s);
+  } else {
+    e = launch_route(topk_ids, T * k, E, pad, wk.counts, wk.offsets, wk.padded_offsets,
+                     wk.row_src, wk.rows, wk.slot_dst, wk.status, wk.status, 5, s);
+    if (e != cudaSuccess) return MEGAMOE_ERR_CUDA;
+    e = launch_amax(x, T, d, d, wk.amax_x, wk.status, false, s);
+  }
   if (e != cudaSuccess) return MEGAMOE_ERR_CUDA;
-  // 2-3. amax of x, then quantise x into its routed rows (padding rows zeroed)
-  e = launch_amax(x, T, d, d, wk.amax_x, wk.status, false, s);
-  if (e != cudaSuccess) return MEGAMOE_ERR_CUDA;
-  e = launch_quant(x, T, d, d, wk.slot_dst, k, wk.row_src, wk.padded_offsets + E, wk.rows,
+  e = launch_quant(x, T, d, d, wk.slot_dst, k, nullptr, wk.padded_offsets + E, wk.rows,
                    wk.amax_x, wk.gs_x, wk.xq_codes, wk.xq_sf, MEGAMOE_SCALES_ROWMAJOR, s);
   if (e != cudaSuccess) return MEGAMOE_ERR_CUDA;
   // 4. L1 gate+up grouped GEMM, SiLU(gate)*up -> bf16 h, amax(h)
@@ -313,9 +322,10 @@ megamoe_status megamoe_forward(const megamoe_weights* w, const uint16_t* x,
   g.zero_amax = false;
   e = launch_grouped_gemm(g, s);
   if (e != cudaSuccess) return MEGAMOE_ERR_CUDA;
-  // 5. requantise h with gs from amax(h)
-  e = launch_quant(wk.h, wk.rows, I, I, nullptr, 1, wk.row_src, wk.padded_offsets + E, wk.rows,
-                   wk.amax_h, wk.gs_h, wk.hq_codes, wk.hq_sf, MEGAMOE_SCALES_ROWMAJOR, s);
+  // 5. requantise the valid rows of h with gs from amax(h) (slot by slot)
+  e = launch_quant(wk.h, static_cast<int64_t>(T) * k, I, I, wk.slot_dst, 1, nullptr,
+                   wk.padded_offsets + E, wk.rows, wk.amax_h, wk.gs_h, wk.hq_codes, wk.hq_sf,
+                   MEGAMOE_SCALES_ROWMAJOR, s, /*slot_rows=*/true);
   if (e != cudaSuccess) return MEGAMOE_ERR_CUDA;
   // 6. L2 down grouped GEMM -> fp32 y
   g.act_codes = wk.hq_codes;

@@ -272,6 +272,46 @@ __device__ __forceinline__ float e4m3_value(uint32_t b) {
   return __uint_as_float(((e + 120u) << 23) | (m << 20));   // (1 + m/8) * 2^(e-7)
 }
 
+__device__ __forceinline__ float bf16_bits_to_float(uint32_t h) { return __uint_as_float(h << 16); }
+
+// Encode 64 consecutive bf16 values (eight 128-bit words) into 8 code words
+// (32 bytes) and one word of four scale bytes.
+__device__ __forceinline__ void encode_slice(const uint4 (&v)[8], float gs, uint32_t (&codes)[8],
+                                             uint32_t& sword) {
+  sword = 0;
+#pragma unroll
+  for (int b = 0; b < 4; ++b) {  // 16-element block b = words 2b, 2b+1
+    float xv[16];
+#pragma unroll
+    for (int w = 0; w < 2; ++w) {
+      const uint4 q = v[2 * b + w];
+      const uint32_t u[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        xv[8 * w + 2 * j] = bf16_bits_to_float(u[j] & 0xFFFFu);
+        xv[8 * w + 2 * j + 1] = bf16_bits_to_float(u[j] >> 16);
+      }
+    }
+    float amax_b = 0.f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) amax_b = fmaxf(amax_b, fabsf(xv[i]));
+    const float s = __fdiv_rn(__fmul_rn(amax_b, gs), 6.0f);
+    const uint32_t s8 = e4m3_code(s);
+    const float sd = e4m3_value(s8);
+    sword |= s8 << (8 * b);
+    uint32_t c0 = 0, c1 = 0;
+    if (sd > 0.f) {
+      const float enc = __fdiv_rn(gs, sd);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) c0 |= e2m1_code(__fmul_rn(xv[i], enc)) << (4 * i);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) c1 |= e2m1_code(__fmul_rn(xv[8 + i], enc)) << (4 * i);
+    }
+    codes[2 * b] = c0;
+    codes[2 * b + 1] = c1;
+  }
+}
+
 // Atom-layout byte offset of the 4-byte scale word of (row, 64-element slice).
 __host__ __device__ __forceinline__ int64_t sf_atom_offset(int64_t row, int slice, int slices) {
   return ((row >> 7) * slices + slice) * 512 + (row & 31) * 16 + ((row >> 5) & 3) * 4;

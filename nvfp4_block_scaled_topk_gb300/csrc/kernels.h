@@ -41,7 +41,16 @@ cudaError_t launch_quant(const uint16_t* x, int64_t rows_in, int K, int64_t ld,
                          const int32_t* slot_dst, int k, const int32_t* row_src,
                          const int32_t* live_rows, int64_t out_rows, const float* amax,
                          float* gs_out, uint8_t* codes, uint8_t* scales, int scale_layout,
-                         cudaStream_t stream);
+                         cudaStream_t stream, bool slot_rows = false);
+
+// Small-batch prologue of the forward in one thread block: route and the amax
+// of x.  Used when prologue_fits(T, d).
+bool prologue_fits(int T, int d);
+cudaError_t launch_prologue(const int32_t* ids, int T, int k, int E, int pad, int32_t* counts,
+                            int32_t* offsets, int32_t* padded_offsets, int32_t* row_src,
+                            int64_t row_capacity, int32_t* slot_dst, uint32_t* status,
+                            uint32_t* zero_words, int n_zero, const uint16_t* x, int d,
+                            float* amax, cudaStream_t stream);
 cudaError_t launch_swizzle(const uint8_t* src, int64_t rows, int K, uint8_t* dst,
                            cudaStream_t stream);
 

@@ -72,47 +72,10 @@ struct QuantArgs {
   uint8_t* codes;
   uint8_t* scales;
   int scale_layout;
+  // true: task rows come from slot_dst (rows_in = number of slots); slot s
+  // with slot_dst[s] >= 0 encodes x row slot_dst[s] into the same out row
+  bool slot_rows;
 };
-
-__device__ __forceinline__ float bf16_bits_to_float(uint32_t h) { return __uint_as_float(h << 16); }
-
-// Encode 64 consecutive bf16 values (eight 128-bit words) into 8 code words
-// (32 bytes) and one word of four scale bytes.
-__device__ __forceinline__ void encode_slice(const uint4 (&v)[8], float gs, uint32_t (&codes)[8],
-                                             uint32_t& sword) {
-  sword = 0;
-#pragma unroll
-  for (int b = 0; b < 4; ++b) {  // 16-element block b = words 2b, 2b+1
-    float xv[16];
-#pragma unroll
-    for (int w = 0; w < 2; ++w) {
-      const uint4 q = v[2 * b + w];
-      const uint32_t u[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        xv[8 * w + 2 * j] = bf16_bits_to_float(u[j] & 0xFFFFu);
-        xv[8 * w + 2 * j + 1] = bf16_bits_to_float(u[j] >> 16);
-      }
-    }
-    float amax_b = 0.f;
-#pragma unroll
-    for (int i = 0; i < 16; ++i) amax_b = fmaxf(amax_b, fabsf(xv[i]));
-    const float s = __fdiv_rn(__fmul_rn(amax_b, gs), 6.0f);
-    const uint32_t s8 = e4m3_code(s);
-    const float sd = e4m3_value(s8);
-    sword |= s8 << (8 * b);
-    uint32_t c0 = 0, c1 = 0;
-    if (sd > 0.f) {
-      const float enc = __fdiv_rn(gs, sd);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) c0 |= e2m1_code(__fmul_rn(xv[i], enc)) << (4 * i);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) c1 |= e2m1_code(__fmul_rn(xv[8 + i], enc)) << (4 * i);
-    }
-    codes[2 * b] = c0;
-    codes[2 * b + 1] = c1;
-  }
-}
 
 __device__ __forceinline__ void store_slice(const QuantArgs& a, int64_t out_row, int slice,
                                             const uint32_t (&c)[8], uint32_t sword) {
@@ -126,10 +89,13 @@ __device__ __forceinline__ void store_slice(const QuantArgs& a, int64_t out_row,
   *reinterpret_cast<uint32_t*>(a.scales + so) = sword;
 }
 
-// Tasks: with slot_dst, [0, rows_in*S) are token rows (scattered to their
-// routed rows) and [rows_in*S, (rows_in+out_rows)*S) zero the padding rows;
-// without slot_dst, [0, out_rows*S) map out row r <- x row r (padding rows
-// zeroed).  S = K/64 slices per row.
+// Tasks (S = K/64 slices per row):
+//  * slot_rows: [0, rows_in*S): slot s encodes row slot_dst[s] in place;
+//  * slot_dst:  [0, rows_in*S) are token rows, scattered to their routed rows,
+//    then, if row_src is given, [rows_in*S, (rows_in+out_rows)*S) zero the
+//    padding rows;
+//  * otherwise  [0, out_rows*S) map out row r <- x row r (padding rows zeroed
+//    when row_src is given).
 __global__ void __launch_bounds__(256) k_quant(const QuantArgs a) {
   pdl_wait();
   pdl_trigger();
@@ -138,8 +104,26 @@ __global__ void __launch_bounds__(256) k_quant(const QuantArgs a) {
   const float gs = amax == 0.f ? 1.f : __fdiv_rn(2688.0f, amax);
   if (blockIdx.x == 0 && threadIdx.x == 0 && a.gs_out) *a.gs_out = gs;
   const int64_t live = a.live_rows ? static_cast<int64_t>(*a.live_rows) : a.out_rows;
+  if (a.slot_rows) {
+    const int64_t total = a.rows_in * S;
+    for (int64_t t = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; t < total;
+         t += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+      const int64_t slot = t / S;
+      const int slice = static_cast<int>(t - slot * S);
+      const int64_t row = a.slot_dst[slot];
+      if (row < 0 || row >= live) continue;
+      const uint4* src = reinterpret_cast<const uint4*>(a.x + row * a.ld) + 8 * slice;
+      uint4 v[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[i] = __ldg(src + i);
+      uint32_t c[8], sword;
+      encode_slice(v, gs, c, sword);
+      store_slice(a, row, slice, c, sword);
+    }
+    return;
+  }
   const int64_t token_tasks = a.slot_dst ? a.rows_in * S : 0;
-  const int64_t total = token_tasks + a.out_rows * S;
+  const int64_t total = token_tasks + ((a.slot_dst && !a.row_src) ? 0 : a.out_rows * S);
   for (int64_t t = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; t < total;
        t += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const bool token_task = t < token_tasks;
@@ -245,11 +229,16 @@ cudaError_t launch_quant(const uint16_t* x, int64_t rows_in, int K, int64_t ld,
                          const int32_t* slot_dst, int k, const int32_t* row_src,
                          const int32_t* live_rows, int64_t out_rows, const float* amax,
                          float* gs_out, uint8_t* codes, uint8_t* scales, int scale_layout,
-                         cudaStream_t stream) {
-  QuantArgs a{x, rows_in, K, ld, slot_dst, k, row_src, live_rows, out_rows, amax,
-              gs_out, codes, scales, scale_layout};
-  const int64_t tasks = ((slot_dst ? rows_in : 0) + out_rows) * (K / 64);
-  return launch_pdl(k_quant, dim3(grid_for(tasks, 256)), dim3(256), 0, stream, a);
+                         cudaStream_t stream, bool slot_rows) {
+  QuantArgs a{x,        rows_in, K,      ld,     slot_dst,     k,        row_src, live_rows,
+              out_rows, amax,    gs_out, codes,  scales,       scale_layout, slot_rows};
+  const int64_t tasks =
+      slot_rows ? rows_in * (K / 64)
+                : ((slot_dst ? rows_in : 0) + ((slot_dst && !row_src) ? 0 : out_rows)) * (K / 64);
+  if (tasks == 0) return cudaSuccess;
+  // encoding is ALU work: few tasks go in small blocks spread over many SMs
+  const int threads = tasks <= 152 * 256 ? 64 : 256;
+  return launch_pdl(k_quant, dim3(grid_for(tasks, threads)), dim3(threads), 0, stream, a);
 }
 
 cudaError_t launch_swizzle(const uint8_t* src, int64_t rows, int K, uint8_t* dst,

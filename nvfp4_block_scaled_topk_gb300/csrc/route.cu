@@ -51,21 +51,21 @@ __device__ __forceinline__ int block_exclusive_scan_1024(int v, int* warp_sums, 
   return r;
 }
 
-__global__ void __launch_bounds__(kRouteThreads, 1)
-    k_route(const int32_t* __restrict__ ids, int n_slots, int E, int pad, int32_t* counts,
-            int32_t* offsets, int32_t* padded_offsets, int32_t* row_src, int64_t row_capacity,
-            int32_t* slot_dst, uint32_t* status, uint32_t* zero_words, int n_zero) {
-  extern __shared__ int smem_route[];
-  int* hist = smem_route;                       // [32][E]
-  int* s_poff = hist + kRouteWarps * E;         // [E+1]
-  int* s_cnt = s_poff + (E + 1);                // [E]
+// The routing itself, for one block of kRouteThreads threads.  `smem` holds
+// 32*E + 2*E + 1 ints.  Ends with the block's global writes issued; callers
+// that read them back in the same block synchronise first.
+__device__ void route_block(const int32_t* __restrict__ ids, int n_slots, int E, int pad,
+                            int32_t* counts, int32_t* offsets, int32_t* padded_offsets,
+                            int32_t* row_src, int64_t row_capacity, int32_t* slot_dst,
+                            uint32_t* status, uint32_t* zero_words, int n_zero, int* smem) {
+  int* hist = smem;                        // [32][E]
+  int* s_poff = hist + kRouteWarps * E;    // [E+1]
+  int* s_cnt = s_poff + (E + 1);           // [E]
   __shared__ int warp_sums[32];
   __shared__ int totals[2];
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  pdl_wait();
-  pdl_trigger();
-  if (tid < n_zero) zero_words[tid] = 0u;
+  for (int i = tid; i < n_zero; i += kRouteThreads) zero_words[i] = 0u;
   for (int i = tid; i < kRouteWarps * E; i += kRouteThreads) hist[i] = 0;
   __syncthreads();
 
@@ -142,6 +142,58 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
   for (int64_t r = s_poff[E] + tid; r < row_capacity; r += kRouteThreads) row_src[r] = -1;
 }
 
+__global__ void __launch_bounds__(kRouteThreads, 1)
+    k_route(const int32_t* __restrict__ ids, int n_slots, int E, int pad, int32_t* counts,
+            int32_t* offsets, int32_t* padded_offsets, int32_t* row_src, int64_t row_capacity,
+            int32_t* slot_dst, uint32_t* status, uint32_t* zero_words, int n_zero) {
+  extern __shared__ int smem_route[];
+  pdl_wait();
+  pdl_trigger();
+  route_block(ids, n_slots, E, pad, counts, offsets, padded_offsets, row_src, row_capacity,
+              slot_dst, status, zero_words, n_zero, smem_route);
+}
+
+// Small batches: route and the amax of x in this one block (the quantisation
+// itself, ALU-heavy, runs spread over many SMs in the next kernel).
+constexpr int64_t kPrologueMaxElems = 262144;  // T * d read by one block
+
+__global__ void __launch_bounds__(kRouteThreads, 1)
+    k_prologue(const int32_t* __restrict__ ids, int T, int k, int E, int pad, int32_t* counts,
+               int32_t* offsets, int32_t* padded_offsets, int32_t* row_src,
+               int64_t row_capacity, int32_t* slot_dst, uint32_t* status, uint32_t* zero_words,
+               int n_zero, const uint16_t* __restrict__ x, int d, float* amax_out) {
+  extern __shared__ int smem_route[];
+  __shared__ uint32_t red[kRouteWarps];
+  pdl_wait();
+  pdl_trigger();
+  route_block(ids, T * k, E, pad, counts, offsets, padded_offsets, row_src, row_capacity,
+              slot_dst, status, zero_words, n_zero, smem_route);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  // amax of x on the bf16 bit patterns (monotone for finite values)
+  const int64_t vecs = static_cast<int64_t>(T) * (d / 8);
+  uint32_t m2 = 0;
+  for (int64_t i = tid; i < vecs; i += kRouteThreads) {
+    const uint4 q = __ldg(reinterpret_cast<const uint4*>(x) + i);
+    m2 = __vmaxu2(m2, q.x & 0x7FFF7FFFu);
+    m2 = __vmaxu2(m2, q.y & 0x7FFF7FFFu);
+    m2 = __vmaxu2(m2, q.z & 0x7FFF7FFFu);
+    m2 = __vmaxu2(m2, q.w & 0x7FFF7FFFu);
+  }
+  uint32_t m = max(m2 & 0xFFFFu, m2 >> 16);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+  if (lane == 0) red[warp] = m;
+  __syncthreads();  // also orders the status word's clearing before the write below
+  if (tid == 0) {
+    for (int w = 1; w < kRouteWarps; ++w) m = max(m, red[w]);
+    if (m >= 0x7F80u) {  // Inf or NaN
+      set_status(status, MEGAMOE_DEV_NONFINITE);
+      m = 0x7F7Fu;
+    }
+    *amax_out = __uint_as_float(m << 16);
+  }
+}
+
 size_t route_smem_bytes(int E) { return sizeof(int) * (static_cast<size_t>(kRouteWarps) * E + 2 * E + 1); }
 
 cudaError_t launch_route(const int32_t* ids, int n_slots, int E, int pad, int32_t* counts,
@@ -155,6 +207,24 @@ cudaError_t launch_route(const int32_t* ids, int n_slots, int E, int pad, int32_
   return launch_pdl(k_route, dim3(1), dim3(kRouteThreads), smem, stream, ids, n_slots, E, pad,
                     counts, offsets, padded_offsets, row_src, row_capacity, slot_dst, status,
                     zero_words, n_zero);
+}
+
+bool prologue_fits(int T, int d) {
+  return static_cast<int64_t>(T) * d <= kPrologueMaxElems && d % 64 == 0;
+}
+
+cudaError_t launch_prologue(const int32_t* ids, int T, int k, int E, int pad, int32_t* counts,
+                            int32_t* offsets, int32_t* padded_offsets, int32_t* row_src,
+                            int64_t row_capacity, int32_t* slot_dst, uint32_t* status,
+                            uint32_t* zero_words, int n_zero, const uint16_t* x, int d,
+                            float* amax, cudaStream_t stream) {
+  const size_t smem = route_smem_bytes(E);
+  cudaError_t err = cudaFuncSetAttribute(k_prologue, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+  if (err != cudaSuccess) return err;
+  return launch_pdl(k_prologue, dim3(1), dim3(kRouteThreads), smem, stream, ids, T, k, E, pad,
+                    counts, offsets, padded_offsets, row_src, row_capacity, slot_dst, status,
+                    zero_words, n_zero, x, d, amax);
 }
 
 }  // namespace megamoe
