@@ -274,42 +274,34 @@ __device__ __forceinline__ float e4m3_value(uint32_t b) {
 
 __device__ __forceinline__ float bf16_bits_to_float(uint32_t h) { return __uint_as_float(h << 16); }
 
-// Encode 64 consecutive bf16 values (eight 128-bit words) into 8 code words
-// (32 bytes) and one word of four scale bytes.
-__device__ __forceinline__ void encode_slice(const uint4 (&v)[8], float gs, uint32_t (&codes)[8],
-                                             uint32_t& sword) {
-  sword = 0;
+// Encode one 16-element block of bf16 values (two 128-bit words): 16 E2M1
+// codes (8 bytes, element 2i in the low nibble of byte i) and the E4M3 scale
+// byte, following the fixed float32 order
+//   s = (amax_b * gs) / 6, s8 = e4m3(s), enc = gs / decode(s8), code = e2m1(x * enc).
+__device__ __forceinline__ void encode_block(uint4 v0, uint4 v1, float gs, uint2& codes,
+                                             uint32_t& s8) {
+  float xv[16];
+  const uint32_t u[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
 #pragma unroll
-  for (int b = 0; b < 4; ++b) {  // 16-element block b = words 2b, 2b+1
-    float xv[16];
-#pragma unroll
-    for (int w = 0; w < 2; ++w) {
-      const uint4 q = v[2 * b + w];
-      const uint32_t u[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        xv[8 * w + 2 * j] = bf16_bits_to_float(u[j] & 0xFFFFu);
-        xv[8 * w + 2 * j + 1] = bf16_bits_to_float(u[j] >> 16);
-      }
-    }
-    float amax_b = 0.f;
-#pragma unroll
-    for (int i = 0; i < 16; ++i) amax_b = fmaxf(amax_b, fabsf(xv[i]));
-    const float s = __fdiv_rn(__fmul_rn(amax_b, gs), 6.0f);
-    const uint32_t s8 = e4m3_code(s);
-    const float sd = e4m3_value(s8);
-    sword |= s8 << (8 * b);
-    uint32_t c0 = 0, c1 = 0;
-    if (sd > 0.f) {
-      const float enc = __fdiv_rn(gs, sd);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) c0 |= e2m1_code(__fmul_rn(xv[i], enc)) << (4 * i);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) c1 |= e2m1_code(__fmul_rn(xv[8 + i], enc)) << (4 * i);
-    }
-    codes[2 * b] = c0;
-    codes[2 * b + 1] = c1;
+  for (int j = 0; j < 8; ++j) {
+    xv[2 * j] = bf16_bits_to_float(u[j] & 0xFFFFu);
+    xv[2 * j + 1] = bf16_bits_to_float(u[j] >> 16);
   }
+  float amax_b = 0.f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) amax_b = fmaxf(amax_b, fabsf(xv[i]));
+  const float s = __fdiv_rn(__fmul_rn(amax_b, gs), 6.0f);
+  s8 = e4m3_code(s);
+  const float sd = e4m3_value(s8);
+  uint32_t c0 = 0, c1 = 0;
+  if (sd > 0.f) {
+    const float enc = __fdiv_rn(gs, sd);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) c0 |= e2m1_code(__fmul_rn(xv[i], enc)) << (4 * i);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) c1 |= e2m1_code(__fmul_rn(xv[8 + i], enc)) << (4 * i);
+  }
+  codes = make_uint2(c0, c1);
 }
 
 // Atom-layout byte offset of the 4-byte scale word of (row, 64-element slice).

@@ -85,7 +85,8 @@ struct GemmCfg {
   static constexpr int SF_COL0 = ACC_STAGES * ACC_COLS;
   static constexpr int BAR_OFF = STAGES * STAGE;
   static constexpr int TOFF_OFF = BAR_OFF + 256;
-  static constexpr int SMEM = 1024 + TOFF_OFF + 4 * (MEGAMOE_MAX_EXPERTS + 1);
+  static constexpr int INFO_OFF = TOFF_OFF + 4 * (MEGAMOE_MAX_EXPERTS + 1);  // counts, poffs
+  static constexpr int SMEM = 1024 + INFO_OFF + 8 * MEGAMOE_MAX_EXPERTS;
   static constexpr uint32_t IDESC = idesc_nvf4(128, BN);
   static_assert(SF_COL0 + STAGES * SF_COLS <= 512, "tensor memory budget");
   static_assert(SMEM <= 232448, "shared memory budget");
@@ -98,8 +99,7 @@ struct TileInfo {
 
 template <int BN>
 __device__ __forceinline__ TileInfo decode_tile(int tile, const int* s_toff, int E,
-                                                const int32_t* offsets,
-                                                const int32_t* padded_offsets) {
+                                                const int* s_cnt, const int* s_poff) {
   int lo = 0, hi = E - 1;
   while (lo < hi) {  // largest e with s_toff[e] <= tile; it always owns tiles
     const int mid = (lo + hi + 1) >> 1;
@@ -108,8 +108,8 @@ __device__ __forceinline__ TileInfo decode_tile(int tile, const int* s_toff, int
   }
   TileInfo t;
   t.e = lo;
-  t.count = __ldg(offsets + lo + 1) - __ldg(offsets + lo);
-  t.poff = __ldg(padded_offsets + lo);
+  t.count = s_cnt[lo];
+  t.poff = s_poff[lo];
   const int ntiles = (t.count + BN - 1) / BN;
   const int local = tile - s_toff[lo];
   t.mt = local / ntiles;
@@ -117,10 +117,11 @@ __device__ __forceinline__ TileInfo decode_tile(int tile, const int* s_toff, int
   return t;
 }
 
-// s_toff[e] = first tile of expert e, s_toff[E] = total tiles.  All threads.
+// s_toff[e] = first tile of expert e, s_toff[E] = total tiles; s_cnt[e] and
+// s_poff[e] = expert e's row count and first padded row.  All threads.
 template <int BN>
-__device__ void build_tile_offsets(const int32_t* offsets, int E, int MT, int* s_toff,
-                                   int* s_scan) {
+__device__ void build_tile_offsets(const int32_t* offsets, const int32_t* padded_offsets, int E,
+                                   int MT, int* s_toff, int* s_cnt, int* s_poff, int* s_scan) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int per = (E + kGemmThreads - 1) / kGemmThreads;
   const int e0 = tid * per, e1 = min(E, e0 + per);
@@ -129,6 +130,8 @@ __device__ void build_tile_offsets(const int32_t* offsets, int E, int MT, int* s
     const int cnt = __ldg(offsets + e + 1) - __ldg(offsets + e);
     const int t = cnt > 0 ? (cnt + BN - 1) / BN * MT : 0;
     s_toff[e] = t;
+    s_cnt[e] = cnt;
+    s_poff[e] = __ldg(padded_offsets + e);
     sum += t;
   }
   int x = sum;
@@ -175,6 +178,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   int* s_toff = reinterpret_cast<int*>(smem + C::TOFF_OFF);
+  int* s_cnt = reinterpret_cast<int*>(smem + C::INFO_OFF);
+  int* s_poff = s_cnt + MEGAMOE_MAX_EXPERTS;
   __shared__ int s_scan[kGemmThreads / 32];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -190,7 +195,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   }
   pdl_wait();  // the routing offsets and activations come from earlier kernels
   pdl_trigger();
-  build_tile_offsets<BN>(p.offsets, E, MT, s_toff, s_scan);
+  build_tile_offsets<BN>(p.offsets, p.padded_offsets, E, MT, s_toff, s_cnt, s_poff, s_scan);
   const int total = s_toff[E];
   if (static_cast<int>(blockIdx.x) >= total) return;  // uniform: no work for this CTA
 
@@ -228,7 +233,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       for (int s = 0; s < STAGES; ++s) issued_parity[s] = -1;
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
-        const TileInfo ti = decode_tile<BN>(tile, s_toff, E, p.offsets, p.padded_offsets);
+        const TileInfo ti = decode_tile<BN>(tile, s_toff, E, s_cnt, s_poff);
         const int w_row0 = ti.e * N + ti.mt * 128;
         const int w_row1 = ti.e * N + N / 2 + ti.mt * 128;  // up rows (L1 only)
         // first 128-row code block of this tile's K = 0 step (paired for L1)
@@ -371,7 +376,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     uint32_t acc_phase = 0;
     float amax = 0.f;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
-      const TileInfo ti = decode_tile<BN>(tile, s_toff, E, p.offsets, p.padded_offsets);
+      const TileInfo ti = decode_tile<BN>(tile, s_toff, E, s_cnt, s_poff);
       const int m_valid = min(BN, ti.count - ti.nt * BN);
       const int64_t row0 = ti.poff + static_cast<int64_t>(ti.nt) * BN;
       const int f = ti.mt * 128 + q * 32 + lane;

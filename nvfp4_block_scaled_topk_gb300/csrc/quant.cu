@@ -8,10 +8,10 @@
 //           |x| maximum is taken on the bf16 bit patterns with packed 16-bit
 //           integer max (monotone for finite values), reduced with warp
 //           shuffles and one atomicMax per block.
-// k_quant   one thread per (row, 64-element slice): 128 bytes of bf16 in
-//           (8 x 128-bit loads), 32 bytes of E2M1 codes and one 32-bit word of
-//           four E4M3 block scales out.  The routed gather is fused: a token
-//           row is encoded once and written to each of its k expert rows.
+// k_quant   one thread per (row, 16-element block): 32 bytes of bf16 in
+//           (2 x 128-bit loads), 8 bytes of E2M1 codes and one E4M3 scale
+//           byte out.  The routed gather is fused: a token row is encoded
+//           once and written to each of its k expert rows.
 // k_swizzle row-major block scales -> the tensor-core atom layout (weights,
 //           once, off the hot path).
 // k_pack    row-major E2M1 codes -> tile-major blocks of 128 rows x 128 bytes
@@ -77,82 +77,75 @@ struct QuantArgs {
   bool slot_rows;
 };
 
-__device__ __forceinline__ void store_slice(const QuantArgs& a, int64_t out_row, int slice,
-                                            const uint32_t (&c)[8], uint32_t sword) {
-  uint4* dst = reinterpret_cast<uint4*>(a.codes + out_row * (a.K / 2) + 32 * slice);
-  dst[0] = make_uint4(c[0], c[1], c[2], c[3]);
-  dst[1] = make_uint4(c[4], c[5], c[6], c[7]);
-  const int slices = a.K / 64;
+__device__ __forceinline__ void store_block(const QuantArgs& a, int64_t out_row, int b, uint2 c,
+                                            uint32_t s8) {
+  *reinterpret_cast<uint2*>(a.codes + out_row * (a.K / 2) + 8 * b) = c;
   const int64_t so = a.scale_layout == MEGAMOE_SCALES_MMA
-                         ? sf_atom_offset(out_row, slice, slices)
-                         : out_row * (a.K / 16) + 4 * slice;
-  *reinterpret_cast<uint32_t*>(a.scales + so) = sword;
+                         ? sf_atom_offset(out_row, b >> 2, a.K / 64) + (b & 3)
+                         : out_row * (a.K / 16) + b;
+  a.scales[so] = static_cast<uint8_t>(s8);
 }
 
-// Tasks (S = K/64 slices per row):
-//  * slot_rows: [0, rows_in*S): slot s encodes row slot_dst[s] in place;
-//  * slot_dst:  [0, rows_in*S) are token rows, scattered to their routed rows,
-//    then, if row_src is given, [rows_in*S, (rows_in+out_rows)*S) zero the
-//    padding rows;
-//  * otherwise  [0, out_rows*S) map out row r <- x row r (padding rows zeroed
-//    when row_src is given).
+// One thread per (row, 16-element block): short dependency chains, many
+// threads.  Tasks (NB = K/16 blocks per row):
+//  * slot_rows: [0, rows_in*NB): slot s encodes row slot_dst[s] in place;
+//  * slot_dst:  [0, rows_in*NB) are token rows, scattered to their routed
+//    rows, then, if row_src is given, [rows_in*NB, (rows_in+out_rows)*NB)
+//    zero the padding rows;
+//  * otherwise  [0, out_rows*NB) map out row r <- x row r (padding rows
+//    zeroed when row_src is given).
 __global__ void __launch_bounds__(256) k_quant(const QuantArgs a) {
   pdl_wait();
   pdl_trigger();
-  const int S = a.K / 64;
+  const int NB = a.K / 16;
   const float amax = *a.amax;
   const float gs = amax == 0.f ? 1.f : __fdiv_rn(2688.0f, amax);
   if (blockIdx.x == 0 && threadIdx.x == 0 && a.gs_out) *a.gs_out = gs;
   const int64_t live = a.live_rows ? static_cast<int64_t>(*a.live_rows) : a.out_rows;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   if (a.slot_rows) {
-    const int64_t total = a.rows_in * S;
-    for (int64_t t = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; t < total;
-         t += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-      const int64_t slot = t / S;
-      const int slice = static_cast<int>(t - slot * S);
+    for (int64_t t = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
+         t < a.rows_in * NB; t += stride) {
+      const int64_t slot = t / NB;
+      const int b = static_cast<int>(t - slot * NB);
       const int64_t row = a.slot_dst[slot];
       if (row < 0 || row >= live) continue;
-      const uint4* src = reinterpret_cast<const uint4*>(a.x + row * a.ld) + 8 * slice;
-      uint4 v[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) v[i] = __ldg(src + i);
-      uint32_t c[8], sword;
-      encode_slice(v, gs, c, sword);
-      store_slice(a, row, slice, c, sword);
+      const uint4* src = reinterpret_cast<const uint4*>(a.x + row * a.ld + 16 * b);
+      uint2 c;
+      uint32_t s8;
+      encode_block(__ldg(src), __ldg(src + 1), gs, c, s8);
+      store_block(a, row, b, c, s8);
     }
     return;
   }
-  const int64_t token_tasks = a.slot_dst ? a.rows_in * S : 0;
-  const int64_t total = token_tasks + ((a.slot_dst && !a.row_src) ? 0 : a.out_rows * S);
+  const int64_t token_tasks = a.slot_dst ? a.rows_in * NB : 0;
+  const int64_t total = token_tasks + ((a.slot_dst && !a.row_src) ? 0 : a.out_rows * NB);
   for (int64_t t = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; t < total;
-       t += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+       t += stride) {
     const bool token_task = t < token_tasks;
     const int64_t u = token_task ? t : t - token_tasks;
-    const int64_t row = u / S;
-    const int slice = static_cast<int>(u - row * S);
+    const int64_t row = u / NB;
+    const int b = static_cast<int>(u - row * NB);
     if (!token_task) {
       if (row >= live) continue;
       const bool pad_row = a.row_src && a.row_src[row] < 0;
       if (a.slot_dst && !pad_row) continue;  // written by its token task
       if (pad_row) {
-        const uint32_t z[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-        store_slice(a, row, slice, z, 0u);
+        store_block(a, row, b, make_uint2(0u, 0u), 0u);
         continue;
       }
     }
-    const uint4* src = reinterpret_cast<const uint4*>(a.x + row * a.ld) + 8 * slice;
-    uint4 v[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) v[i] = __ldg(src + i);
-    uint32_t c[8], sword;
-    encode_slice(v, gs, c, sword);
+    const uint4* src = reinterpret_cast<const uint4*>(a.x + row * a.ld + 16 * b);
+    uint2 c;
+    uint32_t s8;
+    encode_block(__ldg(src), __ldg(src + 1), gs, c, s8);
     if (token_task) {
       for (int j = 0; j < a.k; ++j) {
         const int dst = a.slot_dst[row * a.k + j];
-        if (dst >= 0 && dst < live) store_slice(a, dst, slice, c, sword);
+        if (dst >= 0 && dst < live) store_block(a, dst, b, c, s8);
       }
     } else {
-      store_slice(a, row, slice, c, sword);
+      store_block(a, row, b, c, s8);
     }
   }
 }
@@ -233,8 +226,8 @@ cudaError_t launch_quant(const uint16_t* x, int64_t rows_in, int K, int64_t ld,
   QuantArgs a{x,        rows_in, K,      ld,     slot_dst,     k,        row_src, live_rows,
               out_rows, amax,    gs_out, codes,  scales,       scale_layout, slot_rows};
   const int64_t tasks =
-      slot_rows ? rows_in * (K / 64)
-                : ((slot_dst ? rows_in : 0) + ((slot_dst && !row_src) ? 0 : out_rows)) * (K / 64);
+      slot_rows ? rows_in * (K / 16)
+                : ((slot_dst ? rows_in : 0) + ((slot_dst && !row_src) ? 0 : out_rows)) * (K / 16);
   if (tasks == 0) return cudaSuccess;
   // encoding is ALU work: few tasks go in small blocks spread over many SMs
   const int threads = tasks <= 152 * 256 ? 64 : 256;
