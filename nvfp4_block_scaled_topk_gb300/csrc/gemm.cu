@@ -79,18 +79,19 @@ struct GemmCfg {
   static constexpr int OFF_SFW = OFF_B + B_TILE;
   static constexpr int OFF_SFA_RAW = OFF_SFW + G * SFW;
   static constexpr int STAGE = (OFF_SFA_RAW + SFA_RAW + 1023) / 1024 * 1024;
-  static constexpr uint32_t TX = G * A_TILE + B_TILE + G * SFW + SFA_RAW;
+  static constexpr uint32_t TX = G * A_TILE + B_TILE;     // codes (full barrier)
+  static constexpr uint32_t SF_TX = G * SFW + SFA_RAW;     // scales (sf_full barrier)
   static constexpr int ACC_COLS = G * BN;
   static constexpr int SF_COLS = 16 * G + 16;  // per stage: weight scales + token scales
   static constexpr int SF_COL0 = ACC_STAGES * ACC_COLS;
   static constexpr int BAR_OFF = STAGES * STAGE;
-  static constexpr int TOFF_OFF = BAR_OFF + 256;
+  static constexpr int TOFF_OFF = BAR_OFF + 512;
   static constexpr int INFO_OFF = TOFF_OFF + 4 * (MEGAMOE_MAX_EXPERTS + 1);  // counts, poffs
   static constexpr int SMEM = 1024 + INFO_OFF + 8 * MEGAMOE_MAX_EXPERTS;
   static constexpr uint32_t IDESC = idesc_nvf4(128, BN);
   static_assert(SF_COL0 + STAGES * SF_COLS <= 512, "tensor memory budget");
   static_assert(SMEM <= 232448, "shared memory budget");
-  static_assert((3 * STAGES + 2 * ACC_STAGES + 1) * 8 + 8 <= 256, "barrier area");
+  static_assert((4 * STAGES + 2 * ACC_STAGES + 1) * 8 + 8 <= 512, "barrier area");
 };
 
 struct TileInfo {
@@ -172,7 +173,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
   uint64_t* empty = full + STAGES;
   uint64_t* sf_ready = empty + STAGES;
-  uint64_t* acc_full = sf_ready + STAGES;  // [ACC_STAGES]
+  uint64_t* sf_full = sf_ready + STAGES;   // the stage's block scales have landed
+  uint64_t* acc_full = sf_full + STAGES;   // [ACC_STAGES]
   uint64_t* acc_empty = acc_full + C::ACC_STAGES;  // [ACC_STAGES]
   uint64_t* drain = acc_empty + C::ACC_STAGES;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
@@ -204,6 +206,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
       mbar_init(&sf_ready[s], 4);
+      mbar_init(&sf_full[s], 1);
     }
     for (int a = 0; a < C::ACC_STAGES; ++a) {
       mbar_init(&acc_full[a], 1);
@@ -245,21 +248,24 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             break;
           }
           uint8_t* sb = smem + stage * C::STAGE;
+          // scales first, on their own barrier: the scale warps move them into
+          // tensor memory while the codes are still landing
+          mbar_arrive_expect_tx(&sf_full[stage], C::SF_TX);
+          bulk_load(sb + C::OFF_SFW,
+                    p.w_sf + (static_cast<int64_t>(w_row0 >> 7) * slices + 4 * kt) * 512, C::SFW,
+                    &sf_full[stage], pol_w);
+          if (C::G == 2)
+            bulk_load(sb + C::OFF_SFW + C::SFW,
+                      p.w_sf + (static_cast<int64_t>(w_row1 >> 7) * slices + 4 * kt) * 512,
+                      C::SFW, &sf_full[stage], pol_w);
+          tma_load_2d(sb + C::OFF_SFA_RAW, &tm_asf, &sf_full[stage], kt * 16, a_row0, pol_a);
           mbar_arrive_expect_tx(&full[stage], C::TX);
           tma_load_2d(sb + C::OFF_A, &tm_w, &full[stage], 0, (w_blk0 + kt * C::G) * 128,
                       pol_w);
-          bulk_load(sb + C::OFF_SFW,
-                    p.w_sf + (static_cast<int64_t>(w_row0 >> 7) * slices + 4 * kt) * 512, C::SFW,
-                    &full[stage], pol_w);
-          if (C::G == 2) {
+          if (C::G == 2)
             tma_load_2d(sb + C::OFF_A + C::A_TILE, &tm_w, &full[stage], 0,
                         (w_blk0 + kt * 2 + 1) * 128, pol_w);
-            bulk_load(sb + C::OFF_SFW + C::SFW,
-                      p.w_sf + (static_cast<int64_t>(w_row1 >> 7) * slices + 4 * kt) * 512,
-                      C::SFW, &full[stage], pol_w);
-          }
           tma_load_2d(sb + C::OFF_B, &tm_a, &full[stage], kt * 128, a_row0, pol_a);
-          tma_load_2d(sb + C::OFF_SFA_RAW, &tm_asf, &full[stage], kt * 16, a_row0, pol_a);
           issued_parity[stage] = static_cast<int>(phase);
           if (++stage == STAGES) {
             stage = 0;
@@ -269,7 +275,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
       if (!ok) {  // unwinding: let every copy already in flight land first
         for (int s = 0; s < STAGES; ++s)
-          if (issued_parity[s] >= 0) mbar_drain(&full[s], static_cast<uint32_t>(issued_parity[s]));
+          if (issued_parity[s] >= 0) {
+            mbar_drain(&full[s], static_cast<uint32_t>(issued_parity[s]));
+            mbar_drain(&sf_full[s], static_cast<uint32_t>(issued_parity[s]));
+          }
       }
     }
     __syncwarp();
@@ -334,7 +343,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     bool ok = true;
     for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
       for (int kt = 0; kt < KT; ++kt) {
-        if (!mbar_wait(&full[stage], phase, abort_flag, p.status, p.wait_limit_ns)) {
+        if (!mbar_wait(&sf_full[stage], phase, abort_flag, p.status, p.wait_limit_ns)) {
           ok = false;
           break;
         }
