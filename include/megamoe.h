@@ -183,14 +183,16 @@ megamoe_status megamoe_swizzle_scales(const uint8_t* src, int64_t rows, int K, u
 /*
  * megamoe_pack_weight_codes -- one-time weight preparation: row-major E2M1
  * codes [rows, K/2] -> tile-major blocks of 128 rows x 128 bytes (256
- * elements of K), each block row-major (row r%128 at byte (r%128)*128).
+ * elements of K).  Within a block, row i sits at byte 128*i and its 16-byte
+ * chunk j at chunk j XOR (i % 8): the 128-byte swizzle the tensor cores read
+ * K-major operands in, so the GEMM copies a block to shared memory as is.
  *   half_rows == 0: blocks ordered [rows/128][K/256] (the W2 layout).
  *   half_rows == H: rows come in groups of 2H, H gate rows then H up rows (one
  *                   expert of W13, H = I); the gate and up blocks of the same
  *                   128 features and K step are adjacent:
  *                   [rows/2H][H/128][K/256][gate, up] (the W13 layout).
  * A stage of the grouped GEMM then reads one contiguous 16 KB (W2) or 32 KB
- * (W13) block.  Requires rows a multiple of 128 (of 2H when H > 0), H a
+ * (W13) block with a single bulk copy.  Requires rows a multiple of 128 (of 2H when H > 0), H a
  * multiple of 128, K a multiple of 256, 16-byte alignment.
  */
 megamoe_status megamoe_pack_weight_codes(const uint8_t* src, int64_t rows, int K, int half_rows,
@@ -227,7 +229,8 @@ megamoe_status megamoe_pack_weight_codes(const uint8_t* src, int64_t rows, int K
  * (32, 64 or 128; 0 = choose from the expected tokens per expert,
  * expected_tokens = rows the caller expects per active expert, may be 0).
  * Requires N a multiple of 128 (256 for SILU_MUL), K a multiple of 256,
- * 1 <= E <= 1024, 16-byte aligned pointers, ld_out >= output width.
+ * 1 <= E <= 1024, 16-byte aligned pointers, ld_out >= output width and a
+ * multiple of 16 bytes (4 floats, 8 bf16), else MEGAMOE_ERR_UNSUPPORTED_SHAPE.
  */
 megamoe_status megamoe_grouped_gemm(const uint8_t* act_codes, const uint8_t* act_scales,
                                     const float* act_gs, int64_t act_rows,

@@ -206,12 +206,14 @@ megamoe_status megamoe_grouped_gemm(const uint8_t* act_codes, const uint8_t* act
   if (tile_n != 0 && tile_n != 32 && tile_n != 64 && tile_n != 128) return MEGAMOE_ERR_INVALID_ARG;
   const int width = epilogue == MEGAMOE_EPI_F32 ? N : N / 2;
   if (ld_out < width) return MEGAMOE_ERR_INVALID_ARG;
+  // output rows start on 16-byte boundaries: the epilogue stores 16-byte vectors
+  if (ld_out % (epilogue == MEGAMOE_EPI_F32 ? 4 : 8) != 0) return MEGAMOE_ERR_UNSUPPORTED_SHAPE;
   if (!w_codes || !w_scales || !w_gs || !offsets || !padded_offsets ||
       (act_rows > 0 && (!act_codes || !act_scales || !act_gs || !out)))
     return MEGAMOE_ERR_INVALID_ARG;
   if (epilogue == MEGAMOE_EPI_SILU_MUL && !out_amax) return MEGAMOE_ERR_INVALID_ARG;
   if (!aligned(w_codes, 16) || !aligned(w_scales, 16) || (act_codes && !aligned(act_codes, 16)) ||
-      (act_scales && !aligned(act_scales, 16)))
+      (act_scales && !aligned(act_scales, 16)) || (out && !aligned(out, 16)))
     return MEGAMOE_ERR_UNSUPPORTED_SHAPE;
   GemmLaunch g{};
   g.act_codes = act_codes;

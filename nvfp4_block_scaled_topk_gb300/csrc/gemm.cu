@@ -28,11 +28,11 @@
 //               pipe (a tcgen05.cp costs about as much as an MMA), and the
 //               token tile's first row always lands in the first scale
 //               column whatever row the tile starts at.
-// Every expert's weights live in one tensor (tile-major: blocks of 128 rows x
-// 128 bytes, [E*N/128][K/256] blocks; for L1 the gate and up blocks of the
-// same features and K step are adjacent), so one tensor map serves all
-// experts: the expert is a coordinate, not a new descriptor, and a stage's
-// weights are one contiguous 16 KB (L2) or 32 KB (L1) read.
+// Every expert's weights live in one buffer, packed once into blocks of 128
+// rows x 128 bytes already in the 128-byte swizzle ([E*N/128][K/256] blocks;
+// for L1 the gate and up blocks of the same features and K step adjacent), so
+// the expert is an offset, not a new descriptor, and a stage's weights are one
+// contiguous 16 KB (L2) or 32 KB (L1) bulk copy.  Token tiles use tensor maps.
 // Tiles are numbered expert-major, weight-tile-major, token-tile-minor, so CTAs
 // working on the same expert's weight tile run together and share it in L2.
 #include <cuda.h>
@@ -47,10 +47,13 @@
 
 namespace megamoe {
 
-constexpr int kGemmThreads = 320;
-constexpr int kSfWarp0 = 6;  // warps 6..9 write block scales into TMEM
+constexpr int kGemmThreads = 448;
+constexpr int kSfWarp0 = 6;    // warps 6..9 write block scales into TMEM
+constexpr int kEpiWarp1 = 10;  // warps 2..5 and 10..13 drain the accumulators
+constexpr int kEpiWarps = 8;
 
 struct GemmArgs {
+  const uint8_t* w_codes;  // packed, pre-swizzled 16 KB blocks (megamoe_pack_weight_codes)
   const uint8_t* w_sf;  // atom layout [E*N/128][K/64][512]
   const float* w_gs;    // [E][G]
   const float* a_gs;    // device scalar
@@ -87,7 +90,11 @@ struct GemmCfg {
   static constexpr int BAR_OFF = STAGES * STAGE;
   static constexpr int TOFF_OFF = BAR_OFF + 512;
   static constexpr int INFO_OFF = TOFF_OFF + 4 * (MEGAMOE_MAX_EXPERTS + 1);  // counts, poffs
-  static constexpr int SMEM = 1024 + INFO_OFF + 8 * MEGAMOE_MAX_EXPERTS;
+  // per epilogue warp: 16 token rows x 32 features of output, staged so that
+  // global stores are 16-byte vectors along the feature axis
+  static constexpr int STG_BYTES = 16 * 32 * (EPI == MEGAMOE_EPI_SILU_MUL ? 2 : 4);
+  static constexpr int STG_OFF = (INFO_OFF + 8 * MEGAMOE_MAX_EXPERTS + 15) / 16 * 16;
+  static constexpr int SMEM = 1024 + STG_OFF + kEpiWarps * STG_BYTES;
   static constexpr uint32_t IDESC = idesc_nvf4(128, BN);
   static_assert(SF_COL0 + STAGES * SF_COLS <= 512, "tensor memory budget");
   static_assert(SMEM <= 232448, "shared memory budget");
@@ -164,7 +171,7 @@ __device__ __forceinline__ void mbar_drain(uint64_t* bar, uint32_t parity) {
 
 template <int BN, int EPI, int STAGES>
 __global__ void __launch_bounds__(kGemmThreads, 1)
-    k_grouped_gemm(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_a,
+    k_grouped_gemm(const __grid_constant__ CUtensorMap tm_a,
                    const __grid_constant__ CUtensorMap tm_asf, const GemmArgs p) {
   using C = GemmCfg<BN, EPI, STAGES>;
   extern __shared__ uint8_t smem_raw[];
@@ -191,7 +198,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const int slices = K / 64;
 
   if (warp == 0 && lane == 0) {
-    prefetch_tensormap(&tm_w);
     prefetch_tensormap(&tm_a);
     prefetch_tensormap(&tm_asf);
   }
@@ -210,7 +216,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
     for (int a = 0; a < C::ACC_STAGES; ++a) {
       mbar_init(&acc_full[a], 1);
-      mbar_init(&acc_empty[a], 4);
+      mbar_init(&acc_empty[a], kEpiWarps);
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -260,11 +266,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                       C::SFW, &sf_full[stage], pol_w);
           tma_load_2d(sb + C::OFF_SFA_RAW, &tm_asf, &sf_full[stage], kt * 16, a_row0, pol_a);
           mbar_arrive_expect_tx(&full[stage], C::TX);
-          tma_load_2d(sb + C::OFF_A, &tm_w, &full[stage], 0, (w_blk0 + kt * C::G) * 128,
-                      pol_w);
-          if (C::G == 2)
-            tma_load_2d(sb + C::OFF_A + C::A_TILE, &tm_w, &full[stage], 0,
-                        (w_blk0 + kt * 2 + 1) * 128, pol_w);
+          // the stage's weight blocks (gate then up for L1) are contiguous and
+          // pre-swizzled: one bulk copy
+          bulk_load(sb + C::OFF_A, p.w_codes + static_cast<int64_t>(w_blk0 + kt * C::G) * 16384,
+                    C::G * C::A_TILE, &full[stage], pol_w);
           tma_load_2d(sb + C::OFF_B, &tm_a, &full[stage], kt * 128, a_row0, pol_a);
           issued_parity[stage] = static_cast<int>(phase);
           if (++stage == STAGES) {
@@ -330,7 +335,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       mbar_drain(drain, 0);
     }
     __syncwarp();
-  } else if (warp >= kSfWarp0) {
+  } else if (warp >= kSfWarp0 && warp < kEpiWarp1) {
     // --------------------------------------------------------- scale writers
     // Weight atom of slice c: byte 16 i + 4 j + b = row 32 j + i, block 4c + b;
     // lane i writes word j to column (4c + j) of lane quarter*32 + i.  Token
@@ -379,7 +384,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
   } else {
     // -------------------------------------------------------------- epilogue
-    const int q = warp & 3;  // the TMEM lane quarter this warp may access
+    // Two warps per TMEM lane quarter (a warp reaches only quarter warp % 4)
+    // take alternate 16-column chunks of the tile.  Lane i holds feature i of
+    // the quarter for 16 tokens; the chunk is transposed through the warp's
+    // staging buffer so that each global store is a 16-byte run of features.
+    const int q = warp & 3;
+    const int half = warp >= kEpiWarp1 ? 1 : 0;
+    uint8_t* stg = smem + C::STG_OFF + (half * 4 + q) * C::STG_BYTES;
     const float a_gs = __ldg(p.a_gs);
     int acc = 0;
     uint32_t acc_phase = 0;
@@ -388,7 +399,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const TileInfo ti = decode_tile<BN>(tile, s_toff, E, s_cnt, s_poff);
       const int m_valid = min(BN, ti.count - ti.nt * BN);
       const int64_t row0 = ti.poff + static_cast<int64_t>(ti.nt) * BN;
-      const int f = ti.mt * 128 + q * 32 + lane;
+      const int f0 = ti.mt * 128 + q * 32;  // first feature of this warp's quarter
       float alpha0, alpha1 = 0.f;
       if (C::G == 2) {
         alpha0 = 1.0f / (a_gs * __ldg(p.w_gs + 2 * ti.e));
@@ -400,32 +411,51 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       tc_fence_after();
       const uint32_t lane_base =
           tmem + acc * C::ACC_COLS + (static_cast<uint32_t>(q * 32) << 16);
-      for (int n0 = 0; n0 < m_valid; n0 += 16) {
+      for (int n0 = 16 * half; n0 < m_valid; n0 += 32) {
+        const int rows = min(16, m_valid - n0);
         uint32_t g[16];
         tmem_ld_32x32b_x16(lane_base + n0, g);
         if (C::G == 2) {
           uint32_t u[16];
           tmem_ld_32x32b_x16(lane_base + BN + n0, u);
           tmem_ld_wait();
-          __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
+          __nv_bfloat16* s = reinterpret_cast<__nv_bfloat16*>(stg);
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
-            if (n0 + j < m_valid) {
-              const float gv = __uint_as_float(g[j]) * alpha0;
-              const float uv = __uint_as_float(u[j]) * alpha1;
-              const float h = gv / (1.0f + expf(-gv)) * uv;
-              const __nv_bfloat16 hb = __float2bfloat16_rn(h);
-              amax = fmaxf(amax, fabsf(__bfloat162float(hb)));
-              out[(row0 + n0 + j) * p.ld_out + f] = hb;
-            }
+            const float gv = __uint_as_float(g[j]) * alpha0;
+            const float uv = __uint_as_float(u[j]) * alpha1;
+            // SiLU(g) * u = g * u / (1 + e^-g); e^-g = inf gives the limit 0
+            const __nv_bfloat16 hb = __float2bfloat16_rn(__fdividef(gv, 1.0f + __expf(-gv)) * uv);
+            if (j < rows) amax = fmaxf(amax, fabsf(__bfloat162float(hb)));
+            s[j * 32 + lane] = hb;
+          }
+          __syncwarp();
+          // 16 rows x 64 bytes = 64 chunks of 16 bytes, two per lane
+          __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
+#pragma unroll
+          for (int i = 0; i < 2; ++i) {
+            const int c = lane + 32 * i, r = c >> 2;
+            if (r < rows)
+              *reinterpret_cast<uint4*>(out + (row0 + n0 + r) * p.ld_out + f0 + 8 * (c & 3)) =
+                  reinterpret_cast<const uint4*>(stg)[c];
           }
         } else {
           tmem_ld_wait();
+          float* s = reinterpret_cast<float*>(stg);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) s[j * 32 + lane] = __uint_as_float(g[j]) * alpha0;
+          __syncwarp();
+          // 16 rows x 128 bytes = 128 chunks of 16 bytes, four per lane
           float* out = reinterpret_cast<float*>(p.out);
 #pragma unroll
-          for (int j = 0; j < 16; ++j)
-            if (n0 + j < m_valid) out[(row0 + n0 + j) * p.ld_out + f] = __uint_as_float(g[j]) * alpha0;
+          for (int i = 0; i < 4; ++i) {
+            const int c = lane + 32 * i, r = c >> 3;
+            if (r < rows)
+              *reinterpret_cast<uint4*>(out + (row0 + n0 + r) * p.ld_out + f0 + 4 * (c & 7)) =
+                  reinterpret_cast<const uint4*>(stg)[c];
+          }
         }
+        __syncwarp();  // the staging buffer is rewritten by the next chunk
       }
       tc_fence_before();
       __syncwarp();
@@ -506,15 +536,14 @@ static bool make_scales_map(CUtensorMap* map, const void* base, uint64_t rows, u
 }
 
 template <int BN, int EPI, int STAGES>
-static cudaError_t launch_cfg(const CUtensorMap& tm_w, const CUtensorMap& tm_a,
-                              const CUtensorMap& tm_asf, const GemmArgs& a, cudaStream_t stream) {
+static cudaError_t launch_cfg(const CUtensorMap& tm_a, const CUtensorMap& tm_asf,
+                              const GemmArgs& a, cudaStream_t stream) {
   using C = GemmCfg<BN, EPI, STAGES>;
   auto kern = k_grouped_gemm<BN, EPI, STAGES>;
   cudaError_t err =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (err != cudaSuccess) return err;
-  return launch_pdl(kern, dim3(num_sms()), dim3(kGemmThreads), C::SMEM, stream, tm_w, tm_a, tm_asf,
-                    a);
+  return launch_pdl(kern, dim3(num_sms()), dim3(kGemmThreads), C::SMEM, stream, tm_a, tm_asf, a);
 }
 
 static uint64_t g_wait_limit_ns = kWaitTimeoutNs;
@@ -534,30 +563,28 @@ int pick_tile_n(double expected) {
 cudaError_t launch_grouped_gemm(const GemmLaunch& g, cudaStream_t stream) {
   if (g.act_rows == 0 || g.E == 0) return cudaSuccess;
   const int bn = g.tile_n;
-  CUtensorMap tm_w, tm_a, tm_asf;
-  if (!make_codes_map(&tm_w, g.w_codes, static_cast<uint64_t>(g.E) * g.N * (g.K / 256), 128,
-                      128) ||
-      !make_codes_map(&tm_a, g.act_codes, static_cast<uint64_t>(g.act_rows), g.K / 2, bn) ||
+  CUtensorMap tm_a, tm_asf;
+  if (!make_codes_map(&tm_a, g.act_codes, static_cast<uint64_t>(g.act_rows), g.K / 2, bn) ||
       !make_scales_map(&tm_asf, g.act_scales, static_cast<uint64_t>(g.act_rows), g.K / 16, bn))
     return cudaErrorInvalidValue;
-  GemmArgs a{g.w_scales, g.w_gs,     g.act_gs, g.offsets,         g.padded_offsets, g.out,
-             g.ld_out,   g.out_amax, g.status, wait_limit_ns(), g.E,             g.N,
-             g.K};
+  GemmArgs a{g.w_codes,        g.w_scales, g.w_gs,     g.act_gs, g.offsets,
+             g.padded_offsets, g.out,      g.ld_out,   g.out_amax, g.status,
+             wait_limit_ns(),  g.E,        g.N,        g.K};
   if (g.epilogue == MEGAMOE_EPI_SILU_MUL) {
     if (g.out_amax && g.zero_amax) {
       cudaError_t err = cudaMemsetAsync(g.out_amax, 0, sizeof(float), stream);
       if (err != cudaSuccess) return err;
     }
     switch (bn) {
-      case 32: return launch_cfg<32, MEGAMOE_EPI_SILU_MUL, 5>(tm_w, tm_a, tm_asf, a, stream);
-      case 64: return launch_cfg<64, MEGAMOE_EPI_SILU_MUL, 4>(tm_w, tm_a, tm_asf, a, stream);
-      case 128: return launch_cfg<128, MEGAMOE_EPI_SILU_MUL, 3>(tm_w, tm_a, tm_asf, a, stream);
+      case 32: return launch_cfg<32, MEGAMOE_EPI_SILU_MUL, 5>(tm_a, tm_asf, a, stream);
+      case 64: return launch_cfg<64, MEGAMOE_EPI_SILU_MUL, 4>(tm_a, tm_asf, a, stream);
+      case 128: return launch_cfg<128, MEGAMOE_EPI_SILU_MUL, 3>(tm_a, tm_asf, a, stream);
     }
   } else {
     switch (bn) {
-      case 32: return launch_cfg<32, MEGAMOE_EPI_F32, 8>(tm_w, tm_a, tm_asf, a, stream);
-      case 64: return launch_cfg<64, MEGAMOE_EPI_F32, 7>(tm_w, tm_a, tm_asf, a, stream);
-      case 128: return launch_cfg<128, MEGAMOE_EPI_F32, 5>(tm_w, tm_a, tm_asf, a, stream);
+      case 32: return launch_cfg<32, MEGAMOE_EPI_F32, 8>(tm_a, tm_asf, a, stream);
+      case 64: return launch_cfg<64, MEGAMOE_EPI_F32, 7>(tm_a, tm_asf, a, stream);
+      case 128: return launch_cfg<128, MEGAMOE_EPI_F32, 5>(tm_a, tm_asf, a, stream);
     }
   }
   return cudaErrorInvalidValue;

@@ -14,9 +14,9 @@
 //           once and written to each of its k expert rows.
 // k_swizzle row-major block scales -> the tensor-core atom layout (weights,
 //           once, off the hot path).
-// k_pack    row-major E2M1 codes -> tile-major blocks of 128 rows x 128 bytes
-//           (weights, once): every TMA box of the grouped GEMM then reads one
-//           contiguous 16 KB block instead of 128 rows 3.5 KB apart.
+// k_pack    row-major E2M1 codes -> tile-major blocks of 128 rows x 128 bytes,
+//           pre-swizzled (weights, once): the grouped GEMM fetches a stage's
+//           weights with one contiguous bulk copy.
 #include <cuda_runtime.h>
 
 #include "common.cuh"
@@ -193,7 +193,9 @@ __global__ void __launch_bounds__(256) k_pack(const uint8_t* __restrict__ src, i
     } else {
       block = (r >> 7) * KT + kt;
     }
-    const int64_t o = (block * 128 + (r & 127)) * 128 + (c & 7) * 16;
+    // 16-byte chunk j of row r goes to chunk j ^ (r % 8): the 128-byte swizzle
+    // the tensor cores read, so a plain bulk copy lands the block ready to use
+    const int64_t o = (block * 128 + (r & 127)) * 128 + (((c & 7) ^ (r & 7)) * 16);
     *reinterpret_cast<uint4*>(dst + o) =
         __ldg(reinterpret_cast<const uint4*>(src + r * (K / 2)) + c);
   }

@@ -149,12 +149,24 @@ def test_pack_weight_codes_layout(cuda_lib):
     rows, K = 512, 768
     c = rng.integers(0, 256, (rows, K // 2), dtype=np.uint8)
     got = megamoe.pack_weight_codes(torch.from_numpy(c).cuda()).cpu().numpy().reshape(-1)
+    # 128-byte swizzle inside a block: 16-byte chunk j of row i lands at j ^ (i % 8)
+    i = np.arange(128)[:, None]
+    j = np.arange(8)[None, :]
+    src_chunk = j ^ (i % 8)  # the chunk stored at position j of row i
+
+    def swz(blocks):  # [..., 128 rows, 128 bytes] -> swizzled
+        ch = blocks.reshape(blocks.shape[:-1] + (8, 16))
+        return np.take_along_axis(ch, np.broadcast_to(src_chunk[..., None], ch.shape), -2
+                                  ).reshape(blocks.shape)
+
     # blocks of 128 rows x 128 bytes, ordered [rows/128][K/256]
-    want = c.reshape(rows // 128, 128, K // 256, 128).transpose(0, 2, 1, 3).reshape(-1)
+    want = swz(c.reshape(rows // 128, 128, K // 256, 128).transpose(0, 2, 1, 3)).reshape(-1)
     assert np.array_equal(got, want)
+    # a hand-checked byte: row 3, chunk 1 of block (0, 0) sits at chunk 1 ^ 3 = 2
+    assert np.array_equal(got[3 * 128 + 2 * 16: 3 * 128 + 3 * 16], c[3, 16:32])
     # gate/up pairing: groups of 2H rows, [group][H/128][K/256][gate, up]
     H = 128
     got = megamoe.pack_weight_codes(torch.from_numpy(c).cuda(), H).cpu().numpy().reshape(-1)
-    want = (c.reshape(rows // (2 * H), 2, H // 128, 128, K // 256, 128)
-            .transpose(0, 2, 4, 1, 3, 5).reshape(-1))
+    want = swz(c.reshape(rows // (2 * H), 2, H // 128, 128, K // 256, 128)
+               .transpose(0, 2, 4, 1, 3, 5)).reshape(-1)
     assert np.array_equal(got, want)
