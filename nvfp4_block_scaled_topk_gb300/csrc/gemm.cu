@@ -234,7 +234,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------------------ producer
-      const uint64_t pol_w = policy_evict_first();
+      // A weight tile read by one token tile is dead after it (evict first);
+      // one that the expert's next token tiles re-read stays (evict normal).
+      const uint64_t pol_w_once = policy_evict_first();
+      const uint64_t pol_w_reused = policy_evict_normal();
       const uint64_t pol_a = policy_evict_last();
       int stage = 0;
       uint32_t phase = 0;
@@ -248,6 +251,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         // first 128-row code block of this tile's K = 0 step (paired for L1)
         const int w_blk0 = C::G == 2 ? ((ti.e * MT + ti.mt) * KT) * 2 : (w_row0 >> 7) * KT;
         const int a_row0 = ti.poff + ti.nt * BN;
+        const uint64_t pol_w = ti.count > BN ? pol_w_reused : pol_w_once;
         for (int kt = 0; kt < KT; ++kt) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.status, p.wait_limit_ns)) {
             ok = false;
