@@ -89,11 +89,12 @@ struct GemmCfg {
   static constexpr int SF_COL0 = ACC_STAGES * ACC_COLS;
   static constexpr int BAR_OFF = STAGES * STAGE;
   static constexpr int TOFF_OFF = BAR_OFF + 512;
-  static constexpr int INFO_OFF = TOFF_OFF + 4 * (MEGAMOE_MAX_EXPERTS + 1);  // counts, poffs
-  // per epilogue warp: 16 token rows x 32 features of output, staged so that
-  // global stores are 16-byte vectors along the feature axis
-  static constexpr int STG_BYTES = 16 * 32 * (EPI == MEGAMOE_EPI_SILU_MUL ? 2 : 4);
-  static constexpr int STG_OFF = (INFO_OFF + 8 * MEGAMOE_MAX_EXPERTS + 15) / 16 * 16;
+  // per epilogue warp: STG_ROWS token rows x 32 features of output, staged so
+  // that global stores are 16-byte vectors along the feature axis (512 bytes
+  // for bf16, 2 KB for float)
+  static constexpr int STG_ROWS = EPI == MEGAMOE_EPI_SILU_MUL ? 8 : 16;
+  static constexpr int STG_BYTES = STG_ROWS * 32 * (EPI == MEGAMOE_EPI_SILU_MUL ? 2 : 4);
+  static constexpr int STG_OFF = (TOFF_OFF + 4 * (MEGAMOE_MAX_EXPERTS + 1) + 15) / 16 * 16;
   static constexpr int SMEM = 1024 + STG_OFF + kEpiWarps * STG_BYTES;
   static constexpr uint32_t IDESC = idesc_nvf4(128, BN);
   static_assert(SF_COL0 + STAGES * SF_COLS <= 512, "tensor memory budget");
@@ -102,13 +103,14 @@ struct GemmCfg {
 };
 
 struct TileInfo {
-  int e, mt, nt, count, poff;
+  int e, mt, nt, ntiles;  // expert, feature tile, token tile, token tiles of e
 };
 
-template <int BN>
-__device__ __forceinline__ TileInfo decode_tile(int tile, const int* s_toff, int E,
-                                                const int* s_cnt, const int* s_poff) {
-  int lo = 0, hi = E - 1;
+// Tile -> (expert, feature tile, token tile) from the tile prefix s_toff alone;
+// the expert is searched in [lo, E - 1] (a CTA's tiles never go back in e).
+__device__ __forceinline__ TileInfo decode_tile(int tile, const int* s_toff, int E, int MT,
+                                                int lo = 0) {
+  int hi = E - 1;
   while (lo < hi) {  // largest e with s_toff[e] <= tile; it always owns tiles
     const int mid = (lo + hi + 1) >> 1;
     if (s_toff[mid] <= tile) lo = mid;
@@ -116,20 +118,17 @@ __device__ __forceinline__ TileInfo decode_tile(int tile, const int* s_toff, int
   }
   TileInfo t;
   t.e = lo;
-  t.count = s_cnt[lo];
-  t.poff = s_poff[lo];
-  const int ntiles = (t.count + BN - 1) / BN;
+  t.ntiles = (s_toff[lo + 1] - s_toff[lo]) / MT;
   const int local = tile - s_toff[lo];
-  t.mt = local / ntiles;
-  t.nt = local - t.mt * ntiles;
+  t.mt = local / t.ntiles;
+  t.nt = local - t.mt * t.ntiles;
   return t;
 }
 
-// s_toff[e] = first tile of expert e, s_toff[E] = total tiles; s_cnt[e] and
-// s_poff[e] = expert e's row count and first padded row.  All threads.
+// s_toff[e] = first tile of expert e, s_toff[E] = total tiles.  All threads.
 template <int BN>
-__device__ void build_tile_offsets(const int32_t* offsets, const int32_t* padded_offsets, int E,
-                                   int MT, int* s_toff, int* s_cnt, int* s_poff, int* s_scan) {
+__device__ void build_tile_offsets(const int32_t* offsets, int E, int MT, int* s_toff,
+                                   int* s_scan) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int per = (E + kGemmThreads - 1) / kGemmThreads;
   const int e0 = tid * per, e1 = min(E, e0 + per);
@@ -138,8 +137,6 @@ __device__ void build_tile_offsets(const int32_t* offsets, const int32_t* padded
     const int cnt = __ldg(offsets + e + 1) - __ldg(offsets + e);
     const int t = cnt > 0 ? (cnt + BN - 1) / BN * MT : 0;
     s_toff[e] = t;
-    s_cnt[e] = cnt;
-    s_poff[e] = __ldg(padded_offsets + e);
     sum += t;
   }
   int x = sum;
@@ -187,8 +184,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   int* s_toff = reinterpret_cast<int*>(smem + C::TOFF_OFF);
-  int* s_cnt = reinterpret_cast<int*>(smem + C::INFO_OFF);
-  int* s_poff = s_cnt + MEGAMOE_MAX_EXPERTS;
   __shared__ int s_scan[kGemmThreads / 32];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -203,7 +198,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   }
   pdl_wait();  // the routing offsets and activations come from earlier kernels
   pdl_trigger();
-  build_tile_offsets<BN>(p.offsets, p.padded_offsets, E, MT, s_toff, s_cnt, s_poff, s_scan);
+  build_tile_offsets<BN>(p.offsets, E, MT, s_toff, s_scan);
   const int total = s_toff[E];
   if (static_cast<int>(blockIdx.x) >= total) return;  // uniform: no work for this CTA
 
@@ -244,14 +239,22 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       int issued_parity[STAGES];
       for (int s = 0; s < STAGES; ++s) issued_parity[s] = -1;
       bool ok = true;
+      // the next tile and its expert's first padded row are found one tile ahead
+      TileInfo ti_next = decode_tile(blockIdx.x, s_toff, E, MT);
+      int poff_next = __ldg(p.padded_offsets + ti_next.e);
       for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
-        const TileInfo ti = decode_tile<BN>(tile, s_toff, E, s_cnt, s_poff);
+        const TileInfo ti = ti_next;
+        const int poff = poff_next;
+        if (tile + static_cast<int>(gridDim.x) < total) {
+          ti_next = decode_tile(tile + gridDim.x, s_toff, E, MT, ti.e);
+          poff_next = __ldg(p.padded_offsets + ti_next.e);
+        }
         const int w_row0 = ti.e * N + ti.mt * 128;
         const int w_row1 = ti.e * N + N / 2 + ti.mt * 128;  // up rows (L1 only)
         // first 128-row code block of this tile's K = 0 step (paired for L1)
         const int w_blk0 = C::G == 2 ? ((ti.e * MT + ti.mt) * KT) * 2 : (w_row0 >> 7) * KT;
-        const int a_row0 = ti.poff + ti.nt * BN;
-        const uint64_t pol_w = ti.count > BN ? pol_w_reused : pol_w_once;
+        const int a_row0 = poff + ti.nt * BN;
+        const uint64_t pol_w = ti.ntiles > 1 ? pol_w_reused : pol_w_once;
         for (int kt = 0; kt < KT; ++kt) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.status, p.wait_limit_ns)) {
             ok = false;
@@ -399,18 +402,33 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     float amax = 0.f;
+    // an expert's row count, first padded row and global scales, fetched one
+    // tile ahead so that their latency hides behind the current tile
+    struct ExpertInfo {
+      TileInfo ti;
+      int count, poff;
+      float gs0, gs1;
+    };
+    auto fetch = [&](int tile, int e_lo) {
+      ExpertInfo x;
+      x.ti = decode_tile(tile, s_toff, E, MT, e_lo);
+      const int e = x.ti.e;
+      x.count = __ldg(p.offsets + e + 1) - __ldg(p.offsets + e);
+      x.poff = __ldg(p.padded_offsets + e);
+      x.gs0 = __ldg(p.w_gs + C::G * e);
+      x.gs1 = C::G == 2 ? __ldg(p.w_gs + 2 * e + 1) : 1.f;
+      return x;
+    };
+    ExpertInfo next = fetch(blockIdx.x, 0);
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
-      const TileInfo ti = decode_tile<BN>(tile, s_toff, E, s_cnt, s_poff);
-      const int m_valid = min(BN, ti.count - ti.nt * BN);
-      const int64_t row0 = ti.poff + static_cast<int64_t>(ti.nt) * BN;
+      const ExpertInfo cur = next;
+      const TileInfo& ti = cur.ti;
+      if (tile + static_cast<int>(gridDim.x) < total) next = fetch(tile + gridDim.x, ti.e);
+      const int m_valid = min(BN, cur.count - ti.nt * BN);
+      const int64_t row0 = cur.poff + static_cast<int64_t>(ti.nt) * BN;
       const int f0 = ti.mt * 128 + q * 32;  // first feature of this warp's quarter
-      float alpha0, alpha1 = 0.f;
-      if (C::G == 2) {
-        alpha0 = 1.0f / (a_gs * __ldg(p.w_gs + 2 * ti.e));
-        alpha1 = 1.0f / (a_gs * __ldg(p.w_gs + 2 * ti.e + 1));
-      } else {
-        alpha0 = 1.0f / (a_gs * __ldg(p.w_gs + ti.e));
-      }
+      const float alpha0 = 1.0f / (a_gs * cur.gs0);
+      const float alpha1 = C::G == 2 ? 1.0f / (a_gs * cur.gs1) : 0.f;
       if (!mbar_wait(&acc_full[acc], acc_phase, abort_flag, p.status, p.wait_limit_ns)) break;
       tc_fence_after();
       const uint32_t lane_base =
@@ -424,24 +442,26 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           tmem_ld_32x32b_x16(lane_base + BN + n0, u);
           tmem_ld_wait();
           __nv_bfloat16* s = reinterpret_cast<__nv_bfloat16*>(stg);
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const float gv = __uint_as_float(g[j]) * alpha0;
-            const float uv = __uint_as_float(u[j]) * alpha1;
-            // SiLU(g) * u = g * u / (1 + e^-g); e^-g = inf gives the limit 0
-            const __nv_bfloat16 hb = __float2bfloat16_rn(__fdividef(gv, 1.0f + __expf(-gv)) * uv);
-            if (j < rows) amax = fmaxf(amax, fabsf(__bfloat162float(hb)));
-            s[j * 32 + lane] = hb;
-          }
-          __syncwarp();
-          // 16 rows x 64 bytes = 64 chunks of 16 bytes, two per lane
           __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
 #pragma unroll
-          for (int i = 0; i < 2; ++i) {
-            const int c = lane + 32 * i, r = c >> 2;
+          for (int h8 = 0; h8 < 16; h8 += 8) {  // two staged halves of 8 rows
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const float gv = __uint_as_float(g[h8 + j]) * alpha0;
+              const float uv = __uint_as_float(u[h8 + j]) * alpha1;
+              // SiLU(g) * u = g * u / (1 + e^-g); e^-g = inf gives the limit 0
+              const __nv_bfloat16 hb =
+                  __float2bfloat16_rn(__fdividef(gv, 1.0f + __expf(-gv)) * uv);
+              if (h8 + j < rows) amax = fmaxf(amax, fabsf(__bfloat162float(hb)));
+              s[j * 32 + lane] = hb;
+            }
+            __syncwarp();
+            // 8 rows x 64 bytes = 32 chunks of 16 bytes, one per lane
+            const int r = h8 + (lane >> 2);
             if (r < rows)
-              *reinterpret_cast<uint4*>(out + (row0 + n0 + r) * p.ld_out + f0 + 8 * (c & 3)) =
-                  reinterpret_cast<const uint4*>(stg)[c];
+              *reinterpret_cast<uint4*>(out + (row0 + n0 + r) * p.ld_out + f0 + 8 * (lane & 3)) =
+                  reinterpret_cast<const uint4*>(stg)[lane];
+            __syncwarp();
           }
         } else {
           tmem_ld_wait();
@@ -582,7 +602,7 @@ cudaError_t launch_grouped_gemm(const GemmLaunch& g, cudaStream_t stream) {
     switch (bn) {
       case 32: return launch_cfg<32, MEGAMOE_EPI_SILU_MUL, 5>(tm_a, tm_asf, a, stream);
       case 64: return launch_cfg<64, MEGAMOE_EPI_SILU_MUL, 4>(tm_a, tm_asf, a, stream);
-      case 128: return launch_cfg<128, MEGAMOE_EPI_SILU_MUL, 3>(tm_a, tm_asf, a, stream);
+      case 128: return launch_cfg<128, MEGAMOE_EPI_SILU_MUL, 4>(tm_a, tm_asf, a, stream);
     }
   } else {
     switch (bn) {
