@@ -236,8 +236,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const uint64_t pol_a = policy_evict_last();
       int stage = 0;
       uint32_t phase = 0;
-      int issued_parity[STAGES];
-      for (int s = 0; s < STAGES; ++s) issued_parity[s] = -1;
+      int issued = 0;  // stages issued; issue i used slot i % STAGES, parity (i / STAGES) & 1
       bool ok = true;
       // the next tile and its expert's first padded row are found one tile ahead
       TileInfo ti_next = decode_tile(blockIdx.x, s_toff, E, MT);
@@ -255,6 +254,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const int w_blk0 = C::G == 2 ? ((ti.e * MT + ti.mt) * KT) * 2 : (w_row0 >> 7) * KT;
         const int a_row0 = poff + ti.nt * BN;
         const uint64_t pol_w = ti.ntiles > 1 ? pol_w_reused : pol_w_once;
+        // this tile's K = 0 weight scales (gate, up) and codes; each K step
+        // advances them by 4 atoms and by G code blocks
+        const uint8_t* sfw0 = p.w_sf + static_cast<int64_t>(w_row0 >> 7) * slices * 512;
+        const uint8_t* sfw1 = p.w_sf + static_cast<int64_t>(w_row1 >> 7) * slices * 512;
+        const uint8_t* wcod = p.w_codes + static_cast<int64_t>(w_blk0) * 16384;
         for (int kt = 0; kt < KT; ++kt) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.status, p.wait_limit_ns)) {
             ok = false;
@@ -264,21 +268,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           // scales first, on their own barrier: the scale warps move them into
           // tensor memory while the codes are still landing
           mbar_arrive_expect_tx(&sf_full[stage], C::SF_TX);
-          bulk_load(sb + C::OFF_SFW,
-                    p.w_sf + (static_cast<int64_t>(w_row0 >> 7) * slices + 4 * kt) * 512, C::SFW,
-                    &sf_full[stage], pol_w);
+          bulk_load(sb + C::OFF_SFW, sfw0 + kt * 2048, C::SFW, &sf_full[stage], pol_w);
           if (C::G == 2)
-            bulk_load(sb + C::OFF_SFW + C::SFW,
-                      p.w_sf + (static_cast<int64_t>(w_row1 >> 7) * slices + 4 * kt) * 512,
-                      C::SFW, &sf_full[stage], pol_w);
+            bulk_load(sb + C::OFF_SFW + C::SFW, sfw1 + kt * 2048, C::SFW, &sf_full[stage], pol_w);
           tma_load_2d(sb + C::OFF_SFA_RAW, &tm_asf, &sf_full[stage], kt * 16, a_row0, pol_a);
           mbar_arrive_expect_tx(&full[stage], C::TX);
           // the stage's weight blocks (gate then up for L1) are contiguous and
           // pre-swizzled: one bulk copy
-          bulk_load(sb + C::OFF_A, p.w_codes + static_cast<int64_t>(w_blk0 + kt * C::G) * 16384,
-                    C::G * C::A_TILE, &full[stage], pol_w);
+          bulk_load(sb + C::OFF_A, wcod + kt * (C::G * 16384), C::G * C::A_TILE, &full[stage], pol_w);
           tma_load_2d(sb + C::OFF_B, &tm_a, &full[stage], kt * 128, a_row0, pol_a);
-          issued_parity[stage] = static_cast<int>(phase);
+          ++issued;
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
@@ -286,11 +285,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
       }
       if (!ok) {  // unwinding: let every copy already in flight land first
-        for (int s = 0; s < STAGES; ++s)
-          if (issued_parity[s] >= 0) {
-            mbar_drain(&full[s], static_cast<uint32_t>(issued_parity[s]));
-            mbar_drain(&sf_full[s], static_cast<uint32_t>(issued_parity[s]));
-          }
+        for (int s = 0; s < STAGES && s < issued; ++s) {
+          const uint32_t parity = static_cast<uint32_t>((issued - 1 - s) / STAGES) & 1u;
+          mbar_drain(&full[s], parity);
+          mbar_drain(&sf_full[s], parity);
+        }
       }
     }
     __syncwarp();
