@@ -344,6 +344,7 @@ def run_ours(args):
     value = tokens_total / (ms * 1e-3)
     flops = inputs.algorithmic_flops(cfg, valid_slots)
     alg_bytes = inputs.algorithmic_bytes(cfg, active)
+    w_step = active * 3 * cfg.d * cfg.I * (0.5 + 1.0 / 16)  # weight bytes one step reads
     w_el = cfg.d * cfg.I * (0.5 + 1.0 / 16)
     l1_bytes = active * 2 * w_el + valid_slots * cfg.d * (0.5 + 1 / 16) + valid_slots * cfg.I * 2
     l1_gbs = l1_bytes / (l1_ms * 1e-3) / 1e9
@@ -363,10 +364,12 @@ def run_ours(args):
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "nvfp4 (e2m1 x e4m3 scales, fp32 acc)",
             "data": "synthetic",
-            "config": {"workload": f"{cfg.name}: MegaMoE decode, E={cfg.E} top-{cfg.k} d={cfg.d} "
-                                   f"I={cfg.I} T={cfg.T}, NVFP4 weights resident",
+            "config": {"workload": f"{cfg.name}: MegaMoE routed-expert forward, E={cfg.E} "
+                                   f"top-{cfg.k} d={cfg.d} I={cfg.I} T={cfg.T}, NVFP4 weights "
+                                   "resident",
                        "global_batch": cfg.T * world, "parallelism": f"replicas x{world}",
-                       "l2": "inputs larger than L2 (≈1.1 GB of expert weights read per step)",
+                       "l2": f"inputs larger than L2 (~{w_step / 1e9:.2f} GB of expert weights "
+                             "read per step, L2 is 0.13 GB)",
                        "active_experts": active, "valid_slots": valid_slots},
             "tflops": flops / (ms * 1e-3) / 1e12,
             "hbm_gbs": alg_bytes / (ms * 1e-3) / 1e9,

@@ -21,6 +21,9 @@ its "Test Plan" Phase 2; the activation statistics amax 1.27 / std 0.09 are
             to +-8, ids = top-6 of N(0,1) logits + bias_e, bias_e =
             -1.1 ln(rank_e) (rank from a seeded permutation; Zipf-1.1 load)
   large     384 experts, top-6, d=7168, I=2048, 16384 tokens, uniform ids
+  prefill64 64 experts, top-6, d=7168, I=2048, 2048 tokens, uniform ids: a
+            prefill-shaped case (about 192 tokens per expert) whose weights
+            (about 1.5 GB) are small enough for multi-pass profiler captures
 
 topk_weights are the softmax of the N(0,1) logits at the selected ids.
 
@@ -101,6 +104,9 @@ CONFIGS = {
     "prefill": MoEConfig("prefill", 384, 6, 7168, 2048, 4096, "zipf", seed=1004,
                          outlier_frac=1e-3),
     "large": MoEConfig("large", 384, 6, 7168, 2048, 16384, "uniform", seed=1005),
+    # prefill-shaped case small enough for multi-pass profiler captures:
+    # 64 experts hold about 1.5 GB of weights, ~192 tokens per expert
+    "prefill64": MoEConfig("prefill64", 64, 6, 7168, 2048, 2048, "uniform", seed=1006),
 }
 
 
