@@ -322,6 +322,8 @@ megamoe_status megamoe_forward(const megamoe_weights* w, const uint16_t* x,
   g.tile_n = tile_n;
   g.status = wk.status;
   g.zero_amax = false;
+  // routing finished before the quantiser (and the requantiser) ran
+  g.early_weights = true;
   e = launch_grouped_gemm(g, s);
   if (e != cudaSuccess) return MEGAMOE_ERR_CUDA;
   // 5. requantise the valid rows of h with gs from amax(h) (slot by slot)

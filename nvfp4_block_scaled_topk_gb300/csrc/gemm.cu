@@ -65,6 +65,10 @@ struct GemmArgs {
   uint32_t* status;
   uint64_t wait_limit_ns;  // bound of every pipeline wait (unwinding waits use 4 s)
   int E, N, K;
+  // 1: the routing offsets were complete before the preceding kernel started
+  // (the forward's order), so the tile schedule is built and the first weight
+  // stages are prefetched into L2 while that kernel still runs
+  int early_weights;
 };
 
 template <int BN, int EPI, int STAGES>
@@ -134,7 +138,7 @@ __device__ void build_tile_offsets(const int32_t* offsets, int E, int MT, int* s
   const int e0 = tid * per, e1 = min(E, e0 + per);
   int sum = 0;
   for (int e = e0; e < e1; ++e) {
-    const int cnt = __ldg(offsets + e + 1) - __ldg(offsets + e);
+    const int cnt = __ldcg(offsets + e + 1) - __ldcg(offsets + e);
     const int t = cnt > 0 ? (cnt + BN - 1) / BN * MT : 0;
     s_toff[e] = t;
     sum += t;
@@ -196,9 +200,25 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     prefetch_tensormap(&tm_a);
     prefetch_tensormap(&tm_asf);
   }
-  pdl_wait();  // the routing offsets and activations come from earlier kernels
-  pdl_trigger();
-  build_tile_offsets<BN>(p.offsets, E, MT, s_toff, s_scan);
+  // The activations and their global scale come from the preceding kernel,
+  // the routing offsets from it or (early_weights) from an earlier one.
+  if (p.early_weights) {
+    build_tile_offsets<BN>(p.offsets, E, MT, s_toff, s_scan);
+    if (warp == 2 && lane < min(2 * STAGES, KT) && static_cast<int>(blockIdx.x) < s_toff[E]) {
+      // the first (up to) 2 x STAGES weight stages of this CTA's first tile
+      const TileInfo t0 = decode_tile(blockIdx.x, s_toff, E, MT);
+      const int blk0 = C::G == 2 ? ((t0.e * MT + t0.mt) * KT) * 2
+                                 : ((t0.e * N + t0.mt * 128) >> 7) * KT;
+      bulk_prefetch_l2(p.w_codes + static_cast<int64_t>(blk0 + lane * C::G) * 16384,
+                       C::G * C::A_TILE);
+    }
+    pdl_wait();
+    pdl_trigger();
+  } else {
+    pdl_wait();
+    pdl_trigger();
+    build_tile_offsets<BN>(p.offsets, E, MT, s_toff, s_scan);
+  }
   const int total = s_toff[E];
   if (static_cast<int>(blockIdx.x) >= total) return;  // uniform: no work for this CTA
 
@@ -592,7 +612,7 @@ cudaError_t launch_grouped_gemm(const GemmLaunch& g, cudaStream_t stream) {
     return cudaErrorInvalidValue;
   GemmArgs a{g.w_codes,        g.w_scales, g.w_gs,     g.act_gs, g.offsets,
              g.padded_offsets, g.out,      g.ld_out,   g.out_amax, g.status,
-             wait_limit_ns(),  g.E,        g.N,        g.K};
+             wait_limit_ns(),  g.E,        g.N,        g.K,          g.early_weights ? 1 : 0};
   if (g.epilogue == MEGAMOE_EPI_SILU_MUL) {
     if (g.out_amax && g.zero_amax) {
       cudaError_t err = cudaMemsetAsync(g.out_amax, 0, sizeof(float), stream);

@@ -75,6 +75,10 @@ struct GemmLaunch {
   int tile_n;
   uint32_t* status;
   bool zero_amax = true;  // false when the caller already cleared out_amax
+  // true only when the offsets were written by a kernel that finished before
+  // the one immediately preceding the GEMM (the forward's order): the GEMM
+  // then prefetches its first weight stages while that kernel runs
+  bool early_weights = false;
 };
 // Encodes the tensor maps and launches the persistent grouped GEMM.
 cudaError_t launch_grouped_gemm(const GemmLaunch& g, cudaStream_t stream);
