@@ -1,8 +1,9 @@
 // Top-k weighted combine: out[t] = bf16( sum_j w[t, j] * y[slot_dst[t*k + j]] )
 // (the topk_weights input of "CURRENT_BUG.md -- DeepSeek-V4 Blackwell NVFP4",
 // "Test Plan -- Finding the NaN", Phase 1).  One thread per 4 consecutive
-// features of one token: 128-bit loads of each routed row of y, fp32 sums in
-// ascending j, one bf16 rounding, 64-bit stores.
+// features of one token: 128-bit loads of each routed row of y (up to eight
+// slots' loads in flight at once), fp32 sums in ascending j, one bf16
+// rounding, 64-bit stores.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -21,18 +22,33 @@ __global__ void __launch_bounds__(256) k_combine(const float* __restrict__ y, in
   const int64_t total = static_cast<int64_t>(T) * vecs;
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int t = static_cast<int>(i / vecs);
+    const int t = (i >> 32) == 0 ? static_cast<int>(static_cast<uint32_t>(i) / static_cast<uint32_t>(vecs))
+                                 : static_cast<int>(i / vecs);
     const int v = static_cast<int>(i - static_cast<int64_t>(t) * vecs);
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int j = 0; j < k; ++j) {
-      const int r = __ldg(slot_dst + static_cast<int64_t>(t) * k + j);
-      if (r < 0) continue;
-      const float wt = __ldg(w + static_cast<int64_t>(t) * k + j);
-      const float4 yv = __ldg(reinterpret_cast<const float4*>(y + r * ld_y) + v);
-      acc.x = fmaf(wt, yv.x, acc.x);
-      acc.y = fmaf(wt, yv.y, acc.y);
-      acc.z = fmaf(wt, yv.z, acc.z);
-      acc.w = fmaf(wt, yv.w, acc.w);
+    // eight slots at a time: all their row indices and weights, then all
+    // their rows of y, are in flight together; the sums stay in ascending j
+    for (int j0 = 0; j0 < k; j0 += 8) {
+      int r[8];
+      float wt[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        r[j] = j0 + j < k ? __ldg(slot_dst + static_cast<int64_t>(t) * k + j0 + j) : -1;
+        wt[j] = j0 + j < k ? __ldg(w + static_cast<int64_t>(t) * k + j0 + j) : 0.f;
+      }
+      float4 yv[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        yv[j] = r[j] >= 0 ? __ldg(reinterpret_cast<const float4*>(y + r[j] * ld_y) + v)
+                          : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        if (r[j] < 0) continue;
+        acc.x = fmaf(wt[j], yv[j].x, acc.x);
+        acc.y = fmaf(wt[j], yv[j].y, acc.y);
+        acc.z = fmaf(wt[j], yv[j].z, acc.z);
+        acc.w = fmaf(wt[j], yv[j].w, acc.w);
+      }
     }
     const __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
     const __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);

@@ -262,15 +262,15 @@ __host__ __device__ constexpr uint32_t idesc_nvf4(int M, int N) {
 // ---------------------------------------------------------------------------
 // NVFP4 element and scale codecs (float32 decisions, as the oracle takes them)
 // ---------------------------------------------------------------------------
-// Round-to-nearest-even onto the E2M1 grid {0, .5, 1, 1.5, 2, 3, 4, 6},
-// saturating; the sign bit is copied from q.  Ties go to the even code, so the
-// comparison is strict where the lower neighbour is even and inclusive where
-// the upper one is.
-__device__ __forceinline__ uint32_t e2m1_code(float q) {
-  const float a = fabsf(q);
-  uint32_t m = (a > 0.25f) + (a >= 0.75f) + (a > 1.25f) + (a >= 1.75f) + (a > 2.5f) +
-               (a >= 3.5f) + (a > 5.0f);
-  return m | ((__float_as_uint(q) >> 28) & 8u);
+// Two floats -> one byte of two E2M1 codes, `lo` in the low nibble: the
+// hardware conversion rounds to nearest (ties to the even code) onto the grid
+// {0, .5, 1, 1.5, 2, 3, 4, 6}, saturates to +-6 and keeps the sign of zero.
+__device__ __forceinline__ uint32_t e2m1x2(float lo, float hi) {
+  uint16_t r;
+  asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\tcvt.u16.u8 %0, t;\n\t}"
+      : "=h"(r)
+      : "f"(hi), "f"(lo));
+  return r;
 }
 
 // Non-negative float -> E4M3 byte, round-to-nearest-even, saturating to 448.
@@ -310,9 +310,11 @@ __device__ __forceinline__ void encode_block(uint4 v0, uint4 v1, float gs, uint2
   if (sd > 0.f) {
     const float enc = __fdiv_rn(gs, sd);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) c0 |= e2m1_code(__fmul_rn(xv[i], enc)) << (4 * i);
+    for (int i = 0; i < 4; ++i)
+      c0 |= e2m1x2(__fmul_rn(xv[2 * i], enc), __fmul_rn(xv[2 * i + 1], enc)) << (8 * i);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) c1 |= e2m1_code(__fmul_rn(xv[8 + i], enc)) << (4 * i);
+    for (int i = 0; i < 4; ++i)
+      c1 |= e2m1x2(__fmul_rn(xv[8 + 2 * i], enc), __fmul_rn(xv[9 + 2 * i], enc)) << (8 * i);
   }
   codes = make_uint2(c0, c1);
 }

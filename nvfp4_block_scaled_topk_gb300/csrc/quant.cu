@@ -77,6 +77,13 @@ struct QuantArgs {
   bool slot_rows;
 };
 
+// t / n for a non-negative task index: 32-bit division whenever t fits (the
+// 64-bit one is a long software sequence).
+__device__ __forceinline__ int64_t task_div(int64_t t, int n) {
+  return (t >> 32) == 0 ? static_cast<int64_t>(static_cast<uint32_t>(t) / static_cast<uint32_t>(n))
+                        : t / n;
+}
+
 __device__ __forceinline__ void store_block(const QuantArgs& a, int64_t out_row, int b, uint2 c,
                                             uint32_t s8) {
   *reinterpret_cast<uint2*>(a.codes + out_row * (a.K / 2) + 8 * b) = c;
@@ -106,7 +113,7 @@ __global__ void __launch_bounds__(256) k_quant(const QuantArgs a) {
   if (a.slot_rows) {
     for (int64_t t = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
          t < a.rows_in * NB; t += stride) {
-      const int64_t slot = t / NB;
+      const int64_t slot = task_div(t, NB);
       const int b = static_cast<int>(t - slot * NB);
       const int64_t row = a.slot_dst[slot];
       if (row < 0 || row >= live) continue;
@@ -124,7 +131,7 @@ __global__ void __launch_bounds__(256) k_quant(const QuantArgs a) {
        t += stride) {
     const bool token_task = t < token_tasks;
     const int64_t u = token_task ? t : t - token_tasks;
-    const int64_t row = u / NB;
+    const int64_t row = task_div(u, NB);
     const int b = static_cast<int>(u - row * NB);
     if (!token_task) {
       if (row >= live) continue;

@@ -166,13 +166,30 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
   __shared__ uint32_t red[kRouteWarps];
   pdl_wait();
   pdl_trigger();
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  // amax of x on the bf16 bit patterns (monotone for finite values); the
+  // first kPre vectors per thread are loaded before the routing so that their
+  // latency overlaps it
+  constexpr int kPre = 8;
+  const int64_t vecs = static_cast<int64_t>(T) * (d / 8);
+  uint4 pre[kPre];
+#pragma unroll
+  for (int j = 0; j < kPre; ++j) {
+    const int64_t i = tid + static_cast<int64_t>(j) * kRouteThreads;
+    pre[j] = i < vecs ? __ldg(reinterpret_cast<const uint4*>(x) + i) : make_uint4(0u, 0u, 0u, 0u);
+  }
   route_block(ids, T * k, E, pad, counts, offsets, padded_offsets, row_src, row_capacity,
               slot_dst, status, zero_words, n_zero, smem_route);
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  // amax of x on the bf16 bit patterns (monotone for finite values)
-  const int64_t vecs = static_cast<int64_t>(T) * (d / 8);
   uint32_t m2 = 0;
-  for (int64_t i = tid; i < vecs; i += kRouteThreads) {
+#pragma unroll
+  for (int j = 0; j < kPre; ++j) {
+    m2 = __vmaxu2(m2, pre[j].x & 0x7FFF7FFFu);
+    m2 = __vmaxu2(m2, pre[j].y & 0x7FFF7FFFu);
+    m2 = __vmaxu2(m2, pre[j].z & 0x7FFF7FFFu);
+    m2 = __vmaxu2(m2, pre[j].w & 0x7FFF7FFFu);
+  }
+  for (int64_t i = tid + static_cast<int64_t>(kPre) * kRouteThreads; i < vecs;
+       i += kRouteThreads) {
     const uint4 q = __ldg(reinterpret_cast<const uint4*>(x) + i);
     m2 = __vmaxu2(m2, q.x & 0x7FFF7FFFu);
     m2 = __vmaxu2(m2, q.y & 0x7FFF7FFFu);
