@@ -392,6 +392,74 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+def run_linear(args):
+    """The dense NVFP4 linear (measured-amax activation scale) on one GPU:
+    tokens/s through megamoe_linear_nvfp4 with inputs resident, against the
+    roofline max(bytes / HBM, flops / FP4 tensor peak)."""
+    import torch
+
+    from nvfp4_block_scaled_topk_gb300 import inputs, megamoe
+
+    megamoe.load()
+    cfg = inputs.LINEAR_CONFIGS[args.config]
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    x, c, s, gs = inputs.make_linear(cfg, device=dev)
+    w = megamoe.LinearWeights.prepare(c, s, gs)
+    out = torch.empty(cfg.T, cfg.N, dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(max(256, megamoe.linear_workspace_size(cfg.T, cfg.K)), dtype=torch.uint8,
+                     device=dev)
+    stream = torch.cuda.current_stream()
+    # weights are smaller than L2 for these shapes: a 512 MB buffer is written
+    # between timed steps, outside the events' interval of each step
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    for _ in range(max(3, args.warmup)):
+        megamoe.linear_nvfp4(x, w, out=out, ws=ws)
+    torch.cuda.synchronize()
+    clocks = ClockSampler(0)
+    clocks.start()
+    times = []
+    for _ in range(args.steps):
+        flush.fill_(1)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        megamoe.linear_nvfp4(x, w, out=out, ws=ws)
+        b.record(stream)
+        torch.cuda.synchronize()
+        times.append(a.elapsed_time(b))
+    clk = clocks.stop()
+    ms = statistics.median(times)
+    hbm_gbs, bf16_tf, peak_kind = _peaks()
+    fp4_tf = bf16_tf * 13.5 / 2.25  # measured bf16 x the nominal dense FP4 / BF16 ratio
+    w_bytes = cfg.N * cfg.K * (0.5 + 1.0 / 16)
+    alg_bytes = w_bytes + cfg.T * cfg.K * 2 + cfg.T * cfg.N * 2
+    flops = 2.0 * cfg.T * cfg.N * cfg.K
+    t_hbm, t_fp4 = alg_bytes / (hbm_gbs * 1e9), flops / (fp4_tf * 1e12)
+    bound = "hbm" if t_hbm >= t_fp4 else "tensor"
+    achieved = (alg_bytes / (ms * 1e-3) / 1e9) if bound == "hbm" else flops / (ms * 1e-3) / 1e12
+    peak = hbm_gbs if bound == "hbm" else fp4_tf
+    line = {
+        "op": "linear", "metric": "tokens/s and NVFP4 TFLOP/s, dense NVFP4 linear "
+                                  "(measured-amax activation scale)",
+        "value": cfg.T / (ms * 1e-3), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "dtype": "nvfp4 (e2m1 x e4m3 scales, fp32 acc), bf16 out", "data": "synthetic",
+        "config": {"workload": f"{cfg.name}: x [{cfg.T}, {cfg.K}] bf16 @ W [{cfg.N}, {cfg.K}] "
+                               "NVFP4", "l2": "512 MB written between timed steps"},
+        "tflops": flops / (ms * 1e-3) / 1e12,
+        "hbm_gbs": alg_bytes / (ms * 1e-3) / 1e9,
+        "roofline": {"bound": bound, "achieved": achieved, "peak": peak,
+                     "unit": "GB/s" if bound == "hbm" else "TFLOP/s", "frac": achieved / peak,
+                     "traffic": None, "kernel": "whole call (prologue, quantiser, GEMM)",
+                     "peak_source": peak_kind if bound == "hbm" else
+                     f"{peak_kind} bf16 x 6 (nominal FP4/BF16 ratio)"},
+        "gpu_launches": (3 if cfg.T * cfg.K <= 262144 else 4) * args.steps,
+        "clocks": clk,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -401,8 +469,15 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--ref-tokens", type=int, default=2)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--op", default="forward", choices=["forward", "linear"],
+                    help="forward: the MoE layer (default); linear: the dense NVFP4 linear "
+                         "(--config one of the linear_* workloads)")
     args = ap.parse_args()
-    if args.impl == "reference":
+    if args.op == "linear":
+        if args.config == "decode":
+            args.config = "linear_qa_decode"
+        run_linear(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)

@@ -76,6 +76,7 @@ typedef enum megamoe_status {
 /* Grouped-GEMM epilogues. */
 #define MEGAMOE_EPI_F32 0      /* out[r, n] = fp32 accumulator * alpha            */
 #define MEGAMOE_EPI_SILU_MUL 1 /* out[r, i] = bf16(silu(gate) * up), amax of it   */
+#define MEGAMOE_EPI_BF16 2     /* out[r, n] = bf16(fp32 accumulator * alpha)      */
 
 /* Limits. */
 #define MEGAMOE_MAX_EXPERTS 1024
@@ -211,15 +212,15 @@ megamoe_status megamoe_pack_weight_codes(const uint8_t* src, int64_t rows, int K
  *   act_codes   [act_rows, K/2]; act_scales row-major [act_rows, K/16];
  *               act_gs device float (one global scale)
  *   w_codes     [E*N, K/2] packed by megamoe_pack_weight_codes (half_rows =
- *               N/2 for MEGAMOE_EPI_SILU_MUL, 0 for MEGAMOE_EPI_F32);
+ *               N/2 for MEGAMOE_EPI_SILU_MUL, 0 otherwise);
  *               w_scales atom layout of [E*N, K/16] (megamoe_swizzle_scales)
- *   w_gs        [E, G] float: G = 1 for MEGAMOE_EPI_F32; G = 2 (gate, up) for
- *               MEGAMOE_EPI_SILU_MUL
+ *   w_gs        [E, G] float: G = 2 (gate, up) for MEGAMOE_EPI_SILU_MUL, else 1
  *   offsets, padded_offsets  [E+1] int32 as produced by megamoe_route_permute
  *               with a pad that is a multiple of 32
  * Epilogues:
  *   MEGAMOE_EPI_F32:      out float [act_rows, ld_out], out[r, n] = acc * alpha,
  *                         alpha = 1 / (act_gs * w_gs[e]).
+ *   MEGAMOE_EPI_BF16:     out bf16 [act_rows, ld_out], out[r, n] = bf16(acc * alpha).
  *   MEGAMOE_EPI_SILU_MUL: N = 2I; out bf16 [act_rows, ld_out],
  *                         out[r, i] = bf16(silu(acc[r, i] * alpha_gate) *
  *                                          (acc[r, I + i] * alpha_up)),
@@ -239,6 +240,37 @@ megamoe_status megamoe_grouped_gemm(const uint8_t* act_codes, const uint8_t* act
                                     const int32_t* offsets, const int32_t* padded_offsets,
                                     int epilogue, void* out, int64_t ld_out, float* out_amax,
                                     int tile_n, double expected_tokens, uint32_t* status,
+                                    megamoe_stream_t stream);
+
+/*
+ * megamoe_linear_nvfp4 -- a dense NVFP4 linear layer whose activation global
+ * scale comes from the measured amax of x, not from a stored input scale
+ * ("Current Bug: vLLM produces NaN from layer 0", "Root Cause" and "Key
+ * evidence": the attention projections quantised activations with the
+ * checkpoint's input_scale, whose inverse (~4e3 to 1.6e4) overflowed
+ * activations of amax 2-8).  The one-group case of the grouped GEMM:
+ *   amax = max |x|, gs_x = 2688 / amax (1 if amax = 0), x -> NVFP4 as
+ *   megamoe_quantize_nvfp4 does, then
+ *   out[t, n] = sum_K dequant(x)[t, :] . dequant(w)[n, :]   (fp32 accumulate)
+ * written as bf16 (out_dtype MEGAMOE_EPI_BF16) or float (MEGAMOE_EPI_F32).
+ *   x          bf16 [T, K], row stride ld_x elements
+ *   w_codes    [N, K/2] packed by megamoe_pack_weight_codes (half_rows 0)
+ *   w_scales   atom layout of [N, K/16] (megamoe_swizzle_scales)
+ *   w_gs       device float: the weight's global scale
+ *   out        [T, ld_out] of out_dtype
+ *   ws         device workspace of megamoe_linear_workspace_size(T, K) bytes,
+ *              256-byte aligned, owned by the caller; it also receives the
+ *              measured amax (float at ws + 0) and gs_x (float at ws + 4) and
+ *              the status word (uint32 at ws + 8, read with megamoe_read_status)
+ * Requires K a multiple of 256, N a multiple of 128, ld_x a multiple of 8
+ * and ld_out of 16 bytes, 16-byte aligned pointers.  Argument errors return
+ * before anything is enqueued; non-finite x sets MEGAMOE_DEV_NONFINITE.
+ */
+size_t megamoe_linear_workspace_size(int64_t T, int K);
+megamoe_status megamoe_linear_nvfp4(const uint16_t* x, int64_t T, int K, int64_t ld_x,
+                                    const uint8_t* w_codes, const uint8_t* w_scales,
+                                    const float* w_gs, int N, int out_dtype, void* out,
+                                    int64_t ld_out, void* ws, size_t ws_bytes,
                                     megamoe_stream_t stream);
 
 /*

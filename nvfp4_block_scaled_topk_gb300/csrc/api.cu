@@ -196,15 +196,16 @@ megamoe_status megamoe_grouped_gemm(const uint8_t* act_codes, const uint8_t* act
                                     int tile_n, double expected_tokens, uint32_t* status,
                                     megamoe_stream_t stream) {
   if (act_rows < 0 || E < 1 || N <= 0 || K <= 0) return MEGAMOE_ERR_INVALID_ARG;
-  if (epilogue != MEGAMOE_EPI_F32 && epilogue != MEGAMOE_EPI_SILU_MUL)
+  if (epilogue != MEGAMOE_EPI_F32 && epilogue != MEGAMOE_EPI_SILU_MUL &&
+      epilogue != MEGAMOE_EPI_BF16)
     return MEGAMOE_ERR_INVALID_ARG;
-  if (E > MEGAMOE_MAX_EXPERTS || K % 256 != 0 || N % (epilogue == MEGAMOE_EPI_F32 ? 128 : 256))
+  if (E > MEGAMOE_MAX_EXPERTS || K % 256 != 0 || N % (epilogue == MEGAMOE_EPI_SILU_MUL ? 256 : 128))
     return MEGAMOE_ERR_UNSUPPORTED_SHAPE;
   if (static_cast<int64_t>(E) * N * (K / 256) >= (int64_t{1} << 31) ||
       act_rows >= (int64_t{1} << 31))
     return MEGAMOE_ERR_UNSUPPORTED_SHAPE;
   if (tile_n != 0 && tile_n != 32 && tile_n != 64 && tile_n != 128) return MEGAMOE_ERR_INVALID_ARG;
-  const int width = epilogue == MEGAMOE_EPI_F32 ? N : N / 2;
+  const int width = epilogue == MEGAMOE_EPI_SILU_MUL ? N / 2 : N;
   if (ld_out < width) return MEGAMOE_ERR_INVALID_ARG;
   // output rows start on 16-byte boundaries: the epilogue stores 16-byte vectors
   if (ld_out % (epilogue == MEGAMOE_EPI_F32 ? 4 : 8) != 0) return MEGAMOE_ERR_UNSUPPORTED_SHAPE;
@@ -352,6 +353,74 @@ megamoe_status megamoe_forward(const megamoe_weights* w, const uint16_t* x,
 }
 
 void megamoe_set_wait_limit_ns(uint64_t ns) { set_wait_limit_ns(ns); }
+
+static size_t align256(size_t n) { return (n + 255) / 256 * 256; }
+
+size_t megamoe_linear_workspace_size(int64_t T, int K) {
+  if (T < 0 || K <= 0) return 0;
+  return 256 + align256(static_cast<size_t>(T) * (K / 2)) + align256(static_cast<size_t>(T) * (K / 16));
+}
+
+megamoe_status megamoe_linear_nvfp4(const uint16_t* x, int64_t T, int K, int64_t ld_x,
+                                    const uint8_t* w_codes, const uint8_t* w_scales,
+                                    const float* w_gs, int N, int out_dtype, void* out,
+                                    int64_t ld_out, void* ws, size_t ws_bytes,
+                                    megamoe_stream_t stream) {
+  if (T < 0 || K <= 0 || N <= 0 || ld_x < K || ld_out < N) return MEGAMOE_ERR_INVALID_ARG;
+  if (out_dtype != MEGAMOE_EPI_BF16 && out_dtype != MEGAMOE_EPI_F32) return MEGAMOE_ERR_INVALID_ARG;
+  if (K % 256 != 0 || N % 128 != 0 || ld_x % 8 != 0 ||
+      ld_out % (out_dtype == MEGAMOE_EPI_F32 ? 4 : 8) != 0)
+    return MEGAMOE_ERR_UNSUPPORTED_SHAPE;
+  if (T >= (int64_t{1} << 31) || static_cast<int64_t>(N) * (K / 256) >= (int64_t{1} << 31))
+    return MEGAMOE_ERR_UNSUPPORTED_SHAPE;
+  if (!w_codes || !w_scales || !w_gs || !ws || (T > 0 && (!x || !out)))
+    return MEGAMOE_ERR_INVALID_ARG;
+  if (!aligned(ws, 256) || !aligned(w_codes, 16) || !aligned(w_scales, 16) ||
+      (x && !aligned(x, 16)) || (out && !aligned(out, 16)))
+    return MEGAMOE_ERR_UNSUPPORTED_SHAPE;
+  if (ws_bytes < megamoe_linear_workspace_size(T, K)) return MEGAMOE_ERR_WORKSPACE_TOO_SMALL;
+  if (T == 0) return MEGAMOE_OK;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  float* amax = reinterpret_cast<float*>(base);
+  float* gs = reinterpret_cast<float*>(base + 4);
+  uint32_t* status = reinterpret_cast<uint32_t*>(base + 8);
+  int32_t* groups = reinterpret_cast<int32_t*>(base + 16);  // offsets[2], padded_offsets[2]
+  uint8_t* codes = base + 256;
+  uint8_t* scales = codes + align256(static_cast<size_t>(T) * (K / 2));
+  // 1. status, group offsets, amax (one block when x is small, else k_amax)
+  cudaError_t e = launch_linear_prologue(x, T, K, ld_x, amax, status, groups, s);
+  if (e == cudaSuccess && !linear_prologue_full_amax(T, K))
+    e = launch_amax(x, T, K, ld_x, amax, status, false, s);
+  // 2. x -> NVFP4 with gs = 2688 / amax
+  if (e == cudaSuccess)
+    e = launch_quant(x, T, K, ld_x, nullptr, 1, nullptr, nullptr, T, amax, gs, codes, scales,
+                     MEGAMOE_SCALES_ROWMAJOR, s);
+  if (e != cudaSuccess) return MEGAMOE_ERR_CUDA;
+  // 3. the one-group GEMM
+  GemmLaunch g{};
+  g.act_codes = codes;
+  g.act_scales = scales;
+  g.act_gs = gs;
+  g.act_rows = T;
+  g.w_codes = w_codes;
+  g.w_scales = w_scales;
+  g.w_gs = w_gs;
+  g.E = 1;
+  g.N = N;
+  g.K = K;
+  g.offsets = groups;
+  g.padded_offsets = groups + 2;
+  g.epilogue = out_dtype;
+  g.out = out;
+  g.ld_out = ld_out;
+  g.out_amax = nullptr;
+  g.tile_n = tile_n_setting(static_cast<double>(T));
+  g.status = status;
+  // the offsets were written by the prologue, which finished before the quantiser
+  g.early_weights = true;
+  return cuda_status(launch_grouped_gemm(g, s));
+}
 
 megamoe_status megamoe_read_status(const uint32_t* status, uint32_t* bits,
                                    megamoe_stream_t stream) {

@@ -96,8 +96,9 @@ struct GemmCfg {
   // per epilogue warp: STG_ROWS token rows x 32 features of output, staged so
   // that global stores are 16-byte vectors along the feature axis (512 bytes
   // for bf16, 2 KB for float)
-  static constexpr int STG_ROWS = EPI == MEGAMOE_EPI_SILU_MUL ? 8 : 16;
-  static constexpr int STG_BYTES = STG_ROWS * 32 * (EPI == MEGAMOE_EPI_SILU_MUL ? 2 : 4);
+  static constexpr bool BF16_OUT = EPI != MEGAMOE_EPI_F32;
+  static constexpr int STG_ROWS = BF16_OUT ? 8 : 16;
+  static constexpr int STG_BYTES = STG_ROWS * 32 * (BF16_OUT ? 2 : 4);
   static constexpr int STG_OFF = (TOFF_OFF + 4 * (MEGAMOE_MAX_EXPERTS + 1) + 15) / 16 * 16;
   static constexpr int SMEM = 1024 + STG_OFF + kEpiWarps * STG_BYTES;
   static constexpr uint32_t IDESC = idesc_nvf4(128, BN);
@@ -482,6 +483,22 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                   reinterpret_cast<const uint4*>(stg)[lane];
             __syncwarp();
           }
+        } else if (C::BF16_OUT) {
+          tmem_ld_wait();
+          __nv_bfloat16* s = reinterpret_cast<__nv_bfloat16*>(stg);
+          __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
+#pragma unroll
+          for (int h8 = 0; h8 < 16; h8 += 8) {  // two staged halves of 8 rows
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              s[j * 32 + lane] = __float2bfloat16_rn(__uint_as_float(g[h8 + j]) * alpha0);
+            __syncwarp();
+            const int r = h8 + (lane >> 2);
+            if (r < rows)
+              *reinterpret_cast<uint4*>(out + (row0 + n0 + r) * p.ld_out + f0 + 8 * (lane & 3)) =
+                  reinterpret_cast<const uint4*>(stg)[lane];
+            __syncwarp();
+          }
         } else {
           tmem_ld_wait();
           float* s = reinterpret_cast<float*>(stg);
@@ -622,6 +639,12 @@ cudaError_t launch_grouped_gemm(const GemmLaunch& g, cudaStream_t stream) {
       case 32: return launch_cfg<32, MEGAMOE_EPI_SILU_MUL, 5>(tm_a, tm_asf, a, stream);
       case 64: return launch_cfg<64, MEGAMOE_EPI_SILU_MUL, 4>(tm_a, tm_asf, a, stream);
       case 128: return launch_cfg<128, MEGAMOE_EPI_SILU_MUL, 4>(tm_a, tm_asf, a, stream);
+    }
+  } else if (g.epilogue == MEGAMOE_EPI_BF16) {
+    switch (bn) {
+      case 32: return launch_cfg<32, MEGAMOE_EPI_BF16, 8>(tm_a, tm_asf, a, stream);
+      case 64: return launch_cfg<64, MEGAMOE_EPI_BF16, 7>(tm_a, tm_asf, a, stream);
+      case 128: return launch_cfg<128, MEGAMOE_EPI_BF16, 5>(tm_a, tm_asf, a, stream);
     }
   } else {
     switch (bn) {

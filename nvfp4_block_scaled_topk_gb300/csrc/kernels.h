@@ -37,6 +37,13 @@ cudaError_t launch_route(const int32_t* ids, int n_slots, int E, int pad, int32_
 // zero_first: clear *amax first (false when the caller already cleared it).
 cudaError_t launch_amax(const uint16_t* x, int64_t rows, int K, int64_t ld, float* amax,
                         uint32_t* status, bool zero_first, cudaStream_t stream);
+// Dense linear prologue (one block): status cleared, single-group offsets
+// {0, rows, 0, rows}, and the amax of x when linear_prologue_full_amax (else
+// amax = 0 for a following launch_amax with zero_first = false).
+bool linear_prologue_full_amax(int64_t rows, int K);
+cudaError_t launch_linear_prologue(const uint16_t* x, int64_t rows, int K, int64_t ld,
+                                   float* amax, uint32_t* status, int32_t* groups,
+                                   cudaStream_t stream);
 cudaError_t launch_quant(const uint16_t* x, int64_t rows_in, int K, int64_t ld,
                          const int32_t* slot_dst, int k, const int32_t* row_src,
                          const int32_t* live_rows, int64_t out_rows, const float* amax,

@@ -216,6 +216,70 @@ static int grid_for(int64_t tasks, int threads) {
   return static_cast<int>(b);
 }
 
+// Prologue of the dense NVFP4 linear, one block: clears the status word,
+// writes the single group's offsets ({0, rows} as offsets and as padded
+// offsets) and either the amax of x (full_amax: x small enough for one block)
+// or 0, which k_amax's atomics then raise.
+constexpr int kLinearPrologueThreads = 1024;
+constexpr int64_t kLinearPrologueMaxElems = 262144;
+
+__global__ void __launch_bounds__(kLinearPrologueThreads)
+    k_linear_prologue(const uint16_t* __restrict__ x, int64_t rows, int K, int64_t ld,
+                      float* amax, uint32_t* status, int32_t* groups, int full_amax) {
+  pdl_wait();
+  pdl_trigger();
+  __shared__ uint32_t red[kLinearPrologueThreads / 32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) {
+    groups[0] = 0;
+    groups[1] = static_cast<int32_t>(rows);
+    groups[2] = 0;
+    groups[3] = static_cast<int32_t>(rows);
+  }
+  uint32_t m = 0;
+  if (full_amax) {
+    const int vecs = K / 8;
+    uint32_t m2 = 0;
+    for (int64_t i = tid; i < rows * vecs; i += kLinearPrologueThreads) {
+      const int64_t r = i / vecs;
+      const uint4 q = __ldg(reinterpret_cast<const uint4*>(x + r * ld) + (i - r * vecs));
+      m2 = __vmaxu2(m2, q.x & 0x7FFF7FFFu);
+      m2 = __vmaxu2(m2, q.y & 0x7FFF7FFFu);
+      m2 = __vmaxu2(m2, q.z & 0x7FFF7FFFu);
+      m2 = __vmaxu2(m2, q.w & 0x7FFF7FFFu);
+    }
+    m = max(m2 & 0xFFFFu, m2 >> 16);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if (lane == 0) red[warp] = m;
+    __syncthreads();
+  }
+  if (tid == 0) {
+    uint32_t bits = 0;
+    if (full_amax) {
+      for (int w = 1; w < kLinearPrologueThreads / 32; ++w) m = max(m, red[w]);
+      if (m >= 0x7F80u) {  // Inf or NaN
+        bits = MEGAMOE_DEV_NONFINITE;
+        m = 0x7F7Fu;
+      }
+    }
+    *status = bits;
+    *amax = __uint_as_float(m << 16);
+  }
+}
+
+bool linear_prologue_full_amax(int64_t rows, int K) {
+  return rows * static_cast<int64_t>(K) <= kLinearPrologueMaxElems;
+}
+
+cudaError_t launch_linear_prologue(const uint16_t* x, int64_t rows, int K, int64_t ld,
+                                   float* amax, uint32_t* status, int32_t* groups,
+                                   cudaStream_t stream) {
+  return launch_pdl(k_linear_prologue, dim3(1), dim3(kLinearPrologueThreads), 0, stream, x, rows,
+                    K, ld, amax, status, groups,
+                    linear_prologue_full_amax(rows, K) ? 1 : 0);
+}
+
 cudaError_t launch_amax(const uint16_t* x, int64_t rows, int K, int64_t ld, float* amax,
                         uint32_t* status, bool zero_first, cudaStream_t stream) {
   if (zero_first) {

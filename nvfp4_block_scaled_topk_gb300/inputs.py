@@ -110,6 +110,32 @@ CONFIGS = {
 }
 
 
+@dataclass(frozen=True)
+class LinearConfig:
+    """A dense NVFP4 linear layer x [T, K] @ W[N, K].T."""
+
+    name: str
+    T: int
+    K: int
+    N: int
+    seed: int
+    x_sigma: float = 0.09
+    outlier_frac: float = 0.0
+    outlier_value: float = 8.0
+
+
+#: attention-projection-shaped linear layers.  The pages name the NVFP4
+#: projections (q_a, kv, q_b, o_b) but give no sizes; these take the
+#: DeepSeek-style hidden 7168 -> q_a rank 1536 and 1536 -> 128 heads x 192.
+LINEAR_CONFIGS = {
+    "linear_tiny": LinearConfig("linear_tiny", 40, 512, 256, seed=2001),
+    "linear_qa_decode": LinearConfig("linear_qa_decode", 8, 7168, 1536, seed=2002),
+    "linear_qa_prefill": LinearConfig("linear_qa_prefill", 4096, 7168, 1536, seed=2003,
+                                      outlier_frac=1e-3),
+    "linear_qb_prefill": LinearConfig("linear_qb_prefill", 4096, 1536, 24576, seed=2004),
+}
+
+
 def _gen(seed: int, device) -> torch.Generator:
     g = torch.Generator(device=device)
     g.manual_seed(int(seed) & 0x7FFF_FFFF_FFFF_FFFF)
@@ -219,6 +245,22 @@ def make_all_experts(cfg: MoEConfig, device="cpu") -> dict:
         for key, v in w.items():
             out[key][e] = v.reshape(out[key][e].shape)
     return out
+
+
+def make_linear(cfg: LinearConfig, device="cpu"):
+    """(x [T, K] bf16, codes [N, K/2] u8, scales [N, K/16] u8, gs float) with
+    x ~ N(0, x_sigma) (plus +-outlier_value at outlier_frac of the entries)
+    and the weight drawn like the experts' (NVFP4 bytes from the fixed
+    histograms)."""
+    g = _gen(_mix(cfg.seed, 1), device)
+    x = torch.randn(cfg.T, cfg.K, generator=g, device=device, dtype=torch.float32) * cfg.x_sigma
+    if cfg.outlier_frac > 0 and x.numel():
+        n = max(1, int(round(cfg.outlier_frac * x.numel())))
+        pos = torch.randperm(x.numel(), generator=g, device=device)[:n]
+        sign = torch.randint(0, 2, (n,), generator=g, device=device).float() * 2 - 1
+        x.view(-1)[pos] = sign * cfg.outlier_value
+    codes, scales, gs = _nvfp4_matrix(_mix(cfg.seed, 4), cfg.N, cfg.K, device)
+    return x.to(torch.bfloat16), codes, scales, gs
 
 
 class ExpertSet:

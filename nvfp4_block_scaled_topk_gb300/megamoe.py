@@ -27,6 +27,7 @@ SCALES_ROWMAJOR = 0
 SCALES_MMA = 1
 EPI_F32 = 0
 EPI_SILU_MUL = 1
+EPI_BF16 = 2
 
 #: every function the header declares, with (restype, argtypes)
 _P = ctypes.c_void_p
@@ -49,6 +50,8 @@ SIGNATURES = {
     "megamoe_read_status": (_I, [_P, _P, _P]),
     "megamoe_forward_static": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P, _P]),
     "megamoe_set_wait_limit_ns": (None, [ctypes.c_uint64]),
+    "megamoe_linear_workspace_size": (_SZ, [_I64, _I]),
+    "megamoe_linear_nvfp4": (_I, [_P, _I64, _I, _I64, _P, _P, _P, _I, _I, _P, _I64, _P, _SZ, _P]),
 }
 
 
@@ -198,7 +201,7 @@ def grouped_gemm(act_codes, act_scales, act_gs, w_codes_packed, w_scales_mma, w_
     w_codes = w_codes_packed
     K = half_k * 2
     dev = act_codes.device
-    width = N if epilogue == EPI_F32 else N // 2
+    width = N // 2 if epilogue == EPI_SILU_MUL else N
     if out is None:
         dt = torch.float32 if epilogue == EPI_F32 else torch.bfloat16
         out = torch.full((max(act_rows, 1), width), float("nan"), dtype=dt, device=dev)
@@ -209,6 +212,51 @@ def grouped_gemm(act_codes, act_scales, act_gs, w_codes_packed, w_scales_mma, w_
         _p(w_gs), E, N, K, _p(offsets), _p(padded_offsets), epilogue, _p(out), out.shape[1],
         _p(out_amax), tile_n, float(expected_tokens), _p(status), _stream()))
     return out[:act_rows], out_amax
+
+
+@dataclass
+class LinearWeights:
+    """A dense NVFP4 weight [N, K] prepared for megamoe_linear_nvfp4: codes
+    packed tile-major, block scales in the atom layout, global scale on the
+    device."""
+
+    N: int
+    K: int
+    codes: torch.Tensor
+    scales: torch.Tensor  # atom layout
+    gs: torch.Tensor  # [1] float32
+
+    @classmethod
+    def prepare(cls, codes: torch.Tensor, scales: torch.Tensor, gs) -> "LinearWeights":
+        """From row-major codes [N, K/2], scales [N, K/16] and the global scale."""
+        N, half_k = codes.shape
+        gs_t = torch.as_tensor([float(gs)], dtype=torch.float32, device=codes.device)
+        return cls(N, half_k * 2, pack_weight_codes(codes.contiguous()),
+                   swizzle_scales(scales.contiguous()), gs_t)
+
+
+def linear_workspace_size(T: int, K: int) -> int:
+    return int(load().megamoe_linear_workspace_size(T, K))
+
+
+def linear_nvfp4(x: torch.Tensor, w: LinearWeights, out_dtype=EPI_BF16, out=None, ws=None):
+    """out [T, N] = NVFP4(x, gs from the measured amax of x) @ w.T, in bf16
+    (EPI_BF16) or float32 (EPI_F32).  Returns (out, ws); ws holds amax, gs_x
+    and the status word at bytes 0, 4 and 8."""
+    _dev(x, torch.bfloat16, "x")
+    T, K = x.shape
+    if K != w.K:
+        raise ValueError("x and w disagree on K")
+    need = linear_workspace_size(T, K)
+    if ws is None:
+        ws = torch.empty(max(need, 256), dtype=torch.uint8, device=x.device)
+    if out is None:
+        dt = torch.float32 if out_dtype == EPI_F32 else torch.bfloat16
+        out = torch.empty(T, w.N, dtype=dt, device=x.device)
+    _check("megamoe_linear_nvfp4", load().megamoe_linear_nvfp4(
+        _p(x), T, K, x.stride(0), _p(w.codes), _p(w.scales), _p(w.gs), w.N, out_dtype, _p(out),
+        out.stride(0), _p(ws), ws.numel(), _stream()))
+    return out, ws
 
 
 def combine(y, slot_dst, topk_weights, out=None):

@@ -31,8 +31,8 @@ Sources (titles and sections of the pages this follows):
 The pages never define NVFP4 arithmetic.  The oracle takes the plain
 two-level reading (E2M1 element codes, one E4M3 scale per 16 elements, one
 FP32 global scale per tensor) with the OCP Microscaling v1.0 bit formats for
-E2M1 and E4M3.  Every reading the pages leave open is listed in the design doc of
-the repository and restated at the function that takes it.
+E2M1 and E4M3.  Every reading the pages leave open is stated at the function
+that takes it.
 
 Precision: the GEMMs, SiLU and combine run in float64 on dequantised
 operands.  The quantiser's decisions (scale byte, element code) are taken in
@@ -60,6 +60,7 @@ from .nvfp4 import (  # noqa: F401
     unpack_nibbles,
     unswizzle_scales,
 )
+from .linear import linear  # noqa: F401
 from .moe import (  # noqa: F401
     Routing,
     combine,

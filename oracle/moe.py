@@ -12,7 +12,7 @@ Follows "CURRENT_BUG.md -- DeepSeek-V4 Blackwell NVFP4":
 and "Current Bug: vLLM produces NaN from layer 0", "What we've tried" item 1:
 the activation global scale comes from the measured amax.
 
-Readings taken where the pages are silent (each also listed in the design doc):
+Readings taken where the pages are silent:
   A6  the L1 output h = SiLU(gate) * up is rounded to bf16 before it is
       re-quantised; its global scale comes from the amax of bf16 h over the
       valid rows only.
