@@ -243,6 +243,28 @@ megamoe_status megamoe_grouped_gemm(const uint8_t* act_codes, const uint8_t* act
                                     megamoe_stream_t stream);
 
 /*
+ * megamoe_router_topk -- the router step ahead of megamoe_route_permute
+ * ("CURRENT_BUG.md -- DeepSeek-V4 Blackwell NVFP4", "Test Plan -- Finding the
+ * NaN", Phase 1 item 1: topk_ids and topk_weights come from the router; the
+ * pages do not spell the router out: this is the plain top-k + softmax):
+ *   score[t, e] = fl32(logits[t, e] + bias[e])   (bias nullable: score = logit)
+ *   topk_ids[t, 0..k-1]     = the k experts of highest score, in descending
+ *                             score, ties to the lower expert index
+ *   topk_weights[t, j]      = softmax over the k selected *logits* (fp32)
+ * With shared_expert >= 0 one more column is appended to both outputs:
+ * id shared_expert with weight 1 (a shared expert that every token visits,
+ * to be run by megamoe_forward as one more expert).
+ *   logits        float [T, ld_logits] (ld_logits >= E)
+ *   topk_ids      int32 [T, k_out], topk_weights float [T, k_out],
+ *                 k_out = k + (shared_expert >= 0)
+ * Requires 1 <= k <= min(E, 16), E <= 1024, 4-byte aligned pointers.
+ */
+megamoe_status megamoe_router_topk(const float* logits, int64_t T, int E, int64_t ld_logits,
+                                   const float* bias, int k, int shared_expert,
+                                   int32_t* topk_ids, float* topk_weights,
+                                   megamoe_stream_t stream);
+
+/*
  * megamoe_linear_nvfp4 -- a dense NVFP4 linear layer whose activation global
  * scale comes from the measured amax of x, not from a stored input scale
  * ("Current Bug: vLLM produces NaN from layer 0", "Root Cause" and "Key

@@ -354,6 +354,21 @@ megamoe_status megamoe_forward(const megamoe_weights* w, const uint16_t* x,
 
 void megamoe_set_wait_limit_ns(uint64_t ns) { set_wait_limit_ns(ns); }
 
+megamoe_status megamoe_router_topk(const float* logits, int64_t T, int E, int64_t ld_logits,
+                                   const float* bias, int k, int shared_expert,
+                                   int32_t* topk_ids, float* topk_weights,
+                                   megamoe_stream_t stream) {
+  if (T < 0 || E < 1 || ld_logits < E || k < 1 || k > MEGAMOE_MAX_TOPK || k > E)
+    return MEGAMOE_ERR_INVALID_ARG;
+  if (E > MEGAMOE_MAX_EXPERTS || T >= (int64_t{1} << 40)) return MEGAMOE_ERR_UNSUPPORTED_SHAPE;
+  if (T > 0 && (!logits || !topk_ids || !topk_weights)) return MEGAMOE_ERR_INVALID_ARG;
+  if ((logits && !aligned(logits, 4)) || (bias && !aligned(bias, 4)) ||
+      (topk_ids && !aligned(topk_ids, 4)) || (topk_weights && !aligned(topk_weights, 4)))
+    return MEGAMOE_ERR_UNSUPPORTED_SHAPE;
+  return cuda_status(launch_router(logits, T, E, ld_logits, bias, k, shared_expert, topk_ids,
+                                   topk_weights, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 static size_t align256(size_t n) { return (n + 255) / 256 * 256; }
 
 size_t megamoe_linear_workspace_size(int64_t T, int K) {

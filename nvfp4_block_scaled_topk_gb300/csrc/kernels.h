@@ -94,6 +94,10 @@ int pick_tile_n(double expected_tokens_per_expert);
 void set_wait_limit_ns(uint64_t ns);
 uint64_t wait_limit_ns();
 
+// Router: ids/weights [T, k (+1 with a shared expert)] from fp32 logits.
+cudaError_t launch_router(const float* logits, int64_t T, int E, int64_t ld, const float* bias,
+                          int k, int shared, int32_t* ids, float* weights, cudaStream_t stream);
+
 cudaError_t launch_combine(const float* y, int64_t ld_y, const int32_t* slot_dst,
                            const float* w, int T, int k, int d, uint16_t* out,
                            cudaStream_t stream);

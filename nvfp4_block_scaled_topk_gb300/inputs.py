@@ -190,6 +190,26 @@ def make_routing(cfg: MoEConfig, device="cpu"):
     return ids.to(torch.int32).contiguous(), w.to(torch.float32).contiguous()
 
 
+def make_router_logits(cfg: MoEConfig, device="cpu"):
+    """(logits [T, E] float32 ~ N(0, 1), bias [E] float32 or None): the
+    router's inputs, from their own stream; for the Zipf-loaded configs the
+    bias is -1.1 ln(rank_e) with rank from a seeded permutation."""
+    g = _gen(_mix(cfg.seed, 5), device)
+    logits = torch.randn(cfg.T, cfg.E, generator=g, device=device, dtype=torch.float32)
+    bias = None
+    if cfg.routing == "zipf":
+        rank = torch.randperm(cfg.E, generator=g, device=device).float() + 1.0
+        bias = (-1.1 * torch.log(rank)).to(torch.float32)
+    return logits, bias
+
+
+def with_shared_expert(cfg: MoEConfig) -> MoEConfig:
+    """The same workload with one shared expert: expert index cfg.E (drawn
+    like the routed experts, from its own stream), visited by every token
+    with weight 1 as slot k; so E + 1 experts and k + 1 slots per token."""
+    return replace(cfg, name=cfg.name + "+shared", E=cfg.E + 1, k=cfg.k + 1)
+
+
 # --------------------------------------------------------------------------
 # NVFP4 expert weights
 # --------------------------------------------------------------------------

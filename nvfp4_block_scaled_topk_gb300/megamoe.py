@@ -51,6 +51,7 @@ SIGNATURES = {
     "megamoe_forward_static": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P, _P]),
     "megamoe_set_wait_limit_ns": (None, [ctypes.c_uint64]),
     "megamoe_linear_workspace_size": (_SZ, [_I64, _I]),
+    "megamoe_router_topk": (_I, [_P, _I64, _I, _I64, _P, _I, _I, _P, _P, _P]),
     "megamoe_linear_nvfp4": (_I, [_P, _I64, _I, _I64, _P, _P, _P, _I, _I, _P, _I64, _P, _SZ, _P]),
 }
 
@@ -140,6 +141,24 @@ def route_permute(topk_ids: torch.Tensor, E: int, pad: int = 1, status=None):
     r["row_src"] = r["row_src"][:cap]
     r["slot_dst"] = r["slot_dst"][:T * k]
     return r
+
+
+def router_topk(logits: torch.Tensor, k: int, bias=None, shared_expert: int = -1):
+    """(topk_ids int32 [T, k_out], topk_weights float32 [T, k_out]) from fp32
+    logits [T, E]: top-k of logits + bias, softmax of the selected logits,
+    plus a weight-1 column of ``shared_expert`` when it is >= 0."""
+    _dev(logits, torch.float32, "logits")
+    T, E = logits.shape
+    if logits.stride(1) != 1:
+        raise ValueError("logits must have unit stride along experts")
+    if bias is not None:
+        _dev(bias, torch.float32, "bias")
+    k_out = k + (1 if shared_expert >= 0 else 0)
+    ids = torch.empty(T, k_out, dtype=torch.int32, device=logits.device)
+    w = torch.empty(T, k_out, dtype=torch.float32, device=logits.device)
+    _check("megamoe_router_topk", load().megamoe_router_topk(
+        _p(logits), T, E, logits.stride(0), _p(bias), k, shared_expert, _p(ids), _p(w), _stream()))
+    return ids, w
 
 
 def sf_atom_bytes(rows, K):

@@ -61,11 +61,13 @@ from .nvfp4 import (  # noqa: F401
     unswizzle_scales,
 )
 from .linear import linear  # noqa: F401
+from .router import router_topk  # noqa: F401
 from .moe import (  # noqa: F401
     Routing,
     combine,
     forward,
     forward_unquantized,
+    forward_with_shared,
     grouped_gemm,
     route,
     silu,

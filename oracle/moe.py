@@ -227,6 +227,52 @@ def forward(x, topk_ids, topk_weights, experts, pad: int = 1, return_intermediat
     return out
 
 
+def forward_with_shared(x, topk_ids, topk_weights, experts, shared, pad: int = 1):
+    """The MoE layer with a shared expert, the shared part computed densely.
+
+    out[t] = bf16( sum_j w[t, j] * y[row(t, j)] + y_s[t] ), with y_s the
+    shared expert's SiLU-gated MLP applied to every token.  The pages name
+    shared experts ("What's Been Verified", row "E2E 61-layer (shared
+    experts)") without detail; the reading taken: the shared expert has its
+    own NVFP4 weights (``shared``: the dict of one expert), sees the same
+    NVFP4 activations x as the routed experts, and its h is requantised
+    together with theirs (one global scale over every valid row of the
+    intermediate, routed and shared); its term is added last.  Returns
+    (out, out_f64).
+    """
+    x = np.asarray(x, dtype=np.float32)
+    ids = np.asarray(topk_ids)
+    T, k = ids.shape
+    E = experts.num_experts
+    I = experts.I
+    rt = route(ids, E, pad)
+    R_pad = int(rt.padded_offsets[-1])
+    d = x.shape[1]
+    xq_codes, xq_scales, gs_x, _ = quantize(x)
+    a_codes = np.zeros((R_pad, d // 2), dtype=np.uint8)
+    a_scales = np.zeros((R_pad, d // 16), dtype=np.uint8)
+    valid = rt.row_src >= 0
+    a_codes[valid] = xq_codes[rt.row_src[valid] // k]
+    a_scales[valid] = xq_scales[rt.row_src[valid] // k]
+    h, amax_r = grouped_gemm(a_codes, a_scales, gs_x, experts, "w13", rt, "silu_mul")
+    # the shared expert over all tokens, as plain matrix products
+    xhat = dequantize(xq_codes, xq_scales, gs_x)
+    gate = dequantize(shared["w13_codes"][:I], shared["w13_scales"][:I], shared["w13_gs"][0])
+    up = dequantize(shared["w13_codes"][I:], shared["w13_scales"][I:], shared["w13_gs"][1])
+    h_s = bf16_round(silu(xhat @ gate.T) * (xhat @ up.T))
+    amax_h = np.float32(max(float(amax_r), float(np.max(np.abs(h_s))) if T else 0.0))
+    hq_codes, hq_scales, gs_h, _ = quantize(h.astype(np.float32), amax=amax_h)
+    hq_codes[~valid] = 0
+    hq_scales[~valid] = 0
+    y = grouped_gemm(hq_codes, hq_scales, gs_h, experts, "w2", rt, "f32")
+    hs_codes, hs_scales, _, _ = quantize(h_s.astype(np.float32), amax=amax_h)
+    w2_gs = np.float32(np.asarray(shared["w2_gs"]).reshape(-1)[0])
+    y_s = dequantize(hs_codes, hs_scales, gs_h) @ dequantize(
+        shared["w2_codes"], shared["w2_scales"], w2_gs).T
+    out64 = combine(y, topk_weights, rt.slot_dst, round_bf16=False) + y_s
+    return bf16_round(out64), out64
+
+
 def forward_unquantized(x, topk_ids, topk_weights, experts):
     """The same MoE with no activation quantisation and no bf16 rounding.
 

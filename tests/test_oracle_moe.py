@@ -258,3 +258,25 @@ def test_accuracy_against_unquantized_moe_matches_pages_order():
     ref = oracle.forward_unquantized(x, ids.numpy(), w.numpy(), ex)
     cos = float((out * ref).sum() / np.linalg.norm(out) / np.linalg.norm(ref))
     assert 0.97 < cos < 0.9999
+
+
+def test_shared_expert_dense_equals_one_more_routed_expert():
+    """The dense shared-expert formulation (one matrix product over all
+    tokens) equals running the shared expert as expert E that every token
+    visits with weight 1 through the routed machinery."""
+    rng = np.random.default_rng(41)
+    E, d, I, T, k = 5, 64, 128, 11, 2
+    ex = _rand_experts(rng, E + 1, d, I)
+    routed = Experts(ex.ws[:E], d, I)
+    x = (rng.standard_normal((T, d)) * 0.5).astype(np.float32)
+    ids = rng.integers(-1, E, (T, k))
+    ids[4] = -1  # a token with no routed slot still gets the shared expert
+    w = _softmax_rows(rng.standard_normal((T, k)))
+    out_d, out64_d = oracle.forward_with_shared(x, ids, w, routed, ex.ws[E], pad=4)
+    ids_x = np.concatenate([ids, np.full((T, 1), E)], 1)
+    w_x = np.concatenate([w, np.ones((T, 1), np.float32)], 1)
+    out_x, inter = oracle.forward(x, ids_x, w_x, ex, pad=4, return_intermediates=True)
+    scale = np.abs(out64_d).max()
+    assert np.allclose(out64_d, inter["out_f64"], rtol=0, atol=1e-12 * scale)
+    assert np.array_equal(out_d, out_x)
+    assert np.any(out64_d[4] != 0)
