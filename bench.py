@@ -392,6 +392,34 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+def _time_with_flush(step, steps, dev, stream):
+    """Device time of one `step` whose inputs fit in L2: `steps` back-to-back
+    pairs (write a 512 MB buffer, then the step) minus the same number of
+    buffer writes alone, both between CUDA events on the launching stream, so
+    neither the host's launch latency nor L2-resident inputs enter it."""
+    import torch
+
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+
+    def run(with_step):
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        a.record(stream)
+        for _ in range(steps):
+            flush.fill_(1)
+            if with_step:
+                step()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b)
+
+    run(True)
+    t_pairs = run(True)
+    t_flush = run(False)
+    return max(t_pairs - t_flush, 1e-6) / steps
+
+
 def run_linear(args):
     """The dense NVFP4 linear (measured-amax activation scale) on one GPU:
     tokens/s through megamoe_linear_nvfp4 with inputs resident, against the
@@ -407,29 +435,19 @@ def run_linear(args):
     x, c, s, gs = inputs.make_linear(cfg, device=dev)
     w = megamoe.LinearWeights.prepare(c, s, gs)
     out = torch.empty(cfg.T, cfg.N, dtype=torch.bfloat16, device=dev)
-    ws = torch.empty(max(256, megamoe.linear_workspace_size(cfg.T, cfg.K)), dtype=torch.uint8,
+    ws = torch.empty(max(256, megamoe.linear_workspace_size(cfg.T, cfg.K, cfg.N)), dtype=torch.uint8,
                      device=dev)
     stream = torch.cuda.current_stream()
-    # weights are smaller than L2 for these shapes: a 512 MB buffer is written
-    # between timed steps, outside the events' interval of each step
-    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
     for _ in range(max(3, args.warmup)):
         megamoe.linear_nvfp4(x, w, out=out, ws=ws)
     torch.cuda.synchronize()
     clocks = ClockSampler(0)
     clocks.start()
-    times = []
-    for _ in range(args.steps):
-        flush.fill_(1)
-        a = torch.cuda.Event(enable_timing=True)
-        b = torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        megamoe.linear_nvfp4(x, w, out=out, ws=ws)
-        b.record(stream)
-        torch.cuda.synchronize()
-        times.append(a.elapsed_time(b))
+    # weights and x are smaller than L2 for the decode shape: time with a
+    # 512 MB write between steps, subtracted (see _time_with_flush)
+    ms = _time_with_flush(lambda: megamoe.linear_nvfp4(x, w, out=out, ws=ws), args.steps, dev,
+                          stream)
     clk = clocks.stop()
-    ms = statistics.median(times)
     hbm_gbs, bf16_tf, peak_kind = _peaks()
     fp4_tf = bf16_tf * 13.5 / 2.25  # measured bf16 x the nominal dense FP4 / BF16 ratio
     w_bytes = cfg.N * cfg.K * (0.5 + 1.0 / 16)
@@ -446,7 +464,8 @@ def run_linear(args):
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "dtype": "nvfp4 (e2m1 x e4m3 scales, fp32 acc), bf16 out", "data": "synthetic",
         "config": {"workload": f"{cfg.name}: x [{cfg.T}, {cfg.K}] bf16 @ W [{cfg.N}, {cfg.K}] "
-                               "NVFP4", "l2": "512 MB written between timed steps"},
+                               "NVFP4", "l2": "512 MB written before every step; the writes' "
+                                              "own time subtracted"},
         "tflops": flops / (ms * 1e-3) / 1e12,
         "hbm_gbs": alg_bytes / (ms * 1e-3) / 1e9,
         "roofline": {"bound": bound, "achieved": achieved, "peak": peak,
@@ -455,6 +474,91 @@ def run_linear(args):
                      "peak_source": peak_kind if bound == "hbm" else
                      f"{peak_kind} bf16 x 6 (nominal FP4/BF16 ratio)"},
         "gpu_launches": (3 if cfg.T * cfg.K <= 262144 else 4) * args.steps,
+        "clocks": clk,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_layer(args, router_only=False):
+    """The MoE layer from router logits on one GPU: megamoe_router_topk (k
+    routed experts + the shared expert as expert E) then megamoe_forward over
+    E + 1 experts (router_only: the router alone)."""
+    import torch
+
+    from nvfp4_block_scaled_topk_gb300 import inputs, megamoe
+
+    megamoe.load()
+    base = inputs.CONFIGS[args.config]
+    cfg = inputs.with_shared_expert(base)
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    logits, bias = inputs.make_router_logits(base, device=dev)
+    stream = torch.cuda.current_stream()
+    if router_only:
+        fwd = None
+
+        def step():
+            megamoe.router_topk(logits, base.k, bias, shared_expert=base.E)
+    else:
+        raw = inputs.make_all_experts(cfg, device=dev)
+        weights = megamoe.Weights.prepare(raw)
+        del raw
+        torch.cuda.empty_cache()
+        x = inputs.make_activations(base, device=dev)
+        fwd = megamoe.Forward(weights, base.T, cfg.k, pad=base.pad)
+
+        def step():
+            ids, w = megamoe.router_topk(logits, base.k, bias, shared_expert=base.E)
+            fwd(x, ids, w)
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(0)
+    clocks.start()
+    if router_only:
+        # the router's inputs are small: a 512 MB write before every step,
+        # its own time subtracted
+        ms = _time_with_flush(step, args.steps, dev, stream)
+    else:
+        # the layer reads more expert weights per step than L2 holds: steps
+        # back to back between two events
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(args.steps):
+            step()
+        b.record(stream)
+        torch.cuda.synchronize()
+        ms = a.elapsed_time(b) / args.steps
+    clk = clocks.stop()
+    hbm_gbs, _, peak_kind = _peaks()
+    k_out = base.k + 1
+    if router_only:
+        alg_bytes = base.T * base.E * 4 + base.E * 4 + base.T * k_out * 8
+        kernel, launches = "k_router", 1
+    else:
+        ids, _ = megamoe.router_topk(logits, base.k, bias, shared_expert=base.E)
+        active = int(torch.unique(ids[:, :base.k]).numel()) + 1
+        alg_bytes = (inputs.algorithmic_bytes(cfg, active) + base.T * base.E * 4)
+        kernel, launches = "whole step (router + forward)", 1 + kernels_per_step(cfg)
+    achieved = alg_bytes / (ms * 1e-3) / 1e9
+    line = {
+        "op": "router" if router_only else "layer",
+        "metric": ("tokens/s, router top-k + softmax" if router_only else
+                   "tokens/s, MoE layer from router logits (routed top-k + shared expert)"),
+        "value": base.T / (ms * 1e-3), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "dtype": "fp32 router; nvfp4 experts", "data": "synthetic",
+        "config": {"workload": f"{base.name}: logits [{base.T}, {base.E}] fp32, top-{base.k} "
+                               "+ 1 shared expert" + ("" if router_only else
+                                                      f", d={base.d} I={base.I}"),
+                   "l2": ("512 MB written before every step; the writes' own time "
+                          "subtracted") if router_only else
+                         "expert weights read per step larger than L2"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_gbs, "unit": "GB/s",
+                     "frac": achieved / hbm_gbs, "traffic": None, "kernel": kernel,
+                     "peak_source": peak_kind},
+        "gpu_launches": launches * args.steps,
         "clocks": clk,
     }
     print(json.dumps(line), flush=True)
@@ -469,14 +573,17 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--ref-tokens", type=int, default=2)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--op", default="forward", choices=["forward", "linear"],
-                    help="forward: the MoE layer (default); linear: the dense NVFP4 linear "
-                         "(--config one of the linear_* workloads)")
+    ap.add_argument("--op", default="forward", choices=["forward", "linear", "router", "layer"],
+                    help="forward: the routed-expert forward (default); linear: the dense "
+                         "NVFP4 linear (--config one of the linear_* workloads); router: the "
+                         "router top-k alone; layer: router + forward with a shared expert")
     args = ap.parse_args()
     if args.op == "linear":
         if args.config == "decode":
             args.config = "linear_qa_decode"
         run_linear(args)
+    elif args.op in ("router", "layer"):
+        run_layer(args, router_only=args.op == "router")
     elif args.impl == "reference":
         run_reference(args)
     else:

@@ -280,7 +280,7 @@ megamoe_status megamoe_router_topk(const float* logits, int64_t T, int E, int64_
  *   w_scales   atom layout of [N, K/16] (megamoe_swizzle_scales)
  *   w_gs       device float: the weight's global scale
  *   out        [T, ld_out] of out_dtype
- *   ws         device workspace of megamoe_linear_workspace_size(T, K) bytes,
+ *   ws         device workspace of megamoe_linear_workspace_size(T, K, N) bytes,
  *              256-byte aligned, owned by the caller; it also receives the
  *              measured amax (float at ws + 0) and gs_x (float at ws + 4) and
  *              the status word (uint32 at ws + 8, read with megamoe_read_status)
@@ -288,7 +288,7 @@ megamoe_status megamoe_router_topk(const float* logits, int64_t T, int E, int64_
  * and ld_out of 16 bytes, 16-byte aligned pointers.  Argument errors return
  * before anything is enqueued; non-finite x sets MEGAMOE_DEV_NONFINITE.
  */
-size_t megamoe_linear_workspace_size(int64_t T, int K);
+size_t megamoe_linear_workspace_size(int64_t T, int K, int N);
 megamoe_status megamoe_linear_nvfp4(const uint16_t* x, int64_t T, int K, int64_t ld_x,
                                     const uint8_t* w_codes, const uint8_t* w_scales,
                                     const float* w_gs, int N, int out_dtype, void* out,

@@ -5,6 +5,7 @@
 #include <stdint.h>
 
 #include <algorithm>
+#include <cmath>
 #include <cstdlib>
 
 #include "../../include/megamoe.h"
@@ -40,9 +41,52 @@ struct Workspace {
   uint8_t* hq_codes;
   uint8_t* hq_sf;
   float* y;
-  int64_t rows;  // padded-row capacity
+  float* partial;  // split-K planes, shared by L1 and L2 (they run in turn)
+  int ks1, ks2;    // split-K of L1 and L2 (1 = none)
+  int64_t rows;    // padded-row capacity
   size_t bytes;
 };
+
+// Token tile of the forward's grouped GEMMs: chosen from the expected tokens
+// per expert; the MEGAMOE_TILE_N environment variable (32/64/128) overrides.
+int tile_n_setting(double expected) {
+  static const int forced = [] {
+    const char* e = std::getenv("MEGAMOE_TILE_N");
+    return (e && *e) ? std::atoi(e) : 0;
+  }();
+  if (forced == 32 || forced == 64 || forced == 128) return forced;
+  return pick_tile_n(expected);
+}
+
+// Split-K of a grouped GEMM of about `tiles` tiles: chosen by pick_ksplit;
+// the MEGAMOE_KSPLIT environment variable (1-8) overrides.
+int ksplit_setting(double tiles, int KT, int tile_n) {
+  static const int forced = [] {
+    const char* e = std::getenv("MEGAMOE_KSPLIT");
+    return (e && *e) ? std::atoi(e) : 0;
+  }();
+  if (tile_n > 64 || KT < 4) return 1;
+  if (forced >= 1 && forced <= 8) return std::min(forced, KT / 2);
+  return pick_ksplit(tiles, KT);
+}
+
+// The forward's split-K of L1 and L2.  Measured on the MegaMoE decode
+// shapes, splitting did not shorten the grouped GEMMs (their time at these
+// sizes is start-up latency and the weight stream, not idle SMs) while the
+// finishing kernels cost more, so the forward splits only when the
+// MEGAMOE_KSPLIT environment variable asks for it.
+void forward_splits(int T, int k, int E, int d, int I, int* ks1, int* ks2) {
+  *ks1 = *ks2 = 1;
+  static const int forced = [] {
+    const char* e = std::getenv("MEGAMOE_KSPLIT");
+    return (e && *e) ? std::atoi(e) : 0;
+  }();
+  const int64_t slots = static_cast<int64_t>(T) * k;
+  if (slots == 0 || forced < 2) return;
+  const int tile_n = tile_n_setting(static_cast<double>(slots) / E);
+  *ks1 = ksplit_setting(0.0, d / 256, tile_n);
+  *ks2 = ksplit_setting(0.0, I / 256, tile_n);
+}
 
 Workspace carve(void* base, int T, int k, int E, int d, int I, int pad) {
   Workspace w{};
@@ -73,19 +117,13 @@ Workspace carve(void* base, int T, int k, int E, int d, int I, int pad) {
   w.hq_codes = take(static_cast<size_t>(rows) * (I / 2));
   w.hq_sf = take(static_cast<size_t>(rows) * (I / 16));
   w.y = reinterpret_cast<float*>(take(static_cast<size_t>(rows) * d * 4));
+  forward_splits(T, k, E, d, I, &w.ks1, &w.ks2);
+  const size_t slots = static_cast<size_t>(T) * k;
+  const size_t p1 = w.ks1 > 1 ? w.ks1 * slots * 2 * I : 0;
+  const size_t p2 = w.ks2 > 1 ? w.ks2 * slots * d : 0;
+  w.partial = reinterpret_cast<float*>(take(std::max(p1, p2) * 4));
   w.bytes = off;
   return w;
-}
-
-// Token tile of the forward's grouped GEMMs: chosen from the expected tokens
-// per expert; the MEGAMOE_TILE_N environment variable (32/64/128) overrides.
-int tile_n_setting(double expected) {
-  static const int forced = [] {
-    const char* e = std::getenv("MEGAMOE_TILE_N");
-    return (e && *e) ? std::atoi(e) : 0;
-  }();
-  if (forced == 32 || forced == 64 || forced == 128) return forced;
-  return pick_tile_n(expected);
 }
 
 megamoe_status check_route_args(int T, int k, int E, int pad) {
@@ -325,6 +363,9 @@ megamoe_status megamoe_forward(const megamoe_weights* w, const uint16_t* x,
   g.zero_amax = false;
   // routing finished before the quantiser (and the requantiser) ran
   g.early_weights = true;
+  g.ksplit = wk.ks1;
+  g.partial = wk.partial;
+  g.partial_plane = static_cast<int64_t>(T) * k * 2 * I;
   e = launch_grouped_gemm(g, s);
   if (e != cudaSuccess) return MEGAMOE_ERR_CUDA;
   // 5. requantise the valid rows of h with gs from amax(h) (slot by slot)
@@ -345,6 +386,8 @@ megamoe_status megamoe_forward(const megamoe_weights* w, const uint16_t* x,
   g.out = wk.y;
   g.ld_out = d;
   g.out_amax = nullptr;
+  g.ksplit = wk.ks2;
+  g.partial_plane = static_cast<int64_t>(T) * k * d;
   e = launch_grouped_gemm(g, s);
   if (e != cudaSuccess) return MEGAMOE_ERR_CUDA;
   // 7. top-k weighted combine
@@ -371,9 +414,18 @@ megamoe_status megamoe_router_topk(const float* logits, int64_t T, int E, int64_
 
 static size_t align256(size_t n) { return (n + 255) / 256 * 256; }
 
-size_t megamoe_linear_workspace_size(int64_t T, int K) {
-  if (T < 0 || K <= 0) return 0;
-  return 256 + align256(static_cast<size_t>(T) * (K / 2)) + align256(static_cast<size_t>(T) * (K / 16));
+// The dense linear's split-K, from its shape (one group of T rows).
+static int linear_ksplit(int64_t T, int K, int N) {
+  const int tile_n = tile_n_setting(static_cast<double>(T));
+  const double tiles = std::ceil(static_cast<double>(T) / tile_n) * (N / 128);
+  return ksplit_setting(tiles, K / 256, tile_n);
+}
+
+size_t megamoe_linear_workspace_size(int64_t T, int K, int N) {
+  if (T < 0 || K <= 0 || N <= 0) return 0;
+  const int S = linear_ksplit(T, K, N);
+  return 256 + align256(static_cast<size_t>(T) * (K / 2)) + align256(static_cast<size_t>(T) * (K / 16)) +
+         (S > 1 ? align256(static_cast<size_t>(S) * T * N * 4) : 0);
 }
 
 megamoe_status megamoe_linear_nvfp4(const uint16_t* x, int64_t T, int K, int64_t ld_x,
@@ -393,7 +445,7 @@ megamoe_status megamoe_linear_nvfp4(const uint16_t* x, int64_t T, int K, int64_t
   if (!aligned(ws, 256) || !aligned(w_codes, 16) || !aligned(w_scales, 16) ||
       (x && !aligned(x, 16)) || (out && !aligned(out, 16)))
     return MEGAMOE_ERR_UNSUPPORTED_SHAPE;
-  if (ws_bytes < megamoe_linear_workspace_size(T, K)) return MEGAMOE_ERR_WORKSPACE_TOO_SMALL;
+  if (ws_bytes < megamoe_linear_workspace_size(T, K, N)) return MEGAMOE_ERR_WORKSPACE_TOO_SMALL;
   if (T == 0) return MEGAMOE_OK;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   uint8_t* base = static_cast<uint8_t*>(ws);
@@ -403,6 +455,7 @@ megamoe_status megamoe_linear_nvfp4(const uint16_t* x, int64_t T, int K, int64_t
   int32_t* groups = reinterpret_cast<int32_t*>(base + 16);  // offsets[2], padded_offsets[2]
   uint8_t* codes = base + 256;
   uint8_t* scales = codes + align256(static_cast<size_t>(T) * (K / 2));
+  float* partial = reinterpret_cast<float*>(scales + align256(static_cast<size_t>(T) * (K / 16)));
   // 1. status, group offsets, amax (one block when x is small, else k_amax)
   cudaError_t e = launch_linear_prologue(x, T, K, ld_x, amax, status, groups, s);
   if (e == cudaSuccess && !linear_prologue_full_amax(T, K))
@@ -434,6 +487,9 @@ megamoe_status megamoe_linear_nvfp4(const uint16_t* x, int64_t T, int K, int64_t
   g.status = status;
   // the offsets were written by the prologue, which finished before the quantiser
   g.early_weights = true;
+  g.ksplit = linear_ksplit(T, K, N);
+  g.partial = partial;
+  g.partial_plane = T * N;
   return cuda_status(launch_grouped_gemm(g, s));
 }
 

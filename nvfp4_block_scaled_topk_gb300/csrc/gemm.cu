@@ -40,6 +40,8 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
+#include <cmath>
 #include <mutex>
 
 #include "common.cuh"
@@ -69,11 +71,23 @@ struct GemmArgs {
   // (the forward's order), so the tile schedule is built and the first weight
   // stages are prefetched into L2 while that kernel still runs
   int early_weights;
+  // split-K (kernels instantiated with kEpiPartial*): each tile's K range is
+  // cut into ksplit pieces; piece ks of a tile writes acc * alpha as fp32 to
+  // plane ks of `partial` ([ksplit][offsets[E]][N], rows unpadded:
+  // row - padded_offsets[e] + offsets[e]); k_splitk_finish sums the planes
+  int ksplit;
+  float* partial;
+  int64_t partial_plane;  // elements per plane
 };
+
+// Internal epilogue codes of the split-K kernels (G = 1 and G = 2 operands).
+constexpr int kEpiPartial1 = 16;
+constexpr int kEpiPartial2 = 17;
 
 template <int BN, int EPI, int STAGES>
 struct GemmCfg {
-  static constexpr int G = EPI == MEGAMOE_EPI_SILU_MUL ? 2 : 1;
+  static constexpr int G = (EPI == MEGAMOE_EPI_SILU_MUL || EPI == kEpiPartial2) ? 2 : 1;
+  static constexpr bool PARTIAL = EPI >= kEpiPartial1;
   // Two accumulator slots (the MMA fills one while the epilogue drains the
   // other) whenever tensor memory has room for them.
   static constexpr int ACC_STAGES = (2 * G * BN + STAGES * (16 * G + 16) <= 512) ? 2 : 1;
@@ -96,7 +110,7 @@ struct GemmCfg {
   // per epilogue warp: STG_ROWS token rows x 32 features of output, staged so
   // that global stores are 16-byte vectors along the feature axis (512 bytes
   // for bf16, 2 KB for float)
-  static constexpr bool BF16_OUT = EPI != MEGAMOE_EPI_F32;
+  static constexpr bool BF16_OUT = EPI == MEGAMOE_EPI_SILU_MUL || EPI == MEGAMOE_EPI_BF16;
   static constexpr int STG_ROWS = BF16_OUT ? 8 : 16;
   static constexpr int STG_BYTES = STG_ROWS * 32 * (BF16_OUT ? 2 : 4);
   static constexpr int STG_OFF = (TOFF_OFF + 4 * (MEGAMOE_MAX_EXPERTS + 1) + 15) / 16 * 16;
@@ -196,6 +210,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const int MT = (C::G == 2 ? N / 2 : N) / 128;
   const int KT = K / 256;
   const int slices = K / 64;
+  // pieces per tile (1 unless split-K); piece q -> tile q / S, K range
+  // [ks * KT / S, (ks + 1) * KT / S) with ks = q % S
+  const int S = C::PARTIAL ? p.ksplit : 1;
 
   if (warp == 0 && lane == 0) {
     prefetch_tensormap(&tm_a);
@@ -205,12 +222,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   // the routing offsets from it or (early_weights) from an earlier one.
   if (p.early_weights) {
     build_tile_offsets<BN>(p.offsets, E, MT, s_toff, s_scan);
-    if (warp == 2 && lane < min(2 * STAGES, KT) && static_cast<int>(blockIdx.x) < s_toff[E]) {
-      // the first (up to) 2 x STAGES weight stages of this CTA's first tile
-      const TileInfo t0 = decode_tile(blockIdx.x, s_toff, E, MT);
+    if (warp == 2 && lane < min(2 * STAGES, KT / S) &&
+        static_cast<int>(blockIdx.x) < s_toff[E] * S) {
+      // the first (up to) 2 x STAGES weight stages of this CTA's first piece
+      const int tile0 = static_cast<int>(blockIdx.x) / S;
+      const TileInfo t0 = decode_tile(tile0, s_toff, E, MT);
+      const int kt0 = (static_cast<int>(blockIdx.x) - tile0 * S) * KT / S;
       const int blk0 = C::G == 2 ? ((t0.e * MT + t0.mt) * KT) * 2
                                  : ((t0.e * N + t0.mt * 128) >> 7) * KT;
-      bulk_prefetch_l2(p.w_codes + static_cast<int64_t>(blk0 + lane * C::G) * 16384,
+      bulk_prefetch_l2(p.w_codes + static_cast<int64_t>(blk0 + (kt0 + lane) * C::G) * 16384,
                        C::G * C::A_TILE);
     }
     pdl_wait();
@@ -220,7 +240,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     pdl_trigger();
     build_tile_offsets<BN>(p.offsets, E, MT, s_toff, s_scan);
   }
-  const int total = s_toff[E];
+  const int total = s_toff[E] * S;  // pieces
   if (static_cast<int>(blockIdx.x) >= total) return;  // uniform: no work for this CTA
 
   if (threadIdx.x == 0) {
@@ -260,13 +280,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       int issued = 0;  // stages issued; issue i used slot i % STAGES, parity (i / STAGES) & 1
       bool ok = true;
       // the next tile and its expert's first padded row are found one tile ahead
-      TileInfo ti_next = decode_tile(blockIdx.x, s_toff, E, MT);
+      TileInfo ti_next = decode_tile(static_cast<int>(blockIdx.x) / S, s_toff, E, MT);
       int poff_next = __ldg(p.padded_offsets + ti_next.e);
-      for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+      for (int piece = blockIdx.x; ok && piece < total; piece += gridDim.x) {
         const TileInfo ti = ti_next;
         const int poff = poff_next;
-        if (tile + static_cast<int>(gridDim.x) < total) {
-          ti_next = decode_tile(tile + gridDim.x, s_toff, E, MT, ti.e);
+        const int ks = piece - (piece / S) * S;
+        const int k0 = ks * KT / S, k1 = (ks + 1) * KT / S;
+        if (piece + static_cast<int>(gridDim.x) < total) {
+          ti_next = decode_tile((piece + static_cast<int>(gridDim.x)) / S, s_toff, E, MT, ti.e);
           poff_next = __ldg(p.padded_offsets + ti_next.e);
         }
         const int w_row0 = ti.e * N + ti.mt * 128;
@@ -280,7 +302,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const uint8_t* sfw0 = p.w_sf + static_cast<int64_t>(w_row0 >> 7) * slices * 512;
         const uint8_t* sfw1 = p.w_sf + static_cast<int64_t>(w_row1 >> 7) * slices * 512;
         const uint8_t* wcod = p.w_codes + static_cast<int64_t>(w_blk0) * 16384;
-        for (int kt = 0; kt < KT; ++kt) {
+        for (int kt = k0; kt < k1; ++kt) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.status, p.wait_limit_ns)) {
             ok = false;
             break;
@@ -320,11 +342,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       int stage = 0, acc = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+      for (int piece = blockIdx.x; ok && piece < total; piece += gridDim.x) {
         if (!mbar_wait(&acc_empty[acc], acc_phase ^ 1u, abort_flag, p.status, p.wait_limit_ns)) break;
         tc_fence_after();
         const uint32_t d_col = tmem + acc * C::ACC_COLS;
-        for (int kt = 0; kt < KT; ++kt) {
+        const int ks = piece - (piece / S) * S;
+        const int k0 = ks * KT / S, k1 = (ks + 1) * KT / S;
+        for (int kt = k0; kt < k1; ++kt) {
           if (!mbar_wait(&full[stage], phase, abort_flag, p.status, p.wait_limit_ns) ||
               !mbar_wait(&sf_ready[stage], phase, abort_flag, p.status, p.wait_limit_ns)) {
             ok = false;
@@ -341,7 +365,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             for (int g = 0; g < C::G; ++g) {
               const uint64_t adesc = sdesc_sw128(smem_u32(sb + C::OFF_A + g * C::A_TILE) + 32 * c);
               mma_nvf4(d_col + g * BN, adesc, bdesc, C::IDESC, sf_col + 16 * g + 4 * c,
-                       sfa_col + 4 * c, (kt | c) != 0 ? 1u : 0u);
+                       sfa_col + 4 * c, (kt != k0 || c != 0) ? 1u : 0u);
             }
           }
           tc_commit(&empty[stage]);
@@ -373,8 +397,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
-      for (int kt = 0; kt < KT; ++kt) {
+    for (int piece = blockIdx.x; ok && piece < total; piece += gridDim.x) {
+      const int ks = piece - (piece / S) * S;
+      const int nk = (ks + 1) * KT / S - ks * KT / S;
+      for (int kt = 0; kt < nk; ++kt) {
         if (!mbar_wait(&sf_full[stage], phase, abort_flag, p.status, p.wait_limit_ns)) {
           ok = false;
           break;
@@ -426,7 +452,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // tile ahead so that their latency hides behind the current tile
     struct ExpertInfo {
       TileInfo ti;
-      int count, poff;
+      int count, poff, off;  // valid rows, first padded row, first unpadded row
       float gs0, gs1;
     };
     auto fetch = [&](int tile, int e_lo) {
@@ -435,15 +461,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const int e = x.ti.e;
       x.count = __ldg(p.offsets + e + 1) - __ldg(p.offsets + e);
       x.poff = __ldg(p.padded_offsets + e);
+      x.off = __ldg(p.offsets + e);
       x.gs0 = __ldg(p.w_gs + C::G * e);
       x.gs1 = C::G == 2 ? __ldg(p.w_gs + 2 * e + 1) : 1.f;
       return x;
     };
-    ExpertInfo next = fetch(blockIdx.x, 0);
-    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+    ExpertInfo next = fetch(static_cast<int>(blockIdx.x) / S, 0);
+    for (int piece = blockIdx.x; piece < total; piece += gridDim.x) {
       const ExpertInfo cur = next;
       const TileInfo& ti = cur.ti;
-      if (tile + static_cast<int>(gridDim.x) < total) next = fetch(tile + gridDim.x, ti.e);
+      const int ks = piece - (piece / S) * S;
+      if (piece + static_cast<int>(gridDim.x) < total)
+        next = fetch((piece + static_cast<int>(gridDim.x)) / S, ti.e);
       const int m_valid = min(BN, cur.count - ti.nt * BN);
       const int64_t row0 = cur.poff + static_cast<int64_t>(ti.nt) * BN;
       const int f0 = ti.mt * 128 + q * 32;  // first feature of this warp's quarter
@@ -455,6 +484,32 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           tmem + acc * C::ACC_COLS + (static_cast<uint32_t>(q * 32) << 16);
       for (int n0 = 16 * half; n0 < m_valid; n0 += 32) {
         const int rows = min(16, m_valid - n0);
+        if (C::PARTIAL) {
+          // split-K piece: acc * alpha of each operand matrix, fp32, to plane
+          // ks at the unpadded rows; gate columns [0, N/2), up [N/2, N)
+          float* plane = p.partial + ks * p.partial_plane;
+          const int64_t urow = cur.off + static_cast<int64_t>(ti.nt) * BN + n0;
+#pragma unroll
+          for (int m = 0; m < C::G; ++m) {
+            uint32_t v[16];
+            tmem_ld_32x32b_x16(lane_base + m * BN + n0, v);
+            tmem_ld_wait();
+            const float al = m == 0 ? alpha0 : alpha1;
+            float* st = reinterpret_cast<float*>(stg);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) st[j * 32 + lane] = __uint_as_float(v[j]) * al;
+            __syncwarp();
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int c = lane + 32 * i, r = c >> 3;
+              if (r < rows)
+                *reinterpret_cast<uint4*>(plane + (urow + r) * N + m * (N / 2) + f0 + 4 * (c & 7)) =
+                    reinterpret_cast<const uint4*>(stg)[c];
+            }
+            __syncwarp();
+          }
+          continue;
+        }
         uint32_t g[16];
         tmem_ld_32x32b_x16(lane_base + n0, g);
         if (C::G == 2) {
@@ -525,7 +580,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         acc_phase ^= 1u;
       }
     }
-    if (C::G == 2) {
+    if (EPI == MEGAMOE_EPI_SILU_MUL) {
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
       if (lane == 0 && amax > 0.f)
@@ -536,6 +591,73 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
+  }
+}
+
+// Finishes a split-K GEMM: sums the fp32 planes in plane order and applies
+// the epilogue (SiLU(gate) * up -> bf16 with amax, bf16, or fp32) at the
+// padded output row.  One thread per (valid row, 4 output columns).
+template <int EPI>
+__global__ void __launch_bounds__(256)
+    k_splitk_finish(const float* __restrict__ partial, int S, int64_t plane,
+                    const int32_t* __restrict__ offsets, const int32_t* __restrict__ padded_offsets,
+                    int E, int N, void* out, int64_t ld_out, float* out_amax) {
+  pdl_wait();
+  pdl_trigger();
+  const int width = EPI == MEGAMOE_EPI_SILU_MUL ? N / 2 : N;
+  const int vecs = width / 4;
+  const int64_t total = static_cast<int64_t>(__ldg(offsets + E)) * vecs;
+  float amax = 0.f;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t u = (i >> 32) == 0
+                          ? static_cast<int64_t>(static_cast<uint32_t>(i) / static_cast<uint32_t>(vecs))
+                          : i / vecs;
+    const int v = static_cast<int>(i - u * vecs);
+    int lo = 0, hi = E - 1;  // largest e with offsets[e] <= u: the expert owning row u
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (__ldg(offsets + mid) <= u) lo = mid;
+      else hi = mid - 1;
+    }
+    const int64_t row = __ldg(padded_offsets + lo) + (u - __ldg(offsets + lo));
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
+    for (int ks = 0; ks < S; ++ks) {
+      const float* pl = partial + ks * plane + u * N + 4 * v;
+      const float4 x = __ldg(reinterpret_cast<const float4*>(pl));
+      a.x += x.x; a.y += x.y; a.z += x.z; a.w += x.w;
+      if (EPI == MEGAMOE_EPI_SILU_MUL) {
+        const float4 y = __ldg(reinterpret_cast<const float4*>(pl + N / 2));
+        b.x += y.x; b.y += y.y; b.z += y.z; b.w += y.w;
+      }
+    }
+    if (EPI == MEGAMOE_EPI_F32) {
+      *reinterpret_cast<float4*>(static_cast<float*>(out) + row * ld_out + 4 * v) = a;
+      continue;
+    }
+    float r[4] = {a.x, a.y, a.z, a.w};
+    if (EPI == MEGAMOE_EPI_SILU_MUL) {
+      const float up[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) r[j] = __fdividef(r[j], 1.0f + __expf(-r[j])) * up[j];
+    }
+    uint16_t hb[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const __nv_bfloat16 q = __float2bfloat16_rn(r[j]);
+      hb[j] = *reinterpret_cast<const uint16_t*>(&q);
+      if (EPI == MEGAMOE_EPI_SILU_MUL) amax = fmaxf(amax, fabsf(__bfloat162float(q)));
+    }
+    uint2 pk;
+    pk.x = hb[0] | (static_cast<uint32_t>(hb[1]) << 16);
+    pk.y = hb[2] | (static_cast<uint32_t>(hb[3]) << 16);
+    *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(out) + row * ld_out + 4 * v) = pk;
+  }
+  if (EPI == MEGAMOE_EPI_SILU_MUL) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    if ((threadIdx.x & 31) == 0 && amax > 0.f)
+      atomicMax(reinterpret_cast<unsigned int*>(out_amax), __float_as_uint(amax));
   }
 }
 
@@ -614,6 +736,22 @@ uint64_t wait_limit_ns() { return g_wait_limit_ns; }
 // Token tile from the expected tokens per expert: 32 for decode-sized
 // batches; 128 once experts hold more than ~48 tokens (a 128-wide MMA costs
 // 68 cycles against 51 for 64 wide, so per token it is 1.5x cheaper).
+int pick_ksplit(double tiles, int KT) {
+  if (tiles <= 0) return 1;
+  const int sms = num_sms();
+  if (sms < 8) return 1;
+  int best = 1;
+  double best_waves = std::ceil(tiles / sms);
+  for (int S = 2; S <= 8 && KT / S >= 2; ++S) {
+    const double waves = std::ceil(tiles * S / sms) / S;
+    if (waves < best_waves * 0.95) {  // a split must win by more than its overhead
+      best = S;
+      best_waves = waves;
+    }
+  }
+  return best;
+}
+
 int pick_tile_n(double expected) {
   if (expected <= 24.0) return 32;
   if (expected <= 48.0) return 64;
@@ -629,7 +767,41 @@ cudaError_t launch_grouped_gemm(const GemmLaunch& g, cudaStream_t stream) {
     return cudaErrorInvalidValue;
   GemmArgs a{g.w_codes,        g.w_scales, g.w_gs,     g.act_gs, g.offsets,
              g.padded_offsets, g.out,      g.ld_out,   g.out_amax, g.status,
-             wait_limit_ns(),  g.E,        g.N,        g.K,          g.early_weights ? 1 : 0};
+             wait_limit_ns(),  g.E,        g.N,        g.K,          g.early_weights ? 1 : 0,
+             g.ksplit,         g.partial,  g.partial_plane};
+  if (g.ksplit > 1) {
+    if (!g.partial || bn > 64) return cudaErrorInvalidValue;
+    cudaError_t err = cudaSuccess;
+    if (g.epilogue == MEGAMOE_EPI_SILU_MUL) {
+      if (g.out_amax && g.zero_amax) err = cudaMemsetAsync(g.out_amax, 0, sizeof(float), stream);
+      if (err == cudaSuccess)
+        err = bn == 32 ? launch_cfg<32, kEpiPartial2, 5>(tm_a, tm_asf, a, stream)
+                       : launch_cfg<64, kEpiPartial2, 4>(tm_a, tm_asf, a, stream);
+    } else {
+      err = bn == 32 ? launch_cfg<32, kEpiPartial1, 8>(tm_a, tm_asf, a, stream)
+                     : launch_cfg<64, kEpiPartial1, 7>(tm_a, tm_asf, a, stream);
+    }
+    if (err != cudaSuccess) return err;
+    const int width = g.epilogue == MEGAMOE_EPI_SILU_MUL ? g.N / 2 : g.N;
+    // valid rows are at most act_rows, and at most the plane's rows
+    const int64_t rows = std::min<int64_t>(g.act_rows, g.partial_plane / g.N);
+    const int64_t tasks = rows * (width / 4);
+    const unsigned blocks = static_cast<unsigned>(std::min<int64_t>((tasks + 255) / 256, num_sms() * 8));
+    switch (g.epilogue) {
+      case MEGAMOE_EPI_SILU_MUL:
+        return launch_pdl(k_splitk_finish<MEGAMOE_EPI_SILU_MUL>, dim3(blocks), dim3(256), 0,
+                          stream, g.partial, g.ksplit, g.partial_plane, g.offsets,
+                          g.padded_offsets, g.E, g.N, g.out, g.ld_out, g.out_amax);
+      case MEGAMOE_EPI_BF16:
+        return launch_pdl(k_splitk_finish<MEGAMOE_EPI_BF16>, dim3(blocks), dim3(256), 0,
+                          stream, g.partial, g.ksplit, g.partial_plane, g.offsets,
+                          g.padded_offsets, g.E, g.N, g.out, g.ld_out, g.out_amax);
+      default:
+        return launch_pdl(k_splitk_finish<MEGAMOE_EPI_F32>, dim3(blocks), dim3(256), 0,
+                          stream, g.partial, g.ksplit, g.partial_plane, g.offsets,
+                          g.padded_offsets, g.E, g.N, g.out, g.ld_out, g.out_amax);
+    }
+  }
   if (g.epilogue == MEGAMOE_EPI_SILU_MUL) {
     if (g.out_amax && g.zero_amax) {
       cudaError_t err = cudaMemsetAsync(g.out_amax, 0, sizeof(float), stream);

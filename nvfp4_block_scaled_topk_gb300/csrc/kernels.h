@@ -86,7 +86,17 @@ struct GemmLaunch {
   // the one immediately preceding the GEMM (the forward's order): the GEMM
   // then prefetches its first weight stages while that kernel runs
   bool early_weights = false;
+  // split-K: ksplit > 1 cuts each tile's K range into ksplit pieces (token
+  // tiles of 32 or 64 only); `partial` holds ksplit planes of
+  // partial_plane >= offsets[E] * N floats; a finishing kernel sums them
+  int ksplit = 1;
+  float* partial = nullptr;
+  int64_t partial_plane = 0;
 };
+// Split-K choice for a GEMM of about `tiles` whole-K tiles of KT K steps: the
+// smallest ksplit (<= 8, >= 2 K steps a piece) that minimises the waves of
+// pieces over the SMs, in units of a whole tile.
+int pick_ksplit(double tiles, int KT);
 // Encodes the tensor maps and launches the persistent grouped GEMM.
 cudaError_t launch_grouped_gemm(const GemmLaunch& g, cudaStream_t stream);
 int pick_tile_n(double expected_tokens_per_expert);

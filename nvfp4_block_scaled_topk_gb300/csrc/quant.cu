@@ -238,15 +238,27 @@ __global__ void __launch_bounds__(kLinearPrologueThreads)
   }
   uint32_t m = 0;
   if (full_amax) {
+    // at most 32 vectors a thread (rows * K <= 262144): issued 8 at a time so
+    // that their latencies overlap
     const int vecs = K / 8;
+    const int total = static_cast<int>(rows) * vecs;
     uint32_t m2 = 0;
-    for (int64_t i = tid; i < rows * vecs; i += kLinearPrologueThreads) {
-      const int64_t r = i / vecs;
-      const uint4 q = __ldg(reinterpret_cast<const uint4*>(x + r * ld) + (i - r * vecs));
-      m2 = __vmaxu2(m2, q.x & 0x7FFF7FFFu);
-      m2 = __vmaxu2(m2, q.y & 0x7FFF7FFFu);
-      m2 = __vmaxu2(m2, q.z & 0x7FFF7FFFu);
-      m2 = __vmaxu2(m2, q.w & 0x7FFF7FFFu);
+    for (int base = tid; base < total; base += 8 * kLinearPrologueThreads) {
+      uint4 q[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int i = base + j * kLinearPrologueThreads;
+        const int r = i / vecs;
+        q[j] = i < total ? __ldg(reinterpret_cast<const uint4*>(x + r * ld) + (i - r * vecs))
+                         : make_uint4(0u, 0u, 0u, 0u);
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        m2 = __vmaxu2(m2, q[j].x & 0x7FFF7FFFu);
+        m2 = __vmaxu2(m2, q[j].y & 0x7FFF7FFFu);
+        m2 = __vmaxu2(m2, q[j].z & 0x7FFF7FFFu);
+        m2 = __vmaxu2(m2, q[j].w & 0x7FFF7FFFu);
+      }
     }
     m = max(m2 & 0xFFFFu, m2 >> 16);
 #pragma unroll

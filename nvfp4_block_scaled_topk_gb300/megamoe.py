@@ -50,7 +50,7 @@ SIGNATURES = {
     "megamoe_read_status": (_I, [_P, _P, _P]),
     "megamoe_forward_static": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P, _P]),
     "megamoe_set_wait_limit_ns": (None, [ctypes.c_uint64]),
-    "megamoe_linear_workspace_size": (_SZ, [_I64, _I]),
+    "megamoe_linear_workspace_size": (_SZ, [_I64, _I, _I]),
     "megamoe_router_topk": (_I, [_P, _I64, _I, _I64, _P, _I, _I, _P, _P, _P]),
     "megamoe_linear_nvfp4": (_I, [_P, _I64, _I, _I64, _P, _P, _P, _I, _I, _P, _I64, _P, _SZ, _P]),
 }
@@ -254,8 +254,8 @@ class LinearWeights:
                    swizzle_scales(scales.contiguous()), gs_t)
 
 
-def linear_workspace_size(T: int, K: int) -> int:
-    return int(load().megamoe_linear_workspace_size(T, K))
+def linear_workspace_size(T: int, K: int, N: int) -> int:
+    return int(load().megamoe_linear_workspace_size(T, K, N))
 
 
 def linear_nvfp4(x: torch.Tensor, w: LinearWeights, out_dtype=EPI_BF16, out=None, ws=None):
@@ -266,7 +266,7 @@ def linear_nvfp4(x: torch.Tensor, w: LinearWeights, out_dtype=EPI_BF16, out=None
     T, K = x.shape
     if K != w.K:
         raise ValueError("x and w disagree on K")
-    need = linear_workspace_size(T, K)
+    need = linear_workspace_size(T, K, w.N)
     if ws is None:
         ws = torch.empty(max(need, 256), dtype=torch.uint8, device=x.device)
     if out is None:

@@ -98,7 +98,7 @@ def test_linear_edge_cases(cuda_lib):
     x, c, s, gs, w = _prepared(cfg)
     out, ws = megamoe.linear_nvfp4(x[:0], w)
     assert out.shape == (0, cfg.N)
-    ws = torch.empty(megamoe.linear_workspace_size(cfg.T, cfg.K), dtype=torch.uint8, device="cuda")
+    ws = torch.empty(megamoe.linear_workspace_size(cfg.T, cfg.K, cfg.N), dtype=torch.uint8, device="cuda")
     o = torch.empty(cfg.T, cfg.N, dtype=torch.bfloat16, device="cuda")
     p = megamoe._p
     # K not a multiple of 256, N not a multiple of 128, short workspace, bad dtype
