@@ -265,6 +265,26 @@ megamoe_status megamoe_router_topk(const float* logits, int64_t T, int E, int64_
                                    megamoe_stream_t stream);
 
 /*
+ * megamoe_forward_from_logits -- the MoE layer from router logits: the router
+ * step of megamoe_router_topk (k routed experts among the first n_logits,
+ * plus, with shared_expert >= 0, that expert for every token with weight 1)
+ * followed by megamoe_forward over w's experts with k_out = k + (shared_expert
+ * >= 0) slots per token.  For small batches (T * hidden <= 262144) the router
+ * runs inside the forward's first thread block, ahead of the routing; larger
+ * batches run it as its own kernel.  The ids and weights are written into the
+ * workspace (sized by megamoe_workspace_size(T, k_out, w->num_experts, ...)).
+ *   logits   float [T, ld_logits], n_logits <= w->num_experts columns used;
+ *   bias     float [n_logits] or NULL (selection only)
+ *   shared_expert  -1, or an expert index in [n_logits, w->num_experts)
+ * Otherwise as megamoe_forward; k_out <= 16.
+ */
+megamoe_status megamoe_forward_from_logits(const megamoe_weights* w, const uint16_t* x,
+                                           const float* logits, int64_t ld_logits,
+                                           const float* bias, int n_logits, int k,
+                                           int shared_expert, int T, int pad, uint16_t* out,
+                                           void* ws, size_t ws_bytes, megamoe_stream_t stream);
+
+/*
  * megamoe_linear_nvfp4 -- a dense NVFP4 linear layer whose activation global
  * scale comes from the measured amax of x, not from a stored input scale
  * ("Current Bug: vLLM produces NaN from layer 0", "Root Cause" and "Key

@@ -42,6 +42,8 @@ struct Workspace {
   uint8_t* hq_sf;
   float* y;
   float* partial;  // split-K planes, shared by L1 and L2 (they run in turn)
+  int32_t* r_ids;  // router outputs of megamoe_forward_from_logits [T, k]
+  float* r_w;
   int ks1, ks2;    // split-K of L1 and L2 (1 = none)
   int64_t rows;    // padded-row capacity
   size_t bytes;
@@ -122,6 +124,8 @@ Workspace carve(void* base, int T, int k, int E, int d, int I, int pad) {
   const size_t p1 = w.ks1 > 1 ? w.ks1 * slots * 2 * I : 0;
   const size_t p2 = w.ks2 > 1 ? w.ks2 * slots * d : 0;
   w.partial = reinterpret_cast<float*>(take(std::max(p1, p2) * 4));
+  w.r_ids = reinterpret_cast<int32_t*>(take(4 * slots));
+  w.r_w = reinterpret_cast<float*>(take(4 * slots));
   w.bytes = off;
   return w;
 }
@@ -293,11 +297,15 @@ size_t megamoe_workspace_size(int T, int k, int E, int d, int I, int pad) {
   return carve(nullptr, T, k, E, d, I, pad).bytes;
 }
 
-megamoe_status megamoe_forward(const megamoe_weights* w, const uint16_t* x,
-                               const int32_t* topk_ids, const float* topk_weights, int T, int k,
-                               int pad, uint16_t* out, void* ws, size_t ws_bytes,
-                               megamoe_stream_t stream) {
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+}  // extern "C"
+
+namespace {
+
+// The forward; with `router` the ids and weights are computed here from the
+// router logits (into the workspace) instead of being passed in.
+megamoe_status forward_impl(const megamoe_weights* w, const uint16_t* x, const int32_t* topk_ids,
+                            const float* topk_weights, int T, int k, int pad, uint16_t* out,
+                            void* ws, size_t ws_bytes, cudaStream_t s, RouterArgs* router) {
   if (!w) return MEGAMOE_ERR_INVALID_ARG;
   const int E = w->num_experts, d = w->hidden, I = w->intermediate;
   megamoe_status st = check_route_args(T, k, E, pad);
@@ -307,7 +315,8 @@ megamoe_status megamoe_forward(const megamoe_weights* w, const uint16_t* x,
   if (!w->w13_codes || !w->w13_scales || !w->w13_gs || !w->w2_codes || !w->w2_scales ||
       !w->w2_gs || !ws)
     return MEGAMOE_ERR_INVALID_ARG;
-  if (T > 0 && (!x || !topk_ids || !topk_weights || !out)) return MEGAMOE_ERR_INVALID_ARG;
+  if (T > 0 && (!x || (!router && (!topk_ids || !topk_weights)) || !out))
+    return MEGAMOE_ERR_INVALID_ARG;
   if (!aligned(ws, 256)) return MEGAMOE_ERR_INVALID_ARG;
   if ((x && !aligned(x, 16)) || (out && !aligned(out, 8)) || !aligned(w->w13_codes, 16) ||
       !aligned(w->w2_codes, 16) || !aligned(w->w13_scales, 16) || !aligned(w->w2_scales, 16))
@@ -320,17 +329,28 @@ megamoe_status megamoe_forward(const megamoe_weights* w, const uint16_t* x,
   const double expected = static_cast<double>(T) * k / E;
   const int tile_n = tile_n_setting(expected);
 
-  cudaError_t e;
-  // 1-3. route (its first act clears the status word and the amax
+  cudaError_t e = cudaSuccess;
+  if (router) {  // the ids and weights land in the workspace
+    router->ids_out = wk.r_ids;
+    router->w_out = wk.r_w;
+    topk_ids = wk.r_ids;
+    topk_weights = wk.r_w;
+  }
+  // 0-3. (router,) route (its first act clears the status word and the amax
   //      accumulators), amax of x, quantise x into its routed rows.  Padding
   //      rows are left as they are: each output column of the grouped GEMM
   //      depends on one token row, and columns of padding rows are never
-  //      stored.  Small batches route and take the amax in one thread block.
+  //      stored.  Small batches route (and run the router) and take the amax
+  //      in one thread block.
   if (prologue_fits(T, d)) {
     e = launch_prologue(topk_ids, T, k, E, pad, wk.counts, wk.offsets, wk.padded_offsets,
                         wk.row_src, wk.rows, wk.slot_dst, wk.status, wk.status, 5, x, d,
-                        wk.amax_x, s);
+                        wk.amax_x, s, router);
   } else {
+    if (router)
+      e = launch_router(router->logits, T, router->n_logits, router->ld, router->bias,
+                        router->k_routed, router->shared, wk.r_ids, wk.r_w, s);
+    if (e != cudaSuccess) return MEGAMOE_ERR_CUDA;
     e = launch_route(topk_ids, T * k, E, pad, wk.counts, wk.offsets, wk.padded_offsets,
                      wk.row_src, wk.rows, wk.slot_dst, wk.status, wk.status, 5, s);
     if (e != cudaSuccess) return MEGAMOE_ERR_CUDA;
@@ -393,6 +413,44 @@ megamoe_status megamoe_forward(const megamoe_weights* w, const uint16_t* x,
   // 7. top-k weighted combine
   e = launch_combine(wk.y, d, wk.slot_dst, topk_weights, T, k, d, out, s);
   return cuda_status(e);
+}
+
+}  // namespace
+
+extern "C" {
+
+megamoe_status megamoe_forward(const megamoe_weights* w, const uint16_t* x,
+                               const int32_t* topk_ids, const float* topk_weights, int T, int k,
+                               int pad, uint16_t* out, void* ws, size_t ws_bytes,
+                               megamoe_stream_t stream) {
+  return forward_impl(w, x, topk_ids, topk_weights, T, k, pad, out, ws, ws_bytes,
+                      reinterpret_cast<cudaStream_t>(stream), nullptr);
+}
+
+megamoe_status megamoe_forward_from_logits(const megamoe_weights* w, const uint16_t* x,
+                                           const float* logits, int64_t ld_logits,
+                                           const float* bias, int n_logits, int k,
+                                           int shared_expert, int T, int pad, uint16_t* out,
+                                           void* ws, size_t ws_bytes, megamoe_stream_t stream) {
+  if (!w || n_logits < 1 || n_logits > w->num_experts || ld_logits < n_logits || k < 1 ||
+      k > n_logits)
+    return MEGAMOE_ERR_INVALID_ARG;
+  if (shared_expert >= 0 && (shared_expert < n_logits || shared_expert >= w->num_experts))
+    return MEGAMOE_ERR_INVALID_ARG;
+  if (T > 0 && !logits) return MEGAMOE_ERR_INVALID_ARG;
+  if ((logits && !aligned(logits, 4)) || (bias && !aligned(bias, 4)))
+    return MEGAMOE_ERR_UNSUPPORTED_SHAPE;
+  const int k_out = k + (shared_expert >= 0 ? 1 : 0);
+  if (k_out > MEGAMOE_MAX_TOPK) return MEGAMOE_ERR_UNSUPPORTED_SHAPE;
+  RouterArgs r;
+  r.logits = logits;
+  r.ld = ld_logits;
+  r.bias = bias;
+  r.n_logits = n_logits;
+  r.k_routed = k;
+  r.shared = shared_expert;
+  return forward_impl(w, x, nullptr, nullptr, T, k_out, pad, out, ws, ws_bytes,
+                      reinterpret_cast<cudaStream_t>(stream), &r);
 }
 
 void megamoe_set_wait_limit_ns(uint64_t ns) { set_wait_limit_ns(ns); }

@@ -53,11 +53,23 @@ cudaError_t launch_quant(const uint16_t* x, int64_t rows_in, int K, int64_t ld,
 // Small-batch prologue of the forward in one thread block: route and the amax
 // of x.  Used when prologue_fits(T, d).
 bool prologue_fits(int T, int d);
+// Router fused into the prologue: ids/weights [T, k] (k = k_routed + shared
+// column) are written from logits [T, ld] over n_logits experts, then routed.
+struct RouterArgs {
+  const float* logits = nullptr;
+  int64_t ld = 0;
+  const float* bias = nullptr;
+  int n_logits = 0;
+  int k_routed = 0;
+  int shared = -1;
+  int32_t* ids_out = nullptr;
+  float* w_out = nullptr;
+};
 cudaError_t launch_prologue(const int32_t* ids, int T, int k, int E, int pad, int32_t* counts,
                             int32_t* offsets, int32_t* padded_offsets, int32_t* row_src,
                             int64_t row_capacity, int32_t* slot_dst, uint32_t* status,
                             uint32_t* zero_words, int n_zero, const uint16_t* x, int d,
-                            float* amax, cudaStream_t stream);
+                            float* amax, cudaStream_t stream, const RouterArgs* router = nullptr);
 cudaError_t launch_swizzle(const uint8_t* src, int64_t rows, int K, uint8_t* dst,
                            cudaStream_t stream);
 

@@ -17,6 +17,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "router.cuh"
 
 namespace megamoe {
 
@@ -54,7 +55,7 @@ __device__ __forceinline__ int block_exclusive_scan_1024(int v, int* warp_sums, 
 // The routing itself, for one block of kRouteThreads threads.  `smem` holds
 // 32*E + 2*E + 1 ints.  Ends with the block's global writes issued; callers
 // that read them back in the same block synchronise first.
-__device__ void route_block(const int32_t* __restrict__ ids, int n_slots, int E, int pad,
+__device__ void route_block(const int32_t* ids, int n_slots, int E, int pad,
                             int32_t* counts, int32_t* offsets, int32_t* padded_offsets,
                             int32_t* row_src, int64_t row_capacity, int32_t* slot_dst,
                             uint32_t* status, uint32_t* zero_words, int n_zero, int* smem) {
@@ -143,7 +144,7 @@ __device__ void route_block(const int32_t* __restrict__ ids, int n_slots, int E,
 }
 
 __global__ void __launch_bounds__(kRouteThreads, 1)
-    k_route(const int32_t* __restrict__ ids, int n_slots, int E, int pad, int32_t* counts,
+    k_route(const int32_t* ids, int n_slots, int E, int pad, int32_t* counts,
             int32_t* offsets, int32_t* padded_offsets, int32_t* row_src, int64_t row_capacity,
             int32_t* slot_dst, uint32_t* status, uint32_t* zero_words, int n_zero) {
   extern __shared__ int smem_route[];
@@ -158,10 +159,11 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
 constexpr int64_t kPrologueMaxElems = 262144;  // T * d read by one block
 
 __global__ void __launch_bounds__(kRouteThreads, 1)
-    k_prologue(const int32_t* __restrict__ ids, int T, int k, int E, int pad, int32_t* counts,
+    k_prologue(const int32_t* ids, int T, int k, int E, int pad, int32_t* counts,
                int32_t* offsets, int32_t* padded_offsets, int32_t* row_src,
                int64_t row_capacity, int32_t* slot_dst, uint32_t* status, uint32_t* zero_words,
-               int n_zero, const uint16_t* __restrict__ x, int d, float* amax_out) {
+               int n_zero, const uint16_t* __restrict__ x, int d, float* amax_out,
+               const RouterArgs r) {
   extern __shared__ int smem_route[];
   __shared__ uint32_t red[kRouteWarps];
   pdl_wait();
@@ -177,6 +179,17 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
   for (int j = 0; j < kPre; ++j) {
     const int64_t i = tid + static_cast<int64_t>(j) * kRouteThreads;
     pre[j] = i < vecs ? __ldg(reinterpret_cast<const uint4*>(x) + i) : make_uint4(0u, 0u, 0u, 0u);
+  }
+  if (r.logits) {
+    // the router first: warp w takes tokens w, w + 32, ...; its score row
+    // lives in the routing histogram's shared memory, not yet in use
+    float* s_row = reinterpret_cast<float*>(smem_route) + warp * r.n_logits;
+    for (int t = warp; t < T; t += kRouteWarps)
+      router_token(r.logits + static_cast<int64_t>(t) * r.ld, r.bias, r.n_logits, r.k_routed,
+                   r.shared, s_row, r.ids_out + static_cast<int64_t>(t) * k,
+                   r.w_out + static_cast<int64_t>(t) * k, lane);
+    __syncthreads();  // the ids are read back below by every warp
+    ids = r.ids_out;
   }
   route_block(ids, T * k, E, pad, counts, offsets, padded_offsets, row_src, row_capacity,
               slot_dst, status, zero_words, n_zero, smem_route);
@@ -234,14 +247,15 @@ cudaError_t launch_prologue(const int32_t* ids, int T, int k, int E, int pad, in
                             int32_t* offsets, int32_t* padded_offsets, int32_t* row_src,
                             int64_t row_capacity, int32_t* slot_dst, uint32_t* status,
                             uint32_t* zero_words, int n_zero, const uint16_t* x, int d,
-                            float* amax, cudaStream_t stream) {
+                            float* amax, cudaStream_t stream, const RouterArgs* router) {
   const size_t smem = route_smem_bytes(E);
   cudaError_t err = cudaFuncSetAttribute(k_prologue, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
   if (err != cudaSuccess) return err;
+  const RouterArgs none{};
   return launch_pdl(k_prologue, dim3(1), dim3(kRouteThreads), smem, stream, ids, T, k, E, pad,
                     counts, offsets, padded_offsets, row_src, row_capacity, slot_dst, status,
-                    zero_words, n_zero, x, d, amax);
+                    zero_words, n_zero, x, d, amax, router ? *router : none);
 }
 
 }  // namespace megamoe

@@ -52,6 +52,8 @@ SIGNATURES = {
     "megamoe_set_wait_limit_ns": (None, [ctypes.c_uint64]),
     "megamoe_linear_workspace_size": (_SZ, [_I64, _I, _I]),
     "megamoe_router_topk": (_I, [_P, _I64, _I, _I64, _P, _I, _I, _P, _P, _P]),
+    "megamoe_forward_from_logits": (_I, [_P, _P, _P, _I64, _P, _I, _I, _I, _I, _I, _P, _P, _SZ,
+                                         _P]),
     "megamoe_linear_nvfp4": (_I, [_P, _I64, _I, _I64, _P, _P, _P, _I, _I, _P, _I64, _P, _SZ, _P]),
 }
 
@@ -354,6 +356,24 @@ class Forward:
         _check("megamoe_forward", load().megamoe_forward(
             ctypes.byref(self.cw), _p(x), _p(topk_ids), _p(topk_weights), self.T, self.k,
             self.pad, _p(out), self.ws_ptr, self.ws_bytes, _stream()))
+        return out[:self.T]
+
+    def from_logits(self, x, logits, k: int, bias=None, shared_expert: int = -1, out=None):
+        """megamoe_forward_from_logits: the router (top-k of logits + bias,
+        softmax of the selected logits, plus ``shared_expert`` with weight 1
+        when >= 0) then the forward; this object's k must be k (+1 with a
+        shared expert)."""
+        _dev(x, torch.bfloat16, "x")
+        _dev(logits, torch.float32, "logits")
+        if bias is not None:
+            _dev(bias, torch.float32, "bias")
+        if self.k != k + (1 if shared_expert >= 0 else 0):
+            raise ValueError("Forward was built for a different number of slots")
+        out = self.out if out is None else out
+        _check("megamoe_forward_from_logits", load().megamoe_forward_from_logits(
+            ctypes.byref(self.cw), _p(x), _p(logits), logits.stride(0), _p(bias),
+            logits.shape[1], k, shared_expert, self.T, self.pad, _p(out), self.ws_ptr,
+            self.ws_bytes, _stream()))
         return out[:self.T]
 
     def read_status(self) -> int:

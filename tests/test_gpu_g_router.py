@@ -89,3 +89,40 @@ def test_forward_with_shared_expert(cuda_lib, name, pad):
     _, out64 = oracle.forward_with_shared(x.float().numpy(), ids_o[:, :base.k],
                                           w_gpu[:, :base.k], routed, experts[base.E], pad=pad)
     assert np.allclose(out64, inter["out_f64"], rtol=0, atol=1e-9 * np.abs(out64).max())
+
+
+@pytest.mark.parametrize("name,T", [("tiny", None), ("decode", None), ("decode1", None),
+                                    ("prefill_mid", None)])
+def test_forward_from_logits_equals_router_then_forward(cuda_lib, name, T):
+    """megamoe_forward_from_logits (router fused into the first block for
+    small batches, its own kernel for large ones) gives exactly the output
+    of megamoe_router_topk followed by megamoe_forward, and its ids are the
+    oracle router's."""
+    if name == "prefill_mid":  # 512 tokens x 1024: the router runs as its own kernel
+        base = inputs.MoEConfig("prefill_mid", 64, 6, 1024, 512, 512, "zipf", seed=78)
+    else:
+        base = inputs.CONFIGS[name]
+    cfg = inputs.with_shared_expert(base)
+    torch.cuda.empty_cache()
+    raw = inputs.make_all_experts(cfg, device="cuda")
+    weights = megamoe.Weights.prepare(raw)
+    x = inputs.make_activations(base).cuda()
+    logits, bias = inputs.make_router_logits(base, device="cuda")
+    fwd_a = megamoe.Forward(weights, base.T, cfg.k, pad=32)
+    ids, w = megamoe.router_topk(logits, base.k, bias, shared_expert=base.E)
+    out_a = fwd_a(x, ids, w).clone()
+    fwd_b = megamoe.Forward(weights, base.T, cfg.k, pad=32)
+    out_b = fwd_b.from_logits(x, logits, base.k, bias, shared_expert=base.E).clone()
+    torch.cuda.synchronize()
+    assert fwd_a.read_status() == 0 and fwd_b.read_status() == 0
+    assert torch.equal(out_a, out_b)
+    want_ids, _ = oracle.router_topk(logits.cpu().numpy(), base.k,
+                                     None if bias is None else bias.cpu().numpy(),
+                                     shared_expert=base.E)
+    assert np.array_equal(ids.cpu().numpy(), want_ids)
+    # without a shared expert too
+    fwd_c = megamoe.Forward(weights, base.T, base.k, pad=32)
+    ids2, w2 = megamoe.router_topk(logits, base.k, bias)
+    out_c = fwd_c(x, ids2, w2).clone()
+    out_d = megamoe.Forward(weights, base.T, base.k, pad=32).from_logits(x, logits, base.k, bias)
+    assert torch.equal(out_c, out_d)
