@@ -13,14 +13,19 @@
 // holds the gate AND the up accumulators of the same 128 features (two MMAs
 // per K step into two TMEM ranges), so SiLU(gate) * up is a per-lane epilogue.
 //
-// Roles (320 threads, one CTA per SM, grid = number of SMs):
-//   warp 0      TMA producer: weight tiles and token tiles (128-byte swizzle),
-//               the weights' block-scale atoms (bulk copies) and the token
-//               tile's row-major block scales into a STAGES-deep ring;
+// Roles (448 threads, one CTA per SM, grid = number of SMs):
+//   warp 0      producer (one lane): per stage, the weights' block-scale atoms
+//               (bulk copies) and the token tile's row-major block scales
+//               (tensor map) on one barrier, then the stage's weight codes
+//               (one bulk copy of pre-swizzled blocks) and token codes
+//               (tensor map, 128-byte swizzle) on another, into a
+//               STAGES-deep ring;
 //   warp 1      TMEM allocator; one lane issues tcgen05.mma and commits
 //               stage-free / accumulator-ready;
-//   warps 2..5  epilogue: tcgen05.ld of their 32-lane quarter, alpha scaling,
-//               SiLU * up -> bf16 + amax (L1) or fp32 (L2), masked stores;
+//   warps 2..5, 10..13  epilogue, two warps per 32-lane TMEM quarter taking
+//               alternate 16-column chunks: tcgen05.ld, alpha scaling,
+//               SiLU * up -> bf16 + amax (L1), bf16, or fp32 (L2), staged
+//               through shared memory into 16-byte stores;
 //   warps 6..9  scale writers: each writes the stage's weight and token block
 //               scales into its own 32-lane quarter of tensor memory with
 //               tcgen05.st (every quarter holds the same copy, the layout the
@@ -28,6 +33,9 @@
 //               pipe (a tcgen05.cp costs about as much as an MMA), and the
 //               token tile's first row always lands in the first scale
 //               column whatever row the tile starts at.
+// Split-K (kEpiPartial* instantiations, used by the dense linear when it has
+// fewer tiles than SMs): each tile's K range is cut into pieces whose fp32
+// partial sums go to planes that k_splitk_finish adds in a fixed order.
 // Every expert's weights live in one buffer, packed once into blocks of 128
 // rows x 128 bytes already in the 128-byte swizzle ([E*N/128][K/256] blocks;
 // for L1 the gate and up blocks of the same features and K step adjacent), so
