@@ -93,18 +93,69 @@ __device__ __forceinline__ void store_block(const QuantArgs& a, int64_t out_row,
   a.scales[so] = static_cast<uint8_t>(s8);
 }
 
-// One thread per (row, 16-element block): short dependency chains, many
-// threads.  Tasks (NB = K/16 blocks per row):
+// One thread per (row, group of BPT 16-element blocks).  Tasks (NB = K/16
+// blocks per row, in groups of BPT):
 //  * slot_rows: [0, rows_in*NB): slot s encodes row slot_dst[s] in place;
 //  * slot_dst:  [0, rows_in*NB) are token rows, scattered to their routed
 //    rows, then, if row_src is given, [rows_in*NB, (rows_in+out_rows)*NB)
 //    zero the padding rows;
 //  * otherwise  [0, out_rows*NB) map out row r <- x row r (padding rows
 //    zeroed when row_src is given).
+// BPT consecutive 16-element blocks of one row per task: BPT = 1 for small
+// launches (many short tasks over many SMs), 4 for large ones (32 bytes of
+// codes and one 4-byte scale word per store, fewer index loads).
+template <int BPT>
+struct Group {
+  uint2 c[BPT];
+  uint32_t s8[BPT];
+};
+
+template <int BPT>
+__device__ __forceinline__ Group<BPT> encode_group(const uint16_t* src, float gs) {
+  uint4 v[2 * BPT];
+#pragma unroll
+  for (int i = 0; i < 2 * BPT; ++i) v[i] = __ldg(reinterpret_cast<const uint4*>(src) + i);
+  Group<BPT> g;
+#pragma unroll
+  for (int j = 0; j < BPT; ++j) encode_block(v[2 * j], v[2 * j + 1], gs, g.c[j], g.s8[j]);
+  return g;
+}
+
+template <int BPT>
+__device__ __forceinline__ void store_group(const QuantArgs& a, int64_t out_row, int b0,
+                                            const Group<BPT>& g) {
+  if (BPT == 1) {
+    store_block(a, out_row, b0, g.c[0], g.s8[0]);
+    return;
+  }
+  // BPT = 4: b0 is a multiple of 4, so the codes are 32 aligned bytes and the
+  // four scale bytes one aligned word in either layout
+  uint4* cd = reinterpret_cast<uint4*>(a.codes + out_row * (a.K / 2) + 8 * b0);
+  cd[0] = make_uint4(g.c[0].x, g.c[0].y, g.c[1].x, g.c[1].y);
+  cd[1] = make_uint4(g.c[2].x, g.c[2].y, g.c[3].x, g.c[3].y);
+  const uint32_t w = g.s8[0] | (g.s8[1] << 8) | (g.s8[2] << 16) | (g.s8[3] << 24);
+  const int64_t so = a.scale_layout == MEGAMOE_SCALES_MMA
+                         ? sf_atom_offset(out_row, b0 >> 2, a.K / 64)
+                         : out_row * (a.K / 16) + b0;
+  *reinterpret_cast<uint32_t*>(a.scales + so) = w;
+}
+
+template <int BPT>
+__device__ __forceinline__ Group<BPT> zero_group() {
+  Group<BPT> g;
+#pragma unroll
+  for (int j = 0; j < BPT; ++j) {
+    g.c[j] = make_uint2(0u, 0u);
+    g.s8[j] = 0u;
+  }
+  return g;
+}
+
+template <int BPT>
 __global__ void __launch_bounds__(256) k_quant(const QuantArgs a) {
   pdl_wait();
   pdl_trigger();
-  const int NB = a.K / 16;
+  const int NG = a.K / 16 / BPT;  // tasks per row
   const float amax = *a.amax;
   const float gs = amax == 0.f ? 1.f : __fdiv_rn(2688.0f, amax);
   if (blockIdx.x == 0 && threadIdx.x == 0 && a.gs_out) *a.gs_out = gs;
@@ -112,47 +163,40 @@ __global__ void __launch_bounds__(256) k_quant(const QuantArgs a) {
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   if (a.slot_rows) {
     for (int64_t t = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
-         t < a.rows_in * NB; t += stride) {
-      const int64_t slot = task_div(t, NB);
-      const int b = static_cast<int>(t - slot * NB);
+         t < a.rows_in * NG; t += stride) {
+      const int64_t slot = task_div(t, NG);
+      const int b0 = static_cast<int>(t - slot * NG) * BPT;
       const int64_t row = a.slot_dst[slot];
       if (row < 0 || row >= live) continue;
-      const uint4* src = reinterpret_cast<const uint4*>(a.x + row * a.ld + 16 * b);
-      uint2 c;
-      uint32_t s8;
-      encode_block(__ldg(src), __ldg(src + 1), gs, c, s8);
-      store_block(a, row, b, c, s8);
+      store_group<BPT>(a, row, b0, encode_group<BPT>(a.x + row * a.ld + 16 * b0, gs));
     }
     return;
   }
-  const int64_t token_tasks = a.slot_dst ? a.rows_in * NB : 0;
-  const int64_t total = token_tasks + ((a.slot_dst && !a.row_src) ? 0 : a.out_rows * NB);
+  const int64_t token_tasks = a.slot_dst ? a.rows_in * NG : 0;
+  const int64_t total = token_tasks + ((a.slot_dst && !a.row_src) ? 0 : a.out_rows * NG);
   for (int64_t t = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; t < total;
        t += stride) {
     const bool token_task = t < token_tasks;
     const int64_t u = token_task ? t : t - token_tasks;
-    const int64_t row = task_div(u, NB);
-    const int b = static_cast<int>(u - row * NB);
+    const int64_t row = task_div(u, NG);
+    const int b0 = static_cast<int>(u - row * NG) * BPT;
     if (!token_task) {
       if (row >= live) continue;
       const bool pad_row = a.row_src && a.row_src[row] < 0;
       if (a.slot_dst && !pad_row) continue;  // written by its token task
       if (pad_row) {
-        store_block(a, row, b, make_uint2(0u, 0u), 0u);
+        store_group<BPT>(a, row, b0, zero_group<BPT>());
         continue;
       }
     }
-    const uint4* src = reinterpret_cast<const uint4*>(a.x + row * a.ld + 16 * b);
-    uint2 c;
-    uint32_t s8;
-    encode_block(__ldg(src), __ldg(src + 1), gs, c, s8);
+    const Group<BPT> g = encode_group<BPT>(a.x + row * a.ld + 16 * b0, gs);
     if (token_task) {
       for (int j = 0; j < a.k; ++j) {
         const int dst = a.slot_dst[row * a.k + j];
-        if (dst >= 0 && dst < live) store_block(a, dst, b, c, s8);
+        if (dst >= 0 && dst < live) store_group<BPT>(a, dst, b0, g);
       }
     } else {
-      store_block(a, row, b, c, s8);
+      store_group<BPT>(a, row, b0, g);
     }
   }
 }
@@ -314,9 +358,12 @@ cudaError_t launch_quant(const uint16_t* x, int64_t rows_in, int K, int64_t ld,
       slot_rows ? rows_in * (K / 16)
                 : ((slot_dst ? rows_in : 0) + ((slot_dst && !row_src) ? 0 : out_rows)) * (K / 16);
   if (tasks == 0) return cudaSuccess;
-  // encoding is ALU work: few tasks go in small blocks spread over many SMs
+  // encoding is ALU work: few tasks go in small blocks spread over many SMs,
+  // one 16-element block each; many tasks go four blocks to a thread
+  if (tasks > 152 * 256 * 4)
+    return launch_pdl(k_quant<4>, dim3(grid_for(tasks / 4, 256)), dim3(256), 0, stream, a);
   const int threads = tasks <= 152 * 256 ? 64 : 256;
-  return launch_pdl(k_quant, dim3(grid_for(tasks, threads)), dim3(threads), 0, stream, a);
+  return launch_pdl(k_quant<1>, dim3(grid_for(tasks, threads)), dim3(threads), 0, stream, a);
 }
 
 cudaError_t launch_swizzle(const uint8_t* src, int64_t rows, int K, uint8_t* dst,

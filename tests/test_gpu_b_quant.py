@@ -73,7 +73,8 @@ def test_quant_e2m1_encoder_on_every_bf16_value_in_range(cuda_lib):
     _check_plain(x)
 
 
-@pytest.mark.parametrize("name,pad", [("tiny", 32), ("tiny", 128), ("decode", 32), ("slice", 128)])
+@pytest.mark.parametrize("name,pad", [("tiny", 32), ("tiny", 128), ("decode", 32), ("slice", 128),
+                                      ("prefill", 32)])
 def test_quant_routed_gather_with_zero_padding(cuda_lib, name, pad):
     cfg = inputs.CONFIGS[name]
     x = inputs.make_activations(cfg)
@@ -96,9 +97,10 @@ def test_quant_routed_gather_with_zero_padding(cuda_lib, name, pad):
     assert np.array_equal(q.unswizzle_scales(s, cap, cfg.d // 16)[:R], want_s)
 
 
-def test_requant_mode_given_amax_zeroes_padding_rows(cuda_lib):
+@pytest.mark.parametrize("rows", [200, 3000])  # one and four 16-element blocks per thread
+def test_requant_mode_given_amax_zeroes_padding_rows(cuda_lib, rows):
     rng = np.random.default_rng(21)
-    rows, K = 200, 1024
+    K = 1024
     h = bf16_tensor(rng, (rows, K), 0.01)
     row_src = np.arange(rows, dtype=np.int32)
     row_src[rng.random(rows) < 0.3] = -1

@@ -83,6 +83,16 @@ def test_forward_full_size_prefill_stages(cuda_lib, name):
     assert np.float32(v["gs_x"].item()) == xg
     assert np.array_equal(v["xq_codes"].cpu().numpy()[:R][rt.row_src >= 0],
                           xc[rt.row_src[rt.row_src >= 0] // cfg.k])
+    if name == "prefill":
+        # requantisation of the GPU's own h (valid rows), bit-exact
+        valid = rt.row_src >= 0
+        h_all = v["h"][:R].float().cpu().numpy()[valid]
+        amax_h0 = np.float32(v["amax_h"].item())
+        assert amax_h0 == np.float32(np.abs(h_all).max())
+        hc, hs, hg, _ = q.quantize(h_all, amax=amax_h0)
+        assert np.float32(v["gs_h"].item()) == hg
+        assert np.array_equal(v["hq_codes"].cpu().numpy()[:R][valid], hc)
+        assert np.array_equal(v["hq_sf"].cpu().numpy()[:R][valid], hs)
     # sampled rows of h, one or two per expert, computed by the oracle alone
     rng = np.random.default_rng(5)
     experts = inputs.ExpertSet(cfg, raw)
