@@ -24,22 +24,39 @@
 
 namespace megamoe {
 
+// t / n for a non-negative task index: 32-bit division whenever t fits (the
+// 64-bit one is a long software sequence).
+__device__ __forceinline__ int64_t task_div(int64_t t, int n) {
+  return (t >> 32) == 0 ? static_cast<int64_t>(static_cast<uint32_t>(t) / static_cast<uint32_t>(n))
+                        : t / n;
+}
+
 __global__ void __launch_bounds__(256) k_amax(const uint16_t* __restrict__ x, int64_t rows, int K,
                                               int64_t ld, float* amax, uint32_t* status) {
   pdl_wait();
   pdl_trigger();
   const int vecs = K / 8;
   const int64_t total = rows * vecs;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   uint32_t m2 = 0;  // two packed |bf16| maxima
-  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
-       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int64_t r = i / vecs;
-    const int v = static_cast<int>(i - r * vecs);
-    const uint4 q = __ldg(reinterpret_cast<const uint4*>(x + r * ld) + v);
-    m2 = __vmaxu2(m2, q.x & 0x7FFF7FFFu);
-    m2 = __vmaxu2(m2, q.y & 0x7FFF7FFFu);
-    m2 = __vmaxu2(m2, q.z & 0x7FFF7FFFu);
-    m2 = __vmaxu2(m2, q.w & 0x7FFF7FFFu);
+  // four loads in flight per thread per round
+  for (int64_t i0 = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i0 < total;
+       i0 += 4 * stride) {
+    uint4 q[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int64_t i = i0 + j * stride;
+      const int64_t r = task_div(i, vecs);
+      q[j] = i < total ? __ldg(reinterpret_cast<const uint4*>(x + r * ld) + (i - r * vecs))
+                       : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      m2 = __vmaxu2(m2, q[j].x & 0x7FFF7FFFu);
+      m2 = __vmaxu2(m2, q[j].y & 0x7FFF7FFFu);
+      m2 = __vmaxu2(m2, q[j].z & 0x7FFF7FFFu);
+      m2 = __vmaxu2(m2, q[j].w & 0x7FFF7FFFu);
+    }
   }
   uint32_t m = max(m2 & 0xFFFFu, m2 >> 16);
 #pragma unroll
@@ -77,12 +94,6 @@ struct QuantArgs {
   bool slot_rows;
 };
 
-// t / n for a non-negative task index: 32-bit division whenever t fits (the
-// 64-bit one is a long software sequence).
-__device__ __forceinline__ int64_t task_div(int64_t t, int n) {
-  return (t >> 32) == 0 ? static_cast<int64_t>(static_cast<uint32_t>(t) / static_cast<uint32_t>(n))
-                        : t / n;
-}
 
 __device__ __forceinline__ void store_block(const QuantArgs& a, int64_t out_row, int b, uint2 c,
                                             uint32_t s8) {
