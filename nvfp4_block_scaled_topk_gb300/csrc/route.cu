@@ -74,12 +74,20 @@ __device__ void route_block(const int32_t* ids, int n_slots, int E, int pad,
   const int s_begin = warp * chunk;
   const int s_end = min(n_slots, s_begin + chunk);
 
-  // 1. per-warp histograms
+  // 1. per-warp histograms (four 32-slot groups of ids loaded per round)
   bool bad = false;
-  for (int s = s_begin + lane; s < s_end; s += 32) {
-    const int e = ids[s];
-    if (e >= E) bad = true;
-    else if (e >= 0) atomicAdd(&hist[warp * E + e], 1);
+  for (int b0 = s_begin; b0 < s_end; b0 += 128) {  // warp-uniform bounds
+    int ev[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int sv = b0 + 32 * u + lane;
+      ev[u] = sv < s_end ? ids[sv] : -1;
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      if (ev[u] >= E) bad = true;
+      else if (ev[u] >= 0) atomicAdd(&hist[warp * E + ev[u]], 1);
+    }
   }
   if (__any_sync(0xffffffffu, bad) && lane == 0) set_status(status, MEGAMOE_DEV_BAD_EXPERT_ID);
   __syncthreads();
@@ -110,11 +118,24 @@ __device__ void route_block(const int32_t* ids, int n_slots, int E, int pad,
   }
   __syncthreads();
 
-  // 3. stable scatter, warp by warp over its own chunk
+  // 3. stable scatter, warp by warp over its own chunk, 32 slots at a time in
+  //    order (the ids of four groups loaded per round)
+  int ev[4];
   for (int base = s_begin; base < s_end; base += 32) {
+    const int u = ((base - s_begin) >> 5) & 3;
+    if (u == 0) {
+#pragma unroll
+      for (int v = 0; v < 4; ++v) {
+        const int sv = base + 32 * v + lane;
+        ev[v] = sv < s_end ? ids[sv] : -1;
+      }
+    }
     const int s = base + lane;
     const bool in = s < s_end;
-    int e = in ? ids[s] : -1;
+    int e = -1;
+#pragma unroll
+    for (int v = 0; v < 4; ++v)
+      if (v == u) e = ev[v];
     if (e >= E) e = -1;
     const unsigned active = __ballot_sync(0xffffffffu, in);
     const unsigned peers = __match_any_sync(0xffffffffu, e);
