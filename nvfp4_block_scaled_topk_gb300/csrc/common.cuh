@@ -184,13 +184,6 @@ __device__ __forceinline__ void mma_nvf4(uint32_t d_tmem, uint64_t a_desc, uint6
       : "memory");
 }
 
-// Copy a 32-row x 16-byte matrix from shared memory into 4 tensor-memory
-// columns of 32 lanes, replicated into all four 32-lane quarters.
-__device__ __forceinline__ void tmem_cp_32x128b_x4(uint32_t taddr, uint64_t s_desc) {
-  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(s_desc)
-               : "memory");
-}
-
 // Arrive on `bar` once every tcgen05 operation this thread issued so far is done.
 __device__ __forceinline__ void tc_commit(uint64_t* bar) {
   asm volatile(
@@ -237,16 +230,6 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
   d |= static_cast<uint64_t>(1024 >> 4) << 32;           // stride offset: 8-row atoms
   d |= static_cast<uint64_t>(1) << 46;                   // descriptor version
   d |= static_cast<uint64_t>(2) << 61;                   // 128-byte swizzle
-  return d;
-}
-
-// Descriptor of a plain (unswizzled) 32-row x 16-byte block-scale matrix:
-// 8-row x 16-byte core matrices, 128 bytes apart.
-__device__ __forceinline__ uint64_t sdesc_sf(uint32_t saddr) {
-  uint64_t d = 0;
-  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
-  d |= static_cast<uint64_t>(128 >> 4) << 32;
-  d |= static_cast<uint64_t>(1) << 46;
   return d;
 }
 
