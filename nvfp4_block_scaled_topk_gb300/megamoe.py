@@ -106,6 +106,12 @@ def _dev(t, dtype, name):
         raise TypeError(f"{name} must be a contiguous CUDA {dtype} tensor")
 
 
+def _dev_rows(t, dtype, name):
+    """A CUDA matrix whose rows may be strided (unit stride along columns)."""
+    if not (t.is_cuda and t.dtype == dtype and t.dim() == 2 and (t.stride(1) == 1 or t.shape[1] <= 1)):
+        raise TypeError(f"{name} must be a CUDA {dtype} matrix with unit column stride")
+
+
 def max_padded_rows(T, k, E, pad):
     return int(load().megamoe_max_padded_rows(T, k, E, pad))
 
@@ -264,16 +270,17 @@ def linear_nvfp4(x: torch.Tensor, w: LinearWeights, out_dtype=EPI_BF16, out=None
     """out [T, N] = NVFP4(x, gs from the measured amax of x) @ w.T, in bf16
     (EPI_BF16) or float32 (EPI_F32).  Returns (out, ws); ws holds amax, gs_x
     and the status word at bytes 0, 4 and 8."""
-    _dev(x, torch.bfloat16, "x")
+    _dev_rows(x, torch.bfloat16, "x")
     T, K = x.shape
     if K != w.K:
         raise ValueError("x and w disagree on K")
     need = linear_workspace_size(T, K, w.N)
     if ws is None:
         ws = torch.empty(max(need, 256), dtype=torch.uint8, device=x.device)
+    dt = torch.float32 if out_dtype == EPI_F32 else torch.bfloat16
     if out is None:
-        dt = torch.float32 if out_dtype == EPI_F32 else torch.bfloat16
         out = torch.empty(T, w.N, dtype=dt, device=x.device)
+    _dev_rows(out, dt, "out")
     _check("megamoe_linear_nvfp4", load().megamoe_linear_nvfp4(
         _p(x), T, K, x.stride(0), _p(w.codes), _p(w.scales), _p(w.gs), w.N, out_dtype, _p(out),
         out.stride(0), _p(ws), ws.numel(), _stream()))

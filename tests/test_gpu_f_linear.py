@@ -113,3 +113,21 @@ def test_linear_edge_cases(cuda_lib):
     assert lib.megamoe_linear_nvfp4(p(x), cfg.T, cfg.K, cfg.K, p(w.codes), p(w.scales), p(w.gs),
                                     cfg.N, megamoe.EPI_SILU_MUL, p(o), cfg.N, p(ws), ws.numel(),
                                     None) == 1
+
+
+def test_linear_strided_input_and_output(cuda_lib):
+    """x is a column slice of a wider buffer (ld_x > K) and out a slice of a
+    wider one (ld_out > N): the strides are honoured and nothing outside the
+    slices is written."""
+    cfg = inputs.LINEAR_CONFIGS["linear_tiny"]
+    x, c, s, gs, w = _prepared(cfg)
+    xb = torch.zeros(cfg.T, cfg.K + 64, dtype=torch.bfloat16, device="cuda")
+    xb[:, 32:32 + cfg.K] = x
+    ob = torch.full((cfg.T, cfg.N + 128), 7.0, dtype=torch.bfloat16, device="cuda")
+    xs, os_ = xb[:, 32:32 + cfg.K], ob[:, 64:64 + cfg.N]
+    assert xs.stride(0) == cfg.K + 64 and os_.stride(0) == cfg.N + 128
+    megamoe.linear_nvfp4(xs, w, out=os_)
+    torch.cuda.synchronize()
+    ref, _ = megamoe.linear_nvfp4(x.contiguous(), w)
+    assert torch.equal(os_, ref)
+    assert bool((ob[:, :64] == 7.0).all()) and bool((ob[:, 64 + cfg.N:] == 7.0).all())
