@@ -306,35 +306,87 @@ def run_ours(args):
     clk = clocks.stop()
 
     # ---- end to end through the public call, host buffers, copies inside
-    x_h = x.cpu().pin_memory()
-    ids_h = ids.cpu().pin_memory()
-    w_h = w.cpu().pin_memory()
-    out_h = torch.empty(cfg.T, cfg.d, dtype=torch.bfloat16).pin_memory()
-    x_d = torch.empty_like(x)
-    ids_d = torch.empty_like(ids)
-    w_d = torch.empty_like(w)
+    # x, topk_ids and topk_weights sit in one pinned staging buffer, so each
+    # step's inputs go up in a single host-to-device copy.  Two device copies
+    # of the staging buffer and of the output alternate between steps: one
+    # stream uploads step i+1's inputs and another downloads step i-1's output
+    # while step i computes, as a serving loop would; every step still makes
+    # both copies, and the timed region spans all K steps' copies and compute.
+    nx, ni = x.numel() * 2, ids.numel() * 4
+    stage_h = torch.empty(nx + 2 * ni, dtype=torch.uint8).pin_memory()
+    stage_h[:nx].view(torch.bfloat16).copy_(x.cpu().reshape(-1))
+    stage_h[nx:nx + ni].view(torch.int32).copy_(ids.cpu().reshape(-1))
+    stage_h[nx + ni:].view(torch.float32).copy_(w.cpu().reshape(-1))
+    stage_d = [torch.empty(stage_h.numel(), dtype=torch.uint8, device=dev) for _ in range(2)]
+    views = [(sd[:nx].view(torch.bfloat16).view(cfg.T, cfg.d),
+              sd[nx:nx + ni].view(torch.int32).view(cfg.T, cfg.k),
+              sd[nx + ni:].view(torch.float32).view(cfg.T, cfg.k)) for sd in stage_d]
+    out_d = [torch.empty(cfg.T, cfg.d, dtype=torch.bfloat16, device=dev) for _ in range(2)]
+    out_h = [torch.empty(cfg.T, cfg.d, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    up_stream = torch.cuda.Stream(device=dev)
+    down_stream = torch.cuda.Stream(device=dev)
 
-    def e2e_step():
-        x_d.copy_(x_h, non_blocking=True)
-        ids_d.copy_(ids_h, non_blocking=True)
-        w_d.copy_(w_h, non_blocking=True)
-        o = fwd(x_d, ids_d, w_d)
-        out_h.copy_(o, non_blocking=True)
+    def e2e_steps(n):
+        # on the current stream (the capture stream while a graph records);
+        # the copy streams fork from it and join it at the end
+        comp = torch.cuda.current_stream()
+        fork = torch.cuda.Event()
+        fork.record(comp)
+        up_stream.wait_event(fork)
+        down_stream.wait_event(fork)
+        computed = [None, None]
+        downloaded = [None, None]
+        for i in range(n):
+            b = i % 2
+            up = torch.cuda.Event()
+            with torch.cuda.stream(up_stream):
+                if computed[b] is not None:  # step i-2 is done with buffer b
+                    up_stream.wait_event(computed[b])
+                stage_d[b].copy_(stage_h, non_blocking=True)
+                up.record(up_stream)
+            comp.wait_event(up)
+            if downloaded[b] is not None:  # step i-2's output has left out_d[b]
+                comp.wait_event(downloaded[b])
+            fwd(*views[b], out=out_d[b])
+            computed[b] = torch.cuda.Event()
+            computed[b].record(comp)
+            with torch.cuda.stream(down_stream):
+                down_stream.wait_event(computed[b])
+                out_h[b].copy_(out_d[b], non_blocking=True)
+                downloaded[b] = torch.cuda.Event()
+                downloaded[b].record(down_stream)
+        for ev in downloaded:
+            if ev is not None:
+                comp.wait_event(ev)
 
-    for _ in range(3):
-        e2e_step()
+    # the K steps are recorded once into a CUDA graph (one host call replays
+    # them, so short steps are not bound by the host's launch rate); if the
+    # capture fails the same steps run eagerly
+    e2e_steps(3)
     barrier()
     torch.cuda.synchronize()
+    graph = None
+    try:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            e2e_steps(args.steps)
+        graph.replay()
+        torch.cuda.synchronize()
+    except Exception:
+        graph = None
+        torch.cuda.synchronize()
     a = torch.cuda.Event(enable_timing=True)
     b = torch.cuda.Event(enable_timing=True)
     a.record(stream)
-    for _ in range(args.steps):
-        e2e_step()
+    if graph is not None:
+        graph.replay()
+    else:
+        e2e_steps(args.steps)
     b.record(stream)
     torch.cuda.synchronize()
     e2e_ms = a.elapsed_time(b) / args.steps
-    h2d = x_h.numel() * 2 + ids_h.numel() * 4 + w_h.numel() * 4
-    d2h = out_h.numel() * 2
+    h2d = stage_h.numel()
+    d2h = out_h[0].numel() * 2
 
     # ---- max over ranks
     ms, e2e_ms, l1_ms, l2_ms = max_over_ranks([ms, e2e_ms, l1_ms, l2_ms], world, dev)
@@ -381,7 +433,10 @@ def run_ours(args):
                          "peak_source": peak_kind},
             "cpu_baseline": cpu,
             "e2e": {"value": tokens_total / (e2e_ms * 1e-3), "unit": UNIT,
-                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "loop": ("CUDA graph of the K steps" if graph is not None else "eager") +
+                            ", inputs uploaded and outputs downloaded on two copy streams, "
+                            "double-buffered"},
             "gpu_launches": kernels_per_step(cfg) * args.steps,
             "clocks": clk,
         }
