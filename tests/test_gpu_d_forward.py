@@ -155,3 +155,37 @@ def test_forward_stress_routings(cuda_lib, case):
     _, inter = oracle.forward(x.float().numpy(), ids_ok.numpy(), w.numpy(),
                               inputs.ExpertSet(cfg, raw), pad=32, return_intermediates=True)
     check_forward(cfg, fwd, out, inter, what=case)
+
+
+def test_forward_captures_in_a_cuda_graph(cuda_lib):
+    """The forward records into a CUDA graph (every launch is stream-ordered,
+    no host synchronisation) and replays give exactly the eager results, also
+    for new inputs written into the captured buffers."""
+    cfg = inputs.CONFIGS["tiny"]
+    raw, weights = _weights(cfg)
+    x = inputs.make_activations(cfg).cuda()
+    ids, w = inputs.make_routing(cfg)
+    ids, w = ids.cuda(), w.cuda()
+    fwd = megamoe.Forward(weights, cfg.T, cfg.k, pad=32)
+    want = fwd(x, ids, w).clone()
+    out = torch.empty_like(want)
+    g = torch.cuda.CUDAGraph()
+    fwd(x, ids, w, out=out)  # warm-up on the capture's buffers
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g):
+        fwd(x, ids, w, out=out)
+    out.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out, want)
+    # new inputs in the same buffers: the replay follows them
+    x2 = inputs.make_activations(inputs.MoEConfig("tiny2", 8, 2, 256, 512, 64, "logits", seed=9))
+    ids2, w2 = inputs.make_routing(inputs.MoEConfig("tiny2", 8, 2, 256, 512, 64, "logits", seed=9))
+    want2 = megamoe.Forward(weights, cfg.T, cfg.k, pad=32)(x2.cuda(), ids2.cuda(), w2.cuda()).clone()
+    x.copy_(x2)
+    ids.copy_(ids2)
+    w.copy_(w2)
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out, want2)
+    assert fwd.read_status() == 0
