@@ -1,5 +1,9 @@
 /*
- * megamoe.h -- C ABI of the GB300 (sm_103a) NVFP4 MegaMoE routed-expert forward.
+ * megamoe.h -- C ABI of the GB300 (sm_103a) NVFP4 MegaMoE routed-expert forward,
+ * with, around it, the router (megamoe_router_topk, and
+ * megamoe_forward_from_logits for the whole layer from router logits, a
+ * shared expert included) and the dense NVFP4 linear with a measured-amax
+ * activation scale (megamoe_linear_nvfp4).
  *
  * What it computes (sources are the titles and sections of the pages the
  * method is taken from):
@@ -346,7 +350,9 @@ size_t megamoe_workspace_size(int T, int k, int E, int d, int I, int pad);
  *   ws, ws_bytes  workspace, at least megamoe_workspace_size(...) bytes,
  *                 256-byte aligned; its first 4 bytes are the device status
  *                 word, cleared at the start of every call.
- * Requires the weight shapes above, 1 <= k <= 16, T >= 0.
+ * Requires the weight shapes above, 1 <= k <= 16, T >= 0.  Every step is a
+ * kernel launch on `stream` (no host synchronisation, no memory allocation),
+ * so the call can be recorded into a CUDA graph and replayed.
  */
 megamoe_status megamoe_forward(const megamoe_weights* w, const uint16_t* x,
                                const int32_t* topk_ids, const float* topk_weights, int T, int k,
