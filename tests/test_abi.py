@@ -95,3 +95,37 @@ def test_argument_errors_return_before_any_device_work(lib):
     w_bad = megamoe.CWeights(8, 200, 512, 256, 256, 256, 256, 256, 256)
     assert lib.megamoe_forward(ctypes.byref(w_bad), fake, fake, fake, 4, 2, 32, fake, fake,
                                1 << 30, P) == 2
+
+
+def test_argument_errors_of_the_router_linear_and_layer_calls(lib):
+    P = None
+    fake = ctypes.c_void_p(256)
+    # router: k = 0, k > E, ld < E, E too large
+    assert lib.megamoe_router_topk(fake, 4, 8, 8, P, 0, -1, fake, fake, P) == 1
+    assert lib.megamoe_router_topk(fake, 4, 8, 8, P, 9, -1, fake, fake, P) == 1
+    assert lib.megamoe_router_topk(fake, 4, 8, 4, P, 2, -1, fake, fake, P) == 1
+    assert lib.megamoe_router_topk(fake, 4, 2000, 2000, P, 2, -1, fake, fake, P) == 2
+    # dense linear: K not a multiple of 256, N not a multiple of 128, bad
+    # output type, short workspace
+    ws = lib.megamoe_linear_workspace_size(8, 512, 256)
+    assert ws > 0
+    assert lib.megamoe_linear_nvfp4(fake, 8, 128, 128, fake, fake, fake, 256, 2, fake, 256, fake,
+                                    1 << 30, P) == 2
+    assert lib.megamoe_linear_nvfp4(fake, 8, 512, 512, fake, fake, fake, 200, 2, fake, 256, fake,
+                                    1 << 30, P) == 2
+    assert lib.megamoe_linear_nvfp4(fake, 8, 512, 512, fake, fake, fake, 256, 1, fake, 256, fake,
+                                    1 << 30, P) == 1
+    assert lib.megamoe_linear_nvfp4(fake, 8, 512, 512, fake, fake, fake, 256, 2, fake, 256, fake,
+                                    ws - 1, P) == 3
+    # layer from logits: shared expert inside the routed range or beyond the
+    # weights, more logits than experts, k_out above 16
+    w = megamoe.CWeights(9, 256, 512, 256, 256, 256, 256, 256, 256)
+    assert lib.megamoe_forward_from_logits(ctypes.byref(w), fake, fake, 8, P, 8, 2, 3, 4, 32,
+                                           fake, fake, 1 << 30, P) == 1
+    assert lib.megamoe_forward_from_logits(ctypes.byref(w), fake, fake, 8, P, 8, 2, 9, 4, 32,
+                                           fake, fake, 1 << 30, P) == 1
+    assert lib.megamoe_forward_from_logits(ctypes.byref(w), fake, fake, 10, P, 10, 2, -1, 4, 32,
+                                           fake, fake, 1 << 30, P) == 1
+    w16 = megamoe.CWeights(40, 256, 512, 256, 256, 256, 256, 256, 256)
+    assert lib.megamoe_forward_from_logits(ctypes.byref(w16), fake, fake, 32, P, 32, 16, 33, 4,
+                                           32, fake, fake, 1 << 30, P) == 2
