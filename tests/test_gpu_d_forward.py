@@ -189,3 +189,18 @@ def test_forward_captures_in_a_cuda_graph(cuda_lib):
     torch.cuda.synchronize()
     assert torch.equal(out, want2)
     assert fwd.read_status() == 0
+
+
+@pytest.mark.parametrize("E,k,T,d,I,pad", [(1024, 16, 40, 256, 256, 64),
+                                            (384, 16, 12, 7168, 2048, 32)])
+def test_forward_at_the_interface_maxima(cuda_lib, E, k, T, d, I, pad):
+    """1024 experts (the most the interface takes) and top-16 (the most
+    slots per token), against the oracle's forward."""
+    cfg = inputs.MoEConfig("maxima", E, k, d, I, T, "uniform", seed=501, pad=pad)
+    torch.cuda.empty_cache()
+    _CACHE.clear()
+    raw, fwd, x, ids, w, out, bits = _run(cfg, pad)
+    assert bits == 0
+    _, inter = oracle.forward(x.float().numpy(), ids.numpy(), w.numpy(),
+                              inputs.ExpertSet(cfg, raw), pad=pad, return_intermediates=True)
+    check_forward(cfg, fwd, out, inter, what=f"E={E} k={k}")
