@@ -139,7 +139,10 @@ int64_t megamoe_max_padded_rows(int T, int k, int E, int pad);
  *   slot_dst        [T*k]  padded row of each slot, -1 if skipped (out)
  *   status          device uint32 status word (bits are OR-ed in; may be NULL)
  * Requires 1 <= E <= 1024, 1 <= k <= 16, pad >= 1, T >= 0 and
- * row_capacity >= megamoe_max_padded_rows(T, k, E, pad).  One thread block.
+ * row_capacity >= megamoe_max_padded_rows(T, k, E, pad).  T*k above 2^30 or
+ * megamoe_max_padded_rows at or above 2^31 (offsets are int32) returns
+ * MEGAMOE_ERR_UNSUPPORTED_SHAPE; the forward checks the same.  One thread
+ * block.
  */
 megamoe_status megamoe_route_permute(const int32_t* topk_ids, int T, int k, int E, int pad,
                                      int32_t* counts, int32_t* offsets,

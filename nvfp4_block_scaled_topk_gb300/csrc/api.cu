@@ -134,6 +134,9 @@ megamoe_status check_route_args(int T, int k, int E, int pad) {
   if (T < 0 || k < 1 || E < 1 || pad < 1) return MEGAMOE_ERR_INVALID_ARG;
   if (E > MEGAMOE_MAX_EXPERTS || k > MEGAMOE_MAX_TOPK) return MEGAMOE_ERR_UNSUPPORTED_SHAPE;
   if (static_cast<int64_t>(T) * k > (int64_t{1} << 30)) return MEGAMOE_ERR_UNSUPPORTED_SHAPE;
+  // padded offsets and row indices of the kernels are int32
+  if (megamoe_max_padded_rows(T, k, E, pad) >= (int64_t{1} << 31))
+    return MEGAMOE_ERR_UNSUPPORTED_SHAPE;
   return MEGAMOE_OK;
 }
 

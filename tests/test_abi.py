@@ -66,6 +66,10 @@ def test_argument_errors_return_before_any_device_work(lib):
     assert lib.megamoe_route_permute(P, 1, 1, 0, 1, P, P, P, P, 0, P, P, P) == 1
     assert lib.megamoe_route_permute(P, 1, 1, 2000, 1, P, P, P, P, 0, P, P, P) == 2
     assert lib.megamoe_route_permute(P, 1, 17, 8, 1, P, P, P, P, 0, P, P, P) == 2
+    # padded rows beyond int32: 2^24 slots + 1024 experts padded to 2^21
+    assert megamoe.max_padded_rows(1 << 20, 16, 1024, 1 << 21) >= 1 << 31
+    assert lib.megamoe_route_permute(P, 1 << 20, 16, 1024, 1 << 21, P, P, P, P, 0, P, P,
+                                     P) == 2
     fake = ctypes.c_void_p(256)
     assert lib.megamoe_route_permute(fake, 4, 2, 8, 32, fake, fake, fake, fake, 10, fake, P,
                                      P) == 1
