@@ -163,3 +163,40 @@ def random_experts(rng, E, d, I, oracle_q):
 def bf16_tensor(rng, shape, scale=1.0):
     x = torch.from_numpy((rng.standard_normal(shape) * scale).astype(np.float32))
     return x.to(torch.bfloat16)
+
+
+def check_sampled_tokens(experts, ids, topk_weights, slot_dst, h, hq_codes, hq_sf, gs_h, amax_h,
+                         out, tokens, what=""):
+    """Sampled output tokens of a forward, recomputed one by one from its own h.
+
+    For each routed row of a sampled token: the row's requantised codes and
+    scales must equal the oracle's quantisation of that h row with the
+    forward's amax(h) (row-local given the global scale, so bit-exact); then
+    the oracle's L2 (float64 on dequantised operands) and the weighted sum
+    over the token's slots give the value its bf16 output must meet
+    (assert_close_bf16).  Needs only the token's k rows and experts, so it
+    runs at any size.
+    """
+    from oracle import nvfp4 as q
+
+    k = ids.shape[1]
+    gs_h = np.float32(gs_h)
+    amax_h = np.float32(amax_h)
+    w2 = {}
+    want = np.zeros((len(tokens), out.shape[1]))
+    for i, t in enumerate(tokens):
+        for j in range(k):
+            r = int(slot_dst[int(t) * k + j])
+            if r < 0:
+                continue
+            hc, hs, hg, _ = q.quantize(np.asarray(h[r:r + 1], np.float32), amax=amax_h)
+            assert hg == gs_h, f"{what}: gs_h {gs_h!r} vs {hg!r}"
+            assert np.array_equal(hq_codes[r], hc[0]), f"{what}: requantised codes of row {r}"
+            assert np.array_equal(hq_sf[r], hs[0]), f"{what}: requantised scales of row {r}"
+            e = int(ids[t, j])
+            if e not in w2:
+                ew = experts[e]
+                w2[e] = q.dequantize(ew["w2_codes"], ew["w2_scales"], ew["w2_gs"])
+            y = (q.dequantize(hc, hs, hg) @ w2[e].T)[0]
+            want[i] += np.float64(topk_weights[t, j]) * y
+    assert_close_bf16(np.asarray(out)[np.asarray(tokens)], want, what=what + " sampled tokens")

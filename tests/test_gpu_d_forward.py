@@ -10,7 +10,8 @@ import torch
 import oracle
 from oracle import nvfp4 as q
 from nvfp4_block_scaled_topk_gb300 import inputs, megamoe
-from helpers import assert_close, assert_close_bf16, bf16_to_np, check_forward
+from helpers import (assert_close, assert_close_bf16, bf16_to_np, check_forward,
+                     check_sampled_tokens)
 
 pytestmark = pytest.mark.gpu
 
@@ -68,7 +69,8 @@ def test_forward_prefill_shaped_mid_size(cuda_lib):
 def test_forward_full_size_prefill_stages(cuda_lib, name):
     """Full-size prefill: routing and activation quantisation bit-exact, the
     L1 output on sampled rows against the oracle, the L1 amax bounds the
-    sample, and the output is finite."""
+    sample, the output is finite, and sampled output tokens match the
+    oracle's L2 and combine over the forward's own h."""
     cfg = inputs.CONFIGS[name]
     raw, fwd, x, ids, w, out, bits = _run(cfg, 32)
     assert bits == 0
@@ -113,6 +115,13 @@ def test_forward_full_size_prefill_stages(cuda_lib, name):
         hw64 = (oracle.silu(xh @ gate.T) * (xh @ up.T))[0]
         assert_close_bf16(h_gpu[r], hw64, what=f"h row {r}")
         assert amax_h >= np.abs(q.bf16_round(hw64)).max()
+    # sampled output tokens from the forward's own h: the slot mapping
+    # bit-exact, then requantised rows, L2 and the combine token by token
+    assert np.array_equal(v["slot_dst"].cpu().numpy(), rt.slot_dst)
+    check_sampled_tokens(experts, ids.numpy(), w.numpy(), rt.slot_dst, h_gpu,
+                         v["hq_codes"].cpu().numpy(), v["hq_sf"].cpu().numpy(),
+                         v["gs_h"].item(), amax_h, o, rng.choice(cfg.T, size=4, replace=False),
+                         what=name)
 
 
 def test_forward_ignores_poisoned_workspace(cuda_lib):
