@@ -1,13 +1,14 @@
-"""The sampled-token checker of the full-size GPU tests, on the CPU: it
-accepts the oracle's own forward and rejects planted mistakes (a wrong
-requantised code, swapped routing weights, another token's output)."""
+"""The checkers of the GPU forward tests, on the CPU: each accepts the
+oracle's own forward and rejects planted mistakes (a wrong requantised
+code, swapped routing weights, another token's output)."""
 
 import numpy as np
 import pytest
+import torch
 
 import oracle
 from nvfp4_block_scaled_topk_gb300 import inputs
-from helpers import check_sampled_tokens
+from helpers import check_forward, check_sampled_tokens
 
 
 @pytest.fixture(scope="module")
@@ -56,3 +57,43 @@ def test_rejects_another_tokens_output(tiny_forward):
     out[[2, 7]] = out[[7, 2]]
     with pytest.raises(AssertionError):
         _check(tiny_forward, [2, 7], out=out)
+
+
+class _Stages:
+    """Stands in for a forward: its intermediates are the oracle's own, with
+    NaN in the padding rows of h as a forward may leave them."""
+
+    def __init__(self, inter):
+        valid = inter["routing"].row_src >= 0
+        h = torch.from_numpy(inter["h"].astype(np.float32)).to(torch.bfloat16)
+        h[torch.from_numpy(~valid)] = float("nan")
+        self.v = {"h": h, "hq_codes": torch.from_numpy(inter["hq_codes"].copy()),
+                  "hq_sf": torch.from_numpy(inter["hq_scales"].copy())}
+
+    def intermediates(self):
+        return self.v
+
+
+def test_forward_check_accepts_the_oracle_with_unwritten_padding(tiny_forward):
+    cfg, _, _, _, out, inter = tiny_forward
+    assert (inter["routing"].row_src < 0).any()
+    out_t = torch.from_numpy(out.astype(np.float32)).to(torch.bfloat16)
+    check_forward(cfg, _Stages(inter), out_t, inter)
+
+
+def test_forward_check_rejects_a_requant_flip_without_an_h_difference(tiny_forward):
+    cfg, _, _, _, out, inter = tiny_forward
+    st = _Stages(inter)
+    r = int(inter["routing"].slot_dst[0])
+    st.v["hq_codes"][r, 0] ^= 0x01
+    out_t = torch.from_numpy(out.astype(np.float32)).to(torch.bfloat16)
+    with pytest.raises(AssertionError, match="without an h difference"):
+        check_forward(cfg, st, out_t, inter)
+
+
+def test_forward_check_rejects_a_wrong_output_token(tiny_forward):
+    cfg, _, _, _, out, inter = tiny_forward
+    bad = out.astype(np.float32).copy()
+    bad[5] = -bad[5]
+    with pytest.raises(AssertionError):
+        check_forward(cfg, _Stages(inter), torch.from_numpy(bad).to(torch.bfloat16), inter)
