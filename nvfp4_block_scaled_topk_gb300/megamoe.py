@@ -101,15 +101,24 @@ def _stream():
     return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
 
 
+def _on_current_device(t, name):
+    # the library launches on the current device and its stream
+    if t.device.index != torch.cuda.current_device():
+        raise ValueError(f"{name} is on {t.device}, the current CUDA device is "
+                         f"cuda:{torch.cuda.current_device()}")
+
+
 def _dev(t, dtype, name):
     if not (t.is_cuda and t.dtype == dtype and t.is_contiguous()):
         raise TypeError(f"{name} must be a contiguous CUDA {dtype} tensor")
+    _on_current_device(t, name)
 
 
 def _dev_rows(t, dtype, name):
     """A CUDA matrix whose rows may be strided (unit stride along columns)."""
     if not (t.is_cuda and t.dtype == dtype and t.dim() == 2 and (t.stride(1) == 1 or t.shape[1] <= 1)):
         raise TypeError(f"{name} must be a CUDA {dtype} matrix with unit column stride")
+    _on_current_device(t, name)
 
 
 def max_padded_rows(T, k, E, pad):
