@@ -94,24 +94,30 @@ class ClockSampler:
             self.proc.kill()
         if self._t:
             self._t.join(timeout=2)
-        sm, mx, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
-            parts = [p.strip() for p in ln.split(",")]
-            if len(parts) < 8:
-                continue
-            try:
-                sm.append(float(parts[0]))
-                mx.append(float(parts[1]))
-            except ValueError:
-                continue
-            for n, v in zip(names, parts[4:8]):
-                if v.lower() == "active":
-                    reasons.add(n)
-        if not sm:
-            return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
-                "reasons": sorted(reasons), "samples": len(sm)}
+        return summarize_clocks(self.lines)
+
+
+def summarize_clocks(lines):
+    """The `clocks` object from ClockSampler.FIELDS lines (csv, no header, no
+    units): median and max SM clock, and every throttle reason seen Active."""
+    sm, mx, reasons = [], [], set()
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    for ln in lines:
+        parts = [p.strip() for p in ln.split(",")]
+        if len(parts) < 8:
+            continue
+        try:
+            sm.append(float(parts[0]))
+            mx.append(float(parts[1]))
+        except ValueError:
+            continue
+        for n, v in zip(names, parts[4:8]):
+            if v.lower() == "active":
+                reasons.add(n)
+    if not sm:
+        return None
+    return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+            "reasons": sorted(reasons), "samples": len(sm)}
 
 
 def kernel_source_hash() -> str:

@@ -72,3 +72,19 @@ def test_reference_arm_prints_one_line_on_rank0():
 def test_reference_arm_other_ranks_exit_without_work():
     r = _run_reference({"RANK": "1", "WORLD_SIZE": "2"})
     assert r.returncode == 0 and r.stdout.strip() == ""
+
+
+def test_clock_summary_from_nvidia_smi_lines():
+    sys.path.insert(0, ROOT)
+    import bench
+
+    lines = ["2070, 2070, 900.5, 0x0000000000000000, Not Active, Not Active, Not Active, Not Active",
+             "1980, 2070, 1390.0, 0x0000000000000004, Not Active, Not Active, Not Active, Active",
+             "2070, 2070, 1100.0, 0x0000000000000000, Not Active, Not Active, Not Active, Not Active",
+             "[N/A], 2070, 0, 0x0, Not Active, Not Active, Not Active, Not Active",
+             "truncated, line"]
+    c = bench.summarize_clocks(lines)
+    assert c == {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"], "samples": 3}
+    hot = lines[:1] + ["1500, 2070, 1400, 0x48, Not Active, Active, Not Active, Not Active"]
+    assert bench.summarize_clocks(hot)["reasons"] == ["hw_thermal_slowdown"]
+    assert bench.summarize_clocks([]) is None
