@@ -39,6 +39,22 @@ def kernels_per_step(cfg) -> int:
     return 6 if cfg.T * cfg.d <= PROLOGUE_MAX_ELEMS else 7
 
 
+# kernels of one dense linear: prologue (status, offsets, amax of up to this
+# many elements of x), amax of larger inputs, quantiser, GEMM, and the split-K
+# finishing kernel when the call splits K
+LINEAR_PROLOGUE_MAX_ELEMS = 262144
+
+
+def linear_kernels_per_call(T: int, K: int, ws_bytes: int) -> int:
+    """Launches of one megamoe_linear_nvfp4 call.  Whether it splits K shows in
+    its workspace size: the split-K planes follow the header, codes and scales."""
+    def a256(n):
+        return -(-n // 256) * 256
+
+    split = ws_bytes > 256 + a256(T * (K // 2)) + a256(T * (K // 16))
+    return 3 + int(T * K > LINEAR_PROLOGUE_MAX_ELEMS) + int(split)
+
+
 def _dist():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -543,7 +559,8 @@ def run_linear(args):
                      "traffic": None, "kernel": "whole call (prologue, quantiser, GEMM)",
                      "peak_source": peak_kind if bound == "hbm" else
                      f"{peak_kind} bf16 x 6 (nominal FP4/BF16 ratio)"},
-        "gpu_launches": (3 if cfg.T * cfg.K <= 262144 else 4) * args.steps,
+        "gpu_launches": linear_kernels_per_call(
+            cfg.T, cfg.K, megamoe.linear_workspace_size(cfg.T, cfg.K, cfg.N)) * args.steps,
         "clocks": clk,
     }
     print(json.dumps(line), flush=True)

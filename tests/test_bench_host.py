@@ -88,3 +88,15 @@ def test_clock_summary_from_nvidia_smi_lines():
     hot = lines[:1] + ["1500, 2070, 1400, 0x48, Not Active, Active, Not Active, Not Active"]
     assert bench.summarize_clocks(hot)["reasons"] == ["hw_thermal_slowdown"]
     assert bench.summarize_clocks([]) is None
+
+
+def test_linear_launch_count_follows_the_workspace_layout():
+    sys.path.insert(0, ROOT)
+    import bench
+
+    base = 256 + 8 * 3584 + 8 * 448  # header, codes and scales of 8 x 7168
+    assert bench.linear_kernels_per_call(8, 7168, base) == 3
+    assert bench.linear_kernels_per_call(8, 7168, base + 8 * 8 * 1536 * 4) == 4
+    big = 256 + 4096 * 3584 + 4096 * 448
+    assert bench.linear_kernels_per_call(4096, 7168, big) == 4
+    assert bench.linear_kernels_per_call(4096, 7168, big + 256) == 5
