@@ -167,6 +167,42 @@ def test_quantize_lossless_special_case():
     assert np.array_equal(q.dequantize(codes, scales, gs), x.astype(np.float64))
 
 
+def test_quantize_error_within_the_grid_bound():
+    # From the definitions alone: the block scale sd is the E4M3 round-to-
+    # nearest of s = amax_b * gs / 6, so each block's largest encoded
+    # magnitude amax_b * gs / sd = 6 s / sd lies in [6/(1+2^-4), 6/(1-2^-4)]
+    # (3 mantissa bits; every s here is an E4M3 normal), and it is exactly 6
+    # (scale 448 = 0x7E) in the block holding the tensor amax.  Every element
+    # then decodes within half an E2M1 step of its encoded value x * gs / sd
+    # (steps 0.5 below 2, 1 below 4, 2 up to 6), or to 6 when it lies above.
+    rng = np.random.default_rng(11)
+    rows, K = 64, 256
+    mag = np.exp2(rng.integers(-5, 6, (rows, 1)).astype(np.float64))
+    x = (rng.standard_normal((rows, K)) * mag).astype(np.float32)
+    x[7, 32:48] = 0.0  # an all-zero block
+    codes, s8, gs, amax = q.quantize(x)
+    assert amax == np.float32(np.abs(x).max())
+    sd = q.e4m3_decode(s8).astype(np.float64)
+    blocks = x.astype(np.float64).reshape(rows, K // 16, 16)
+    amax_b = np.abs(blocks).max(axis=2)
+    zero = amax_b == 0
+    assert np.array_equal(zero, sd == 0)
+    s = amax_b * np.float64(gs) / 6.0
+    assert np.all(s[~zero] >= 2.0 ** -6)
+    qmax = np.where(zero, 0.0, 6.0 * s / np.where(zero, 1.0, sd))
+    assert np.all(qmax[~zero] >= 6.0 / (1 + 2.0 ** -4) * (1 - 1e-6))
+    assert np.all(qmax[~zero] <= 6.0 / (1 - 2.0 ** -4) * (1 + 1e-6))
+    r, c = np.unravel_index(np.argmax(np.abs(x)), x.shape)
+    assert s8[r, c // 16] == 0x7E and abs(qmax[r, c // 16] - 6.0) < 1e-6  # gs rounded to fp32
+    enc = np.where(zero, 0.0, np.float64(gs) / np.where(zero, 1.0, sd))[..., None]
+    qv = np.abs(blocks) * enc
+    allowed = np.where(qv > 6, qv - 6, np.where(qv < 2, 0.25, np.where(qv < 4, 0.5, 1.0)))
+    xh = q.dequantize(codes, s8, gs).reshape(rows, K // 16, 16)
+    err = np.abs(xh - blocks) * enc
+    assert np.all(err <= allowed * (1 + 1e-6) + 1e-9)
+    assert not xh[7, 2].any()
+
+
 def test_swizzle_layout_position_and_roundtrip():
     rows, nb = 200, 8  # K = 128
     s = (np.arange(rows * nb) % 251).astype(np.uint8).reshape(rows, nb)
