@@ -186,6 +186,36 @@ def test_forward_matches_brute_force_4_tokens_2_experts():
     assert np.array_equal(got, got32)  # padding changes nothing
 
 
+def test_unquantized_forward_matches_scalar_loops():
+    """The accuracy comparison point (float64 x and h, nothing rounded)
+    against scalar loops with math.fsum and math.exp on a tiny case."""
+    rng = np.random.default_rng(8)
+    d, I, T, k, E = 16, 16, 3, 2, 3
+    ex = _rand_experts(rng, E, d, I)
+    x = rng.standard_normal((T, d)) * 0.7
+    ids = np.array([[0, 2], [2, -1], [1, 1]])
+    w = _softmax_rows(rng.standard_normal((T, k)))
+    got = oracle.forward_unquantized(x, ids, w, ex)
+    want = np.zeros((T, d))
+    for t in range(T):
+        for j in range(k):
+            e = int(ids[t, j])
+            if e < 0:
+                continue
+            we = ex[e]
+            gate = q.dequantize(we["w13_codes"][:I], we["w13_scales"][:I], we["w13_gs"][0])
+            up = q.dequantize(we["w13_codes"][I:], we["w13_scales"][I:], we["w13_gs"][1])
+            down = q.dequantize(we["w2_codes"], we["w2_scales"], we["w2_gs"])
+            h = []
+            for i in range(I):
+                g = math.fsum(x[t, c] * gate[i, c] for c in range(d))
+                u = math.fsum(x[t, c] * up[i, c] for c in range(d))
+                h.append(g / (1.0 + math.exp(-g)) * u)
+            for c in range(d):
+                want[t, c] += float(w[t, j]) * math.fsum(h[i] * down[c, i] for i in range(I))
+    np.testing.assert_allclose(got, want, rtol=0, atol=1e-12 * np.abs(want).max())
+
+
 def test_forward_invariant_to_expert_relabelling():
     rng = np.random.default_rng(7)
     d, I, T, k, E = 64, 32, 12, 3, 5

@@ -54,6 +54,7 @@ MUTANTS = {
     "gate takes the up scale": ("moe", 'w["w13_scales"][:I], w["w13_gs"][0])',
                                 'w["w13_scales"][:I], w["w13_gs"][1])'),
     "combine weight index": ("moe", "acc = acc + w[t, j] * y[r]", "acc = acc + w[t, 0] * y[r]"),
+    "unquantised forward unweighted": ("moe", "out[t] += w[t, j] * (d_w @ hv)", "out[t] += d_w @ hv"),
     # router
     "ties to the higher index": ("router", "np.lexsort((idx, -score), axis=-1)",
                                  "np.lexsort((-idx, -score), axis=-1)"),
