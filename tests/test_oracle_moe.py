@@ -297,16 +297,25 @@ def test_shared_expert_dense_equals_one_more_routed_expert():
     rng = np.random.default_rng(41)
     E, d, I, T, k = 5, 64, 128, 11, 2
     ex = _rand_experts(rng, E + 1, d, I)
-    routed = Experts(ex.ws[:E], d, I)
     x = (rng.standard_normal((T, d)) * 0.5).astype(np.float32)
     ids = rng.integers(-1, E, (T, k))
     ids[4] = -1  # a token with no routed slot still gets the shared expert
     w = _softmax_rows(rng.standard_normal((T, k)))
-    out_d, out64_d = oracle.forward_with_shared(x, ids, w, routed, ex.ws[E], pad=4)
     ids_x = np.concatenate([ids, np.full((T, 1), E)], 1)
     w_x = np.concatenate([w, np.ones((T, 1), np.float32)], 1)
-    out_x, inter = oracle.forward(x, ids_x, w_x, ex, pad=4, return_intermediates=True)
-    scale = np.abs(out64_d).max()
-    assert np.allclose(out64_d, inter["out_f64"], rtol=0, atol=1e-12 * scale)
-    assert np.array_equal(out_d, out_x)
-    assert np.any(out64_d[4] != 0)
+    # as drawn, then with the shared expert's gate and up 4x larger so that
+    # its h holds the amax of the intermediate (the scale both parts share)
+    for boost in (1.0, 4.0):
+        shared = dict(ex.ws[E], w13_gs=(ex.ws[E]["w13_gs"] / np.float32(boost)).astype(np.float32))
+        full = Experts(ex.ws[:E] + [shared], d, I)
+        out_d, out64_d = oracle.forward_with_shared(x, ids, w, Experts(ex.ws[:E], d, I), shared,
+                                                    pad=4)
+        out_x, inter = oracle.forward(x, ids_x, w_x, full, pad=4, return_intermediates=True)
+        scale = np.abs(out64_d).max()
+        assert np.allclose(out64_d, inter["out_f64"], rtol=0, atol=1e-12 * scale)
+        assert np.array_equal(out_d, out_x)
+        assert np.any(out64_d[4] != 0)
+        rt = inter["routing"]
+        r0, r1 = int(rt.padded_offsets[E]), int(rt.padded_offsets[E] + rt.counts[E])
+        shared_amax = np.float32(np.abs(inter["h"][r0:r1]).max())
+        assert (shared_amax == inter["amax_h"]) == (boost > 1)

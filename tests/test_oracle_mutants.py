@@ -55,6 +55,10 @@ MUTANTS = {
                                 'w["w13_scales"][:I], w["w13_gs"][1])'),
     "combine weight index": ("moe", "acc = acc + w[t, j] * y[r]", "acc = acc + w[t, 0] * y[r]"),
     "unquantised forward unweighted": ("moe", "out[t] += w[t, j] * (d_w @ hv)", "out[t] += d_w @ hv"),
+    "shared h with its own scale": ("moe", "hs_codes, hs_scales, _, _ = quantize(h_s.astype(np.float32), amax=amax_h)",
+                                    "hs_codes, hs_scales, _, _ = quantize(h_s.astype(np.float32))"),
+    "shared amax from routed rows only": ("moe", "amax_h = np.float32(max(float(amax_r), float(np.max(np.abs(h_s))) if T else 0.0))",
+                                          "amax_h = np.float32(amax_r)"),
     # router
     "ties to the higher index": ("router", "np.lexsort((idx, -score), axis=-1)",
                                  "np.lexsort((-idx, -score), axis=-1)"),
