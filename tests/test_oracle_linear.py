@@ -58,6 +58,9 @@ def test_linear_lossless_equals_plain_matmul():
     e[0, 5] = 6.0 / 1024.0
     out1, _ = oracle.linear(e, w_codes, w_scales, gs_w, amax=2.625, round_bf16=False)
     assert np.array_equal(out1[0], w[:, 5] * 6.0 / 1024.0)
+    # the default output is that product rounded once to bf16
+    out_bf16, _ = oracle.linear(x, w_codes, w_scales, gs_w, amax=2.625)
+    assert np.array_equal(out_bf16, q.bf16_round(out)) and np.any(out_bf16 != out)
 
 
 def test_linear_measured_amax_avoids_the_stored_scale_overflow():

@@ -40,6 +40,14 @@ MUTANTS = {
     "encode factor halved": ("nvfp4", "enc = np.where(nz, gs / np.where(nz, sd, np.float32(1))",
                              "enc = np.where(nz, np.float32(0.5) * gs / np.where(nz, sd, np.float32(1))"),
     "zero block keeps codes": ("nvfp4", "codes[~nz] = 0", "pass"),
+    "e2m1 tie 2.5 rounds up": ("nvfp4", "+ (a > 2.5)", "+ (a >= 2.5)"),
+    "e2m1 tie 0.75 rounds down": ("nvfp4", "+ (a >= 0.75)", "+ (a > 0.75)"),
+    "e2m1 sign dropped": ("nvfp4", "return (mag | (np.signbit(x).astype(np.uint8) << 3))",
+                          "return (mag | (np.zeros_like(mag) << 3))"),
+    "dequantise multiplies by gs": ("nvfp4", "* sd / np.float64(gs)).reshape(rows, K)",
+                                    "* sd * np.float64(gs)).reshape(rows, K)"),
+    "scales of the next block": ("nvfp4", "sd = _SCALE_TABLE[np.asarray(scales, dtype=np.uint8)][..., None]",
+                                 "sd = np.roll(_SCALE_TABLE[np.asarray(scales, dtype=np.uint8)], -1, axis=-1)[..., None]"),
     # route, GEMM, SiLU, combine
     "route order descending": ("moe", "slots = np.nonzero(flat == e)[0]",
                                "slots = np.nonzero(flat == e)[0][::-1]"),
@@ -54,6 +62,13 @@ MUTANTS = {
     "gate takes the up scale": ("moe", 'w["w13_scales"][:I], w["w13_gs"][0])',
                                 'w["w13_scales"][:I], w["w13_gs"][1])'),
     "combine weight index": ("moe", "acc = acc + w[t, j] * y[r]", "acc = acc + w[t, 0] * y[r]"),
+    "gather by slot modulo k": ("moe", "valid = rt.row_src >= 0\n    a_codes[valid] = xq_codes[rt.row_src[valid] // k]\n"
+                                "    a_scales[valid] = xq_scales[rt.row_src[valid] // k]\n\n    h, amax_h, h64",
+                                "valid = rt.row_src >= 0\n    a_codes[valid] = xq_codes[rt.row_src[valid] % k]\n"
+                                "    a_scales[valid] = xq_scales[rt.row_src[valid] % k]\n\n    h, amax_h, h64"),
+    "expert rows shifted by one": ("moe", "out[r0:r0 + m] = ahat[r0:r0 + m] @ wm.T",
+                                   "out[r0:r0 + m] = np.roll(ahat, 1, axis=0)[r0:r0 + m] @ wm.T"),
+    "combine not rounded": ("moe", "    out = bf16_round(out64)\n", "    out = out64\n"),
     "unquantised forward unweighted": ("moe", "out[t] += w[t, j] * (d_w @ hv)", "out[t] += d_w @ hv"),
     "shared h with its own scale": ("moe", "hs_codes, hs_scales, _, _ = quantize(h_s.astype(np.float32), amax=amax_h)",
                                     "hs_codes, hs_scales, _, _ = quantize(h_s.astype(np.float32))"),
@@ -71,6 +86,8 @@ MUTANTS = {
     # dense linear
     "linear output columns reversed": ("linear", "out = xhat @ what.T", "out = xhat @ what.T[:, ::-1]"),
     "linear ignores the given amax": ("linear", "quantize(x, amax=amax)", "quantize(x)"),
+    "linear output not rounded": ("linear", "return (bf16_round(out) if round_bf16 else out), inter",
+                                  "return out, inter"),
 }
 
 
