@@ -97,3 +97,35 @@ def test_forward_check_rejects_a_wrong_output_token(tiny_forward):
     bad[5] = -bad[5]
     with pytest.raises(AssertionError):
         check_forward(cfg, _Stages(inter), torch.from_numpy(bad).to(torch.bfloat16), inter)
+
+
+def test_tolerance_checks_accept_rounding_and_reject_errors():
+    from helpers import assert_close, assert_close_bf16, bf16_round
+
+    rng = np.random.default_rng(2)
+    want = rng.standard_normal(4096)
+    # fp32 output: exact and fp32-rounded pass; 3e-3 relative noise, one
+    # outlier of 2e-2 rms, a NaN or a swapped pair fail
+    assert_close(want.astype(np.float32), want)
+    for bad in (want * (1 + 3e-3 * rng.standard_normal(want.size)),
+                np.where(np.arange(want.size) == 7, want + 0.02, want),
+                np.where(np.arange(want.size) == 7, np.nan, want),
+                want[np.r_[1, 0, 2:want.size]]):
+        with pytest.raises(AssertionError):
+            assert_close(bad, want)
+    # bf16 output: the oracle's own rounding passes, and so does the other
+    # neighbour of a value that sits next to a rounding midpoint; two ulps off
+    # a large value do not
+    got = bf16_round(want)
+    assert_close_bf16(got, want)
+    i = int(np.argmax(np.abs(want)))
+    ulp = np.ldexp(1.0, int(np.floor(np.log2(abs(want[i])))) - 7)
+    mid = want.copy()
+    mid[i] = got[i] + np.sign(want[i] - got[i] or 1.0) * ulp * 0.499
+    other = bf16_round(mid)
+    other[i] = got[i] + np.sign(want[i] - got[i] or 1.0) * ulp
+    assert_close_bf16(other, mid)
+    far = got.copy()
+    far[i] += 2 * ulp * np.sign(want[i])
+    with pytest.raises(AssertionError):
+        assert_close_bf16(far, want)
