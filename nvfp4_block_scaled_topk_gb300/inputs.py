@@ -37,7 +37,14 @@ subset of experts regenerates identically:
 The two histograms were measured on a block-quantised N(0, 0.02) tensor of
 4096 x 7168 elements (gs = 2688 / amax), rounded to the counts below, so the
 weights have the statistics of "N(0, 0.02) then NVFP4-quantised" without any
-quantiser running here.
+quantiser running here (the coarse counts put the dequantised standard
+deviation at about 0.021-0.022).
+
+Every draw depends on its generator's device as well as its seed: torch's
+CPU and CUDA generators give different streams.  The same workload drawn on
+the GPU and on the CPU is therefore two samples of one recipe (the prefill
+routing activates 130 experts drawn on the GPU and 126 drawn on the CPU);
+each comparison with the oracle uses the draws of its own run.
 """
 
 from __future__ import annotations

@@ -47,3 +47,26 @@ def test_shared_expert_workload_and_linear_workloads():
     lc = inputs.LINEAR_CONFIGS["linear_tiny"]
     assert x.shape == (lc.T, lc.K) and c.shape == (lc.N, lc.K // 2) and sc.shape == (lc.N, lc.K // 16)
     assert 2688 / 0.12 <= gs <= 2688 / 0.105 + 1e-3
+
+
+def test_recipe_statistics():
+    """Each statistic the recipe states, on the CPU draws."""
+    from oracle import nvfp4 as q
+
+    x = inputs.make_activations(inputs.CONFIGS["decode"]).float()
+    assert abs(float(x.std()) - 0.09) < 0.002 and float(x.abs().max()) < 0.6
+    p = inputs.CONFIGS["prefill"]
+    xp = inputs.make_activations(p).float()
+    assert abs(float((xp.abs() == 8).float().mean()) - 1e-3) < 1e-5
+    ids, _ = inputs.make_routing(p)
+    load = np.bincount(ids.numpy().reshape(-1), minlength=p.E)
+    assert (load > 0).sum() == 126 and load.max() > 10 * load[load > 0].mean()
+    big = inputs.CONFIGS["large"]
+    ids, _ = inputs.make_routing(big)
+    assert np.all(np.bincount(ids.numpy().reshape(-1), minlength=big.E) > 0)
+    e = inputs.make_expert(inputs.CONFIGS["decode"], 5)
+    mags = q.unpack_nibbles(e["w2_codes"].numpy()) & 7
+    hist = np.bincount(mags.reshape(-1), minlength=8) / mags.size
+    assert np.allclose(hist, np.array(inputs.MAG_COUNTS) / 128, atol=2e-3)
+    w2 = q.dequantize(e["w2_codes"].numpy(), e["w2_scales"].numpy(), float(e["w2_gs"][0]))
+    assert 0.020 < w2.std() < 0.023
