@@ -133,3 +133,15 @@ def test_argument_errors_of_the_router_linear_and_layer_calls(lib):
     w16 = megamoe.CWeights(40, 256, 512, 256, 256, 256, 256, 256, 256)
     assert lib.megamoe_forward_from_logits(ctypes.byref(w16), fake, fake, 32, P, 32, 16, 33, 4,
                                            32, fake, fake, 1 << 30, P) == 2
+
+
+def test_missing_library_fails_loudly(monkeypatch):
+    # no CPU or PyTorch fallback: without the built library every call raises
+    monkeypatch.setattr(megamoe, "_LIB", None)
+    missing = os.path.join(ROOT, "nvfp4_block_scaled_topk_gb300", "no_such_libmegamoe.so")
+    with pytest.raises(RuntimeError, match="missing"):
+        megamoe.load(missing)
+    monkeypatch.setattr(megamoe, "LIB_PATH", missing)
+    monkeypatch.setattr(megamoe.load, "__defaults__", (missing,))
+    with pytest.raises(RuntimeError, match="missing"):
+        megamoe.max_padded_rows(8, 6, 384, 32)
