@@ -145,3 +145,36 @@ def test_missing_library_fails_loudly(monkeypatch):
     monkeypatch.setattr(megamoe.load, "__defaults__", (missing,))
     with pytest.raises(RuntimeError, match="missing"):
         megamoe.max_padded_rows(8, 6, 384, 32)
+
+
+def _c_to_ctypes(decl):
+    """ctypes type of one C parameter or return type of the header."""
+    import ctypes as C
+
+    t = " ".join(decl.replace("*", " * ").split())
+    if "*" in t:
+        return C.c_char_p if t == "const char *" else C.c_void_p
+    t = t.replace("const ", "")
+    table = {"int": C.c_int, "int32_t": C.c_int32, "int64_t": C.c_int64, "size_t": C.c_size_t,
+             "double": C.c_double, "uint64_t": C.c_uint64, "megamoe_status": C.c_int,
+             "megamoe_stream_t": C.c_void_p, "void": None}
+    return table[t]
+
+
+def test_binding_signatures_match_the_header_types():
+    src = open(os.path.join(ROOT, "include", "megamoe.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    protos = re.findall(r"([A-Za-z_][\w\s\*]*?)\s*\b(megamoe_[a-z_0-9]+)\s*\(([^)]*)\)\s*;", src)
+    assert len(protos) == len(megamoe.SIGNATURES)
+    for ret, name, params in protos:
+        ret = ret.split("\n")[-1].strip()
+        want_args = []
+        for p in params.split(","):
+            p = " ".join(p.split())
+            if p in ("", "void"):
+                continue
+            typ = re.sub(r"\b[A-Za-z_]\w*$", "", p).strip()  # drop the parameter name
+            want_args.append(_c_to_ctypes(typ))
+        res, args = megamoe.SIGNATURES[name]
+        assert res == _c_to_ctypes(ret), (name, ret)
+        assert args == want_args, name
