@@ -178,3 +178,18 @@ def test_binding_signatures_match_the_header_types():
         res, args = megamoe.SIGNATURES[name]
         assert res == _c_to_ctypes(ret), (name, ret)
         assert args == want_args, name
+
+
+def test_weights_struct_matches_the_header():
+    src = open(os.path.join(ROOT, "include", "megamoe.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    body = re.search(r"typedef struct megamoe_weights\s*\{(.*?)\}\s*megamoe_weights;", src, re.S).group(1)
+    fields = []
+    for decl in body.split(";"):
+        decl = " ".join(decl.split())
+        if not decl:
+            continue
+        name = re.search(r"([A-Za-z_]\w*)$", decl).group(1)
+        fields.append((name, _c_to_ctypes(decl[: -len(name)])))
+    got = [(n, t) for n, t in megamoe.CWeights._fields_]
+    assert got == fields
