@@ -193,3 +193,30 @@ def test_weights_struct_matches_the_header():
         fields.append((name, _c_to_ctypes(decl[: -len(name)])))
     got = [(n, t) for n, t in megamoe.CWeights._fields_]
     assert got == fields
+
+
+@pytest.mark.parametrize("T,k,E,d,I,pad", [(8, 6, 384, 7168, 2048, 32), (64, 2, 8, 256, 512, 128),
+                                           (1, 1, 1, 256, 256, 32), (4096, 6, 384, 7168, 2048, 32)])
+def test_stage_views_mirror_the_workspace_layout(lib, T, k, E, d, I, pad):
+    """The binding's views of the forward's stages lie where the library
+    carves them: the same regions in the same order and sizes, each 256-byte
+    aligned, and the library's size is those regions plus its two
+    router-output regions (no split-K planes unless asked for)."""
+    import torch
+
+    size = megamoe.workspace_size(T, k, E, d, I, pad)
+    ws = torch.empty(size, dtype=torch.uint8, device="meta")
+    v = megamoe._carve_views(ws, 0, T, k, E, d, I, pad)
+    rows = megamoe.max_padded_rows(T, k, E, pad)
+    regions = [("counts", 4 * E), ("offsets", 4 * (E + 1)), ("padded_offsets", 4 * (E + 1)),
+               ("slot_dst", 4 * T * k), ("row_src", 4 * rows), ("xq_codes", rows * d // 2),
+               ("xq_sf", rows * d // 16), ("h", rows * I * 2), ("hq_codes", rows * I // 2),
+               ("hq_sf", rows * I // 16), ("y", rows * d * 4)]
+    a256 = lambda n: -(-n // 256) * 256
+    off = 256  # the status word and the scalars
+    for name, nbytes in regions:
+        t = v[name]
+        assert t.storage_offset() * t.element_size() == off, name
+        assert t.numel() * t.element_size() == nbytes, name
+        off = a256(off + nbytes)
+    assert size == off + 2 * a256(4 * T * k)
