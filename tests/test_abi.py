@@ -220,3 +220,52 @@ def test_stage_views_mirror_the_workspace_layout(lib, T, k, E, d, I, pad):
         assert t.numel() * t.element_size() == nbytes, name
         off = a256(off + nbytes)
     assert size == off + 2 * a256(4 * T * k)
+
+
+def test_plain_c_program_compiles_links_and_calls_the_host_helpers(lib):
+    """The boundary is plain C: a C99 program includes the header, links
+    against the library, references every declared call and runs the
+    host-only helpers and an argument check (no device work)."""
+    import shutil
+    import subprocess
+
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    names = _declared_functions()
+    refs = ",\n    ".join(f"(void (*)(void)){n}" for n in names)
+    prog = f"""
+#include <stdio.h>
+#include <string.h>
+#include "megamoe.h"
+static void (*const every_call[])(void) = {{
+    {refs}
+}};
+int main(void) {{
+  size_t i;
+  for (i = 0; i < sizeof every_call / sizeof every_call[0]; ++i)
+    if (!every_call[i]) return 10;
+  if (megamoe_max_padded_rows(8, 6, 384, 32) != 48 + 48 * 31) return 1;
+  if (megamoe_workspace_size(8, 6, 384, 7168, 2048, 32) % 256 != 0) return 2;
+  if (strcmp(megamoe_status_string(MEGAMOE_ERR_WORKSPACE_TOO_SMALL), "workspace too small"))
+    return 3;
+  if (megamoe_route_permute(NULL, 1, 1, 0, 1, NULL, NULL, NULL, NULL, 0, NULL, NULL, NULL) !=
+      MEGAMOE_ERR_INVALID_ARG)
+    return 4;
+  puts("ok");
+  return 0;
+}}
+"""
+    out_dir = os.path.join(ROOT, "_build", "c_consumer")
+    os.makedirs(out_dir, exist_ok=True)
+    src = os.path.join(out_dir, "consumer.c")
+    exe = os.path.join(out_dir, "consumer")
+    with open(src, "w") as f:
+        f.write(prog)
+    libdir = os.path.dirname(megamoe.LIB_PATH)
+    r = subprocess.run([cc, "-std=c99", "-Wall", "-Wextra", "-Werror", "-I",
+                        os.path.join(ROOT, "include"), src, "-o", exe, "-L", libdir, "-lmegamoe",
+                        f"-Wl,-rpath,{libdir}"], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    r = subprocess.run([exe], capture_output=True, text=True, timeout=60)
+    assert r.returncode == 0 and r.stdout.strip() == "ok", (r.returncode, r.stdout, r.stderr)
