@@ -170,7 +170,10 @@ megamoe_status megamoe_route_permute(const int32_t* topk_ids, int T, int k, int 
  *   row_src != NULL:  out rows with row_src[r] < 0 are written as zero codes
  *                     and zero scales instead (padding rows).
  *   live_rows != NULL: device int32; out rows >= *live_rows are not touched.
- * Requires K a multiple of 64, rows >= 0, out_rows >= 0.
+ * Requires rows >= 0, out_rows >= 0, ld >= K and, with slot_dst == NULL,
+ * rows >= out_rows (else MEGAMOE_ERR_INVALID_ARG); K a multiple of 64, ld a
+ * multiple of 8, x and codes 16-byte aligned, scales 4-byte aligned (else
+ * MEGAMOE_ERR_UNSUPPORTED_SHAPE).
  */
 megamoe_status megamoe_quantize_nvfp4(const uint16_t* x, int64_t rows, int K, int64_t ld,
                                       const int32_t* slot_dst, int k, const int32_t* row_src,
