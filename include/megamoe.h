@@ -186,7 +186,7 @@ megamoe_status megamoe_quantize_nvfp4(const uint16_t* x, int64_t rows, int K, in
  * megamoe_swizzle_scales -- one-time weight preparation: row-major block
  * scales [rows, K/16] -> atom layout (see the file comment).  Rows are padded
  * to a multiple of 128 with zero bytes; dst holds ceil(rows/128)*128*K/16
- * bytes.  Requires K a multiple of 64.
+ * bytes.  Requires K a multiple of 64 and 4-byte aligned src and dst.
  */
 megamoe_status megamoe_swizzle_scales(const uint8_t* src, int64_t rows, int K, uint8_t* dst,
                                       megamoe_stream_t stream);
@@ -331,7 +331,8 @@ megamoe_status megamoe_linear_nvfp4(const uint16_t* x, int64_t T, int K, int64_t
  *   out[t, :] = bf16( sum_{j=0..k-1, slot_dst[t*k+j] >= 0}
  *                     topk_weights[t*k+j] * y[slot_dst[t*k+j], :] )
  * summed in fp32 in ascending j.  y is float [*, ld_y]; out bf16 [T, d].
- * Requires d a multiple of 4, ld_y a multiple of 4.
+ * Requires d and ld_y multiples of 4, y 16-byte and out 8-byte aligned
+ * (else MEGAMOE_ERR_UNSUPPORTED_SHAPE).
  */
 megamoe_status megamoe_combine(const float* y, int64_t ld_y, const int32_t* slot_dst,
                                const float* topk_weights, int T, int k, int d, uint16_t* out,
@@ -356,7 +357,8 @@ size_t megamoe_workspace_size(int T, int k, int E, int d, int I, int pad);
  *   ws, ws_bytes  workspace, at least megamoe_workspace_size(...) bytes,
  *                 256-byte aligned; its first 4 bytes are the device status
  *                 word, cleared at the start of every call.
- * Requires the weight shapes above, 1 <= k <= 16, T >= 0.  Every step is a
+ * Requires the weight shapes above, 1 <= k <= 16, T >= 0, x and the weight
+ * codes and scales 16-byte aligned, out 8-byte aligned.  Every step is a
  * kernel launch on `stream` (no host synchronisation, no memory allocation),
  * so the call can be recorded into a CUDA graph and replayed.
  */
