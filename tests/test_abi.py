@@ -269,3 +269,27 @@ int main(void) {{
     assert r.returncode == 0, r.stderr
     r = subprocess.run([exe], capture_output=True, text=True, timeout=60)
     assert r.returncode == 0 and r.stdout.strip() == "ok", (r.returncode, r.stdout, r.stderr)
+
+
+def test_alignment_errors_return_before_any_device_work(lib):
+    P = None
+    a16 = ctypes.c_void_p(4096)
+    odd = ctypes.c_void_p(4096 + 4)  # 4-byte but not 16-byte aligned
+    # quantise: ld not a multiple of 8; x or codes misaligned
+    assert lib.megamoe_quantize_nvfp4(a16, 4, 64, 68, P, 1, P, P, 4, P, a16, a16, a16, a16,
+                                      0, P, P) == 2
+    assert lib.megamoe_quantize_nvfp4(odd, 4, 64, 64, P, 1, P, P, 4, P, a16, a16, a16, a16,
+                                      0, P, P) == 2
+    assert lib.megamoe_quantize_nvfp4(a16, 4, 64, 64, P, 1, P, P, 4, P, a16, a16, odd, a16,
+                                      0, P, P) == 2
+    # combine: y misaligned
+    assert lib.megamoe_combine(odd, 8, a16, a16, 2, 2, 8, a16, P) == 2
+    # grouped GEMM: output rows not on 16-byte boundaries (bf16 ld of 4)
+    assert lib.megamoe_grouped_gemm(a16, a16, a16, 8, a16, a16, a16, 1, 256, 256, a16, a16, 2,
+                                    a16, 260, P, 0, 0.0, P, P) == 2
+    # forward: x misaligned; workspace not 256-byte aligned
+    w = megamoe.CWeights(8, 256, 512, 4096, 4096, 4096, 4096, 4096, 4096)
+    assert lib.megamoe_forward(ctypes.byref(w), odd, a16, a16, 4, 2, 32, a16, a16, 1 << 30,
+                               P) == 2
+    assert lib.megamoe_forward(ctypes.byref(w), a16, a16, a16, 4, 2, 32, a16, odd, 1 << 30,
+                               P) == 1
