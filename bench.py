@@ -453,7 +453,9 @@ def run_ours(args):
                        "global_batch": cfg.T * world, "parallelism": f"replicas x{world}",
                        "l2": f"inputs larger than L2 (~{w_step / 1e9:.2f} GB of expert weights "
                              "read per step, L2 is 0.13 GB)",
-                       "active_experts": active, "valid_slots": valid_slots},
+                       "active_experts": active, "valid_slots": valid_slots,
+                       "max_expert_load": int(counts.max()),
+                       "zero_token_experts": int((counts == 0).sum())},
             "tflops": flops / (ms * 1e-3) / 1e12,
             "hbm_gbs": alg_bytes / (ms * 1e-3) / 1e9,
             "hbm_frac_of_measured": alg_bytes / (ms * 1e-3) / 1e9 / hbm_gbs,
