@@ -2,11 +2,14 @@
 
 One step = one megamoe_forward (route -> amax -> quantise -> L1 grouped GEMM
 with SiLU*up -> requantise -> L2 grouped GEMM -> combine) over one batch of
-the MegaMoE decode workload (384 experts, top-6, d 7168, I 2048, 8 tokens,
-NVFP4 weights resident in HBM).  Prints one JSON line.
+the largest single-GPU MegaMoE workload (384 experts, top-6, d 7168, I 2048,
+16384 tokens with uniform routing, NVFP4 weights resident in HBM).  Prints one
+JSON line; beside the headline it carries sub-records of the 4096-token
+Zipf-skewed prefill and of the 8- and 1-token decode batches, each with its
+own roofline and stage times.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--config decode]
-                  [--impl ours|reference]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config large]
+                  [--no-sub] [--impl ours|reference]
 
 --impl reference times the CPU oracle (the float64 reference of the method)
 on a bounded sample of the same workload.  Under torchrun every rank runs its
@@ -239,25 +242,61 @@ def run_reference(args):
 # --------------------------------------------------------------------------
 # our arm
 # --------------------------------------------------------------------------
-def run_ours(args):
+#: sub-records measured beside the headline workload (its own weights each)
+SUB_CONFIGS = ("prefill", "decode", "decode1")
+
+
+def fp4_peak_tflops(bf16_tf: float) -> float:
+    """Dense NVFP4 tensor peak: the measured bf16 peak x the nominal dense
+    FP4 / BF16 ratio (13.5 / 2.25)."""
+    return bf16_tf * 13.5 / 2.25
+
+
+def gemm_roofline(name, bytes_, flops, ms, hbm_gbs, fp4_tf, peak_kind, traffic=None):
+    """Roofline object of one grouped-GEMM launch: the binding roof is the
+    larger of bytes / HBM and flops / FP4 peak; `achieved` and `frac` are
+    against that roof (measured peaks), and the other roof's fraction plus
+    both fractions against the datasheet figures (~8 TB/s, 13.5 PFLOP/s)
+    are given beside it."""
+    t = ms * 1e-3
+    gbs = bytes_ / t / 1e9
+    tfs = flops / t / 1e12
+    t_hbm = bytes_ / (hbm_gbs * 1e9)
+    t_fp4 = flops / (fp4_tf * 1e12)
+    hbm_bound = t_hbm >= t_fp4
+    return {
+        "bound": "hbm" if hbm_bound else "tensor",
+        "achieved": gbs if hbm_bound else tfs,
+        "peak": hbm_gbs if hbm_bound else fp4_tf,
+        "unit": "GB/s" if hbm_bound else "TFLOP/s",
+        "frac": gbs / hbm_gbs if hbm_bound else tfs / fp4_tf,
+        "traffic": traffic,
+        "kernel": name,
+        "peak_source": (f"{peak_kind} HBM copy" if hbm_bound else
+                        f"{peak_kind} bf16 x 6 (nominal dense FP4/BF16 ratio)"),
+        "hbm_frac": gbs / hbm_gbs, "fp4_frac": tfs / fp4_tf,
+        "attainable_frac": max(t_hbm, t_fp4) / t,
+        "datasheet_hbm_frac": gbs / 8000.0, "datasheet_fp4_frac": tfs / 13500.0,
+        "algorithmic_bytes": bytes_, "algorithmic_flops": flops,
+    }
+
+
+def measure_forward(cfg, args, dev, world, rank, local, with_e2e=True, with_cpu=True):
+    """Every number of one workload: the device-timed forward (inputs
+    resident), the two grouped GEMMs timed alone on the forward's own
+    intermediates, the roofline of the dominant one, the end-to-end loop
+    through the public call with host copies, and the oracle on the host."""
     import numpy as np
     import torch
 
-    from nvfp4_block_scaled_topk_gb300 import build, inputs, megamoe
+    from nvfp4_block_scaled_topk_gb300 import inputs, megamoe
 
-    rank, world, local = _dist()
-    if world > 1:
-        import torch.distributed as dist
-
-        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    build.build()
-    megamoe.load()
-
-    cfg = inputs.CONFIGS[args.config]
     raw = inputs.make_all_experts(cfg, device=dev)
     weights = megamoe.Weights.prepare(raw)
+    if not (with_cpu and rank == 0 and not args.no_cpu_baseline):
+        del raw
+        raw = None
+    torch.cuda.empty_cache()
     x = inputs.make_activations(cfg, device=dev)
     ids, w = inputs.make_routing(cfg, device=dev)
     fwd = megamoe.Forward(weights, cfg.T, cfg.k, pad=cfg.pad)
@@ -296,8 +335,8 @@ def run_ours(args):
     barrier()
     ms = ev0.elapsed_time(ev1) / args.steps
 
-    # ---- dominant kernel (L1 grouped GEMM) timed alone on the forward's own
-    # intermediates, CUDA events on the launching stream
+    # ---- the grouped GEMMs timed alone on the forward's own intermediates,
+    # CUDA events on the launching stream
     l1_out = torch.empty_like(v["h"])
     l1_amax = torch.empty(1, dtype=torch.float32, device=dev)
     expected = cfg.slots / cfg.E  # the forward's token-tile choice (tile_n 0 = auto)
@@ -330,105 +369,125 @@ def run_ours(args):
     l2_ms = timed(l2, max(args.steps, 10))
     clk = clocks.stop()
 
-    # ---- end to end through the public call, host buffers, copies inside
+    # ---- end to end through the public call, host buffers, copies inside.
     # x, topk_ids and topk_weights sit in one pinned staging buffer, so each
     # step's inputs go up in a single host-to-device copy.  Two device copies
     # of the staging buffer and of the output alternate between steps: one
     # stream uploads step i+1's inputs and another downloads step i-1's output
     # while step i computes, as a serving loop would; every step still makes
     # both copies, and the timed region spans all K steps' copies and compute.
-    nx, ni = x.numel() * 2, ids.numel() * 4
-    stage_h = torch.empty(nx + 2 * ni, dtype=torch.uint8).pin_memory()
-    stage_h[:nx].view(torch.bfloat16).copy_(x.cpu().reshape(-1))
-    stage_h[nx:nx + ni].view(torch.int32).copy_(ids.cpu().reshape(-1))
-    stage_h[nx + ni:].view(torch.float32).copy_(w.cpu().reshape(-1))
-    stage_d = [torch.empty(stage_h.numel(), dtype=torch.uint8, device=dev) for _ in range(2)]
-    views = [(sd[:nx].view(torch.bfloat16).view(cfg.T, cfg.d),
-              sd[nx:nx + ni].view(torch.int32).view(cfg.T, cfg.k),
-              sd[nx + ni:].view(torch.float32).view(cfg.T, cfg.k)) for sd in stage_d]
-    out_d = [torch.empty(cfg.T, cfg.d, dtype=torch.bfloat16, device=dev) for _ in range(2)]
-    out_h = [torch.empty(cfg.T, cfg.d, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
-    up_stream = torch.cuda.Stream(device=dev)
-    down_stream = torch.cuda.Stream(device=dev)
+    e2e = None
+    if with_e2e:
+        nx, ni = x.numel() * 2, ids.numel() * 4
+        stage_h = torch.empty(nx + 2 * ni, dtype=torch.uint8).pin_memory()
+        stage_h[:nx].view(torch.bfloat16).copy_(x.cpu().reshape(-1))
+        stage_h[nx:nx + ni].view(torch.int32).copy_(ids.cpu().reshape(-1))
+        stage_h[nx + ni:].view(torch.float32).copy_(w.cpu().reshape(-1))
+        stage_d = [torch.empty(stage_h.numel(), dtype=torch.uint8, device=dev) for _ in range(2)]
+        views = [(sd[:nx].view(torch.bfloat16).view(cfg.T, cfg.d),
+                  sd[nx:nx + ni].view(torch.int32).view(cfg.T, cfg.k),
+                  sd[nx + ni:].view(torch.float32).view(cfg.T, cfg.k)) for sd in stage_d]
+        out_d = [torch.empty(cfg.T, cfg.d, dtype=torch.bfloat16, device=dev) for _ in range(2)]
+        out_h = [torch.empty(cfg.T, cfg.d, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+        up_stream = torch.cuda.Stream(device=dev)
+        down_stream = torch.cuda.Stream(device=dev)
 
-    def e2e_steps(n):
-        # on the current stream (the capture stream while a graph records);
-        # the copy streams fork from it and join it at the end
-        comp = torch.cuda.current_stream()
-        fork = torch.cuda.Event()
-        fork.record(comp)
-        up_stream.wait_event(fork)
-        down_stream.wait_event(fork)
-        computed = [None, None]
-        downloaded = [None, None]
-        for i in range(n):
-            b = i % 2
-            up = torch.cuda.Event()
-            with torch.cuda.stream(up_stream):
-                if computed[b] is not None:  # step i-2 is done with buffer b
-                    up_stream.wait_event(computed[b])
-                stage_d[b].copy_(stage_h, non_blocking=True)
-                up.record(up_stream)
-            comp.wait_event(up)
-            if downloaded[b] is not None:  # step i-2's output has left out_d[b]
-                comp.wait_event(downloaded[b])
-            fwd(*views[b], out=out_d[b])
-            computed[b] = torch.cuda.Event()
-            computed[b].record(comp)
-            with torch.cuda.stream(down_stream):
-                down_stream.wait_event(computed[b])
-                out_h[b].copy_(out_d[b], non_blocking=True)
-                downloaded[b] = torch.cuda.Event()
-                downloaded[b].record(down_stream)
-        for ev in downloaded:
-            if ev is not None:
-                comp.wait_event(ev)
+        def e2e_steps(n):
+            # on the current stream (the capture stream while a graph records);
+            # the copy streams fork from it and join it at the end
+            comp = torch.cuda.current_stream()
+            fork = torch.cuda.Event()
+            fork.record(comp)
+            up_stream.wait_event(fork)
+            down_stream.wait_event(fork)
+            computed = [None, None]
+            downloaded = [None, None]
+            for i in range(n):
+                b = i % 2
+                up = torch.cuda.Event()
+                with torch.cuda.stream(up_stream):
+                    if computed[b] is not None:  # step i-2 is done with buffer b
+                        up_stream.wait_event(computed[b])
+                    stage_d[b].copy_(stage_h, non_blocking=True)
+                    up.record(up_stream)
+                comp.wait_event(up)
+                if downloaded[b] is not None:  # step i-2's output has left out_d[b]
+                    comp.wait_event(downloaded[b])
+                fwd(*views[b], out=out_d[b])
+                computed[b] = torch.cuda.Event()
+                computed[b].record(comp)
+                with torch.cuda.stream(down_stream):
+                    down_stream.wait_event(computed[b])
+                    out_h[b].copy_(out_d[b], non_blocking=True)
+                    downloaded[b] = torch.cuda.Event()
+                    downloaded[b].record(down_stream)
+            for ev in downloaded:
+                if ev is not None:
+                    comp.wait_event(ev)
 
-    # the K steps are recorded once into a CUDA graph (one host call replays
-    # them, so short steps are not bound by the host's launch rate); if the
-    # capture fails the same steps run eagerly
-    e2e_steps(3)
-    barrier()
-    torch.cuda.synchronize()
-    graph = None
-    try:
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph):
-            e2e_steps(args.steps)
-        graph.replay()
+        # the K steps are recorded once into a CUDA graph (one host call
+        # replays them, so short steps are not bound by the host's launch
+        # rate); if the capture fails the same steps run eagerly
+        e2e_steps(3)
+        barrier()
         torch.cuda.synchronize()
-    except Exception:
         graph = None
+        try:
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph):
+                e2e_steps(args.steps)
+            graph.replay()
+            torch.cuda.synchronize()
+        except Exception:
+            graph = None
+            torch.cuda.synchronize()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        if graph is not None:
+            graph.replay()
+        else:
+            e2e_steps(args.steps)
+        b.record(stream)
         torch.cuda.synchronize()
-    a = torch.cuda.Event(enable_timing=True)
-    b = torch.cuda.Event(enable_timing=True)
-    a.record(stream)
-    if graph is not None:
-        graph.replay()
-    else:
-        e2e_steps(args.steps)
-    b.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = a.elapsed_time(b) / args.steps
-    h2d = stage_h.numel()
-    d2h = out_h[0].numel() * 2
+        e2e_ms = a.elapsed_time(b) / args.steps
+        e2e = {"ms": e2e_ms, "h2d": stage_h.numel(), "d2h": out_h[0].numel() * 2,
+               "loop": ("CUDA graph of the K steps" if graph is not None else "eager") +
+                       ", inputs uploaded and outputs downloaded on two copy streams, "
+                       "double-buffered"}
+        del graph, stage_d, out_d
 
     # ---- max over ranks
-    ms, e2e_ms, l1_ms, l2_ms = max_over_ranks([ms, e2e_ms, l1_ms, l2_ms], world, dev)
+    vals = [ms, l1_ms, l2_ms] + ([e2e["ms"]] if e2e else [])
+    vals = max_over_ranks(vals, world, dev)
+    ms, l1_ms, l2_ms = vals[:3]
+    if e2e:
+        e2e["ms"] = vals[3]
 
     hbm_gbs, bf16_tf, peak_kind = _peaks()
-    tokens_total = cfg.T * world
-    value = tokens_total / (ms * 1e-3)
+    fp4_tf = fp4_peak_tflops(bf16_tf)
     flops = inputs.algorithmic_flops(cfg, valid_slots)
     alg_bytes = inputs.algorithmic_bytes(cfg, active)
-    w_step = active * 3 * cfg.d * cfg.I * (0.5 + 1.0 / 16)  # weight bytes one step reads
     w_el = cfg.d * cfg.I * (0.5 + 1.0 / 16)
-    l1_bytes = active * 2 * w_el + valid_slots * cfg.d * (0.5 + 1 / 16) + valid_slots * cfg.I * 2
-    l1_gbs = l1_bytes / (l1_ms * 1e-3) / 1e9
-    traffic = _profile_traffic(f"l1_gemm_{cfg.name}.json")
+    a_row1 = cfg.d * (0.5 + 1 / 16)  # one quantised token row of x
+    a_row2 = cfg.I * (0.5 + 1 / 16)  # one requantised row of h
+    # per launch: the active experts' weights once, each routed row's
+    # activations in and its output row out
+    l1_bytes = active * 2 * w_el + valid_slots * (a_row1 + cfg.I * 2)
+    l2_bytes = active * w_el + valid_slots * (a_row2 + cfg.d * 4)
+    l1_flops = 4 * cfg.d * cfg.I * valid_slots
+    l2_flops = 2 * cfg.d * cfg.I * valid_slots
+    rl1 = gemm_roofline("k_grouped_gemm (L1 gate+up, SiLU*up epilogue)", l1_bytes, l1_flops,
+                        l1_ms, hbm_gbs, fp4_tf, peak_kind,
+                        _profile_traffic(f"l1_gemm_{cfg.name}.json"))
+    rl2 = gemm_roofline("k_grouped_gemm (L2 down, fp32 epilogue)", l2_bytes, l2_flops, l2_ms,
+                        hbm_gbs, fp4_tf, peak_kind,
+                        _profile_traffic(f"l2_gemm_{cfg.name}.json"))
+    t_floor = max(alg_bytes / (hbm_gbs * 1e9), flops / (fp4_tf * 1e12))
+    tokens_total = cfg.T * world
 
     cpu = None
-    if rank == 0 and not args.no_cpu_baseline:
+    if raw is not None:
         tokens = max(1, min(cfg.T, args.ref_tokens))
         ex = inputs.ExpertSet(cfg, raw)
         # the same sample repeated until about 10 s of CPU work is timed
@@ -440,38 +499,89 @@ def run_ours(args):
                "sample": f"first {tokens} of {cfg.T} tokens of the {cfg.name} batch, full float64 "
                          f"forward over the experts they touch, {reps} times "
                          f"({total:.1f} s); weights fetched before timing"}
+    rec = {
+        "value": tokens_total / (ms * 1e-3), "ms_per_step": ms,
+        "workload": f"{cfg.name}: MegaMoE routed-expert forward, E={cfg.E} top-{cfg.k} "
+                    f"d={cfg.d} I={cfg.I} T={cfg.T}, NVFP4 weights resident",
+        "global_batch": cfg.T * world,
+        "l2": f"inputs larger than L2 (~{active * 3 * w_el / 1e9:.2f} GB of expert weights "
+              "read per step, L2 is 0.13 GB)",
+        "active_experts": active, "valid_slots": valid_slots,
+        "max_expert_load": int(counts.max()), "zero_token_experts": int((counts == 0).sum()),
+        "tflops": flops / (ms * 1e-3) / 1e12,
+        "hbm_gbs": alg_bytes / (ms * 1e-3) / 1e9,
+        "hbm_frac_of_measured": alg_bytes / (ms * 1e-3) / 1e9 / hbm_gbs,
+        "fp4_frac_of_measured": flops / (ms * 1e-3) / 1e12 / fp4_tf,
+        "attainable_frac": t_floor / (ms * 1e-3),
+        "stage_ms": {"l1_gemm": l1_ms, "l2_gemm": l2_ms},
+        "roofline": rl1 if l1_ms >= l2_ms else rl2,
+        "roofline_other_gemm": rl2 if l1_ms >= l2_ms else rl1,
+        "cpu_baseline": cpu,
+        "e2e": None if e2e is None else {
+            "value": tokens_total / (e2e["ms"] * 1e-3), "unit": UNIT,
+            "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
+            "loop": e2e["loop"]},
+        "gpu_launches": kernels_per_step(cfg) * args.steps,
+        "clocks": clk,
+    }
+    del fwd, weights, raw, x, ids, w, v, l1_out
+    torch.cuda.empty_cache()
+    return rec
 
+
+def run_ours(args):
+    import torch
+
+    from nvfp4_block_scaled_topk_gb300 import build, inputs, megamoe
+
+    rank, world, local = _dist()
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    build.build()
+    megamoe.load()
+
+    cfg = inputs.CONFIGS[args.config]
+    main = measure_forward(cfg, args, dev, world, rank, local)
+    subs = {}
+    if not args.no_sub:
+        for name in SUB_CONFIGS:
+            if name == cfg.name:
+                continue
+            r = measure_forward(inputs.CONFIGS[name], args, dev, world, rank, local,
+                                with_e2e=True, with_cpu=False)
+            subs[name] = {key: r[key] for key in (
+                "value", "ms_per_step", "workload", "active_experts", "valid_slots",
+                "max_expert_load", "zero_token_experts", "tflops", "hbm_gbs",
+                "hbm_frac_of_measured", "fp4_frac_of_measured", "attainable_frac", "stage_ms",
+                "roofline", "roofline_other_gemm", "e2e", "clocks")}
     if rank == 0:
         line = {
-            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "nvfp4 (e2m1 x e4m3 scales, fp32 acc)",
-            "data": "synthetic",
-            "config": {"workload": f"{cfg.name}: MegaMoE routed-expert forward, E={cfg.E} "
-                                   f"top-{cfg.k} d={cfg.d} I={cfg.I} T={cfg.T}, NVFP4 weights "
-                                   "resident",
-                       "global_batch": cfg.T * world, "parallelism": f"replicas x{world}",
-                       "l2": f"inputs larger than L2 (~{w_step / 1e9:.2f} GB of expert weights "
-                             "read per step, L2 is 0.13 GB)",
-                       "active_experts": active, "valid_slots": valid_slots,
-                       "max_expert_load": int(counts.max()),
-                       "zero_token_experts": int((counts == 0).sum())},
-            "tflops": flops / (ms * 1e-3) / 1e12,
-            "hbm_gbs": alg_bytes / (ms * 1e-3) / 1e9,
-            "hbm_frac_of_measured": alg_bytes / (ms * 1e-3) / 1e9 / hbm_gbs,
-            "stage_ms": {"l1_gemm": l1_ms, "l2_gemm": l2_ms},
-            "roofline": {"bound": "hbm", "achieved": l1_gbs, "peak": hbm_gbs, "unit": "GB/s",
-                         "frac": l1_gbs / hbm_gbs, "traffic": traffic,
-                         "kernel": "k_grouped_gemm (L1 gate+up, SiLU*up epilogue)",
-                         "peak_source": peak_kind},
-            "cpu_baseline": cpu,
-            "e2e": {"value": tokens_total / (e2e_ms * 1e-3), "unit": UNIT,
-                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                    "loop": ("CUDA graph of the K steps" if graph is not None else "eager") +
-                            ", inputs uploaded and outputs downloaded on two copy streams, "
-                            "double-buffered"},
-            "gpu_launches": kernels_per_step(cfg) * args.steps,
-            "clocks": clk,
+            "metric": METRIC, "value": main["value"], "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": main["ms_per_step"],
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "nvfp4 (e2m1 x e4m3 scales, fp32 acc)", "data": "synthetic",
+            "config": {"workload": main["workload"], "global_batch": main["global_batch"],
+                       "parallelism": f"replicas x{world}", "l2": main["l2"],
+                       "active_experts": main["active_experts"],
+                       "valid_slots": main["valid_slots"],
+                       "max_expert_load": main["max_expert_load"],
+                       "zero_token_experts": main["zero_token_experts"]},
+            "tflops": main["tflops"], "hbm_gbs": main["hbm_gbs"],
+            "hbm_frac_of_measured": main["hbm_frac_of_measured"],
+            "fp4_frac_of_measured": main["fp4_frac_of_measured"],
+            "attainable_frac": main["attainable_frac"],
+            "stage_ms": main["stage_ms"],
+            "roofline": main["roofline"],
+            "roofline_other_gemm": main["roofline_other_gemm"],
+            "cpu_baseline": main["cpu_baseline"],
+            "e2e": main["e2e"],
+            "gpu_launches": main["gpu_launches"],
+            "clocks": main["clocks"],
+            "sub_records": subs,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -658,7 +768,10 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--config", default="decode")
+    ap.add_argument("--config", default="large",
+                    help="headline workload (default: large, the largest single-GPU one)")
+    ap.add_argument("--no-sub", action="store_true",
+                    help="skip the prefill / decode / decode1 sub-records")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--ref-tokens", type=int, default=1)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -668,10 +781,12 @@ def main():
                          "router top-k alone; layer: router + forward with a shared expert")
     args = ap.parse_args()
     if args.op == "linear":
-        if args.config == "decode":
+        if args.config == "large":
             args.config = "linear_qa_decode"
         run_linear(args)
     elif args.op in ("router", "layer"):
+        if args.config == "large" and args.op == "router":
+            args.config = "decode"
         run_layer(args, router_only=args.op == "router")
     elif args.impl == "reference":
         run_reference(args)

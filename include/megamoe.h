@@ -389,23 +389,28 @@ megamoe_status megamoe_read_status(const uint32_t* status, uint32_t* bits,
 /*
  * megamoe_forward_static -- megamoe_forward without a caller-provided
  * workspace, for callers that cannot allocate device memory where they run
- * the forward: code inside a CUDA stream capture whose graph must hold no
- * allocation nodes, plugins in a host process that owns every allocation
- * (an inference server with its own memory pool), hot loops that must never
- * enter the allocator.  (The source pages have no counterpart: this is a
- * deployment variant of megamoe_forward, not a step of the method.)
+ * the forward: plugins in a host process that owns every device allocation
+ * (an inference server with its own memory pool, which forbids side
+ * allocations), embedded callers that link only this library and have no
+ * allocator at hand, hot loops that must never enter the allocator.  (The
+ * source pages have no counterpart: this is a deployment variant of
+ * megamoe_forward, not a step of the method.)
  *
  * The workspace is a fixed device array inside the library of
  * MEGAMOE_STATIC_WS_BYTES (64 MiB), held by every GPU that loads the library
  * until the process exits.  Nothing is allocated or freed by this call.
  * Arguments are those of megamoe_forward, minus ws/ws_bytes, plus:
  *   status_out  device uint32 (may be NULL): receives the forward's device
- *               status word (see MEGAMOE_DEV_*), copied on `stream`.
- * Returns MEGAMOE_ERR_WORKSPACE_TOO_SMALL when
+ *               status word (see MEGAMOE_DEV_*), copied on `stream`; written
+ *               only when the call returns MEGAMOE_OK.
+ * Argument and shape errors are those of megamoe_forward and are reported
+ * first; then MEGAMOE_ERR_WORKSPACE_TOO_SMALL when
  * megamoe_workspace_size(T, k, E, d, I, pad) exceeds MEGAMOE_STATIC_WS_BYTES
  * (for E = 384, d = 7168, I = 2048, k = 6, pad = 32 that is T > 9 tokens).
  * The first call on a device looks the array up for that device (with it
- * current) and should come before any stream capture.  All calls share the
+ * current) and should come before any stream capture; a call under a new
+ * driver context of the device (after cudaDeviceReset, or a context made
+ * current through the driver API) looks it up again.  All calls share the
  * array: calls that overlap on the GPU race, so the caller serialises them
  * (one stream per device, or its own ordering).
  */

@@ -142,6 +142,30 @@ megamoe_status check_route_args(int T, int k, int E, int pad) {
 
 }  // namespace
 
+namespace megamoe {
+
+megamoe_status check_forward_args(const megamoe_weights* w, const uint16_t* x,
+                                  const int32_t* topk_ids, const float* topk_weights, int T, int k,
+                                  int pad, const uint16_t* out, bool router) {
+  if (!w) return MEGAMOE_ERR_INVALID_ARG;
+  const int E = w->num_experts, d = w->hidden, I = w->intermediate;
+  megamoe_status st = check_route_args(T, k, E, pad);
+  if (st != MEGAMOE_OK) return st;
+  if (d <= 0 || I <= 0) return MEGAMOE_ERR_INVALID_ARG;
+  if (d % 256 != 0 || I % 256 != 0 || pad % 32 != 0) return MEGAMOE_ERR_UNSUPPORTED_SHAPE;
+  if (!w->w13_codes || !w->w13_scales || !w->w13_gs || !w->w2_codes || !w->w2_scales ||
+      !w->w2_gs)
+    return MEGAMOE_ERR_INVALID_ARG;
+  if (T > 0 && (!x || (!router && (!topk_ids || !topk_weights)) || !out))
+    return MEGAMOE_ERR_INVALID_ARG;
+  if ((x && !aligned(x, 16)) || (out && !aligned(out, 8)) || !aligned(w->w13_codes, 16) ||
+      !aligned(w->w2_codes, 16) || !aligned(w->w13_scales, 16) || !aligned(w->w2_scales, 16))
+    return MEGAMOE_ERR_UNSUPPORTED_SHAPE;
+  return MEGAMOE_OK;
+}
+
+}  // namespace megamoe
+
 extern "C" {
 
 const char* megamoe_status_string(megamoe_status s) {
@@ -309,21 +333,11 @@ namespace {
 megamoe_status forward_impl(const megamoe_weights* w, const uint16_t* x, const int32_t* topk_ids,
                             const float* topk_weights, int T, int k, int pad, uint16_t* out,
                             void* ws, size_t ws_bytes, cudaStream_t s, RouterArgs* router) {
-  if (!w) return MEGAMOE_ERR_INVALID_ARG;
-  const int E = w->num_experts, d = w->hidden, I = w->intermediate;
-  megamoe_status st = check_route_args(T, k, E, pad);
+  megamoe_status st =
+      megamoe::check_forward_args(w, x, topk_ids, topk_weights, T, k, pad, out, router != nullptr);
   if (st != MEGAMOE_OK) return st;
-  if (d <= 0 || I <= 0) return MEGAMOE_ERR_INVALID_ARG;
-  if (d % 256 != 0 || I % 256 != 0 || pad % 32 != 0) return MEGAMOE_ERR_UNSUPPORTED_SHAPE;
-  if (!w->w13_codes || !w->w13_scales || !w->w13_gs || !w->w2_codes || !w->w2_scales ||
-      !w->w2_gs || !ws)
-    return MEGAMOE_ERR_INVALID_ARG;
-  if (T > 0 && (!x || (!router && (!topk_ids || !topk_weights)) || !out))
-    return MEGAMOE_ERR_INVALID_ARG;
-  if (!aligned(ws, 256)) return MEGAMOE_ERR_INVALID_ARG;
-  if ((x && !aligned(x, 16)) || (out && !aligned(out, 8)) || !aligned(w->w13_codes, 16) ||
-      !aligned(w->w2_codes, 16) || !aligned(w->w13_scales, 16) || !aligned(w->w2_scales, 16))
-    return MEGAMOE_ERR_UNSUPPORTED_SHAPE;
+  if (!ws || !aligned(ws, 256)) return MEGAMOE_ERR_INVALID_ARG;
+  const int E = w->num_experts, d = w->hidden, I = w->intermediate;
   Workspace wk = carve(ws, T, k, E, d, I, pad);
   if (ws_bytes < wk.bytes) return MEGAMOE_ERR_WORKSPACE_TOO_SMALL;
 

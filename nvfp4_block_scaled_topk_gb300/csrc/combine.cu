@@ -63,8 +63,10 @@ cudaError_t launch_combine(const float* y, int64_t ld_y, const int32_t* slot_dst
                            int T, int k, int d, uint16_t* out, cudaStream_t stream) {
   const int64_t tasks = static_cast<int64_t>(T) * (d / 4);
   if (tasks == 0) return cudaSuccess;
+  // up to 16 resident blocks of 256 threads per SM, grid-stride beyond that
   int64_t blocks = (tasks + 255) / 256;
-  if (blocks > 152 * 16) blocks = 152 * 16;
+  const int64_t cap = static_cast<int64_t>(num_sms()) * 16;
+  if (blocks > cap) blocks = cap;
   return launch_pdl(k_combine, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, y, ld_y,
                     slot_dst, w, T, k, d, out);
 }

@@ -702,7 +702,7 @@ static bool make_codes_map(CUtensorMap* map, const void* base, uint64_t rows, ui
   return r == CUDA_SUCCESS;
 }
 
-static int num_sms() {
+int num_sms() {
   int dev = 0, n = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);

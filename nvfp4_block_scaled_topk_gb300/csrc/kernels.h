@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "../../include/megamoe.h"
+
 namespace megamoe {
 
 // Launch on `stream` with programmatic stream serialization: the kernel may be
@@ -119,6 +121,15 @@ uint64_t wait_limit_ns();
 // Router: ids/weights [T, k (+1 with a shared expert)] from fp32 logits.
 cudaError_t launch_router(const float* logits, int64_t T, int E, int64_t ld, const float* bias,
                           int k, int shared, int32_t* ids, float* weights, cudaStream_t stream);
+
+// Argument and shape checks of megamoe_forward that do not involve the
+// workspace (router: the ids and weights come from a fused router).
+megamoe_status check_forward_args(const megamoe_weights* w, const uint16_t* x,
+                                  const int32_t* topk_ids, const float* topk_weights, int T, int k,
+                                  int pad, const uint16_t* out, bool router);
+
+// Number of SMs of the current device (at least 1).
+int num_sms();
 
 cudaError_t launch_combine(const float* y, int64_t ld_y, const int32_t* slot_dst,
                            const float* w, int T, int k, int d, uint16_t* out,

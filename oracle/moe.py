@@ -183,7 +183,8 @@ def combine(y, topk_weights, slot_dst, round_bf16=True):
     return bf16_round(out) if round_bf16 else out
 
 
-def forward(x, topk_ids, topk_weights, experts, pad: int = 1, return_intermediates=False):
+def forward(x, topk_ids, topk_weights, experts, pad: int = 1, return_intermediates=False,
+            amax_x=None, amax_h=None):
     """The routed-expert forward, step by step as the pages order it.
 
     1. route: bucket slots per expert (expert_offsets / padded offsets);
@@ -194,6 +195,13 @@ def forward(x, topk_ids, topk_weights, experts, pad: int = 1, return_intermediat
     6. top-k weighted combine, rounded once to bf16.
     ``x`` is [T, d] (bf16 values as float32); ``experts[e]`` holds expert e's
     NVFP4 weights.  Returns the [T, d] output as float64 bf16 values.
+
+    ``amax_x`` / ``amax_h``: when the given tokens are a sample of a larger
+    batch, the amax of the whole batch's x and of its whole intermediate
+    (reading A2: one global scale per tensor, so a sampled token is quantised
+    with the batch's scales); by default both are measured over the tokens
+    given.  Every other step is unchanged: each token's output depends on the
+    batch only through these two scalars.
     """
     x = np.asarray(x, dtype=np.float32)
     ids = np.asarray(topk_ids)
@@ -203,7 +211,7 @@ def forward(x, topk_ids, topk_weights, experts, pad: int = 1, return_intermediat
     R_pad = int(rt.padded_offsets[-1])
     d = x.shape[1]
 
-    xq_codes, xq_scales, gs_x, amax_x = quantize(x)
+    xq_codes, xq_scales, gs_x, amax_x = quantize(x, amax=amax_x)
     # gather quantised token rows into padded-row order (padding rows zero)
     a_codes = np.zeros((R_pad, d // 2), dtype=np.uint8)
     a_scales = np.zeros((R_pad, d // 16), dtype=np.uint8)
@@ -211,8 +219,10 @@ def forward(x, topk_ids, topk_weights, experts, pad: int = 1, return_intermediat
     a_codes[valid] = xq_codes[rt.row_src[valid] // k]
     a_scales[valid] = xq_scales[rt.row_src[valid] // k]
 
-    h, amax_h, h64 = grouped_gemm(a_codes, a_scales, gs_x, experts, "w13", rt, "silu_mul",
-                                  return_unrounded=True)
+    h, amax_h_own, h64 = grouped_gemm(a_codes, a_scales, gs_x, experts, "w13", rt, "silu_mul",
+                                      return_unrounded=True)
+    if amax_h is None:
+        amax_h = amax_h_own
     hq_codes, hq_scales, gs_h, _ = quantize(h.astype(np.float32), amax=amax_h)
     hq_codes[~valid] = 0
     hq_scales[~valid] = 0
@@ -222,7 +232,8 @@ def forward(x, topk_ids, topk_weights, experts, pad: int = 1, return_intermediat
     if return_intermediates:
         return out, dict(routing=rt, out_f64=out64, h_f64=h64, gs_x=gs_x, amax_x=amax_x, xq_codes=xq_codes,
                          xq_scales=xq_scales, a_codes=a_codes, a_scales=a_scales,
-                         h=h, amax_h=amax_h, gs_h=gs_h, hq_codes=hq_codes,
+                         h=h, amax_h=np.float32(amax_h), amax_h_own=amax_h_own, gs_h=gs_h,
+                         hq_codes=hq_codes,
                          hq_scales=hq_scales, y=y)
     return out
 

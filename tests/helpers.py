@@ -65,54 +65,89 @@ def bf16_round(x):
     return np.ldexp(np.rint(m * 256.0), e - 8)
 
 
-def check_forward(cfg, fwd, out, inter, what=""):
-    """The GPU forward against the oracle's forward.
+def _rows_np(t, rows):
+    """Rows of a (device or host) tensor or array as float64 / uint8 NumPy."""
+    if isinstance(t, torch.Tensor):
+        sel = t[torch.as_tensor(np.asarray(rows, dtype=np.int64), device=t.device)]
+        if sel.dtype == torch.bfloat16:
+            sel = sel.float()
+        a = sel.cpu().numpy()
+    else:
+        a = np.asarray(t)[np.asarray(rows, dtype=np.int64)]
+    return a.astype(np.float64) if a.dtype.kind == "f" else a
+
+
+def _scalar(v):
+    return v.item() if isinstance(v, torch.Tensor) else float(v)
+
+
+def check_forward(fwd, out, inter, experts, ids, topk_weights, tokens=None, what=""):
+    """The GPU forward against the oracle's forward, token by token.
+
+    ``inter`` holds the oracle's intermediates for the checked tokens: the
+    whole batch (``tokens`` None), or the sample ``tokens`` run through the
+    oracle with the whole batch's global amax values (``oracle.forward(...,
+    amax_x=..., amax_h=...)``).  ``ids`` / ``topk_weights`` are the whole
+    batch's routing inputs.
 
     The L1 output h is rounded to bf16 and then re-quantised to NVFP4; both
     are decisions.  The GPU accumulates L1 in fp32 and the oracle in float64,
     so a few h values can land one bf16 ulp apart, and an NVFP4 code or block
     scale of h decided from such a value can differ; that step is a
     discontinuity of the method, not an error of either side.  So:
-      * h meets the stated tolerance against the oracle's h before its bf16
-        rounding (assert_close_bf16), and at most 1e-3 of the valid h
-        elements differ from the oracle's rounded h;
-      * every row whose requantised codes or scales differ contains such an
-        h difference, and at most 1 % of the tokens (at least one) own one;
+      * h of every checked slot meets the stated tolerance against the
+        oracle's h before its bf16 rounding (assert_close_bf16), and at most
+        1e-3 of those h elements differ from the oracle's rounded h;
+      * every requantised block whose codes or scale differ contains such an
+        h difference, and at most 1 % of the checked tokens (at least one)
+        own one;
       * the output of every other token meets the stated tolerance against the
-        oracle's value before its final rounding (assert_close_bf16).
+        oracle's value before its final rounding (assert_close_bf16);
+      * each token that owns a flip is recomputed from the forward's own h
+        (check_sampled_tokens: its requantised rows bit-exact given the
+        forward's amax(h), then the oracle's L2 and combine), so no token goes
+        unchecked.
     """
     v = fwd.intermediates()
-    rt = inter["routing"]
-    R = int(rt.padded_offsets[-1])
-    valid = rt.row_src >= 0
-    got = bf16_to_np(out)
-    if R == 0:
+    ids = np.asarray(ids)
+    w = np.asarray(topk_weights)
+    T, k = ids.shape
+    tokens = np.arange(T) if tokens is None else np.asarray(tokens, dtype=np.int64)
+    rt = inter["routing"]  # the oracle's routing of the checked tokens
+    got_all = bf16_to_np(out)
+    got = got_all[tokens]
+    slot_gpu = _rows_np(v["slot_dst"], np.arange(T * k)).astype(np.int64).reshape(T, k)
+    g_rows = slot_gpu[tokens].reshape(-1)
+    o_rows = np.asarray(rt.slot_dst, dtype=np.int64).reshape(-1)
+    assert np.array_equal(g_rows >= 0, o_rows >= 0), f"{what}: skipped slots differ"
+    sel = o_rows >= 0
+    slot_tok = np.repeat(np.arange(tokens.size), k)[sel]  # index into tokens
+    g_rows, o_rows = g_rows[sel], o_rows[sel]
+    if g_rows.size == 0:
         assert_close_bf16(got, inter["out_f64"], what=what)
         return
-    # the forward writes valid rows only; padding rows of h hold whatever the
-    # workspace held (a pad row reaches only pad rows of each GEMM's result,
-    # which are never stored), so they are masked before the cast
-    h_gpu = np.where(valid[:, None], v["h"][:R].float().cpu().numpy(), 0.0).astype(np.float64)
-    h_or = inter["h"]
-    diff = (h_gpu != h_or) & valid[:, None]
-    assert_close_bf16(h_gpu[valid], inter["h_f64"][valid], what=what + " h")
-    assert diff.sum() <= max(1, 1e-3 * valid.sum() * h_or.shape[1]), f"{what}: {diff.sum()} h diffs"
-    hq = v["hq_codes"][:R].cpu().numpy()
-    hs = v["hq_sf"][:R].cpu().numpy()
-    K = h_or.shape[1]
-    code_flip = (hq != inter["hq_codes"]).reshape(R, K // 16, 8).any(axis=2)
-    scale_flip = hs != inter["hq_scales"]
-    block_flip = (code_flip | scale_flip) & valid[:, None]
-    h_block_diff = diff.reshape(R, K // 16, 16).any(axis=2)
+    h_gpu = _rows_np(v["h"], g_rows)
+    h_or = inter["h"][o_rows]
+    assert_close_bf16(h_gpu, inter["h_f64"][o_rows], what=what + " h")
+    diff = h_gpu != h_or
+    assert diff.sum() <= max(1, 1e-3 * diff.size), f"{what}: {diff.sum()} h diffs"
+    hq = _rows_np(v["hq_codes"], g_rows)
+    hs = _rows_np(v["hq_sf"], g_rows)
+    n, I = h_or.shape
+    code_flip = (hq != inter["hq_codes"][o_rows]).reshape(n, I // 16, 8).any(axis=2)
+    scale_flip = hs != inter["hq_scales"][o_rows]
+    block_flip = code_flip | scale_flip
+    h_block_diff = diff.reshape(n, I // 16, 16).any(axis=2)
     assert np.all(h_block_diff[block_flip]), f"{what}: a requant flip without an h difference"
-    T = got.shape[0]
-    k = rt.slot_dst.size // T
-    flip_rows = np.nonzero(block_flip.any(axis=1))[0]
-    flip_tokens = np.unique(rt.row_src[flip_rows] // k)
-    assert flip_tokens.size <= max(1, 0.01 * T), f"{what}: {flip_tokens.size} tokens with flips"
-    keep = np.ones(T, dtype=bool)
-    keep[flip_tokens] = False
+    flip_tok = np.unique(slot_tok[block_flip.any(axis=1)])
+    assert flip_tok.size <= max(1, 0.01 * tokens.size), f"{what}: {flip_tok.size} tokens with flips"
+    keep = np.ones(tokens.size, dtype=bool)
+    keep[flip_tok] = False
     assert_close_bf16(got[keep], inter["out_f64"][keep], what=what)
+    if flip_tok.size:
+        check_sampled_tokens(experts, ids, w, slot_gpu.reshape(-1), v["h"], v["hq_codes"],
+                             v["hq_sf"], _scalar(v["gs_h"]), _scalar(v["amax_h"]), got_all,
+                             tokens[flip_tok], what=what + " (tokens with a requant flip)")
     assert np.all(np.isfinite(got))
 
 
@@ -189,10 +224,12 @@ def check_sampled_tokens(experts, ids, topk_weights, slot_dst, h, hq_codes, hq_s
             r = int(slot_dst[int(t) * k + j])
             if r < 0:
                 continue
-            hc, hs, hg, _ = q.quantize(np.asarray(h[r:r + 1], np.float32), amax=amax_h)
+            hc, hs, hg, _ = q.quantize(_rows_np(h, [r]).astype(np.float32), amax=amax_h)
             assert hg == gs_h, f"{what}: gs_h {gs_h!r} vs {hg!r}"
-            assert np.array_equal(hq_codes[r], hc[0]), f"{what}: requantised codes of row {r}"
-            assert np.array_equal(hq_sf[r], hs[0]), f"{what}: requantised scales of row {r}"
+            assert np.array_equal(_rows_np(hq_codes, [r])[0], hc[0]), \
+                f"{what}: requantised codes of row {r}"
+            assert np.array_equal(_rows_np(hq_sf, [r])[0], hs[0]), \
+                f"{what}: requantised scales of row {r}"
             e = int(ids[t, j])
             if e not in w2:
                 ew = experts[e]

@@ -170,3 +170,99 @@ def test_pack_weight_codes_layout(cuda_lib):
     want = swz(c.reshape(rows // (2 * H), 2, H // 128, 128, K // 256, 128)
                .transpose(0, 2, 4, 1, 3, 5)).reshape(-1)
     assert np.array_equal(got, want)
+
+
+def _hist_experts(E, d, I, seed):
+    """Experts drawn like the workloads' (NVFP4 bytes from the fixed
+    histograms), with edge blocks planted in every matrix: all-zero block
+    scales (0x00), subnormal block scales (0x01..0x07), and blocks holding
+    the largest codes (+-6).  Returns (NumpyExperts, stacked torch dict)."""
+    from nvfp4_block_scaled_topk_gb300 import inputs
+    from helpers import NumpyExperts
+
+    cfg = inputs.MoEConfig("gemm_edges", E, 1, d, I, 1, "uniform", seed=seed)
+    rng = np.random.default_rng(seed)
+    ws = []
+    for e in range(E):
+        w = {k: v.numpy().copy() for k, v in inputs.make_expert(cfg, e).items()}
+        for cname, sname in (("w13_codes", "w13_scales"), ("w2_codes", "w2_scales")):
+            sc, co = w[sname], w[cname]
+            n = sc.size // 50
+            flat = rng.choice(sc.size, size=3 * n, replace=False)
+            sc.reshape(-1)[flat[:n]] = 0
+            sc.reshape(-1)[flat[n:2 * n]] = rng.integers(1, 8, size=n)
+            rows, blk = np.unravel_index(flat[2 * n:], sc.shape)
+            for r, b in zip(rows, blk):
+                co[r, 8 * b:8 * b + 8] = rng.choice([0x77, 0xFF, 0x7F, 0xF7], size=8)
+        w["w2_gs"] = np.float32(w["w2_gs"][0])
+        ws.append(w)
+    stacked = dict(
+        w13_codes=torch.from_numpy(np.stack([w["w13_codes"] for w in ws])),
+        w13_scales=torch.from_numpy(np.stack([w["w13_scales"] for w in ws])),
+        w13_gs=torch.from_numpy(np.stack([w["w13_gs"] for w in ws])),
+        w2_codes=torch.from_numpy(np.stack([w["w2_codes"] for w in ws])),
+        w2_scales=torch.from_numpy(np.stack([w["w2_scales"] for w in ws])),
+        w2_gs=torch.from_numpy(np.array([w["w2_gs"] for w in ws], np.float32)),
+    )
+    return NumpyExperts(ws, d, I), stacked
+
+
+def _edge_rows(rng, rt, R, K):
+    """Token rows (padded-row order) ~ N(0, 0.09) with one outlier at 8 and,
+    in some rows, an all-zero block and a block small enough (1e-4) for a
+    subnormal block scale; quantised by the oracle."""
+    x = bf16_tensor(rng, (R, K), 0.09).float().numpy()
+    valid = np.nonzero(rt.row_src >= 0)[0]
+    x[valid[0], 5] = 8.0
+    for r in valid[::7]:
+        b = rng.integers(0, K // 16, size=2)
+        x[r, 16 * b[0]:16 * b[0] + 16] = 0.0
+        x[r, 16 * b[1]:16 * b[1] + 16] = bf16_tensor(rng, (16,), 1e-4).float().numpy()
+    x[rt.row_src < 0] = 0
+    c, s, g, _ = q.quantize(x)
+    assert (s[valid] == 0).any() and ((s[valid] > 0) & (s[valid] < 8)).any()
+    return c, s, g
+
+
+@pytest.mark.parametrize("which", ["w13", "w2"])
+def test_grouped_gemm_real_shape_tile128_several_tiles(cuda_lib, which):
+    """The prefill path's GEMM configuration: token tile 128 at the MegaMoE
+    shapes (L1: K = 7168, 28 K steps; L2: K = 2048, 8 K steps, so the stage
+    ring wraps many times), experts holding 3, 2, 1 and 0 token tiles with
+    ragged tails, and edge blocks in weights and activations."""
+    from nvfp4_block_scaled_topk_gb300 import megamoe
+
+    E, d, I = 4, 7168, 2048
+    counts = [300, 0, 129, 1]
+    rng = np.random.default_rng(90)
+    ex, stacked = _hist_experts(E, d, I, seed=91)
+    ids = np.concatenate([np.full(c, e) for e, c in enumerate(counts)])
+    rng.shuffle(ids)
+    rt = oracle.route(ids.reshape(-1, 1), E, 32)
+    R = int(rt.padded_offsets[-1])
+    K = d if which == "w13" else I
+    ac, asc, ag = _edge_rows(rng, rt, R, K)
+    wcodes, wsc, wgs = _dev_weights(stacked, which, megamoe)
+    if which == "w2":
+        wgs = wgs.view(-1, 1)
+    epi = megamoe.EPI_SILU_MUL if which == "w13" else megamoe.EPI_F32
+    out, amax = megamoe.grouped_gemm(
+        torch.from_numpy(ac).cuda(), torch.from_numpy(np.ascontiguousarray(asc)).cuda(),
+        torch.tensor([float(ag)], dtype=torch.float32).cuda(), wcodes, wsc, wgs,
+        torch.from_numpy(rt.offsets.astype(np.int32)).cuda(),
+        torch.from_numpy(rt.padded_offsets.astype(np.int32)).cuda(), epi, tile_n=128)
+    torch.cuda.synchronize()
+    got = out.float().cpu().numpy().astype(np.float64)
+    v = rt.row_src >= 0
+    if which == "w13":
+        gu = oracle.grouped_gemm(ac, asc, ag, ex, "w13", rt, "f32")
+        h64 = oracle.silu(gu[v][:, :I]) * gu[v][:, I:]
+        assert_close_bf16(got[v], h64, what="L1 tile 128")
+        want_h, want_amax = oracle.grouped_gemm(ac, asc, ag, ex, "w13", rt, "silu_mul")
+        assert np.mean(got[v] == want_h[v]) > 0.99
+        assert abs(amax.item() - float(want_amax)) <= 2 ** -7 * float(want_amax)
+    else:
+        want = oracle.grouped_gemm(ac, asc, ag, ex, "w2", rt, "f32")
+        err, _ = assert_close(got[v], want[v], what="L2 tile 128")
+        assert err < 1e-5  # identical operands: only fp32 accumulation differs
+        assert np.all(np.isnan(got[~v]))  # padding rows untouched

@@ -31,6 +31,7 @@ def test_wait_that_runs_out_sets_timeout_and_context_survives(cuda_lib):
     # the context is intact: the next forward is correct and clean
     out = fwd(x.cuda(), ids.cuda(), w.cuda())
     assert fwd.read_status() == 0
-    _, inter = oracle.forward(x.float().numpy(), ids.numpy(), w.numpy(),
-                              inputs.ExpertSet(cfg, raw), pad=32, return_intermediates=True)
-    check_forward(cfg, fwd, out, inter, what="after timeout")
+    ex = inputs.ExpertSet(cfg, raw)
+    _, inter = oracle.forward(x.float().numpy(), ids.numpy(), w.numpy(), ex, pad=32,
+                              return_intermediates=True)
+    check_forward(fwd, out, inter, ex, ids.numpy(), w.numpy(), what="after timeout")

@@ -84,7 +84,7 @@ def test_forward_with_shared_expert(cuda_lib, name, pad):
     w_gpu = w.cpu().numpy()
     _, inter = oracle.forward(x.float().numpy(), ids_o, w_gpu, experts, pad=pad,
                               return_intermediates=True)
-    check_forward(cfg, fwd, out, inter, what=cfg.name)
+    check_forward(fwd, out, inter, experts, ids_o, w_gpu, what=cfg.name)
     routed = inputs.ExpertSet(replace(base), raw)
     _, out64 = oracle.forward_with_shared(x.float().numpy(), ids_o[:, :base.k],
                                           w_gpu[:, :base.k], routed, experts[base.E], pad=pad)
@@ -126,3 +126,28 @@ def test_forward_from_logits_equals_router_then_forward(cuda_lib, name, T):
     out_c = fwd_c(x, ids2, w2).clone()
     out_d = megamoe.Forward(weights, base.T, base.k, pad=32).from_logits(x, logits, base.k, bias)
     assert torch.equal(out_c, out_d)
+
+
+@pytest.mark.parametrize("name", ["tiny", "decode"])
+def test_forward_from_logits_matches_oracle(cuda_lib, name):
+    """The layer from router logits (router fused ahead of the routing, one
+    shared expert) against the oracle alone: the oracle's router picks the
+    ids and weights, the oracle's forward runs on them, and the whole output
+    and every stage of the fused call meet the forward checks."""
+    base = inputs.CONFIGS[name]
+    cfg = inputs.with_shared_expert(base)
+    torch.cuda.empty_cache()
+    raw = inputs.make_all_experts(cfg, device="cuda")
+    weights = megamoe.Weights.prepare(raw)
+    x = inputs.make_activations(base)
+    logits, bias = inputs.make_router_logits(base)
+    fwd = megamoe.Forward(weights, base.T, cfg.k, pad=32)
+    out = fwd.from_logits(x.cuda(), logits.cuda(), base.k,
+                          None if bias is None else bias.cuda(), shared_expert=base.E)
+    assert fwd.read_status() == 0
+    ids_o, w_o = oracle.router_topk(logits.numpy(), base.k,
+                                    None if bias is None else bias.numpy(), shared_expert=base.E)
+    experts = inputs.ExpertSet(cfg, raw)
+    _, inter = oracle.forward(x.float().numpy(), ids_o, w_o, experts, pad=32,
+                              return_intermediates=True)
+    check_forward(fwd, out, inter, experts, ids_o, w_o, what=f"{name} from logits")

@@ -319,3 +319,32 @@ def test_shared_expert_dense_equals_one_more_routed_expert():
         r0, r1 = int(rt.padded_offsets[E]), int(rt.padded_offsets[E] + rt.counts[E])
         shared_amax = np.float32(np.abs(inter["h"][r0:r1]).max())
         assert (shared_amax == inter["amax_h"]) == (boost > 1)
+
+
+def test_token_sample_with_the_batch_global_scales_reproduces_the_batch():
+    """A token's output depends on the rest of the batch only through the two
+    global scales (one per tensor): the forward over a sample of the tokens,
+    given the whole batch's amax of x and of h, equals the whole batch's
+    forward on those tokens (bit for bit after the bf16 rounding); measured
+    over the sample alone, the
+    scales (and so the outputs) differ, because the sample leaves out the
+    token holding the batch's amax."""
+    rng = np.random.default_rng(11)
+    d, I, T, k, E = 64, 32, 16, 2, 4
+    ex = _rand_experts(rng, E, d, I)
+    x = q.bf16_round(rng.standard_normal((T, d)) * 0.3).astype(np.float32)
+    x[5, 3] = 4.0  # the batch's amax of x sits in token 5
+    ids = np.stack([rng.permutation(E)[:k] for _ in range(T)])
+    w = _softmax_rows(rng.standard_normal((T, k)))
+    full, inter = oracle.forward(x, ids, w, ex, pad=8, return_intermediates=True)
+    sample = np.array([0, 2, 3, 9, 14])
+    sub, sub_inter = oracle.forward(x[sample], ids[sample], w[sample], ex, pad=8,
+                                    return_intermediates=True, amax_x=inter["amax_x"],
+                                    amax_h=inter["amax_h"])
+    assert sub_inter["gs_x"] == inter["gs_x"] and sub_inter["gs_h"] == inter["gs_h"]
+    assert np.array_equal(sub, full[sample])
+    # float64 sums agree to BLAS blocking order
+    np.testing.assert_allclose(sub_inter["out_f64"], inter["out_f64"][sample], rtol=0,
+                               atol=1e-12 * np.abs(inter["out_f64"]).max())
+    own = oracle.forward(x[sample], ids[sample], w[sample], ex, pad=8)
+    assert not np.array_equal(own, full[sample])

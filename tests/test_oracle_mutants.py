@@ -63,9 +63,12 @@ MUTANTS = {
                                 'w["w13_scales"][:I], w["w13_gs"][1])'),
     "combine weight index": ("moe", "acc = acc + w[t, j] * y[r]", "acc = acc + w[t, 0] * y[r]"),
     "gather by slot modulo k": ("moe", "valid = rt.row_src >= 0\n    a_codes[valid] = xq_codes[rt.row_src[valid] // k]\n"
-                                "    a_scales[valid] = xq_scales[rt.row_src[valid] // k]\n\n    h, amax_h, h64",
+                                "    a_scales[valid] = xq_scales[rt.row_src[valid] // k]\n\n    h, amax_h_own, h64",
                                 "valid = rt.row_src >= 0\n    a_codes[valid] = xq_codes[rt.row_src[valid] % k]\n"
-                                "    a_scales[valid] = xq_scales[rt.row_src[valid] % k]\n\n    h, amax_h, h64"),
+                                "    a_scales[valid] = xq_scales[rt.row_src[valid] % k]\n\n    h, amax_h_own, h64"),
+    "sample ignores the batch's amax of x": ("moe", "quantize(x, amax=amax_x)", "quantize(x)"),
+    "sample ignores the batch's amax of h": ("moe", "    if amax_h is None:\n        amax_h = amax_h_own",
+                                             "    amax_h = amax_h_own"),
     "expert rows shifted by one": ("moe", "out[r0:r0 + m] = ahat[r0:r0 + m] @ wm.T",
                                    "out[r0:r0 + m] = np.roll(ahat, 1, axis=0)[r0:r0 + m] @ wm.T"),
     "combine not rounded": ("moe", "    out = bf16_round(out64)\n", "    out = out64\n"),
