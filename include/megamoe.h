@@ -237,8 +237,14 @@ megamoe_status megamoe_pack_weight_codes(const uint8_t* src, int64_t rows, int K
  *                         out_amax (device float, zeroed here) = max |out| over
  *                         valid rows.
  * Padding rows of `out` are not written.  tile_n selects the token tile
- * (32, 64 or 128; 0 = choose from the expected tokens per expert,
- * expected_tokens = rows the caller expects per active expert, may be 0).
+ * (0 = choose from the expected tokens per expert, expected_tokens = rows the
+ * caller expects per active expert, may be 0):
+ *   32, 64, 128  every tile of an expert is tile_n rows wide;
+ *   192, 256     wide tiles: expert e's rows are cut into ceil(count_e / W)
+ *                tiles of equal width (a multiple of 32), W = tile_n for the
+ *                F32 and BF16 epilogues and W = 160 for SILU_MUL (whose two
+ *                accumulators fill tensor memory), so a short tail costs no
+ *                extra pass over the expert's weights.
  * Requires N a multiple of 128 (256 for SILU_MUL), K a multiple of 256,
  * 1 <= E <= 1024, 16-byte aligned pointers, ld_out >= output width and a
  * multiple of 16 bytes (4 floats, 8 bf16), else MEGAMOE_ERR_UNSUPPORTED_SHAPE.
@@ -377,6 +383,55 @@ megamoe_status megamoe_forward(const megamoe_weights* w, const uint16_t* x,
  * diagnosis; the default never fires in normal operation.
  */
 void megamoe_set_wait_limit_ns(uint64_t ns);
+
+/*
+ * Expert-parallel forward, one shard (one process and GPU) of G: the shard
+ * holds experts [expert_base, expert_base + w_shard->num_experts) of
+ * num_experts_total ("CURRENT_BUG.md -- DeepSeek-V4 Blackwell NVFP4", "Test
+ * Plan -- Finding the NaN", Phase 2: the EP8 slice of 48 of the 384 experts).
+ * The layer's tokens are first gathered on every shard (x, topk_ids and
+ * topk_weights of all T tokens, global expert ids); then:
+ *
+ *   megamoe_ep_forward_begin  routes the shard's slots (ids of other shards
+ *     skipped, ids >= num_experts_total flagged MEGAMOE_DEV_BAD_EXPERT_ID and
+ *     skipped), takes amax(x) over all T tokens (the same on every shard, so
+ *     x's global scale needs no exchange), quantises x and runs the L1 GEMM
+ *     with SiLU(gate)*up; the shard's amax(h) is left as a float at bytes
+ *     [12, 16) of ws.
+ *   The caller replaces that float on every shard by the maximum over all
+ *     shards (an all-reduce(max) of 4 bytes): h has one global scale over
+ *     every valid row of the layer's intermediate, whichever shard holds it.
+ *   megamoe_ep_forward_end  requantises h with that global amax, runs the L2
+ *     GEMM and writes out_partial [T, d] fp32 = sum over the shard's slots j
+ *     (ascending) of topk_weights[t, j] * y (0 for tokens with no slot on the
+ *     shard), before any rounding.
+ *   The caller sums the shards' out_partial (an all-reduce or reduce-scatter)
+ *     and rounds once with megamoe_round_bf16.
+ *
+ * With the same inputs the result equals megamoe_forward's up to the order of
+ * the fp32 additions across shards.  w_shard, T, k, pad and ws are those of
+ * megamoe_forward on the shard's experts (ws: megamoe_workspace_size(T, k,
+ * w_shard->num_experts, d, I, pad) bytes, 256-byte aligned, the same buffer
+ * for begin and end); out_partial is 16-byte aligned.  Errors as
+ * megamoe_forward, plus MEGAMOE_ERR_INVALID_ARG when the shard's range does
+ * not fit in [0, num_experts_total).
+ */
+megamoe_status megamoe_ep_forward_begin(const megamoe_weights* w_shard, const uint16_t* x,
+                                        const int32_t* topk_ids, int T, int k, int expert_base,
+                                        int num_experts_total, int pad, void* ws, size_t ws_bytes,
+                                        megamoe_stream_t stream);
+megamoe_status megamoe_ep_forward_end(const megamoe_weights* w_shard, const float* topk_weights,
+                                      int T, int k, int num_experts_total, int pad,
+                                      float* out_partial, void* ws, size_t ws_bytes,
+                                      megamoe_stream_t stream);
+
+/*
+ * megamoe_round_bf16 -- out[i] = bf16(in[i]), round to nearest even, i < n
+ * (the single rounding of the expert-parallel sum).  n a multiple of 4, in
+ * 16-byte and out 8-byte aligned, else MEGAMOE_ERR_UNSUPPORTED_SHAPE.
+ */
+megamoe_status megamoe_round_bf16(const float* in, int64_t n, uint16_t* out,
+                                  megamoe_stream_t stream);
 
 /*
  * megamoe_read_status -- synchronise `stream`, copy the device status word at

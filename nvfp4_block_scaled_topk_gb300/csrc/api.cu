@@ -56,7 +56,8 @@ int tile_n_setting(double expected) {
     const char* e = std::getenv("MEGAMOE_TILE_N");
     return (e && *e) ? std::atoi(e) : 0;
   }();
-  if (forced == 32 || forced == 64 || forced == 128) return forced;
+  if (forced == 32 || forced == 64 || forced == 128 || forced == 192 || forced == 256)
+    return forced;
   return pick_tile_n(expected);
 }
 
@@ -144,9 +145,7 @@ megamoe_status check_route_args(int T, int k, int E, int pad) {
 
 namespace megamoe {
 
-megamoe_status check_forward_args(const megamoe_weights* w, const uint16_t* x,
-                                  const int32_t* topk_ids, const float* topk_weights, int T, int k,
-                                  int pad, const uint16_t* out, bool router) {
+megamoe_status check_forward_shape(const megamoe_weights* w, int T, int k, int pad) {
   if (!w) return MEGAMOE_ERR_INVALID_ARG;
   const int E = w->num_experts, d = w->hidden, I = w->intermediate;
   megamoe_status st = check_route_args(T, k, E, pad);
@@ -156,11 +155,20 @@ megamoe_status check_forward_args(const megamoe_weights* w, const uint16_t* x,
   if (!w->w13_codes || !w->w13_scales || !w->w13_gs || !w->w2_codes || !w->w2_scales ||
       !w->w2_gs)
     return MEGAMOE_ERR_INVALID_ARG;
+  if (!aligned(w->w13_codes, 16) || !aligned(w->w2_codes, 16) || !aligned(w->w13_scales, 16) ||
+      !aligned(w->w2_scales, 16))
+    return MEGAMOE_ERR_UNSUPPORTED_SHAPE;
+  return MEGAMOE_OK;
+}
+
+megamoe_status check_forward_args(const megamoe_weights* w, const uint16_t* x,
+                                  const int32_t* topk_ids, const float* topk_weights, int T, int k,
+                                  int pad, const uint16_t* out, bool router) {
+  megamoe_status st = check_forward_shape(w, T, k, pad);
+  if (st != MEGAMOE_OK) return st;
   if (T > 0 && (!x || (!router && (!topk_ids || !topk_weights)) || !out))
     return MEGAMOE_ERR_INVALID_ARG;
-  if ((x && !aligned(x, 16)) || (out && !aligned(out, 8)) || !aligned(w->w13_codes, 16) ||
-      !aligned(w->w2_codes, 16) || !aligned(w->w13_scales, 16) || !aligned(w->w2_scales, 16))
-    return MEGAMOE_ERR_UNSUPPORTED_SHAPE;
+  if ((x && !aligned(x, 16)) || (out && !aligned(out, 8))) return MEGAMOE_ERR_UNSUPPORTED_SHAPE;
   return MEGAMOE_OK;
 }
 
@@ -273,7 +281,9 @@ megamoe_status megamoe_grouped_gemm(const uint8_t* act_codes, const uint8_t* act
   if (static_cast<int64_t>(E) * N * (K / 256) >= (int64_t{1} << 31) ||
       act_rows >= (int64_t{1} << 31))
     return MEGAMOE_ERR_UNSUPPORTED_SHAPE;
-  if (tile_n != 0 && tile_n != 32 && tile_n != 64 && tile_n != 128) return MEGAMOE_ERR_INVALID_ARG;
+  if (tile_n != 0 && tile_n != 32 && tile_n != 64 && tile_n != 128 && tile_n != 192 &&
+      tile_n != 256)
+    return MEGAMOE_ERR_INVALID_ARG;
   const int width = epilogue == MEGAMOE_EPI_SILU_MUL ? N / 2 : N;
   if (ld_out < width) return MEGAMOE_ERR_INVALID_ARG;
   // output rows start on 16-byte boundaries: the epilogue stores 16-byte vectors
@@ -315,7 +325,7 @@ megamoe_status megamoe_combine(const float* y, int64_t ld_y, const int32_t* slot
   if (T > 0 && (!y || !slot_dst || !topk_weights || !out)) return MEGAMOE_ERR_INVALID_ARG;
   if (T > 0 && (!aligned(y, 16) || !aligned(out, 8))) return MEGAMOE_ERR_UNSUPPORTED_SHAPE;
   return cuda_status(
-      launch_combine(y, ld_y, slot_dst, topk_weights, T, k, d, out,
+      launch_combine(y, ld_y, slot_dst, topk_weights, T, k, d, out, false,
                      reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -330,29 +340,15 @@ namespace {
 
 // The forward; with `router` the ids and weights are computed here from the
 // router logits (into the workspace) instead of being passed in.
-megamoe_status forward_impl(const megamoe_weights* w, const uint16_t* x, const int32_t* topk_ids,
-                            const float* topk_weights, int T, int k, int pad, uint16_t* out,
-                            void* ws, size_t ws_bytes, cudaStream_t s, RouterArgs* router) {
-  megamoe_status st =
-      megamoe::check_forward_args(w, x, topk_ids, topk_weights, T, k, pad, out, router != nullptr);
-  if (st != MEGAMOE_OK) return st;
-  if (!ws || !aligned(ws, 256)) return MEGAMOE_ERR_INVALID_ARG;
+// Steps 0-4 of the forward: (router,) route, amax of x, quantise x into its
+// routed rows, L1 gate+up grouped GEMM with SiLU(gate)*up -> bf16 h and
+// amax(h).  `expected` is the caller's expected rows per expert (the token
+// tile's choice).
+cudaError_t forward_l1(const megamoe_weights* w, const uint16_t* x, const int32_t* topk_ids,
+                       int T, int k, int pad, const Workspace& wk, cudaStream_t s,
+                       RouterArgs* router, int tile_n) {
   const int E = w->num_experts, d = w->hidden, I = w->intermediate;
-  Workspace wk = carve(ws, T, k, E, d, I, pad);
-  if (ws_bytes < wk.bytes) return MEGAMOE_ERR_WORKSPACE_TOO_SMALL;
-
-  if (T == 0) return cudaMemsetAsync(wk.status, 0, 256, s) == cudaSuccess ? MEGAMOE_OK
-                                                                         : MEGAMOE_ERR_CUDA;
-  const double expected = static_cast<double>(T) * k / E;
-  const int tile_n = tile_n_setting(expected);
-
   cudaError_t e = cudaSuccess;
-  if (router) {  // the ids and weights land in the workspace
-    router->ids_out = wk.r_ids;
-    router->w_out = wk.r_w;
-    topk_ids = wk.r_ids;
-    topk_weights = wk.r_w;
-  }
   // 0-3. (router,) route (its first act clears the status word and the amax
   //      accumulators), amax of x, quantise x into its routed rows.  Padding
   //      rows are left as they are: each output column of the grouped GEMM
@@ -367,16 +363,16 @@ megamoe_status forward_impl(const megamoe_weights* w, const uint16_t* x, const i
     if (router)
       e = launch_router(router->logits, T, router->n_logits, router->ld, router->bias,
                         router->k_routed, router->shared, wk.r_ids, wk.r_w, s);
-    if (e != cudaSuccess) return MEGAMOE_ERR_CUDA;
+    if (e != cudaSuccess) return e;
     e = launch_route(topk_ids, T * k, E, pad, wk.counts, wk.offsets, wk.padded_offsets,
                      wk.row_src, wk.rows, wk.slot_dst, wk.status, wk.status, 5, s);
-    if (e != cudaSuccess) return MEGAMOE_ERR_CUDA;
+    if (e != cudaSuccess) return e;
     e = launch_amax(x, T, d, d, wk.amax_x, wk.status, false, s);
   }
-  if (e != cudaSuccess) return MEGAMOE_ERR_CUDA;
+  if (e != cudaSuccess) return e;
   e = launch_quant(x, T, d, d, wk.slot_dst, k, nullptr, wk.padded_offsets + E, wk.rows,
                    wk.amax_x, wk.gs_x, wk.xq_codes, wk.xq_sf, MEGAMOE_SCALES_ROWMAJOR, s);
-  if (e != cudaSuccess) return MEGAMOE_ERR_CUDA;
+  if (e != cudaSuccess) return e;
   // 4. L1 gate+up grouped GEMM, SiLU(gate)*up -> bf16 h, amax(h)
   GemmLaunch g{};
   g.act_codes = wk.xq_codes;
@@ -403,33 +399,97 @@ megamoe_status forward_impl(const megamoe_weights* w, const uint16_t* x, const i
   g.ksplit = wk.ks1;
   g.partial = wk.partial;
   g.partial_plane = static_cast<int64_t>(T) * k * 2 * I;
-  e = launch_grouped_gemm(g, s);
-  if (e != cudaSuccess) return MEGAMOE_ERR_CUDA;
+  return launch_grouped_gemm(g, s);
+}
+
+// Steps 5-7: requantise h with gs from the amax(h) held in the workspace, L2
+// down grouped GEMM -> fp32 y, top-k weighted combine (bf16 out, or the fp32
+// sum before its rounding with out_f32).
+cudaError_t forward_l2(const megamoe_weights* w, const float* topk_weights, int T, int k,
+                       void* out, bool out_f32, const Workspace& wk, cudaStream_t s,
+                       int tile_n) {
+  const int E = w->num_experts, d = w->hidden, I = w->intermediate;
   // 5. requantise the valid rows of h with gs from amax(h) (slot by slot)
-  e = launch_quant(wk.h, static_cast<int64_t>(T) * k, I, I, wk.slot_dst, 1, nullptr,
-                   wk.padded_offsets + E, wk.rows, wk.amax_h, wk.gs_h, wk.hq_codes, wk.hq_sf,
-                   MEGAMOE_SCALES_ROWMAJOR, s, /*slot_rows=*/true);
-  if (e != cudaSuccess) return MEGAMOE_ERR_CUDA;
+  cudaError_t e = launch_quant(wk.h, static_cast<int64_t>(T) * k, I, I, wk.slot_dst, 1, nullptr,
+                               wk.padded_offsets + E, wk.rows, wk.amax_h, wk.gs_h, wk.hq_codes,
+                               wk.hq_sf, MEGAMOE_SCALES_ROWMAJOR, s, /*slot_rows=*/true);
+  if (e != cudaSuccess) return e;
   // 6. L2 down grouped GEMM -> fp32 y
+  GemmLaunch g{};
   g.act_codes = wk.hq_codes;
   g.act_scales = wk.hq_sf;
   g.act_gs = wk.gs_h;
+  g.act_rows = wk.rows;
   g.w_codes = w->w2_codes;
   g.w_scales = w->w2_scales;
   g.w_gs = w->w2_gs;
+  g.E = E;
   g.N = d;
   g.K = I;
+  g.offsets = wk.offsets;
+  g.padded_offsets = wk.padded_offsets;
   g.epilogue = MEGAMOE_EPI_F32;
   g.out = wk.y;
   g.ld_out = d;
   g.out_amax = nullptr;
+  g.tile_n = tile_n;
+  g.status = wk.status;
+  g.early_weights = true;
   g.ksplit = wk.ks2;
+  g.partial = wk.partial;
   g.partial_plane = static_cast<int64_t>(T) * k * d;
   e = launch_grouped_gemm(g, s);
-  if (e != cudaSuccess) return MEGAMOE_ERR_CUDA;
+  if (e != cudaSuccess) return e;
   // 7. top-k weighted combine
-  e = launch_combine(wk.y, d, wk.slot_dst, topk_weights, T, k, d, out, s);
+  return launch_combine(wk.y, d, wk.slot_dst, topk_weights, T, k, d, out, out_f32, s);
+}
+
+// The forward; with `router` the ids and weights are computed here from the
+// router logits (into the workspace) instead of being passed in.
+megamoe_status forward_impl(const megamoe_weights* w, const uint16_t* x, const int32_t* topk_ids,
+                            const float* topk_weights, int T, int k, int pad, uint16_t* out,
+                            void* ws, size_t ws_bytes, cudaStream_t s, RouterArgs* router) {
+  megamoe_status st =
+      megamoe::check_forward_args(w, x, topk_ids, topk_weights, T, k, pad, out, router != nullptr);
+  if (st != MEGAMOE_OK) return st;
+  if (!ws || !aligned(ws, 256)) return MEGAMOE_ERR_INVALID_ARG;
+  const int E = w->num_experts, d = w->hidden, I = w->intermediate;
+  Workspace wk = carve(ws, T, k, E, d, I, pad);
+  if (ws_bytes < wk.bytes) return MEGAMOE_ERR_WORKSPACE_TOO_SMALL;
+
+  if (T == 0) return cudaMemsetAsync(wk.status, 0, 256, s) == cudaSuccess ? MEGAMOE_OK
+                                                                         : MEGAMOE_ERR_CUDA;
+  const int tile_n = tile_n_setting(static_cast<double>(T) * k / E);
+  if (router) {  // the ids and weights land in the workspace
+    router->ids_out = wk.r_ids;
+    router->w_out = wk.r_w;
+    topk_ids = wk.r_ids;
+    topk_weights = wk.r_w;
+  }
+  cudaError_t e = forward_l1(w, x, topk_ids, T, k, pad, wk, s, router, tile_n);
+  if (e == cudaSuccess) e = forward_l2(w, topk_weights, T, k, out, false, wk, s, tile_n);
   return cuda_status(e);
+}
+
+// Checks and workspace of one expert-parallel shard (the shard's weights hold
+// its experts only; ids are global).
+megamoe_status ep_setup(const megamoe_weights* w, int T, int k, int expert_base,
+                        int num_experts_total, int pad, void* ws, size_t ws_bytes, Workspace* wk) {
+  megamoe_status st = megamoe::check_forward_shape(w, T, k, pad);
+  if (st != MEGAMOE_OK) return st;
+  if (expert_base < 0 || num_experts_total < 1 || num_experts_total > MEGAMOE_MAX_EXPERTS ||
+      static_cast<int64_t>(expert_base) + w->num_experts > num_experts_total)
+    return MEGAMOE_ERR_INVALID_ARG;
+  if (!ws || !aligned(ws, 256)) return MEGAMOE_ERR_INVALID_ARG;
+  *wk = carve(ws, T, k, w->num_experts, w->hidden, w->intermediate, pad);
+  if (ws_bytes < wk->bytes) return MEGAMOE_ERR_WORKSPACE_TOO_SMALL;
+  return MEGAMOE_OK;
+}
+
+// Token tile of a shard: the expected rows per expert of the whole layer
+// (each shard holds E / G experts and receives about T k / G of the slots).
+int ep_tile_n(int T, int k, int num_experts_total) {
+  return tile_n_setting(static_cast<double>(T) * k / num_experts_total);
 }
 
 }  // namespace
@@ -442,6 +502,51 @@ megamoe_status megamoe_forward(const megamoe_weights* w, const uint16_t* x,
                                megamoe_stream_t stream) {
   return forward_impl(w, x, topk_ids, topk_weights, T, k, pad, out, ws, ws_bytes,
                       reinterpret_cast<cudaStream_t>(stream), nullptr);
+}
+
+megamoe_status megamoe_ep_forward_begin(const megamoe_weights* w_shard, const uint16_t* x,
+                                        const int32_t* topk_ids, int T, int k, int expert_base,
+                                        int num_experts_total, int pad, void* ws, size_t ws_bytes,
+                                        megamoe_stream_t stream) {
+  Workspace wk{};
+  megamoe_status st =
+      ep_setup(w_shard, T, k, expert_base, num_experts_total, pad, ws, ws_bytes, &wk);
+  if (st != MEGAMOE_OK) return st;
+  if (T > 0 && (!x || !topk_ids)) return MEGAMOE_ERR_INVALID_ARG;
+  if (x && !aligned(x, 16)) return MEGAMOE_ERR_UNSUPPORTED_SHAPE;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (T == 0) return cudaMemsetAsync(wk.status, 0, 256, s) == cudaSuccess ? MEGAMOE_OK
+                                                                         : MEGAMOE_ERR_CUDA;
+  // global ids -> this shard's local ids (other shards' experts skipped)
+  cudaError_t e = launch_ep_remap(topk_ids, static_cast<int64_t>(T) * k, expert_base,
+                                  w_shard->num_experts, num_experts_total, wk.r_ids, s);
+  if (e == cudaSuccess)
+    e = forward_l1(w_shard, x, wk.r_ids, T, k, pad, wk, s, nullptr,
+                   ep_tile_n(T, k, num_experts_total));
+  return cuda_status(e);
+}
+
+megamoe_status megamoe_ep_forward_end(const megamoe_weights* w_shard, const float* topk_weights,
+                                      int T, int k, int num_experts_total, int pad,
+                                      float* out_partial, void* ws, size_t ws_bytes,
+                                      megamoe_stream_t stream) {
+  Workspace wk{};
+  megamoe_status st = ep_setup(w_shard, T, k, 0, num_experts_total, pad, ws, ws_bytes, &wk);
+  if (st != MEGAMOE_OK) return st;
+  if (T > 0 && (!topk_weights || !out_partial)) return MEGAMOE_ERR_INVALID_ARG;
+  if (out_partial && !aligned(out_partial, 16)) return MEGAMOE_ERR_UNSUPPORTED_SHAPE;
+  if (T == 0) return MEGAMOE_OK;
+  return cuda_status(forward_l2(w_shard, topk_weights, T, k, out_partial, true, wk,
+                                reinterpret_cast<cudaStream_t>(stream),
+                                ep_tile_n(T, k, num_experts_total)));
+}
+
+megamoe_status megamoe_round_bf16(const float* in, int64_t n, uint16_t* out,
+                                  megamoe_stream_t stream) {
+  if (n < 0 || (n > 0 && (!in || !out))) return MEGAMOE_ERR_INVALID_ARG;
+  if (n % 4 != 0 || (in && !aligned(in, 16)) || (out && !aligned(out, 8)))
+    return MEGAMOE_ERR_UNSUPPORTED_SHAPE;
+  return cuda_status(launch_round_bf16(in, n, out, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 megamoe_status megamoe_forward_from_logits(const megamoe_weights* w, const uint16_t* x,

@@ -3,7 +3,9 @@
 // "Test Plan -- Finding the NaN", Phase 1).  One thread per 4 consecutive
 // features of one token: 128-bit loads of each routed row of y (up to eight
 // slots' loads in flight at once), fp32 sums in ascending j, one bf16
-// rounding, 64-bit stores.
+// rounding, 64-bit stores.  An expert-parallel shard writes the fp32 sum of
+// its own slots instead, and the shards' sums are added and rounded once
+// after the exchange (k_round_bf16).
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -12,10 +14,11 @@
 
 namespace megamoe {
 
+template <bool F32_OUT>
 __global__ void __launch_bounds__(256) k_combine(const float* __restrict__ y, int64_t ld_y,
                                                  const int32_t* __restrict__ slot_dst,
                                                  const float* __restrict__ w, int T, int k, int d,
-                                                 uint16_t* __restrict__ out) {
+                                                 void* __restrict__ out) {
   pdl_wait();
   pdl_trigger();
   const int vecs = d / 4;
@@ -50,25 +53,60 @@ __global__ void __launch_bounds__(256) k_combine(const float* __restrict__ y, in
         acc.w = fmaf(wt[j], yv[j].w, acc.w);
       }
     }
+    if (F32_OUT) {  // the sum before its rounding (one shard's share of the output)
+      reinterpret_cast<float4*>(static_cast<float*>(out) + static_cast<int64_t>(t) * d)[v] = acc;
+      continue;
+    }
     const __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
     const __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
     uint2 pk;
     pk.x = *reinterpret_cast<const uint32_t*>(&lo);
     pk.y = *reinterpret_cast<const uint32_t*>(&hi);
-    reinterpret_cast<uint2*>(out + static_cast<int64_t>(t) * d)[v] = pk;
+    reinterpret_cast<uint2*>(static_cast<uint16_t*>(out) + static_cast<int64_t>(t) * d)[v] = pk;
   }
 }
 
-cudaError_t launch_combine(const float* y, int64_t ld_y, const int32_t* slot_dst, const float* w,
-                           int T, int k, int d, uint16_t* out, cudaStream_t stream) {
-  const int64_t tasks = static_cast<int64_t>(T) * (d / 4);
-  if (tasks == 0) return cudaSuccess;
-  // up to 16 resident blocks of 256 threads per SM, grid-stride beyond that
+// out[i] = bf16_rne(in[i]): four elements per thread, grid-stride.
+__global__ void __launch_bounds__(256) k_round_bf16(const float4* __restrict__ in, int64_t n4,
+                                                    uint2* __restrict__ out) {
+  pdl_wait();
+  pdl_trigger();
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n4;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const float4 a = __ldg(in + i);
+    const __nv_bfloat162 lo = __floats2bfloat162_rn(a.x, a.y);
+    const __nv_bfloat162 hi = __floats2bfloat162_rn(a.z, a.w);
+    uint2 pk;
+    pk.x = *reinterpret_cast<const uint32_t*>(&lo);
+    pk.y = *reinterpret_cast<const uint32_t*>(&hi);
+    out[i] = pk;
+  }
+}
+
+// Up to 16 resident blocks of 256 threads per SM, grid-stride beyond that.
+static unsigned stream_blocks(int64_t tasks) {
   int64_t blocks = (tasks + 255) / 256;
   const int64_t cap = static_cast<int64_t>(num_sms()) * 16;
-  if (blocks > cap) blocks = cap;
-  return launch_pdl(k_combine, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, y, ld_y,
-                    slot_dst, w, T, k, d, out);
+  return static_cast<unsigned>(blocks > cap ? cap : blocks);
+}
+
+cudaError_t launch_combine(const float* y, int64_t ld_y, const int32_t* slot_dst, const float* w,
+                           int T, int k, int d, void* out, bool out_f32, cudaStream_t stream) {
+  const int64_t tasks = static_cast<int64_t>(T) * (d / 4);
+  if (tasks == 0) return cudaSuccess;
+  const dim3 grid(stream_blocks(tasks));
+  if (out_f32)
+    return launch_pdl(k_combine<true>, grid, dim3(256), 0, stream, y, ld_y, slot_dst, w, T, k, d,
+                      out);
+  return launch_pdl(k_combine<false>, grid, dim3(256), 0, stream, y, ld_y, slot_dst, w, T, k, d,
+                    out);
+}
+
+cudaError_t launch_round_bf16(const float* in, int64_t n, uint16_t* out, cudaStream_t stream) {
+  const int64_t n4 = n / 4;
+  if (n4 == 0) return cudaSuccess;
+  return launch_pdl(k_round_bf16, dim3(stream_blocks(n4)), dim3(256), 0, stream,
+                    reinterpret_cast<const float4*>(in), n4, reinterpret_cast<uint2*>(out));
 }
 
 }  // namespace megamoe

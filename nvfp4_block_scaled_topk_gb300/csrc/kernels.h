@@ -122,6 +122,8 @@ uint64_t wait_limit_ns();
 cudaError_t launch_router(const float* logits, int64_t T, int E, int64_t ld, const float* bias,
                           int k, int shared, int32_t* ids, float* weights, cudaStream_t stream);
 
+// Shape and weight-pointer checks of megamoe_forward.
+megamoe_status check_forward_shape(const megamoe_weights* w, int T, int k, int pad);
 // Argument and shape checks of megamoe_forward that do not involve the
 // workspace (router: the ids and weights come from a fused router).
 megamoe_status check_forward_args(const megamoe_weights* w, const uint16_t* x,
@@ -131,8 +133,17 @@ megamoe_status check_forward_args(const megamoe_weights* w, const uint16_t* x,
 // Number of SMs of the current device (at least 1).
 int num_sms();
 
+// out: bf16 [T, d] (one rounding of the fp32 sum), or with out_f32 the fp32
+// sum itself.
 cudaError_t launch_combine(const float* y, int64_t ld_y, const int32_t* slot_dst,
-                           const float* w, int T, int k, int d, uint16_t* out,
+                           const float* w, int T, int k, int d, void* out, bool out_f32,
                            cudaStream_t stream);
+// out[i] = bf16_rne(in[i]), n a multiple of 4.
+cudaError_t launch_round_bf16(const float* in, int64_t n, uint16_t* out, cudaStream_t stream);
+// Expert-parallel shard: ids in [base, base + E_local) -> id - base; other
+// valid ids and ids < 0 -> -1 (skipped); ids >= E_total -> E_local (out of
+// range for the shard, so the routing flags and skips them).
+cudaError_t launch_ep_remap(const int32_t* ids, int64_t n, int base, int E_local, int E_total,
+                            int32_t* out, cudaStream_t stream);
 
 }  // namespace megamoe

@@ -245,6 +245,35 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
   }
 }
 
+// Expert-parallel shard (experts [base, base + E_local) of E_total): a global
+// id becomes the shard's local id, -1 (skipped) when another shard owns it or
+// it is negative, and E_local (out of the shard's range: flagged and skipped
+// by the routing) when it is not a valid expert at all.
+__global__ void __launch_bounds__(256) k_ep_remap(const int32_t* __restrict__ ids, int64_t n,
+                                                  int base, int E_local, int E_total,
+                                                  int32_t* __restrict__ out) {
+  pdl_wait();
+  pdl_trigger();
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int id = __ldg(ids + i);
+    int r = -1;
+    if (id >= E_total) r = E_local;
+    else if (id >= base && id < base + E_local) r = id - base;
+    out[i] = r;
+  }
+}
+
+cudaError_t launch_ep_remap(const int32_t* ids, int64_t n, int base, int E_local, int E_total,
+                            int32_t* out, cudaStream_t stream) {
+  if (n == 0) return cudaSuccess;
+  int64_t blocks = (n + 255) / 256;
+  const int64_t cap = static_cast<int64_t>(num_sms()) * 8;
+  if (blocks > cap) blocks = cap;
+  return launch_pdl(k_ep_remap, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, ids, n,
+                    base, E_local, E_total, out);
+}
+
 size_t route_smem_bytes(int E) { return sizeof(int) * (static_cast<size_t>(kRouteWarps) * E + 2 * E + 1); }
 
 cudaError_t launch_route(const int32_t* ids, int n_slots, int E, int pad, int32_t* counts,

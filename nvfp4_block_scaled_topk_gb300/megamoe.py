@@ -55,6 +55,9 @@ SIGNATURES = {
     "megamoe_forward_from_logits": (_I, [_P, _P, _P, _I64, _P, _I, _I, _I, _I, _I, _P, _P, _SZ,
                                          _P]),
     "megamoe_linear_nvfp4": (_I, [_P, _I64, _I, _I64, _P, _P, _P, _I, _I, _P, _I64, _P, _SZ, _P]),
+    "megamoe_ep_forward_begin": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _SZ, _P]),
+    "megamoe_ep_forward_end": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _SZ, _P]),
+    "megamoe_round_bf16": (_I, [_P, _I64, _P, _P]),
 }
 
 
@@ -336,6 +339,19 @@ class Weights:
         return cls(E, d, I, c13, s13, w["w13_gs"].contiguous(), c2, s2,
                    w["w2_gs"].reshape(E).contiguous())
 
+    def shard(self, first: int, count: int) -> "Weights":
+        """Experts [first, first + count) as their own weight set (views: each
+        expert's packed codes and atom-layout scales are contiguous)."""
+        if first < 0 or count < 1 or first + count > self.E:
+            raise ValueError("expert range out of bounds")
+        r13 = 2 * self.I * (self.d // 16)  # scale bytes of one expert's W13
+        r2 = self.d * (self.I // 16)
+        return Weights(count, self.d, self.I, self.w13_codes[first:first + count],
+                       self.w13_scales[first * r13:(first + count) * r13],
+                       self.w13_gs[first:first + count], self.w2_codes[first:first + count],
+                       self.w2_scales[first * r2:(first + count) * r2],
+                       self.w2_gs[first:first + count])
+
     def cstruct(self) -> CWeights:
         return CWeights(self.E, self.d, self.I, self.w13_codes.data_ptr(),
                         self.w13_scales.data_ptr(), self.w13_gs.data_ptr(),
@@ -403,6 +419,70 @@ class Forward:
         """Views into the workspace (for debugging and stage-level tests)."""
         return _carve_views(self.ws, self.ws_off, self.T, self.k, self.w.E, self.w.d, self.w.I,
                             self.pad)
+
+
+class ShardForward:
+    """The two halves of the forward on one expert-parallel shard
+    (megamoe_ep_forward_begin / _end): the shard's weights hold experts
+    [expert_base, expert_base + weights.E) of num_experts_total; x, ids and
+    weights are the whole layer's T tokens (global ids)."""
+
+    def __init__(self, weights: Weights, expert_base: int, num_experts_total: int, T: int, k: int,
+                 pad: int = 32, device=None):
+        self.w = weights
+        self.cw = weights.cstruct()
+        self.base, self.E_total = expert_base, num_experts_total
+        self.T, self.k, self.pad = T, k, pad
+        dev = device or weights.w13_codes.device
+        self.ws_bytes = workspace_size(T, k, weights.E, weights.d, weights.I, pad)
+        self.ws = torch.empty(self.ws_bytes + 256, dtype=torch.uint8, device=dev)
+        self.ws_off = (-self.ws.data_ptr()) % 256
+        self.partial = torch.empty(max(T, 1), weights.d, dtype=torch.float32, device=dev)
+
+    @property
+    def ws_ptr(self):
+        return ctypes.c_void_p(self.ws.data_ptr() + self.ws_off)
+
+    def amax_h(self) -> torch.Tensor:
+        """The shard's amax(h) after begin(): a device float [1] view into the
+        workspace, to be replaced by the maximum over all shards."""
+        return self.ws[self.ws_off + 12:self.ws_off + 16].view(torch.float32)
+
+    def begin(self, x, topk_ids) -> torch.Tensor:
+        _dev(x, torch.bfloat16, "x")
+        _dev(topk_ids, torch.int32, "topk_ids")
+        _check("megamoe_ep_forward_begin", load().megamoe_ep_forward_begin(
+            ctypes.byref(self.cw), _p(x), _p(topk_ids), self.T, self.k, self.base, self.E_total,
+            self.pad, self.ws_ptr, self.ws_bytes, _stream()))
+        return self.amax_h()
+
+    def end(self, topk_weights) -> torch.Tensor:
+        """fp32 [T, d]: this shard's share of the output, before rounding."""
+        _dev(topk_weights, torch.float32, "topk_weights")
+        _check("megamoe_ep_forward_end", load().megamoe_ep_forward_end(
+            ctypes.byref(self.cw), _p(topk_weights), self.T, self.k, self.E_total, self.pad,
+            _p(self.partial), self.ws_ptr, self.ws_bytes, _stream()))
+        return self.partial[:self.T]
+
+    def read_status(self) -> int:
+        bits = ctypes.c_uint32(0)
+        code = load().megamoe_read_status(self.ws_ptr, ctypes.byref(bits), _stream())
+        if code not in (OK, 5):
+            raise MegaMoEError("megamoe_read_status", code)
+        return int(bits.value)
+
+    def intermediates(self):
+        return _carve_views(self.ws, self.ws_off, self.T, self.k, self.w.E, self.w.d, self.w.I,
+                            self.pad)
+
+
+def round_bf16(x: torch.Tensor, out=None) -> torch.Tensor:
+    """bf16 copy of a float32 CUDA tensor (round to nearest even), by the library."""
+    _dev(x, torch.float32, "x")
+    if out is None:
+        out = torch.empty(x.shape, dtype=torch.bfloat16, device=x.device)
+    _check("megamoe_round_bf16", load().megamoe_round_bf16(_p(x), x.numel(), _p(out), _stream()))
+    return out
 
 
 def forward_static(weights: Weights, x, topk_ids, topk_weights, pad: int = 32, out=None,

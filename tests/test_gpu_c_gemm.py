@@ -53,7 +53,9 @@ def _dev_weights(stacked, which, megamoe):
 COUNTS = [37, 0, 1, 130, 64, 0, 5, 260]
 
 
-@pytest.mark.parametrize("tile_n", [32, 64, 128])
+# 192 / 256: wide tiles, balanced per expert (260 rows -> two tiles of 160,
+# 130 -> one of 160, 37 -> one of 64)
+@pytest.mark.parametrize("tile_n", [32, 64, 128, 192, 256])
 def test_grouped_gemm_f32_epilogue(cuda_lib, tile_n):
     from nvfp4_block_scaled_topk_gb300 import megamoe
 
@@ -76,7 +78,7 @@ def test_grouped_gemm_f32_epilogue(cuda_lib, tile_n):
     assert np.all(np.isnan(got[~v]))  # padding rows untouched
 
 
-@pytest.mark.parametrize("tile_n", [32, 64, 128])
+@pytest.mark.parametrize("tile_n", [32, 64, 128, 256])
 def test_grouped_gemm_silu_mul_epilogue(cuda_lib, tile_n):
     from nvfp4_block_scaled_topk_gb300 import megamoe
 
@@ -224,11 +226,13 @@ def _edge_rows(rng, rt, R, K):
     return c, s, g
 
 
+@pytest.mark.parametrize("tile_n", [128, 256])
 @pytest.mark.parametrize("which", ["w13", "w2"])
-def test_grouped_gemm_real_shape_tile128_several_tiles(cuda_lib, which):
-    """The prefill path's GEMM configuration: token tile 128 at the MegaMoE
-    shapes (L1: K = 7168, 28 K steps; L2: K = 2048, 8 K steps, so the stage
-    ring wraps many times), experts holding 3, 2, 1 and 0 token tiles with
+def test_grouped_gemm_real_shape_prefill_tiles(cuda_lib, which, tile_n):
+    """The prefill path's GEMM configurations: token tiles of 128, and wide
+    balanced tiles (up to 160 rows for L1, 256 for L2), at the MegaMoE shapes
+    (L1: K = 7168, 28 K steps; L2: K = 2048, 8 K steps, so the stage ring
+    wraps many times), experts holding several, one and no token tiles with
     ragged tails, and edge blocks in weights and activations."""
     from nvfp4_block_scaled_topk_gb300 import megamoe
 
@@ -250,19 +254,19 @@ def test_grouped_gemm_real_shape_tile128_several_tiles(cuda_lib, which):
         torch.from_numpy(ac).cuda(), torch.from_numpy(np.ascontiguousarray(asc)).cuda(),
         torch.tensor([float(ag)], dtype=torch.float32).cuda(), wcodes, wsc, wgs,
         torch.from_numpy(rt.offsets.astype(np.int32)).cuda(),
-        torch.from_numpy(rt.padded_offsets.astype(np.int32)).cuda(), epi, tile_n=128)
+        torch.from_numpy(rt.padded_offsets.astype(np.int32)).cuda(), epi, tile_n=tile_n)
     torch.cuda.synchronize()
     got = out.float().cpu().numpy().astype(np.float64)
     v = rt.row_src >= 0
     if which == "w13":
         gu = oracle.grouped_gemm(ac, asc, ag, ex, "w13", rt, "f32")
         h64 = oracle.silu(gu[v][:, :I]) * gu[v][:, I:]
-        assert_close_bf16(got[v], h64, what="L1 tile 128")
+        assert_close_bf16(got[v], h64, what=f"L1 tile {tile_n}")
         want_h, want_amax = oracle.grouped_gemm(ac, asc, ag, ex, "w13", rt, "silu_mul")
         assert np.mean(got[v] == want_h[v]) > 0.99
         assert abs(amax.item() - float(want_amax)) <= 2 ** -7 * float(want_amax)
     else:
         want = oracle.grouped_gemm(ac, asc, ag, ex, "w2", rt, "f32")
-        err, _ = assert_close(got[v], want[v], what="L2 tile 128")
+        err, _ = assert_close(got[v], want[v], what=f"L2 tile {tile_n}")
         assert err < 1e-5  # identical operands: only fp32 accumulation differs
         assert np.all(np.isnan(got[~v]))  # padding rows untouched
