@@ -142,7 +142,7 @@ def summarize_clocks(lines):
 def kernel_source_hash() -> str:
     """sha256 (16 hex digits) of the grouped-GEMM kernel sources."""
     h = hashlib.sha256()
-    for name in ("gemm.cu", "common.cuh"):
+    for name in ("gemm.cu", "gemm_tm.cu", "gemm_common.cuh", "common.cuh"):
         with open(os.path.join(ROOT, "nvfp4_block_scaled_topk_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]

@@ -236,15 +236,14 @@ megamoe_status megamoe_pack_weight_codes(const uint8_t* src, int64_t rows, int K
  *                                          (acc[r, I + i] * alpha_up)),
  *                         out_amax (device float, zeroed here) = max |out| over
  *                         valid rows.
- * Padding rows of `out` are not written.  tile_n selects the token tile
+ * Padding rows of `out` are not written.  tile_n selects the tile shape
  * (0 = choose from the expected tokens per expert, expected_tokens = rows the
  * caller expects per active expert, may be 0):
- *   32, 64, 128  every tile of an expert is tile_n rows wide;
- *   192, 256     wide tiles: expert e's rows are cut into ceil(count_e / W)
- *                tiles of equal width (a multiple of 32), W = tile_n for the
- *                F32 and BF16 epilogues and W = 160 for SILU_MUL (whose two
- *                accumulators fill tensor memory), so a short tail costs no
- *                extra pass over the expert's weights.
+ *   32, 64, 128  tiles of 128 weight rows x tile_n token rows (weights on the
+ *                MMA's M side, tokens on N);
+ *   256          token-major tiles: 128 token rows x 256 weight rows (tokens on
+ *                M, weights on N; for SILU_MUL the gate and up rows of 128
+ *                features in one MMA); requires N a multiple of 256.
  * Requires N a multiple of 128 (256 for SILU_MUL), K a multiple of 256,
  * 1 <= E <= 1024, 16-byte aligned pointers, ld_out >= output width and a
  * multiple of 16 bytes (4 floats, 8 bf16), else MEGAMOE_ERR_UNSUPPORTED_SHAPE.

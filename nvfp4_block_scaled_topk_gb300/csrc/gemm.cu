@@ -53,61 +53,18 @@
 #include <mutex>
 
 #include "common.cuh"
+#include "gemm_common.cuh"
 #include "kernels.h"
 
 namespace megamoe {
-
-constexpr int kGemmThreads = 448;
-constexpr int kSfWarp0 = 6;    // warps 6..9 write block scales into TMEM
-constexpr int kEpiWarp1 = 10;  // warps 2..5 and 10..13 drain the accumulators
-constexpr int kEpiWarps = 8;
-
-struct GemmArgs {
-  const uint8_t* w_codes;  // packed, pre-swizzled 16 KB blocks (megamoe_pack_weight_codes)
-  const uint8_t* w_sf;  // atom layout [E*N/128][K/64][512]
-  const float* w_gs;    // [E][G]
-  const float* a_gs;    // device scalar
-  const int32_t* offsets;
-  const int32_t* padded_offsets;
-  void* out;
-  int64_t ld_out;
-  float* out_amax;
-  uint32_t* status;
-  uint64_t wait_limit_ns;  // bound of every pipeline wait (unwinding waits use 4 s)
-  int E, N, K;
-  // 1: the routing offsets were complete before the preceding kernel started
-  // (the forward's order), so the tile schedule is built and the first weight
-  // stages are prefetched into L2 while that kernel still runs
-  int early_weights;
-  // split-K (kernels instantiated with kEpiPartial*): each tile's K range is
-  // cut into ksplit pieces; piece ks of a tile writes acc * alpha as fp32 to
-  // plane ks of `partial` ([ksplit][offsets[E]][N], rows unpadded:
-  // row - padded_offsets[e] + offsets[e]); k_splitk_finish sums the planes
-  int ksplit;
-  float* partial;
-  int64_t partial_plane;  // elements per plane
-};
-
-// Internal epilogue codes of the split-K kernels (G = 1 and G = 2 operands).
-constexpr int kEpiPartial1 = 16;
-constexpr int kEpiPartial2 = 17;
 
 template <int BN, int EPI, int STAGES>
 struct GemmCfg {
   static constexpr int G = (EPI == MEGAMOE_EPI_SILU_MUL || EPI == kEpiPartial2) ? 2 : 1;
   static constexpr bool PARTIAL = EPI >= kEpiPartial1;
-  // Wide tiles (BN > 128): each expert's rows are cut into ceil(count / BN)
-  // tiles of equal width n_e (a multiple of 32, at most BN), so a short tail
-  // does not cost a whole extra pass over the expert's weights; the MMA's N
-  // is n_e (a run-time instruction descriptor) and the token tile arrives in
-  // 32-row boxes.  Token scales then take 8 tensor-memory columns per 64-K
-  // slice (column j: token rows 32 j .. 32 j + 31) instead of 4.
-  static constexpr bool WIDE = BN > 128;
-  static constexpr int TOK_SF = WIDE ? 8 : 4;  // token-scale columns per 64-K slice
   // Two accumulator slots (the MMA fills one while the epilogue drains the
   // other) whenever tensor memory has room for them.
-  static constexpr int ACC_STAGES =
-      (2 * G * BN + STAGES * (16 * G + 4 * TOK_SF) <= 512) ? 2 : 1;
+  static constexpr int ACC_STAGES = (2 * G * BN + STAGES * (16 * G + 16) <= 512) ? 2 : 1;
   static constexpr int A_TILE = 128 * 128;  // one weight matrix, 128 rows x 128 bytes
   static constexpr int B_TILE = BN * 128;
   static constexpr int SFW = 2048;     // 4 atoms of 512 bytes (one per 64-element slice)
@@ -120,7 +77,7 @@ struct GemmCfg {
   static constexpr uint32_t TX = G * A_TILE + B_TILE;     // codes (full barrier)
   static constexpr uint32_t SF_TX = G * SFW + SFA_RAW;     // scales (sf_full barrier)
   static constexpr int ACC_COLS = G * BN;
-  static constexpr int SF_COLS = 16 * G + 4 * TOK_SF;  // per stage: weight + token scales
+  static constexpr int SF_COLS = 16 * G + 16;  // per stage: weight scales + token scales
   static constexpr int SF_COL0 = ACC_STAGES * ACC_COLS;
   static constexpr int BAR_OFF = STAGES * STAGE;
   static constexpr int TOFF_OFF = BAR_OFF + 512;
@@ -138,83 +95,9 @@ struct GemmCfg {
   static_assert((4 * STAGES + 2 * ACC_STAGES + 1) * 8 + 8 <= 512, "barrier area");
 };
 
-struct TileInfo {
-  int e, mt, nt, ntiles;  // expert, feature tile, token tile, token tiles of e
-};
-
-// Tile -> (expert, feature tile, token tile) from the tile prefix s_toff alone;
-// the expert is searched in [lo, E - 1] (a CTA's tiles never go back in e).
-__device__ __forceinline__ TileInfo decode_tile(int tile, const int* s_toff, int E, int MT,
-                                                int lo = 0) {
-  int hi = E - 1;
-  while (lo < hi) {  // largest e with s_toff[e] <= tile; it always owns tiles
-    const int mid = (lo + hi + 1) >> 1;
-    if (s_toff[mid] <= tile) lo = mid;
-    else hi = mid - 1;
-  }
-  TileInfo t;
-  t.e = lo;
-  t.ntiles = (s_toff[lo + 1] - s_toff[lo]) / MT;
-  const int local = tile - s_toff[lo];
-  t.mt = local / t.ntiles;
-  t.nt = local - t.mt * t.ntiles;
-  return t;
-}
-
-// Wide tiles: expert rows `count` cut into ceil(count / BN) tiles of equal
-// width, rounded up to a multiple of 32 rows (never above BN).
-template <int BN>
-__device__ __forceinline__ int wide_tile_rows(int count) {
-  const int t = (count + BN - 1) / BN;
-  const int per = (count + t - 1) / t;
-  return (per + 31) & ~31;
-}
-
-// s_toff[e] = first tile of expert e, s_toff[E] = total tiles.  All threads.
-template <int BN>
-__device__ void build_tile_offsets(const int32_t* offsets, int E, int MT, int* s_toff,
-                                   int* s_scan) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int per = (E + kGemmThreads - 1) / kGemmThreads;
-  const int e0 = tid * per, e1 = min(E, e0 + per);
-  int sum = 0;
-  for (int e = e0; e < e1; ++e) {
-    const int cnt = __ldcg(offsets + e + 1) - __ldcg(offsets + e);
-    const int t = cnt > 0 ? (cnt + BN - 1) / BN * MT : 0;
-    s_toff[e] = t;
-    sum += t;
-  }
-  int x = sum;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, x, o);
-    if (lane >= o) x += y;
-  }
-  if (lane == 31) s_scan[warp] = x;
-  __syncthreads();
-  int base = x - sum;
-  for (int w = 0; w < warp; ++w) base += s_scan[w];
-  for (int e = e0; e < e1; ++e) {
-    const int t = s_toff[e];
-    s_toff[e] = base;
-    base += t;
-  }
-  if (tid == kGemmThreads - 1) s_toff[E] = base;
-  __syncthreads();
-}
-
-// Waits that ignore the abort flag (used only while unwinding).
-__device__ __forceinline__ void mbar_drain(uint64_t* bar, uint32_t parity) {
-  const uint64_t t0 = globaltimer();
-  while (!mbar_try_wait(bar, parity)) {
-    if (globaltimer() - t0 > kWaitTimeoutNs) break;
-  }
-}
-
 template <int BN, int EPI, int STAGES>
 __global__ void __launch_bounds__(kGemmThreads, 1)
-    k_grouped_gemm(const __grid_constant__ CUtensorMap tm_a,
-                   const __grid_constant__ CUtensorMap tm_asf, const GemmArgs p) {
+    k_grouped_gemm(const __grid_constant__ TokenMaps maps, const GemmArgs p) {
   using C = GemmCfg<BN, EPI, STAGES>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -241,8 +124,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const int S = C::PARTIAL ? p.ksplit : 1;
 
   if (warp == 0 && lane == 0) {
-    prefetch_tensormap(&tm_a);
-    prefetch_tensormap(&tm_asf);
+    prefetch_tensormap(&maps.codes);
+    prefetch_tensormap(&maps.scales);
   }
   // The activations and their global scale come from the preceding kernel,
   // the routing offsets from it or (early_weights) from an earlier one.
@@ -308,26 +191,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       // the next tile and its expert's first padded row are found one tile ahead
       TileInfo ti_next = decode_tile(static_cast<int>(blockIdx.x) / S, s_toff, E, MT);
       int poff_next = __ldg(p.padded_offsets + ti_next.e);
-      int cnt_next =
-          C::WIDE ? __ldg(p.offsets + ti_next.e + 1) - __ldg(p.offsets + ti_next.e) : 0;
       for (int piece = blockIdx.x; ok && piece < total; piece += gridDim.x) {
         const TileInfo ti = ti_next;
         const int poff = poff_next;
-        const int cnt = cnt_next;
         const int ks = piece - (piece / S) * S;
         const int k0 = ks * KT / S, k1 = (ks + 1) * KT / S;
         if (piece + static_cast<int>(gridDim.x) < total) {
           ti_next = decode_tile((piece + static_cast<int>(gridDim.x)) / S, s_toff, E, MT, ti.e);
           poff_next = __ldg(p.padded_offsets + ti_next.e);
-          if (C::WIDE) cnt_next = __ldg(p.offsets + ti_next.e + 1) - __ldg(p.offsets + ti_next.e);
         }
         const int w_row0 = ti.e * N + ti.mt * 128;
         const int w_row1 = ti.e * N + N / 2 + ti.mt * 128;  // up rows (L1 only)
         // first 128-row code block of this tile's K = 0 step (paired for L1)
         const int w_blk0 = C::G == 2 ? ((ti.e * MT + ti.mt) * KT) * 2 : (w_row0 >> 7) * KT;
-        // token rows of this tile: BN, or the expert's balanced width (wide)
-        const int n_rows = C::WIDE ? wide_tile_rows<BN>(cnt) : BN;
-        const int a_row0 = poff + ti.nt * n_rows;
+        const int a_row0 = poff + ti.nt * BN;
         const uint64_t pol_w = ti.ntiles > 1 ? pol_w_reused : pol_w_once;
         // this tile's K = 0 weight scales (gate, up) and codes; each K step
         // advances them by 4 atoms and by G code blocks
@@ -342,30 +219,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           uint8_t* sb = smem + stage * C::STAGE;
           // scales first, on their own barrier: the scale warps move them into
           // tensor memory while the codes are still landing
-          mbar_arrive_expect_tx(&sf_full[stage],
-                                C::WIDE ? C::G * C::SFW + n_rows * 16 : C::SF_TX);
+          mbar_arrive_expect_tx(&sf_full[stage], C::SF_TX);
           bulk_load(sb + C::OFF_SFW, sfw0 + kt * 2048, C::SFW, &sf_full[stage], pol_w);
           if (C::G == 2)
             bulk_load(sb + C::OFF_SFW + C::SFW, sfw1 + kt * 2048, C::SFW, &sf_full[stage], pol_w);
-          if (C::WIDE) {  // 32-row boxes: 512 bytes of scales each
-            for (int b = 0; b < n_rows / 32; ++b)
-              tma_load_2d(sb + C::OFF_SFA_RAW + b * 512, &tm_asf, &sf_full[stage], kt * 16,
-                          a_row0 + 32 * b, pol_a);
-          } else {
-            tma_load_2d(sb + C::OFF_SFA_RAW, &tm_asf, &sf_full[stage], kt * 16, a_row0, pol_a);
-          }
-          mbar_arrive_expect_tx(&full[stage],
-                                C::WIDE ? C::G * C::A_TILE + n_rows * 128 : C::TX);
+          tma_load_2d(sb + C::OFF_SFA_RAW, &maps.scales, &sf_full[stage], kt * 16, a_row0, pol_a);
+          mbar_arrive_expect_tx(&full[stage], C::TX);
           // the stage's weight blocks (gate then up for L1) are contiguous and
           // pre-swizzled: one bulk copy
           bulk_load(sb + C::OFF_A, wcod + kt * (C::G * 16384), C::G * C::A_TILE, &full[stage], pol_w);
-          if (C::WIDE) {  // 32-row boxes of 4 KB; the 128-byte swizzle repeats every 8 rows
-            for (int b = 0; b < n_rows / 32; ++b)
-              tma_load_2d(sb + C::OFF_B + b * 4096, &tm_a, &full[stage], kt * 128, a_row0 + 32 * b,
-                          pol_a);
-          } else {
-            tma_load_2d(sb + C::OFF_B, &tm_a, &full[stage], kt * 128, a_row0, pol_a);
-          }
+          tma_load_2d(sb + C::OFF_B, &maps.codes, &full[stage], kt * 128, a_row0, pol_a);
           ++issued;
           if (++stage == STAGES) {
             stage = 0;
@@ -388,19 +251,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       int stage = 0, acc = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
-      // wide tiles: the MMA's N is the tile's row count, found one tile ahead
-      auto tile_idesc = [&](int piece, int e_lo, int* e_out) -> uint32_t {
-        const TileInfo t = decode_tile(piece / S, s_toff, E, MT, e_lo);
-        *e_out = t.e;
-        return idesc_nvf4(128, wide_tile_rows<BN>(__ldg(p.offsets + t.e + 1) -
-                                                  __ldg(p.offsets + t.e)));
-      };
-      int e_next = 0;
-      uint32_t idesc_next = C::WIDE ? tile_idesc(blockIdx.x, 0, &e_next) : C::IDESC;
       for (int piece = blockIdx.x; ok && piece < total; piece += gridDim.x) {
-        const uint32_t idesc = idesc_next;
-        if (C::WIDE && piece + static_cast<int>(gridDim.x) < total)
-          idesc_next = tile_idesc(piece + gridDim.x, e_next, &e_next);
         if (!mbar_wait(&acc_empty[acc], acc_phase ^ 1u, abort_flag, p.status, p.wait_limit_ns)) break;
         tc_fence_after();
         const uint32_t d_col = tmem + acc * C::ACC_COLS;
@@ -422,8 +273,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 #pragma unroll
             for (int g = 0; g < C::G; ++g) {
               const uint64_t adesc = sdesc_sw128(smem_u32(sb + C::OFF_A + g * C::A_TILE) + 32 * c);
-              mma_nvf4(d_col + g * BN, adesc, bdesc, idesc, sf_col + 16 * g + 4 * c,
-                       sfa_col + C::TOK_SF * c, (kt != k0 || c != 0) ? 1u : 0u);
+              mma_nvf4(d_col + g * BN, adesc, bdesc, C::IDESC, sf_col + 16 * g + 4 * c,
+                       sfa_col + 4 * c, (kt != k0 || c != 0) ? 1u : 0u);
             }
           }
           tc_commit(&empty[stage]);
@@ -475,32 +326,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
         const uint4* raw = reinterpret_cast<const uint4*>(sb + C::OFF_SFA_RAW);
         const uint32_t sfa_col = sf_col + 16 * C::G;
-        if (C::WIDE) {
-          // token rows 32 j + lane, j < 8: column 8 c + j of slice c.  Rows
-          // at or past the tile's width hold stale bytes; the MMA's N stops
-          // before them.
-          uint4 r[8];
+        uint4 r[4];
 #pragma unroll
-          for (int j = 0; j < 8; ++j)
-            r[j] = (32 * j < BN) ? raw[32 * j + lane] : make_uint4(0u, 0u, 0u, 0u);
-          tmem_st_32x32b_x4(sfa_col + 0, r[0].x, r[1].x, r[2].x, r[3].x);
-          tmem_st_32x32b_x4(sfa_col + 4, r[4].x, r[5].x, r[6].x, r[7].x);
-          tmem_st_32x32b_x4(sfa_col + 8, r[0].y, r[1].y, r[2].y, r[3].y);
-          tmem_st_32x32b_x4(sfa_col + 12, r[4].y, r[5].y, r[6].y, r[7].y);
-          tmem_st_32x32b_x4(sfa_col + 16, r[0].z, r[1].z, r[2].z, r[3].z);
-          tmem_st_32x32b_x4(sfa_col + 20, r[4].z, r[5].z, r[6].z, r[7].z);
-          tmem_st_32x32b_x4(sfa_col + 24, r[0].w, r[1].w, r[2].w, r[3].w);
-          tmem_st_32x32b_x4(sfa_col + 28, r[4].w, r[5].w, r[6].w, r[7].w);
-        } else {
-          uint4 r[4];
-#pragma unroll
-          for (int j = 0; j < 4; ++j)
-            r[j] = (32 * j + lane < BN) ? raw[32 * j + lane] : make_uint4(0u, 0u, 0u, 0u);
-          tmem_st_32x32b_x4(sfa_col + 0, r[0].x, r[1].x, r[2].x, r[3].x);
-          tmem_st_32x32b_x4(sfa_col + 4, r[0].y, r[1].y, r[2].y, r[3].y);
-          tmem_st_32x32b_x4(sfa_col + 8, r[0].z, r[1].z, r[2].z, r[3].z);
-          tmem_st_32x32b_x4(sfa_col + 12, r[0].w, r[1].w, r[2].w, r[3].w);
-        }
+        for (int j = 0; j < 4; ++j)
+          r[j] = (32 * j + lane < BN) ? raw[32 * j + lane] : make_uint4(0u, 0u, 0u, 0u);
+        tmem_st_32x32b_x4(sfa_col + 0, r[0].x, r[1].x, r[2].x, r[3].x);
+        tmem_st_32x32b_x4(sfa_col + 4, r[0].y, r[1].y, r[2].y, r[3].y);
+        tmem_st_32x32b_x4(sfa_col + 8, r[0].z, r[1].z, r[2].z, r[3].z);
+        tmem_st_32x32b_x4(sfa_col + 12, r[0].w, r[1].w, r[2].w, r[3].w);
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
@@ -549,9 +382,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const int ks = piece - (piece / S) * S;
       if (piece + static_cast<int>(gridDim.x) < total)
         next = fetch((piece + static_cast<int>(gridDim.x)) / S, ti.e);
-      const int n_rows = C::WIDE ? wide_tile_rows<BN>(cur.count) : BN;
-      const int m_valid = min(n_rows, cur.count - ti.nt * n_rows);
-      const int64_t row0 = cur.poff + static_cast<int64_t>(ti.nt) * n_rows;
+      const int m_valid = min(BN, cur.count - ti.nt * BN);
+      const int64_t row0 = cur.poff + static_cast<int64_t>(ti.nt) * BN;
       const int f0 = ti.mt * 128 + q * 32;  // first feature of this warp's quarter
       const float alpha0 = 1.0f / (a_gs * cur.gs0);
       const float alpha1 = C::G == 2 ? 1.0f / (a_gs * cur.gs1) : 0.f;
@@ -795,14 +627,13 @@ static bool make_scales_map(CUtensorMap* map, const void* base, uint64_t rows, u
 }
 
 template <int BN, int EPI, int STAGES>
-static cudaError_t launch_cfg(const CUtensorMap& tm_a, const CUtensorMap& tm_asf,
-                              const GemmArgs& a, cudaStream_t stream) {
+static cudaError_t launch_cfg(const TokenMaps& maps, const GemmArgs& a, cudaStream_t stream) {
   using C = GemmCfg<BN, EPI, STAGES>;
   auto kern = k_grouped_gemm<BN, EPI, STAGES>;
   cudaError_t err =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (err != cudaSuccess) return err;
-  return launch_pdl(kern, dim3(num_sms()), dim3(kGemmThreads), C::SMEM, stream, tm_a, tm_asf, a);
+  return launch_pdl(kern, dim3(num_sms()), dim3(kGemmThreads), C::SMEM, stream, maps, a);
 }
 
 static uint64_t g_wait_limit_ns = kWaitTimeoutNs;
@@ -838,27 +669,36 @@ int pick_tile_n(double expected) {
 cudaError_t launch_grouped_gemm(const GemmLaunch& g, cudaStream_t stream) {
   if (g.act_rows == 0 || g.E == 0) return cudaSuccess;
   const int bn = g.tile_n;
-  // wide tiles (192 or 256 requested) load their token rows in 32-row boxes
-  const uint32_t box = bn > 128 ? 32 : static_cast<uint32_t>(bn);
-  CUtensorMap tm_a, tm_asf;
-  if (!make_codes_map(&tm_a, g.act_codes, static_cast<uint64_t>(g.act_rows), g.K / 2, box) ||
-      !make_scales_map(&tm_asf, g.act_scales, static_cast<uint64_t>(g.act_rows), g.K / 16, box))
+  // token-major tiles (256): 128-row boxes; otherwise BN-row boxes
+  TokenMaps maps;
+  const uint32_t box = bn == 256 ? 128u : static_cast<uint32_t>(bn);
+  if (!make_codes_map(&maps.codes, g.act_codes, static_cast<uint64_t>(g.act_rows), g.K / 2, box) ||
+      !make_scales_map(&maps.scales, g.act_scales, static_cast<uint64_t>(g.act_rows), g.K / 16,
+                       box))
     return cudaErrorInvalidValue;
   GemmArgs a{g.w_codes,        g.w_scales, g.w_gs,     g.act_gs, g.offsets,
              g.padded_offsets, g.out,      g.ld_out,   g.out_amax, g.status,
              wait_limit_ns(),  g.E,        g.N,        g.K,          g.early_weights ? 1 : 0,
              g.ksplit,         g.partial,  g.partial_plane};
+  if (bn == 256) {  // token-major tiles: 128 token rows x 256 weight rows
+    if (g.ksplit > 1) return cudaErrorInvalidValue;
+    if (g.epilogue == MEGAMOE_EPI_SILU_MUL && g.out_amax && g.zero_amax) {
+      cudaError_t err = cudaMemsetAsync(g.out_amax, 0, sizeof(float), stream);
+      if (err != cudaSuccess) return err;
+    }
+    return launch_grouped_gemm_tm(maps, a, g.epilogue, stream);
+  }
   if (g.ksplit > 1) {
     if (!g.partial || bn > 64) return cudaErrorInvalidValue;
     cudaError_t err = cudaSuccess;
     if (g.epilogue == MEGAMOE_EPI_SILU_MUL) {
       if (g.out_amax && g.zero_amax) err = cudaMemsetAsync(g.out_amax, 0, sizeof(float), stream);
       if (err == cudaSuccess)
-        err = bn == 32 ? launch_cfg<32, kEpiPartial2, 5>(tm_a, tm_asf, a, stream)
-                       : launch_cfg<64, kEpiPartial2, 4>(tm_a, tm_asf, a, stream);
+        err = bn == 32 ? launch_cfg<32, kEpiPartial2, 5>(maps, a, stream)
+                       : launch_cfg<64, kEpiPartial2, 4>(maps, a, stream);
     } else {
-      err = bn == 32 ? launch_cfg<32, kEpiPartial1, 8>(tm_a, tm_asf, a, stream)
-                     : launch_cfg<64, kEpiPartial1, 7>(tm_a, tm_asf, a, stream);
+      err = bn == 32 ? launch_cfg<32, kEpiPartial1, 8>(maps, a, stream)
+                     : launch_cfg<64, kEpiPartial1, 7>(maps, a, stream);
     }
     if (err != cudaSuccess) return err;
     const int width = g.epilogue == MEGAMOE_EPI_SILU_MUL ? g.N / 2 : g.N;
@@ -887,29 +727,21 @@ cudaError_t launch_grouped_gemm(const GemmLaunch& g, cudaStream_t stream) {
       if (err != cudaSuccess) return err;
     }
     switch (bn) {
-      case 32: return launch_cfg<32, MEGAMOE_EPI_SILU_MUL, 5>(tm_a, tm_asf, a, stream);
-      case 64: return launch_cfg<64, MEGAMOE_EPI_SILU_MUL, 4>(tm_a, tm_asf, a, stream);
-      case 128: return launch_cfg<128, MEGAMOE_EPI_SILU_MUL, 4>(tm_a, tm_asf, a, stream);
-      // wide: the gate and up accumulators of 160 token columns and three
-      // stages of scales fill the 512 tensor-memory columns
-      case 192:
-      case 256: return launch_cfg<160, MEGAMOE_EPI_SILU_MUL, 3>(tm_a, tm_asf, a, stream);
+      case 32: return launch_cfg<32, MEGAMOE_EPI_SILU_MUL, 5>(maps, a, stream);
+      case 64: return launch_cfg<64, MEGAMOE_EPI_SILU_MUL, 4>(maps, a, stream);
+      case 128: return launch_cfg<128, MEGAMOE_EPI_SILU_MUL, 4>(maps, a, stream);
     }
   } else if (g.epilogue == MEGAMOE_EPI_BF16) {
     switch (bn) {
-      case 32: return launch_cfg<32, MEGAMOE_EPI_BF16, 8>(tm_a, tm_asf, a, stream);
-      case 64: return launch_cfg<64, MEGAMOE_EPI_BF16, 7>(tm_a, tm_asf, a, stream);
-      case 128: return launch_cfg<128, MEGAMOE_EPI_BF16, 5>(tm_a, tm_asf, a, stream);
-      case 192: return launch_cfg<192, MEGAMOE_EPI_BF16, 4>(tm_a, tm_asf, a, stream);
-      case 256: return launch_cfg<256, MEGAMOE_EPI_BF16, 3>(tm_a, tm_asf, a, stream);
+      case 32: return launch_cfg<32, MEGAMOE_EPI_BF16, 8>(maps, a, stream);
+      case 64: return launch_cfg<64, MEGAMOE_EPI_BF16, 7>(maps, a, stream);
+      case 128: return launch_cfg<128, MEGAMOE_EPI_BF16, 5>(maps, a, stream);
     }
   } else {
     switch (bn) {
-      case 32: return launch_cfg<32, MEGAMOE_EPI_F32, 8>(tm_a, tm_asf, a, stream);
-      case 64: return launch_cfg<64, MEGAMOE_EPI_F32, 7>(tm_a, tm_asf, a, stream);
-      case 128: return launch_cfg<128, MEGAMOE_EPI_F32, 5>(tm_a, tm_asf, a, stream);
-      case 192: return launch_cfg<192, MEGAMOE_EPI_F32, 4>(tm_a, tm_asf, a, stream);
-      case 256: return launch_cfg<256, MEGAMOE_EPI_F32, 3>(tm_a, tm_asf, a, stream);
+      case 32: return launch_cfg<32, MEGAMOE_EPI_F32, 8>(maps, a, stream);
+      case 64: return launch_cfg<64, MEGAMOE_EPI_F32, 7>(maps, a, stream);
+      case 128: return launch_cfg<128, MEGAMOE_EPI_F32, 5>(maps, a, stream);
     }
   }
   return cudaErrorInvalidValue;

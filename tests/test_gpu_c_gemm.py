@@ -53,9 +53,8 @@ def _dev_weights(stacked, which, megamoe):
 COUNTS = [37, 0, 1, 130, 64, 0, 5, 260]
 
 
-# 192 / 256: wide tiles, balanced per expert (260 rows -> two tiles of 160,
-# 130 -> one of 160, 37 -> one of 64)
-@pytest.mark.parametrize("tile_n", [32, 64, 128, 192, 256])
+# 256: token-major tiles (128 tokens x 256 weight rows)
+@pytest.mark.parametrize("tile_n", [32, 64, 128, 256])
 def test_grouped_gemm_f32_epilogue(cuda_lib, tile_n):
     from nvfp4_block_scaled_topk_gb300 import megamoe
 
@@ -229,8 +228,8 @@ def _edge_rows(rng, rt, R, K):
 @pytest.mark.parametrize("tile_n", [128, 256])
 @pytest.mark.parametrize("which", ["w13", "w2"])
 def test_grouped_gemm_real_shape_prefill_tiles(cuda_lib, which, tile_n):
-    """The prefill path's GEMM configurations: token tiles of 128, and wide
-    balanced tiles (up to 160 rows for L1, 256 for L2), at the MegaMoE shapes
+    """The prefill path's GEMM configurations: token tiles of 128, and
+    token-major tiles (128 tokens x 256 weight rows), at the MegaMoE shapes
     (L1: K = 7168, 28 K steps; L2: K = 2048, 8 K steps, so the stage ring
     wraps many times), experts holding several, one and no token tiles with
     ragged tails, and edge blocks in weights and activations."""
