@@ -44,6 +44,7 @@ struct Workspace {
   float* partial;  // split-K planes, shared by L1 and L2 (they run in turn)
   int32_t* r_ids;  // router outputs of megamoe_forward_from_logits [T, k]
   float* r_w;
+  int32_t* route_hist;  // per-block expert histograms of the multi-block routing
   int ks1, ks2;    // split-K of L1 and L2 (1 = none)
   int64_t rows;    // padded-row capacity
   size_t bytes;
@@ -127,6 +128,10 @@ Workspace carve(void* base, int T, int k, int E, int d, int I, int pad) {
   w.partial = reinterpret_cast<float*>(take(std::max(p1, p2) * 4));
   w.r_ids = reinterpret_cast<int32_t*>(take(4 * slots));
   w.r_w = reinterpret_cast<float*>(take(4 * slots));
+  w.route_hist = reinterpret_cast<int32_t*>(
+      take(slots >= static_cast<size_t>(kRouteMultiMinSlots)
+               ? 4 * static_cast<size_t>(kRouteMaxBlocks) * E
+               : 0));
   w.bytes = off;
   return w;
 }
@@ -377,7 +382,8 @@ cudaError_t forward_l1(const megamoe_weights* w, const uint16_t* x, const int32_
                         router->k_routed, router->shared, wk.r_ids, wk.r_w, s);
     if (e != cudaSuccess) return e;
     e = launch_route(topk_ids, T * k, E, pad, wk.counts, wk.offsets, wk.padded_offsets,
-                     wk.row_src, wk.rows, wk.slot_dst, wk.status, wk.status, 5, s);
+                     wk.row_src, wk.rows, wk.slot_dst, wk.status, wk.status, 5, s,
+                     wk.route_hist);
     if (e != cudaSuccess) return e;
     e = launch_amax(x, T, d, d, wk.amax_x, wk.status, false, s);
   }

@@ -29,12 +29,17 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
 }
 
 size_t route_smem_bytes(int E);
+// Routing over many blocks (three passes) from this many slots on, when the
+// caller passes a block_hist scratch of kRouteMaxBlocks * E ints.
+constexpr int kRouteMultiMinSlots = 16384;
+constexpr int kRouteMaxBlocks = 256;
 // zero_words (may be null): n_zero 32-bit words cleared before anything else
 // (the forward's status word and amax accumulators).
 cudaError_t launch_route(const int32_t* ids, int n_slots, int E, int pad, int32_t* counts,
                          int32_t* offsets, int32_t* padded_offsets, int32_t* row_src,
                          int64_t row_capacity, int32_t* slot_dst, uint32_t* status,
-                         uint32_t* zero_words, int n_zero, cudaStream_t stream);
+                         uint32_t* zero_words, int n_zero, cudaStream_t stream,
+                         int32_t* block_hist = nullptr);
 
 // zero_first: clear *amax first (false when the caller already cleared it).
 cudaError_t launch_amax(const uint16_t* x, int64_t rows, int K, int64_t ld, float* amax,

@@ -15,6 +15,8 @@
 //      count of that expert in this warp.
 #include <cuda_runtime.h>
 
+#include <algorithm>
+
 #include "common.cuh"
 #include "kernels.h"
 #include "router.cuh"
@@ -175,6 +177,143 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
               slot_dst, status, zero_words, n_zero, smem_route);
 }
 
+// ---------------------------------------------------------------------------
+// Large batches: the same routing over many blocks, in three passes.  Block b
+// owns the contiguous slot chunk [b * chunk, (b + 1) * chunk), so "block,
+// then warp, then position" is still the flat slot order and the result is
+// identical to route_block's:
+//   1. k_route_hist: per-block expert histograms -> hist[b][e];
+//   2. k_route_offsets (one block): counts, offsets, padded offsets, and each
+//      block's exclusive base per expert (hist rewritten in place);
+//   3. k_route_scatter: per block, per-warp histograms of its chunk on top of
+//      the block's bases, then the stable scatter as in route_block; the
+//      padding rows are spread over the blocks; ids >= E are flagged here
+//      (after pass 1 cleared the status word).
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kRouteThreads) k_route_hist(const int32_t* __restrict__ ids,
+                                                              int n_slots, int E, int chunk,
+                                                              int32_t* __restrict__ hist,
+                                                              uint32_t* zero_words, int n_zero) {
+  extern __shared__ int sh_hist[];  // [E]
+  pdl_wait();
+  pdl_trigger();
+  const int tid = threadIdx.x;
+  if (blockIdx.x == 0)
+    for (int i = tid; i < n_zero; i += kRouteThreads) zero_words[i] = 0u;
+  for (int e = tid; e < E; e += kRouteThreads) sh_hist[e] = 0;
+  __syncthreads();
+  const int s0 = blockIdx.x * chunk, s1 = min(n_slots, s0 + chunk);
+  for (int sv = s0 + tid; sv < s1; sv += kRouteThreads) {
+    const int e = __ldg(ids + sv);
+    if (e >= 0 && e < E) atomicAdd(&sh_hist[e], 1);
+  }
+  __syncthreads();
+  for (int e = tid; e < E; e += kRouteThreads) hist[static_cast<int64_t>(blockIdx.x) * E + e] = sh_hist[e];
+}
+
+__global__ void __launch_bounds__(kRouteThreads, 1)
+    k_route_offsets(int n_blocks, int E, int pad, int32_t* __restrict__ hist,
+                    int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+                    int32_t* __restrict__ padded_offsets) {
+  __shared__ int warp_sums[32];
+  __shared__ int totals[2];
+  pdl_wait();
+  pdl_trigger();
+  const int tid = threadIdx.x;
+  int cnt = 0, padded = 0;
+  if (tid < E) {  // E <= 1024: one expert per thread
+    for (int b = 0; b < n_blocks; ++b) {
+      const int h = hist[static_cast<int64_t>(b) * E + tid];
+      hist[static_cast<int64_t>(b) * E + tid] = cnt;
+      cnt += h;
+    }
+    padded = (cnt + pad - 1) / pad * pad;
+  }
+  const int off = block_exclusive_scan_1024(cnt, warp_sums, &totals[0]);
+  const int poff = block_exclusive_scan_1024(padded, warp_sums, &totals[1]);
+  if (tid < E) {
+    counts[tid] = cnt;
+    offsets[tid] = off;
+    padded_offsets[tid] = poff;
+  }
+  if (tid == 0) {
+    offsets[E] = totals[0];
+    padded_offsets[E] = totals[1];
+  }
+}
+
+__global__ void __launch_bounds__(kRouteThreads, 1)
+    k_route_scatter(const int32_t* __restrict__ ids, int n_slots, int E, int chunk,
+                    const int32_t* __restrict__ hist, const int32_t* __restrict__ counts,
+                    const int32_t* __restrict__ padded_offsets, int32_t* row_src,
+                    int64_t row_capacity, int32_t* slot_dst, uint32_t* status) {
+  extern __shared__ int smem_sc[];
+  int* whist = smem_sc;                 // [32][E]: per-warp running rows
+  int* s_poff = whist + kRouteWarps * E;  // [E + 1]
+  pdl_wait();
+  pdl_trigger();
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  for (int i = tid; i < kRouteWarps * E; i += kRouteThreads) whist[i] = 0;
+  for (int e = tid; e <= E; e += kRouteThreads) s_poff[e] = padded_offsets[e];
+  __syncthreads();
+  const int b0 = blockIdx.x * chunk, b1 = min(n_slots, b0 + chunk);
+  const int wchunk = (max(b1 - b0, 0) + kRouteWarps - 1) / kRouteWarps;
+  const int s_begin = min(b1, b0 + warp * wchunk);
+  const int s_end = min(b1, s_begin + wchunk);
+  // per-warp histograms of the warp's part of the chunk
+  bool bad = false;
+  for (int c0 = s_begin; c0 < s_end; c0 += 32) {  // warp-uniform bounds
+    const int sv = c0 + lane;
+    const int e = sv < s_end ? __ldg(ids + sv) : -1;
+    if (e >= E) bad = true;
+    else if (e >= 0) atomicAdd(&whist[warp * E + e], 1);
+  }
+  if (__any_sync(0xffffffffu, bad) && lane == 0) set_status(status, MEGAMOE_DEV_BAD_EXPERT_ID);
+  __syncthreads();
+  // exclusive over warps, on top of this block's base from pass 2
+  for (int e = tid; e < E; e += kRouteThreads) {
+    int base = hist[static_cast<int64_t>(blockIdx.x) * E + e];
+    for (int w = 0; w < kRouteWarps; ++w) {
+      const int h = whist[w * E + e];
+      whist[w * E + e] = base;
+      base += h;
+    }
+  }
+  __syncthreads();
+  // stable scatter, 32 slots at a time in order
+  for (int c0 = s_begin; c0 < s_end; c0 += 32) {
+    const int sv = c0 + lane;
+    const bool in = sv < s_end;
+    int e = in ? __ldg(ids + sv) : -1;
+    if (e >= E) e = -1;
+    const unsigned active = __ballot_sync(0xffffffffu, in);
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    if (in) {
+      if (e >= 0) {
+        const unsigned lower = peers & ((1u << lane) - 1u);
+        const int row = s_poff[e] + whist[warp * E + e] + __popc(lower);
+        row_src[row] = sv;
+        slot_dst[sv] = row;
+      } else {
+        slot_dst[sv] = -1;
+      }
+    }
+    __syncwarp();
+    if (in && e >= 0 && (31 - __clz(peers & active)) == lane)
+      whist[warp * E + e] += __popc(peers & active);
+    __syncwarp();
+  }
+  // padding rows of every expert, then everything past the last expert,
+  // spread over the blocks
+  const int gtid = blockIdx.x * kRouteThreads + tid;
+  const int gthreads = gridDim.x * kRouteThreads;
+  for (int e = gtid; e < E; e += gthreads) {
+    const int c = __ldg(counts + e);
+    for (int r = s_poff[e] + c; r < s_poff[e + 1]; ++r) row_src[r] = -1;
+  }
+  for (int64_t r = s_poff[E] + gtid; r < row_capacity; r += gthreads) row_src[r] = -1;
+}
+
 // Small batches: route and the amax of x in this one block (the quantisation
 // itself, ALU-heavy, runs spread over many SMs in the next kernel).
 constexpr int64_t kPrologueMaxElems = 262144;  // T * d read by one block
@@ -279,8 +418,32 @@ size_t route_smem_bytes(int E) { return sizeof(int) * (static_cast<size_t>(kRout
 cudaError_t launch_route(const int32_t* ids, int n_slots, int E, int pad, int32_t* counts,
                          int32_t* offsets, int32_t* padded_offsets, int32_t* row_src,
                          int64_t row_capacity, int32_t* slot_dst, uint32_t* status,
-                         uint32_t* zero_words, int n_zero, cudaStream_t stream) {
+                         uint32_t* zero_words, int n_zero, cudaStream_t stream,
+                         int32_t* block_hist) {
   const size_t smem = route_smem_bytes(E);
+  if (block_hist && n_slots >= kRouteMultiMinSlots) {
+    // chunks of at least 1024 slots, one per block, at most one block per SM
+    const int blocks_max = std::min(kRouteMaxBlocks, num_sms());
+    int chunk = (n_slots + blocks_max - 1) / blocks_max;
+    chunk = std::max(1024, (chunk + 31) / 32 * 32);
+    const int blocks = (n_slots + chunk - 1) / chunk;
+    cudaError_t err = launch_pdl(k_route_hist, dim3(blocks), dim3(kRouteThreads),
+                                 sizeof(int) * static_cast<size_t>(E), stream, ids, n_slots, E,
+                                 chunk, block_hist, zero_words, n_zero);
+    if (err == cudaSuccess)
+      err = launch_pdl(k_route_offsets, dim3(1), dim3(kRouteThreads), 0, stream, blocks, E, pad,
+                       block_hist, counts, offsets, padded_offsets);
+    if (err == cudaSuccess)
+      err = cudaFuncSetAttribute(k_route_scatter, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(smem));
+    if (err == cudaSuccess)
+      err = launch_pdl(k_route_scatter, dim3(blocks), dim3(kRouteThreads), smem, stream, ids,
+                       n_slots, E, chunk, static_cast<const int32_t*>(block_hist),
+                       static_cast<const int32_t*>(counts),
+                       static_cast<const int32_t*>(padded_offsets), row_src, row_capacity,
+                       slot_dst, status);
+    return err;
+  }
   cudaError_t err = cudaFuncSetAttribute(k_route, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
   if (err != cudaSuccess) return err;

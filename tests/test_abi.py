@@ -201,7 +201,9 @@ def test_stage_views_mirror_the_workspace_layout(lib, T, k, E, d, I, pad):
     """The binding's views of the forward's stages lie where the library
     carves them: the same regions in the same order and sizes, each 256-byte
     aligned, and the library's size is those regions plus its two
-    router-output regions (no split-K planes unless asked for)."""
+    router-output regions (no split-K planes unless asked for) and, from
+    16384 slots on, the multi-block routing's per-block histograms (256
+    blocks x E ints)."""
     import torch
 
     size = megamoe.workspace_size(T, k, E, d, I, pad)
@@ -219,7 +221,8 @@ def test_stage_views_mirror_the_workspace_layout(lib, T, k, E, d, I, pad):
         assert t.storage_offset() * t.element_size() == off, name
         assert t.numel() * t.element_size() == nbytes, name
         off = a256(off + nbytes)
-    assert size == off + 2 * a256(4 * T * k)
+    hist = 4 * 256 * E if T * k >= 16384 else 0
+    assert size == off + 2 * a256(4 * T * k) + a256(hist)
 
 
 def test_plain_c_program_compiles_links_and_calls_the_host_helpers(lib):

@@ -65,3 +65,41 @@ def test_route_flags_and_skips_out_of_range_ids(cuda_lib):
     ids[3, 1] = 10
     ids[17, 0] = 1000
     assert _check(ids, 10, 32) & megamoe.DEV_BAD_EXPERT_ID
+
+
+@pytest.mark.parametrize("case", ["uniform", "all_one_expert", "skipped_and_bad", "zipf_1024"])
+def test_multi_block_routing_in_the_forward(cuda_lib, case):
+    """From 16384 slots on, the forward routes over many blocks (per-block
+    histograms, one-block offsets, per-block stable scatter); its routing
+    views must equal the oracle's stable sort exactly, padding and all."""
+    E, k, T = (1024, 8, 4096) if case == "zipf_1024" else (64, 6, 4096)
+    routing = "zipf" if case == "zipf_1024" else "uniform"
+    cfg = inputs.MoEConfig("route_multi", E, k, 256, 256, T, routing, seed=321)
+    raw = inputs.make_all_experts(cfg, device="cuda")
+    weights = megamoe.Weights.prepare(raw)
+    x = inputs.make_activations(cfg).cuda()
+    ids, w = inputs.make_routing(cfg)
+    ids = ids.clone()
+    if case == "all_one_expert":
+        ids[:, 0] = 5
+        ids[:, 1:] = -1
+    elif case == "skipped_and_bad":
+        g = torch.Generator().manual_seed(3)
+        ids[torch.rand(ids.shape, generator=g) < 0.2] = -1
+        ids[torch.rand(ids.shape, generator=g) < 0.01] = E + 7
+    assert T * k >= 16384
+    fwd = megamoe.Forward(weights, T, k, pad=32)
+    fwd(x, ids.cuda(), w.cuda())
+    bits = fwd.read_status()
+    assert bool(bits & megamoe.DEV_BAD_EXPERT_ID) == (case == "skipped_and_bad")
+    ids_np = ids.numpy()
+    want = oracle.route(np.where(ids_np >= E, -1, ids_np), E, 32)
+    v = fwd.intermediates()
+    R = int(want.padded_offsets[-1])
+    assert np.array_equal(v["counts"].cpu().numpy(), want.counts)
+    assert np.array_equal(v["offsets"].cpu().numpy(), want.offsets)
+    assert np.array_equal(v["padded_offsets"].cpu().numpy(), want.padded_offsets)
+    rs = v["row_src"].cpu().numpy()
+    assert np.array_equal(rs[:R], want.row_src)
+    assert np.all(rs[R:] == -1)
+    assert np.array_equal(v["slot_dst"].cpu().numpy(), want.slot_dst)
