@@ -384,6 +384,24 @@ megamoe_status megamoe_forward(const megamoe_weights* w, const uint16_t* x,
 void megamoe_set_wait_limit_ns(uint64_t ns);
 
 /*
+ * megamoe_set_fused_requant -- where megamoe_forward / _from_logits /
+ * _static requantise h (north_star's "requant fused into the L1 epilogue";
+ * host setting of this library, all devices, for forwards launched
+ * afterwards):
+ *   0 (default)  a separate kernel after the L1 GEMM reads h once and encodes
+ *                it with the global scale of amax(h);
+ *   1            the L1 GEMM kernel does it: after its last tile each CTA
+ *                arrives on a grid-wide count in the workspace and waits
+ *                (bounded by the pipeline wait limit; MEGAMOE_DEV_TIMEOUT on
+ *                expiry) until every CTA with tiles has, so amax(h) is
+ *                final, then encodes the h rows of its own tiles.
+ * Both give bit-identical results.  The default is the faster on GB300 (the
+ * separate kernel lets CTAs that finish early free their SM for the next
+ * kernel); an L1 GEMM split along K always uses the separate kernel.
+ */
+void megamoe_set_fused_requant(int enable);
+
+/*
  * Expert-parallel forward, one shard (one process and GPU) of G: the shard
  * holds experts [expert_base, expert_base + w_shard->num_experts) of
  * num_experts_total ("CURRENT_BUG.md -- DeepSeek-V4 Blackwell NVFP4", "Test

@@ -30,6 +30,7 @@ struct Workspace {
   float* gs_x;
   float* amax_h;
   float* gs_h;
+  uint32_t* l1_arrivals;  // the fused requantisation's grid-wide arrival count
   int32_t* counts;
   int32_t* offsets;
   int32_t* padded_offsets;
@@ -109,6 +110,7 @@ Workspace carve(void* base, int T, int k, int E, int d, int I, int pad) {
     w.gs_x = reinterpret_cast<float*>(hdr + 8);
     w.amax_h = reinterpret_cast<float*>(hdr + 12);
     w.gs_h = reinterpret_cast<float*>(hdr + 16);
+    w.l1_arrivals = reinterpret_cast<uint32_t*>(hdr + 20);
   }
   w.counts = reinterpret_cast<int32_t*>(take(4 * static_cast<size_t>(E)));
   w.offsets = reinterpret_cast<int32_t*>(take(4 * static_cast<size_t>(E + 1)));
@@ -363,7 +365,7 @@ namespace {
 // tile's choice).
 cudaError_t forward_l1(const megamoe_weights* w, const uint16_t* x, const int32_t* topk_ids,
                        int T, int k, int pad, const Workspace& wk, cudaStream_t s,
-                       RouterArgs* router, int tile_n) {
+                       RouterArgs* router, int tile_n, bool fuse_requant) {
   const int E = w->num_experts, d = w->hidden, I = w->intermediate;
   cudaError_t e = cudaSuccess;
   // 0-3. (router,) route (its first act clears the status word and the amax
@@ -374,7 +376,7 @@ cudaError_t forward_l1(const megamoe_weights* w, const uint16_t* x, const int32_
   //      in one thread block.
   if (prologue_fits(T, d)) {
     e = launch_prologue(topk_ids, T, k, E, pad, wk.counts, wk.offsets, wk.padded_offsets,
-                        wk.row_src, wk.rows, wk.slot_dst, wk.status, wk.status, 5, x, d,
+                        wk.row_src, wk.rows, wk.slot_dst, wk.status, wk.status, 6, x, d,
                         wk.amax_x, s, router);
   } else {
     if (router)
@@ -382,7 +384,7 @@ cudaError_t forward_l1(const megamoe_weights* w, const uint16_t* x, const int32_
                         router->k_routed, router->shared, wk.r_ids, wk.r_w, s);
     if (e != cudaSuccess) return e;
     e = launch_route(topk_ids, T * k, E, pad, wk.counts, wk.offsets, wk.padded_offsets,
-                     wk.row_src, wk.rows, wk.slot_dst, wk.status, wk.status, 5, s,
+                     wk.row_src, wk.rows, wk.slot_dst, wk.status, wk.status, 6, s,
                      wk.route_hist);
     if (e != cudaSuccess) return e;
     e = launch_amax(x, T, d, d, wk.amax_x, wk.status, false, s);
@@ -417,21 +419,42 @@ cudaError_t forward_l1(const megamoe_weights* w, const uint16_t* x, const int32_
   g.ksplit = wk.ks1;
   g.partial = wk.partial;
   g.partial_plane = static_cast<int64_t>(T) * k * 2 * I;
+  if (fuse_requant) {  // 5. (fused) requantise h inside the L1 kernel
+    g.rq_arrivals = wk.l1_arrivals;
+    g.rq_codes = wk.hq_codes;
+    g.rq_scales = wk.hq_sf;
+    g.rq_gs = wk.gs_h;
+  }
   return launch_grouped_gemm(g, s);
 }
+
+// Whether the forward requantises h inside the L1 kernel (behind a grid-wide
+// arrival count) instead of in its own kernel after it: only when asked
+// (megamoe_set_fused_requant) and the L1 GEMM is not split along K.
+// Measured on GB300 the separate kernel is faster: 3.72 against 4.01 ms at
+// 16384 tokens, 1.20 against 1.28 ms at 4096, 182 against 190 us at 8 --
+// CTAs that finish their last tile early exit and free their SM for the next
+// kernel's start, while behind the grid-wide wait every CTA holds its SM
+// until the slowest is done.
+bool g_fused_requant = false;
+bool requant_fused(const Workspace& wk) { return g_fused_requant && wk.ks1 <= 1; }
 
 // Steps 5-7: requantise h with gs from the amax(h) held in the workspace, L2
 // down grouped GEMM -> fp32 y, top-k weighted combine (bf16 out, or the fp32
 // sum before its rounding with out_f32).
 cudaError_t forward_l2(const megamoe_weights* w, const float* topk_weights, int T, int k,
                        void* out, bool out_f32, const Workspace& wk, cudaStream_t s,
-                       int tile_n) {
+                       int tile_n, bool requant_done) {
   const int E = w->num_experts, d = w->hidden, I = w->intermediate;
-  // 5. requantise the valid rows of h with gs from amax(h) (slot by slot)
-  cudaError_t e = launch_quant(wk.h, static_cast<int64_t>(T) * k, I, I, wk.slot_dst, 1, nullptr,
-                               wk.padded_offsets + E, wk.rows, wk.amax_h, wk.gs_h, wk.hq_codes,
-                               wk.hq_sf, MEGAMOE_SCALES_ROWMAJOR, s, /*slot_rows=*/true);
-  if (e != cudaSuccess) return e;
+  cudaError_t e = cudaSuccess;
+  // 5. requantise the valid rows of h with gs from amax(h) (slot by slot),
+  //    unless the L1 kernel already did
+  if (!requant_done) {
+    e = launch_quant(wk.h, static_cast<int64_t>(T) * k, I, I, wk.slot_dst, 1, nullptr,
+                     wk.padded_offsets + E, wk.rows, wk.amax_h, wk.gs_h, wk.hq_codes, wk.hq_sf,
+                     MEGAMOE_SCALES_ROWMAJOR, s, /*slot_rows=*/true);
+    if (e != cudaSuccess) return e;
+  }
   // 6. L2 down grouped GEMM -> fp32 y
   GemmLaunch g{};
   g.act_codes = wk.hq_codes;
@@ -484,8 +507,9 @@ megamoe_status forward_impl(const megamoe_weights* w, const uint16_t* x, const i
     topk_ids = wk.r_ids;
     topk_weights = wk.r_w;
   }
-  cudaError_t e = forward_l1(w, x, topk_ids, T, k, pad, wk, s, router, l1_tile(tile_n));
-  if (e == cudaSuccess) e = forward_l2(w, topk_weights, T, k, out, false, wk, s, tile_n);
+  const bool fused = requant_fused(wk);
+  cudaError_t e = forward_l1(w, x, topk_ids, T, k, pad, wk, s, router, l1_tile(tile_n), fused);
+  if (e == cudaSuccess) e = forward_l2(w, topk_weights, T, k, out, false, wk, s, tile_n, fused);
   return cuda_status(e);
 }
 
@@ -539,8 +563,9 @@ megamoe_status megamoe_ep_forward_begin(const megamoe_weights* w_shard, const ui
   cudaError_t e = launch_ep_remap(topk_ids, static_cast<int64_t>(T) * k, expert_base,
                                   w_shard->num_experts, num_experts_total, wk.r_ids, s);
   if (e == cudaSuccess)
+    // the shard's h is requantised only after the amax(h) exchange
     e = forward_l1(w_shard, x, wk.r_ids, T, k, pad, wk, s, nullptr,
-                   l1_tile(ep_tile_n(T, k, num_experts_total)));
+                   l1_tile(ep_tile_n(T, k, num_experts_total)), false);
   return cuda_status(e);
 }
 
@@ -556,7 +581,7 @@ megamoe_status megamoe_ep_forward_end(const megamoe_weights* w_shard, const floa
   if (T == 0) return MEGAMOE_OK;
   return cuda_status(forward_l2(w_shard, topk_weights, T, k, out_partial, true, wk,
                                 reinterpret_cast<cudaStream_t>(stream),
-                                ep_tile_n(T, k, num_experts_total)));
+                                ep_tile_n(T, k, num_experts_total), false));
 }
 
 megamoe_status megamoe_round_bf16(const float* in, int64_t n, uint16_t* out,
@@ -594,6 +619,8 @@ megamoe_status megamoe_forward_from_logits(const megamoe_weights* w, const uint1
 }
 
 void megamoe_set_wait_limit_ns(uint64_t ns) { set_wait_limit_ns(ns); }
+
+void megamoe_set_fused_requant(int enable) { g_fused_requant = enable != 0; }
 
 megamoe_status megamoe_router_topk(const float* logits, int64_t T, int E, int64_t ld_logits,
                                    const float* bias, int k, int shared_expert,

@@ -501,6 +501,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
+  if (EPI == MEGAMOE_EPI_SILU_MUL && p.rq_arrivals) {  // never split (S = 1)
+    __shared__ int s_rq_ok;
+    fused_requant(p, s_toff, MT, total, BN, &s_rq_ok);
+  }
 }
 
 // Finishes a split-K GEMM: sums the fp32 planes in plane order and applies
@@ -680,6 +684,13 @@ cudaError_t launch_grouped_gemm(const GemmLaunch& g, cudaStream_t stream) {
              g.padded_offsets, g.out,      g.ld_out,   g.out_amax, g.status,
              wait_limit_ns(),  g.E,        g.N,        g.K,          g.early_weights ? 1 : 0,
              g.ksplit,         g.partial,  g.partial_plane};
+  if (g.epilogue == MEGAMOE_EPI_SILU_MUL && g.ksplit <= 1 && g.rq_arrivals) {
+    if (!g.rq_codes || !g.rq_scales || !g.rq_gs || !g.out_amax) return cudaErrorInvalidValue;
+    a.rq_arrivals = g.rq_arrivals;
+    a.rq_codes = g.rq_codes;
+    a.rq_scales = g.rq_scales;
+    a.rq_gs = g.rq_gs;
+  }
   if (bn == 256) {  // token-major tiles: 128 token rows x 256 weight rows
     if (g.ksplit > 1) return cudaErrorInvalidValue;
     if (g.epilogue == MEGAMOE_EPI_SILU_MUL && g.out_amax && g.zero_amax) {

@@ -40,6 +40,16 @@ struct GemmArgs {
   int ksplit;
   float* partial;
   int64_t partial_plane;  // elements per plane
+  // Requantisation of h fused into the SiLU*up kernel (null: not fused).
+  // After its last tile every CTA with tiles adds one to *rq_arrivals (zeroed
+  // before the launch) and waits, bounded, until all of them have; then each
+  // encodes the h rows of its own tiles with gs = 2688 / amax(h) into
+  // rq_codes [rows, N/4] and row-major rq_scales [rows, N/32], and CTA 0
+  // stores gs in *rq_gs.
+  uint32_t* rq_arrivals;
+  uint8_t* rq_codes;
+  uint8_t* rq_scales;
+  float* rq_gs;
 };
 
 // Tensor maps of the token tile: codes (128-byte swizzle) and row-major
@@ -118,6 +128,78 @@ __device__ __forceinline__ void mbar_drain(uint64_t* bar, uint32_t parity) {
   const uint64_t t0 = globaltimer();
   while (!mbar_try_wait(bar, parity)) {
     if (globaltimer() - t0 > kWaitTimeoutNs) break;
+  }
+}
+
+// Grid-wide arrival of this CTA (thread 0 only), then a bounded wait until
+// `expected` CTAs have arrived.  The fence before the arrival publishes this
+// CTA's earlier writes (ordered before by the caller's __syncthreads); the
+// acquire load and the fence after it make every arrived CTA's writes
+// visible.  False (with MEGAMOE_DEV_TIMEOUT set) if the wait ran out.
+__device__ __forceinline__ bool grid_arrive_and_wait(uint32_t* arrivals, uint32_t expected,
+                                                     uint32_t* status, uint64_t limit_ns) {
+  __threadfence();
+  atomicAdd(arrivals, 1u);
+  const uint64_t t0 = globaltimer();
+  while (true) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(arrivals) : "memory");
+    if (v >= expected) break;
+    if (globaltimer() - t0 > limit_ns) {
+      set_status(status, MEGAMOE_DEV_TIMEOUT);
+      return false;
+    }
+    __nanosleep(64);
+  }
+  __threadfence();
+  return true;
+}
+
+// The fused requantisation of h (GemmArgs::rq_*), by every thread of a CTA
+// that had tiles, after its last tile's epilogue and a __syncthreads.  Tiles
+// are BN token rows x 128 features of h (h = the kernel's bf16 output,
+// ld_out = N/2); two tasks per row of a tile, each four 16-element blocks:
+// 32 bytes of codes and one 4-byte word of scales, encoded exactly as
+// k_quant does (encode_block, gs = fl32(2688 / amax)).
+__device__ __forceinline__ void fused_requant(const GemmArgs& p, const int* s_toff, int MT,
+                                              int total, int BN, int* s_ok) {
+  if (threadIdx.x == 0) {
+    const uint32_t expected = static_cast<uint32_t>(min(static_cast<int>(gridDim.x), total));
+    *s_ok = grid_arrive_and_wait(p.rq_arrivals, expected, p.status, p.wait_limit_ns) ? 1 : 0;
+  }
+  __syncthreads();
+  if (!*s_ok) return;
+  const float amax = __ldcg(p.out_amax);
+  const float gs = amax == 0.f ? 1.f : __fdiv_rn(2688.0f, amax);
+  if (blockIdx.x == 0 && threadIdx.x == 0) *p.rq_gs = gs;
+  const int I = p.N / 2;
+  const uint16_t* h = static_cast<const uint16_t*>(p.out);
+  int e_lo = 0;
+  for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+    const TileInfo ti = decode_tile(tile, s_toff, p.E, MT, e_lo);
+    e_lo = ti.e;
+    const int cnt = __ldg(p.offsets + ti.e + 1) - __ldg(p.offsets + ti.e);
+    const int m_valid = min(BN, cnt - ti.nt * BN);
+    const int64_t row0 = __ldg(p.padded_offsets + ti.e) + static_cast<int64_t>(ti.nt) * BN;
+    for (int t = threadIdx.x; t < 2 * m_valid; t += blockDim.x) {
+      const int64_t row = row0 + (t >> 1);
+      const int f = ti.mt * 128 + (t & 1) * 64;  // first of four 16-element blocks
+      // h was written by this CTA in this kernel: read through L2, not the
+      // non-coherent path
+      const uint4* src = reinterpret_cast<const uint4*>(h + row * p.ld_out + f);
+      uint4 v[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[i] = __ldcg(src + i);
+      uint2 c[4];
+      uint32_t s8[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) encode_block(v[2 * j], v[2 * j + 1], gs, c[j], s8[j]);
+      uint4* cd = reinterpret_cast<uint4*>(p.rq_codes + row * (I / 2) + f / 2);
+      cd[0] = make_uint4(c[0].x, c[0].y, c[1].x, c[1].y);
+      cd[1] = make_uint4(c[2].x, c[2].y, c[3].x, c[3].y);
+      *reinterpret_cast<uint32_t*>(p.rq_scales + row * (I / 16) + f / 16) =
+          s8[0] | (s8[1] << 8) | (s8[2] << 16) | (s8[3] << 24);
+    }
   }
 }
 

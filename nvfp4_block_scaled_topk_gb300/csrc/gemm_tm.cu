@@ -424,6 +424,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
+  if (C::SILU && p.rq_arrivals) {
+    __shared__ int s_rq_ok;
+    fused_requant(p, s_toff, MT, total, C::BM, &s_rq_ok);
+  }
 }
 
 template <int EPI, int STAGES>

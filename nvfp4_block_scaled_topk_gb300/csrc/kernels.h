@@ -111,6 +111,13 @@ struct GemmLaunch {
   int ksplit = 1;
   float* partial = nullptr;
   int64_t partial_plane = 0;
+  // requantisation of h fused into the SILU_MUL kernel (ksplit 1 only):
+  // arrival counter zeroed before the launch, codes [rows, N/4], row-major
+  // scales [rows, N/32], global scale out (all null: not fused)
+  uint32_t* rq_arrivals = nullptr;
+  uint8_t* rq_codes = nullptr;
+  uint8_t* rq_scales = nullptr;
+  float* rq_gs = nullptr;
 };
 // Split-K choice for a GEMM of about `tiles` whole-K tiles of KT K steps: the
 // smallest ksplit (<= 8, >= 2 K steps a piece) that minimises the waves of

@@ -50,6 +50,7 @@ SIGNATURES = {
     "megamoe_read_status": (_I, [_P, _P, _P]),
     "megamoe_forward_static": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P, _P]),
     "megamoe_set_wait_limit_ns": (None, [ctypes.c_uint64]),
+    "megamoe_set_fused_requant": (None, [_I]),
     "megamoe_linear_workspace_size": (_SZ, [_I64, _I, _I]),
     "megamoe_router_topk": (_I, [_P, _I64, _I, _I64, _P, _I, _I, _P, _P, _P]),
     "megamoe_forward_from_logits": (_I, [_P, _P, _P, _I64, _P, _I, _I, _I, _I, _I, _P, _P, _SZ,
@@ -135,6 +136,12 @@ def workspace_size(T, k, E, d, I, pad):
 def set_wait_limit_ns(ns: int):
     """Bound of the grouped GEMM's pipeline waits (0 restores 4 s)."""
     load().megamoe_set_wait_limit_ns(int(ns))
+
+
+def set_fused_requant(enable: bool):
+    """Requantise h inside the L1 GEMM kernel (True) or in its own kernel
+    after it (False, the default and the faster)."""
+    load().megamoe_set_fused_requant(1 if enable else 0)
 
 
 def status_string(code):

@@ -221,3 +221,36 @@ def test_forward_at_the_interface_maxima(cuda_lib, E, k, T, d, I, pad):
     _, inter = oracle.forward(x.float().numpy(), ids.numpy(), w.numpy(), ex, pad=pad,
                               return_intermediates=True)
     check_forward(fwd, out, inter, ex, ids.numpy(), w.numpy(), what=f"E={E} k={k}")
+
+
+@pytest.mark.parametrize("E,k,d,I,T", [(384, 6, 7168, 2048, 8), (64, 6, 2048, 1024, 1024)])
+def test_fused_requant_equals_the_separate_kernel(cuda_lib, E, k, d, I, T):
+    """The requantisation of h inside the L1 kernel (megamoe_set_fused_requant)
+    against the default separate kernel: the same requantised codes, block
+    scales, global scale and output, bit for bit, with the 32-token tiles of
+    decode and the token-major tiles of larger batches."""
+    cfg = inputs.MoEConfig("fused_rq", E, k, d, I, T, "uniform", seed=612)
+    torch.cuda.empty_cache()
+    _CACHE.clear()
+    raw, weights = _weights(cfg)
+    x = inputs.make_activations(cfg).cuda()
+    ids, w = inputs.make_routing(cfg)
+    ids, w = ids.cuda(), w.cuda()
+    res = []
+    for fused in (False, True):
+        fwd = megamoe.Forward(weights, T, k, pad=32)
+        try:
+            megamoe.set_fused_requant(fused)
+            out = fwd(x, ids, w).clone()
+        finally:
+            megamoe.set_fused_requant(False)
+        assert fwd.read_status() == 0
+        v = fwd.intermediates()
+        R = int(v["padded_offsets"][-1].item())
+        valid = v["row_src"][:R] >= 0
+        res.append((out, v["hq_codes"][:R][valid].clone(), v["hq_sf"][:R][valid].clone(),
+                    v["gs_h"].item()))
+    (o0, c0, s0, g0), (o1, c1, s1, g1) = res
+    assert g0 == g1
+    assert torch.equal(c0, c1) and torch.equal(s0, s1)
+    assert torch.equal(o0, o1)

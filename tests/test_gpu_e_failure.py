@@ -75,3 +75,33 @@ def test_grouped_gemm_wait_that_runs_out_unwinds(cuda_lib, tile_n):
     assert status.item() == 0
     valid = v["row_src"][:int(v["padded_offsets"][-1].item())] >= 0
     assert torch.equal(got[:valid.numel()][valid], want[:valid.numel()][valid])
+
+
+def test_fused_requant_barrier_that_runs_out(cuda_lib):
+    """The forward with the requantisation of h fused into its L1 kernel
+    (token-major tiles, a grid-wide arrival count behind the last tile):
+    with a 100 ns limit every wait, that one included, runs out; the timeout
+    bit is set, the kernel returns, and the next forward equals a clean one."""
+    cfg = inputs.MoEConfig("fail_fused", 8, 2, 512, 512, 256, "uniform", seed=78)
+    raw = inputs.make_all_experts(cfg, device="cuda")
+    weights = megamoe.Weights.prepare(raw)
+    x = inputs.make_activations(cfg).cuda()
+    ids, w = inputs.make_routing(cfg)
+    ids, w = ids.cuda(), w.cuda()
+    fwd = megamoe.Forward(weights, cfg.T, cfg.k, pad=32)
+    try:
+        megamoe.set_fused_requant(True)
+        want = fwd(x, ids, w).clone()
+        assert fwd.read_status() == 0
+        try:
+            megamoe.set_wait_limit_ns(100)
+            fwd(x, ids, w)
+            bits = fwd.read_status()
+        finally:
+            megamoe.set_wait_limit_ns(0)
+        assert bits & megamoe.DEV_TIMEOUT
+        out = fwd(x, ids, w)
+        assert fwd.read_status() == 0
+        assert torch.equal(out, want)
+    finally:
+        megamoe.set_fused_requant(False)
