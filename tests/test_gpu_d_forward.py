@@ -254,3 +254,37 @@ def test_fused_requant_equals_the_separate_kernel(cuda_lib, E, k, d, I, T):
     assert g0 == g1
     assert torch.equal(c0, c1) and torch.equal(s0, s1)
     assert torch.equal(o0, o1)
+
+
+def test_forward_with_edge_blocks_in_the_weights(cuda_lib):
+    """The workloads' weight bytes come from fixed histograms with no zero or
+    subnormal block scales; here every expert matrix also holds blocks whose
+    E4M3 scale is 0x00 (the block decodes to zero) or subnormal (0x01..0x07),
+    and blocks of +-6 codes, through the whole forward against the oracle."""
+    cfg = inputs.MoEConfig("edges", 16, 4, 1024, 512, 96, "uniform", seed=808)
+    raw = inputs.make_all_experts(cfg, device="cuda")
+    g = torch.Generator(device="cuda").manual_seed(9)
+    for cname, sname in (("w13_codes", "w13_scales"), ("w2_codes", "w2_scales")):
+        sc, co = raw[sname], raw[cname]
+        n = sc.numel()
+        pick = torch.randperm(n, generator=g, device="cuda")[: 3 * (n // 40)]
+        sc.view(-1)[pick[: n // 40]] = 0
+        sc.view(-1)[pick[n // 40: 2 * (n // 40)]] = torch.randint(
+            1, 8, (n // 40,), generator=g, device="cuda", dtype=torch.uint8)
+        six = pick[2 * (n // 40):]
+        rows, blk = six // sc.shape[-1], six % sc.shape[-1]
+        flat = co.view(-1, co.shape[-1])
+        for b in range(8):  # the block's 8 code bytes: +-6 pairs
+            flat.view(-1, co.shape[-1])[rows, 8 * blk + b] = torch.tensor(
+                [0x77, 0xFF, 0x7F, 0xF7][b % 4], dtype=torch.uint8, device="cuda")
+    assert (raw["w13_scales"] == 0).any() and ((raw["w2_scales"] > 0) & (raw["w2_scales"] < 8)).any()
+    weights = megamoe.Weights.prepare(raw)
+    x = inputs.make_activations(cfg)
+    ids, w = inputs.make_routing(cfg)
+    fwd = megamoe.Forward(weights, cfg.T, cfg.k, pad=32)
+    out = fwd(x.cuda(), ids.cuda(), w.cuda())
+    assert fwd.read_status() == 0
+    ex = inputs.ExpertSet(cfg, raw)
+    _, inter = oracle.forward(x.float().numpy(), ids.numpy(), w.numpy(), ex, pad=32,
+                              return_intermediates=True)
+    check_forward(fwd, out, inter, ex, ids.numpy(), w.numpy(), what="edge blocks")
