@@ -54,15 +54,16 @@ __global__ void __launch_bounds__(256) k_combine(const float* __restrict__ y, in
       }
     }
     if (F32_OUT) {  // the sum before its rounding (one shard's share of the output)
-      reinterpret_cast<float4*>(static_cast<float*>(out) + static_cast<int64_t>(t) * d)[v] = acc;
-      continue;
+      float* o = static_cast<float*>(out) + static_cast<int64_t>(t) * d + 4 * v;
+      __stcs(reinterpret_cast<float4*>(o), acc);
+    } else {
+      const __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
+      const __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
+      uint2 pk;
+      pk.x = *reinterpret_cast<const uint32_t*>(&lo);
+      pk.y = *reinterpret_cast<const uint32_t*>(&hi);
+      reinterpret_cast<uint2*>(static_cast<uint16_t*>(out) + static_cast<int64_t>(t) * d)[v] = pk;
     }
-    const __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
-    const __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
-    uint2 pk;
-    pk.x = *reinterpret_cast<const uint32_t*>(&lo);
-    pk.y = *reinterpret_cast<const uint32_t*>(&hi);
-    reinterpret_cast<uint2*>(static_cast<uint16_t*>(out) + static_cast<int64_t>(t) * d)[v] = pk;
   }
 }
 

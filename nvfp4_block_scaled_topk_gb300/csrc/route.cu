@@ -182,9 +182,11 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
 // owns the contiguous slot chunk [b * chunk, (b + 1) * chunk), so "block,
 // then warp, then position" is still the flat slot order and the result is
 // identical to route_block's:
-//   1. k_route_hist: per-block expert histograms -> hist[b][e];
+//   1. k_route_hist: per-block expert histograms -> hist[e][b] (expert-major,
+//      rows of bstride >= blocks ints, bstride a multiple of 4);
 //   2. k_route_offsets (one block): counts, offsets, padded offsets, and each
-//      block's exclusive base per expert (hist rewritten in place);
+//      block's exclusive base per expert (hist rewritten in place; thread e
+//      walks its row in 16-byte loads, eight in flight);
 //   3. k_route_scatter: per block, per-warp histograms of its chunk on top of
 //      the block's bases, then the stable scatter as in route_block; the
 //      padding rows are spread over the blocks; ids >= E are flagged here
@@ -192,6 +194,7 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kRouteThreads) k_route_hist(const int32_t* __restrict__ ids,
                                                               int n_slots, int E, int chunk,
+                                                              int bstride,
                                                               int32_t* __restrict__ hist,
                                                               uint32_t* zero_words, int n_zero) {
   extern __shared__ int sh_hist[];  // [E]
@@ -208,11 +211,12 @@ __global__ void __launch_bounds__(kRouteThreads) k_route_hist(const int32_t* __r
     if (e >= 0 && e < E) atomicAdd(&sh_hist[e], 1);
   }
   __syncthreads();
-  for (int e = tid; e < E; e += kRouteThreads) hist[static_cast<int64_t>(blockIdx.x) * E + e] = sh_hist[e];
+  for (int e = tid; e < E; e += kRouteThreads)
+    hist[static_cast<int64_t>(e) * bstride + blockIdx.x] = sh_hist[e];
 }
 
 __global__ void __launch_bounds__(kRouteThreads, 1)
-    k_route_offsets(int n_blocks, int E, int pad, int32_t* __restrict__ hist,
+    k_route_offsets(int n_blocks, int bstride, int E, int pad, int32_t* __restrict__ hist,
                     int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
                     int32_t* __restrict__ padded_offsets) {
   __shared__ int warp_sums[32];
@@ -221,11 +225,28 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
   pdl_trigger();
   const int tid = threadIdx.x;
   int cnt = 0, padded = 0;
-  if (tid < E) {  // E <= 1024: one expert per thread
-    for (int b = 0; b < n_blocks; ++b) {
-      const int h = hist[static_cast<int64_t>(b) * E + tid];
-      hist[static_cast<int64_t>(b) * E + tid] = cnt;
-      cnt += h;
+  if (tid < E) {  // E <= 1024: one expert per thread, its row of block counts
+    int4* row = reinterpret_cast<int4*>(hist + static_cast<int64_t>(tid) * bstride);
+    const int vecs = bstride / 4;
+    for (int j0 = 0; j0 < vecs; j0 += 8) {
+      int4 v[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[i] = j0 + i < vecs ? row[j0 + i] : make_int4(0, 0, 0, 0);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        if (j0 + i >= vecs) break;
+        const int b = 4 * (j0 + i);  // entries past the last block are not counts
+        int4 o;
+        o.x = cnt;
+        cnt += b + 0 < n_blocks ? v[i].x : 0;
+        o.y = cnt;
+        cnt += b + 1 < n_blocks ? v[i].y : 0;
+        o.z = cnt;
+        cnt += b + 2 < n_blocks ? v[i].z : 0;
+        o.w = cnt;
+        cnt += b + 3 < n_blocks ? v[i].w : 0;
+        row[j0 + i] = o;
+      }
     }
     padded = (cnt + pad - 1) / pad * pad;
   }
@@ -243,7 +264,7 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
 }
 
 __global__ void __launch_bounds__(kRouteThreads, 1)
-    k_route_scatter(const int32_t* __restrict__ ids, int n_slots, int E, int chunk,
+    k_route_scatter(const int32_t* __restrict__ ids, int n_slots, int E, int chunk, int bstride,
                     const int32_t* __restrict__ hist, const int32_t* __restrict__ counts,
                     const int32_t* __restrict__ padded_offsets, int32_t* row_src,
                     int64_t row_capacity, int32_t* slot_dst, uint32_t* status) {
@@ -272,7 +293,7 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
   __syncthreads();
   // exclusive over warps, on top of this block's base from pass 2
   for (int e = tid; e < E; e += kRouteThreads) {
-    int base = hist[static_cast<int64_t>(blockIdx.x) * E + e];
+    int base = hist[static_cast<int64_t>(e) * bstride + blockIdx.x];
     for (int w = 0; w < kRouteWarps; ++w) {
       const int h = whist[w * E + e];
       whist[w * E + e] = base;
@@ -427,18 +448,19 @@ cudaError_t launch_route(const int32_t* ids, int n_slots, int E, int pad, int32_
     int chunk = (n_slots + blocks_max - 1) / blocks_max;
     chunk = std::max(1024, (chunk + 31) / 32 * 32);
     const int blocks = (n_slots + chunk - 1) / chunk;
+    const int bstride = (blocks + 3) / 4 * 4;  // <= kRouteMaxBlocks
     cudaError_t err = launch_pdl(k_route_hist, dim3(blocks), dim3(kRouteThreads),
                                  sizeof(int) * static_cast<size_t>(E), stream, ids, n_slots, E,
-                                 chunk, block_hist, zero_words, n_zero);
+                                 chunk, bstride, block_hist, zero_words, n_zero);
     if (err == cudaSuccess)
-      err = launch_pdl(k_route_offsets, dim3(1), dim3(kRouteThreads), 0, stream, blocks, E, pad,
-                       block_hist, counts, offsets, padded_offsets);
+      err = launch_pdl(k_route_offsets, dim3(1), dim3(kRouteThreads), 0, stream, blocks, bstride,
+                       E, pad, block_hist, counts, offsets, padded_offsets);
     if (err == cudaSuccess)
       err = cudaFuncSetAttribute(k_route_scatter, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(smem));
     if (err == cudaSuccess)
       err = launch_pdl(k_route_scatter, dim3(blocks), dim3(kRouteThreads), smem, stream, ids,
-                       n_slots, E, chunk, static_cast<const int32_t*>(block_hist),
+                       n_slots, E, chunk, bstride, static_cast<const int32_t*>(block_hist),
                        static_cast<const int32_t*>(counts),
                        static_cast<const int32_t*>(padded_offsets), row_src, row_capacity,
                        slot_dst, status);
