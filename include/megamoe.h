@@ -451,6 +451,33 @@ megamoe_status megamoe_round_bf16(const float* in, int64_t n, uint16_t* out,
                                   megamoe_stream_t stream);
 
 /*
+ * megamoe_forward_scan_stages -- debug aid: which stage of the last forward
+ * run with this workspace produced a non-finite value ("CURRENT_BUG.md --
+ * DeepSeek-V4 Blackwell NVFP4", "Test Plan -- Finding the NaN", Phase 1
+ * item 3: check after the L1 GEMM and SiLU, and after the L2 GEMM).  ws and
+ * (T, k, E = w->num_experts, d, I, pad) are those of a megamoe_forward /
+ * _from_logits call already enqueued on `stream`; out its output.  Scans
+ * the valid rows (padding rows are never written and may hold anything) and
+ * writes to *flags (device uint32, cleared here) the bits of every stage
+ * that holds one:
+ *   MEGAMOE_STAGE_XQ_SCALE  a block scale of the quantised x is an E4M3 NaN byte
+ *   MEGAMOE_STAGE_H         h = bf16(SiLU(gate) * up) holds Inf or NaN
+ *   MEGAMOE_STAGE_HQ_SCALE  a block scale of the requantised h is an E4M3 NaN byte
+ *   MEGAMOE_STAGE_Y         the L2 output y (fp32) holds Inf or NaN
+ *   MEGAMOE_STAGE_OUT       the combined output holds Inf or NaN
+ * Reads every intermediate once (~3.7 GB at 16384 tokens): for diagnosis,
+ * not the forward's path.  Asynchronous on `stream`.
+ */
+#define MEGAMOE_STAGE_XQ_SCALE 0x01u
+#define MEGAMOE_STAGE_H 0x02u
+#define MEGAMOE_STAGE_HQ_SCALE 0x04u
+#define MEGAMOE_STAGE_Y 0x08u
+#define MEGAMOE_STAGE_OUT 0x10u
+megamoe_status megamoe_forward_scan_stages(const megamoe_weights* w, int T, int k, int pad,
+                                           const uint16_t* out, const void* ws, size_t ws_bytes,
+                                           uint32_t* flags, megamoe_stream_t stream);
+
+/*
  * megamoe_read_status -- synchronise `stream`, copy the device status word at
  * `status` (for megamoe_forward: the first 4 bytes of ws) into *bits (host),
  * and return MEGAMOE_ERR_DEVICE_STATUS if any bit is set, else MEGAMOE_OK.

@@ -2,6 +2,7 @@
 // forward orchestration.  No allocation, no synchronisation on the compute
 // path; every launch goes to the caller's stream.
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 #include <stdint.h>
 
 #include <algorithm>
@@ -16,6 +17,14 @@ using namespace megamoe;
 namespace {
 
 inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// NVTX range around the enqueueing of a stage (named "megamoe.<stage>"), so a
+// profiler's timeline groups each stage's launches; no-ops unless a tool is
+// attached.
+struct StageRange {
+  explicit StageRange(const char* name) { nvtxRangePushA(name); }
+  ~StageRange() { nvtxRangePop(); }
+};
 
 inline size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
@@ -375,23 +384,31 @@ cudaError_t forward_l1(const megamoe_weights* w, const uint16_t* x, const int32_
   //      stored.  Small batches route (and run the router) and take the amax
   //      in one thread block.
   if (prologue_fits(T, d)) {
+    StageRange r("megamoe.route+amax_x");
     e = launch_prologue(topk_ids, T, k, E, pad, wk.counts, wk.offsets, wk.padded_offsets,
                         wk.row_src, wk.rows, wk.slot_dst, wk.status, wk.status, 6, x, d,
                         wk.amax_x, s, router);
   } else {
-    if (router)
+    if (router) {
+      StageRange r("megamoe.router");
       e = launch_router(router->logits, T, router->n_logits, router->ld, router->bias,
                         router->k_routed, router->shared, wk.r_ids, wk.r_w, s);
+    }
     if (e != cudaSuccess) return e;
+    StageRange r("megamoe.route");
     e = launch_route(topk_ids, T * k, E, pad, wk.counts, wk.offsets, wk.padded_offsets,
                      wk.row_src, wk.rows, wk.slot_dst, wk.status, wk.status, 6, s,
                      wk.route_hist);
     if (e != cudaSuccess) return e;
+    StageRange ra("megamoe.amax_x");
     e = launch_amax(x, T, d, d, wk.amax_x, wk.status, false, s);
   }
   if (e != cudaSuccess) return e;
-  e = launch_quant(x, T, d, d, wk.slot_dst, k, nullptr, wk.padded_offsets + E, wk.rows,
-                   wk.amax_x, wk.gs_x, wk.xq_codes, wk.xq_sf, MEGAMOE_SCALES_ROWMAJOR, s);
+  {
+    StageRange r("megamoe.quant_x");
+    e = launch_quant(x, T, d, d, wk.slot_dst, k, nullptr, wk.padded_offsets + E, wk.rows,
+                     wk.amax_x, wk.gs_x, wk.xq_codes, wk.xq_sf, MEGAMOE_SCALES_ROWMAJOR, s);
+  }
   if (e != cudaSuccess) return e;
   // 4. L1 gate+up grouped GEMM, SiLU(gate)*up -> bf16 h, amax(h)
   GemmLaunch g{};
@@ -425,6 +442,7 @@ cudaError_t forward_l1(const megamoe_weights* w, const uint16_t* x, const int32_
     g.rq_scales = wk.hq_sf;
     g.rq_gs = wk.gs_h;
   }
+  StageRange r("megamoe.l1_gemm");
   return launch_grouped_gemm(g, s);
 }
 
@@ -450,6 +468,7 @@ cudaError_t forward_l2(const megamoe_weights* w, const float* topk_weights, int 
   // 5. requantise the valid rows of h with gs from amax(h) (slot by slot),
   //    unless the L1 kernel already did
   if (!requant_done) {
+    StageRange r("megamoe.requant_h");
     e = launch_quant(wk.h, static_cast<int64_t>(T) * k, I, I, wk.slot_dst, 1, nullptr,
                      wk.padded_offsets + E, wk.rows, wk.amax_h, wk.gs_h, wk.hq_codes, wk.hq_sf,
                      MEGAMOE_SCALES_ROWMAJOR, s, /*slot_rows=*/true);
@@ -479,9 +498,13 @@ cudaError_t forward_l2(const megamoe_weights* w, const float* topk_weights, int 
   g.ksplit = wk.ks2;
   g.partial = wk.partial;
   g.partial_plane = static_cast<int64_t>(T) * k * d;
-  e = launch_grouped_gemm(g, s);
+  {
+    StageRange r("megamoe.l2_gemm");
+    e = launch_grouped_gemm(g, s);
+  }
   if (e != cudaSuccess) return e;
   // 7. top-k weighted combine
+  StageRange r("megamoe.combine");
   return launch_combine(wk.y, d, wk.slot_dst, topk_weights, T, k, d, out, out_f32, s);
 }
 
@@ -501,6 +524,7 @@ megamoe_status forward_impl(const megamoe_weights* w, const uint16_t* x, const i
   if (T == 0) return cudaMemsetAsync(wk.status, 0, 256, s) == cudaSuccess ? MEGAMOE_OK
                                                                          : MEGAMOE_ERR_CUDA;
   const int tile_n = tile_n_setting(static_cast<double>(T) * k / E);
+  StageRange whole("megamoe.forward");
   if (router) {  // the ids and weights land in the workspace
     router->ids_out = wk.r_ids;
     router->w_out = wk.r_w;
@@ -582,6 +606,23 @@ megamoe_status megamoe_ep_forward_end(const megamoe_weights* w_shard, const floa
   return cuda_status(forward_l2(w_shard, topk_weights, T, k, out_partial, true, wk,
                                 reinterpret_cast<cudaStream_t>(stream),
                                 ep_tile_n(T, k, num_experts_total), false));
+}
+
+megamoe_status megamoe_forward_scan_stages(const megamoe_weights* w, int T, int k, int pad,
+                                           const uint16_t* out, const void* ws, size_t ws_bytes,
+                                           uint32_t* flags, megamoe_stream_t stream) {
+  megamoe_status st = megamoe::check_forward_shape(w, T, k, pad);
+  if (st != MEGAMOE_OK) return st;
+  if (!ws || !aligned(ws, 256) || !flags || (T > 0 && !out)) return MEGAMOE_ERR_INVALID_ARG;
+  if (out && !aligned(out, 16)) return MEGAMOE_ERR_UNSUPPORTED_SHAPE;
+  Workspace wk = carve(const_cast<void*>(ws), T, k, w->num_experts, w->hidden, w->intermediate,
+                       pad);
+  if (ws_bytes < wk.bytes) return MEGAMOE_ERR_WORKSPACE_TOO_SMALL;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (T == 0) return cuda_status(cudaMemsetAsync(flags, 0, sizeof(uint32_t), s));
+  return cuda_status(launch_stage_scan(wk.row_src, wk.padded_offsets + w->num_experts, wk.xq_sf,
+                                       wk.h, wk.hq_sf, wk.y, out, T, w->hidden, w->intermediate,
+                                       flags, s));
 }
 
 megamoe_status megamoe_round_bf16(const float* in, int64_t n, uint16_t* out,

@@ -59,7 +59,13 @@ SIGNATURES = {
     "megamoe_ep_forward_begin": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _SZ, _P]),
     "megamoe_ep_forward_end": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _SZ, _P]),
     "megamoe_round_bf16": (_I, [_P, _I64, _P, _P]),
+    "megamoe_forward_scan_stages": (_I, [_P, _I, _I, _I, _P, _P, _SZ, _P, _P]),
 }
+STAGE_XQ_SCALE = 0x01
+STAGE_H = 0x02
+STAGE_HQ_SCALE = 0x04
+STAGE_Y = 0x08
+STAGE_OUT = 0x10
 
 
 class MegaMoEError(RuntimeError):
@@ -421,6 +427,16 @@ class Forward:
         if code not in (OK, 5):
             raise MegaMoEError("megamoe_read_status", code)
         return int(bits.value)
+
+    def scan_stages(self, out=None) -> int:
+        """megamoe_forward_scan_stages after the last call: the STAGE_* bits of
+        every stage whose valid rows hold a non-finite value (synchronises)."""
+        out = self.out if out is None else out
+        flags = torch.empty(1, dtype=torch.int32, device=self.ws.device)
+        _check("megamoe_forward_scan_stages", load().megamoe_forward_scan_stages(
+            ctypes.byref(self.cw), self.T, self.k, self.pad, _p(out), self.ws_ptr, self.ws_bytes,
+            _p(flags), _stream()))
+        return int(flags.item()) & 0xFFFFFFFF
 
     def intermediates(self):
         """Views into the workspace (for debugging and stage-level tests)."""

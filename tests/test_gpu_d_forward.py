@@ -288,3 +288,38 @@ def test_forward_with_edge_blocks_in_the_weights(cuda_lib):
     _, inter = oracle.forward(x.float().numpy(), ids.numpy(), w.numpy(), ex, pad=32,
                               return_intermediates=True)
     check_forward(fwd, out, inter, ex, ids.numpy(), w.numpy(), what="edge blocks")
+
+
+@pytest.mark.parametrize("name", ["tiny", "decode"])
+def test_stage_scan_finds_the_stage_that_holds_a_nan(cuda_lib, name):
+    """megamoe_forward_scan_stages (the pages' stage-by-stage NaN hunt): clean
+    on a clean forward, also with NaN in the unwritten padding rows; a
+    non-finite value planted in a valid row of one stage sets that stage's
+    bit and no other."""
+    cfg = inputs.CONFIGS[name]
+    raw, weights = _weights(cfg)
+    x = inputs.make_activations(cfg).cuda()
+    ids, w = inputs.make_routing(cfg)
+    fwd = megamoe.Forward(weights, cfg.T, cfg.k, pad=32)
+    fwd.ws.fill_(0xFF)  # padding rows keep NaN patterns
+    out = fwd(x, ids.cuda(), w.cuda())
+    assert fwd.read_status() == 0
+    assert fwd.scan_stages() == 0
+    v = fwd.intermediates()
+    R = int(v["padded_offsets"][-1].item())
+    valid = torch.nonzero(v["row_src"][:R] >= 0).flatten()
+    assert (v["row_src"][:R] < 0).any() or R == valid.numel()
+    r = int(valid[valid.numel() // 2].item())
+    cases = [("xq_sf", megamoe.STAGE_XQ_SCALE, 0x7F), ("h", megamoe.STAGE_H, float("nan")),
+             ("hq_sf", megamoe.STAGE_HQ_SCALE, 0xFF), ("y", megamoe.STAGE_Y, float("inf"))]
+    for key, bit, bad in cases:
+        t = v[key]
+        keep = t[r, 3].clone()
+        t[r, 3] = bad
+        assert fwd.scan_stages() == bit, key
+        t[r, 3] = keep
+    assert fwd.scan_stages() == 0
+    keep = out[1, 5].clone()
+    out[1, 5] = float("nan")
+    assert fwd.scan_stages(out) == megamoe.STAGE_OUT
+    out[1, 5] = keep
