@@ -85,8 +85,12 @@ struct GemmCfg {
   // that global stores are 16-byte vectors along the feature axis (512 bytes
   // for bf16, 2 KB for float)
   static constexpr bool BF16_OUT = EPI == MEGAMOE_EPI_SILU_MUL || EPI == MEGAMOE_EPI_BF16;
+  // (the fp32 epilogue stores straight from registers: for each token a
+  // warp's 32 lanes hold 32 consecutive features, one 128-byte run, so it
+  // needs no staging and its shared memory goes to pipeline stages)
+  static constexpr bool STAGED = BF16_OUT || PARTIAL;
   static constexpr int STG_ROWS = BF16_OUT ? 8 : 16;
-  static constexpr int STG_BYTES = STG_ROWS * 32 * (BF16_OUT ? 2 : 4);
+  static constexpr int STG_BYTES = STAGED ? STG_ROWS * 32 * (BF16_OUT ? 2 : 4) : 0;
   static constexpr int STG_OFF = (TOFF_OFF + 4 * (MEGAMOE_MAX_EXPERTS + 1) + 15) / 16 * 16;
   static constexpr int SMEM = 1024 + STG_OFF + kEpiWarps * STG_BYTES;
   static constexpr uint32_t IDESC = idesc_nvf4(128, BN);
@@ -465,19 +469,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           }
         } else {
           tmem_ld_wait();
-          float* s = reinterpret_cast<float*>(stg);
+          // token n0 + j: lanes write features f0 .. f0 + 31, one 128-byte run
+          float* out = reinterpret_cast<float*>(p.out) + (row0 + n0) * p.ld_out + f0 + lane;
 #pragma unroll
-          for (int j = 0; j < 16; ++j) s[j * 32 + lane] = __uint_as_float(g[j]) * alpha0;
-          __syncwarp();
-          // 16 rows x 128 bytes = 128 chunks of 16 bytes, four per lane
-          float* out = reinterpret_cast<float*>(p.out);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int c = lane + 32 * i, r = c >> 3;
-            if (r < rows)
-              *reinterpret_cast<uint4*>(out + (row0 + n0 + r) * p.ld_out + f0 + 4 * (c & 7)) =
-                  reinterpret_cast<const uint4*>(stg)[c];
-          }
+          for (int j = 0; j < 16; ++j)
+            if (j < rows) out[j * p.ld_out] = __uint_as_float(g[j]) * alpha0;
         }
         __syncwarp();  // the staging buffer is rewritten by the next chunk
       }
@@ -750,9 +746,9 @@ cudaError_t launch_grouped_gemm(const GemmLaunch& g, cudaStream_t stream) {
     }
   } else {
     switch (bn) {
-      case 32: return launch_cfg<32, MEGAMOE_EPI_F32, 8>(maps, a, stream);
-      case 64: return launch_cfg<64, MEGAMOE_EPI_F32, 7>(maps, a, stream);
-      case 128: return launch_cfg<128, MEGAMOE_EPI_F32, 5>(maps, a, stream);
+      case 32: return launch_cfg<32, MEGAMOE_EPI_F32, 9>(maps, a, stream);
+      case 64: return launch_cfg<64, MEGAMOE_EPI_F32, 8>(maps, a, stream);
+      case 128: return launch_cfg<128, MEGAMOE_EPI_F32, 6>(maps, a, stream);
     }
   }
   return cudaErrorInvalidValue;
