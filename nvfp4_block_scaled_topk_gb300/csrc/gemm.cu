@@ -672,10 +672,20 @@ cudaError_t launch_grouped_gemm(const GemmLaunch& g, cudaStream_t stream) {
   // token-major tiles (256): 128-row boxes; otherwise BN-row boxes
   TokenMaps maps;
   const uint32_t box = bn == 256 ? 128u : static_cast<uint32_t>(bn);
-  if (!make_codes_map(&maps.codes, g.act_codes, static_cast<uint64_t>(g.act_rows), g.K / 2, box) ||
-      !make_scales_map(&maps.scales, g.act_scales, static_cast<uint64_t>(g.act_rows), g.K / 16,
-                       box))
+  const uint64_t rows = static_cast<uint64_t>(g.act_rows);
+  if (!make_codes_map(&maps.codes, g.act_codes, rows, g.K / 2, box) ||
+      !make_scales_map(&maps.scales, g.act_scales, rows, g.K / 16, box))
     return cudaErrorInvalidValue;
+  if (bn == 256) {  // short boxes for an expert's last tile of few rows
+    if (!make_codes_map(&maps.codes32, g.act_codes, rows, g.K / 2, 32) ||
+        !make_scales_map(&maps.scales32, g.act_scales, rows, g.K / 16, 32) ||
+        !make_codes_map(&maps.codes64, g.act_codes, rows, g.K / 2, 64) ||
+        !make_scales_map(&maps.scales64, g.act_scales, rows, g.K / 16, 64))
+      return cudaErrorInvalidValue;
+  } else {  // unused by weights-on-M tiles
+    maps.codes32 = maps.codes64 = maps.codes;
+    maps.scales32 = maps.scales64 = maps.scales;
+  }
   GemmArgs a{g.w_codes,        g.w_scales, g.w_gs,     g.act_gs, g.offsets,
              g.padded_offsets, g.out,      g.ld_out,   g.out_amax, g.status,
              wait_limit_ns(),  g.E,        g.N,        g.K,          g.early_weights ? 1 : 0,

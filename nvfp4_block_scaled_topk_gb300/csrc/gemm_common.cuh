@@ -53,11 +53,19 @@ struct GemmArgs {
 };
 
 // Tensor maps of the token tile: codes (128-byte swizzle) and row-major
-// block scales, boxes of the tile's token rows.
+// block scales, boxes of the tile's token rows.  Token-major launches also
+// carry 32- and 64-row boxes over the same matrices: an expert's last tile
+// that holds at most 32 (64) valid rows loads only those.
 struct TokenMaps {
   CUtensorMap codes;
   CUtensorMap scales;
+  CUtensorMap codes32, scales32, codes64, scales64;
 };
+
+// Rows of the token box for a 128-row tile with `rows` valid rows.
+__device__ __forceinline__ int short_box_rows(int rows) {
+  return rows <= 32 ? 32 : rows <= 64 ? 64 : 128;
+}
 
 // Token-major tiles (tokens on the MMA's M side, 256 weight rows on N).
 cudaError_t launch_grouped_gemm_tm(const TokenMaps& maps, const GemmArgs& a, int epilogue,

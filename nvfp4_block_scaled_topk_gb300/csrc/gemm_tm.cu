@@ -104,6 +104,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   if (warp == 0 && lane == 0) {
     prefetch_tensormap(&maps.codes);
     prefetch_tensormap(&maps.scales);
+    prefetch_tensormap(&maps.codes32);
+    prefetch_tensormap(&maps.scales32);
+    prefetch_tensormap(&maps.codes64);
+    prefetch_tensormap(&maps.scales64);
   }
   if (p.early_weights) {
     build_tile_offsets<128>(p.offsets, E, MT, s_toff, s_scan);
@@ -162,15 +166,29 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       uint32_t phase = 0;
       int issued = 0;
       bool ok = true;
+      auto rows_of = [&](const TileInfo& t) {
+        return __ldg(p.offsets + t.e + 1) - __ldg(p.offsets + t.e);
+      };
       TileInfo ti_next = decode_tile(blockIdx.x, s_toff, E, MT);
       int poff_next = __ldg(p.padded_offsets + ti_next.e);
+      int cnt_next = rows_of(ti_next);
       for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
         const TileInfo ti = ti_next;
         const int poff = poff_next;
+        const int cnt = cnt_next;
         if (tile + static_cast<int>(gridDim.x) < total) {
           ti_next = decode_tile(tile + gridDim.x, s_toff, E, MT, ti.e);
           poff_next = __ldg(p.padded_offsets + ti_next.e);
+          cnt_next = rows_of(ti_next);
         }
+        // an expert's last tile with at most 32 (64) valid rows loads only a
+        // 32 (64)-row token box; the MMA still computes 128 rows, and the
+        // rows past the box (stale shared memory) are never stored
+        const int box = short_box_rows(cnt - ti.nt * C::BM);
+        const CUtensorMap* map_c =
+            box == 32 ? &maps.codes32 : box == 64 ? &maps.codes64 : &maps.codes;
+        const CUtensorMap* map_s =
+            box == 32 ? &maps.scales32 : box == 64 ? &maps.scales64 : &maps.scales;
         int r0, r1;
         w_rows(ti.e, ti.mt, &r0, &r1);
         const int a_row0 = poff + ti.nt * C::BM;
@@ -189,19 +207,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             break;
           }
           uint8_t* sb = smem + stage * C::STAGE;
-          mbar_arrive_expect_tx(&sf_full[stage], C::SF_TX);
+          mbar_arrive_expect_tx(&sf_full[stage], C::SFW + box * 16);
           bulk_load(sb + C::OFF_SFW, sfw0 + kt * 2048, 2048, &sf_full[stage], pol_w);
           bulk_load(sb + C::OFF_SFW + 2048, sfw1 + kt * 2048, 2048, &sf_full[stage], pol_w);
-          tma_load_2d(sb + C::OFF_SFA_RAW, &maps.scales, &sf_full[stage], kt * 16, a_row0,
-                      pol_a);
-          mbar_arrive_expect_tx(&full[stage], C::TX);
+          tma_load_2d(sb + C::OFF_SFA_RAW, map_s, &sf_full[stage], kt * 16, a_row0, pol_a);
+          mbar_arrive_expect_tx(&full[stage], C::B_TILE + box * 128);
           if (C::SILU) {
             bulk_load(sb + C::OFF_B, wc0 + kt * 32768, 32768, &full[stage], pol_w);
           } else {
             bulk_load(sb + C::OFF_B, wc0 + kt * 16384, 16384, &full[stage], pol_w);
             bulk_load(sb + C::OFF_B + 16384, wc1 + kt * 16384, 16384, &full[stage], pol_w);
           }
-          tma_load_2d(sb + C::OFF_A, &maps.codes, &full[stage], kt * 128, a_row0, pol_a);
+          tma_load_2d(sb + C::OFF_A, map_c, &full[stage], kt * 128, a_row0, pol_a);
           ++issued;
           if (++stage == STAGES) {
             stage = 0;
