@@ -355,8 +355,8 @@ def measure_forward(cfg, args, dev, world, rank, local, with_e2e=True, with_cpu=
     def l2():
         megamoe.grouped_gemm(v["hq_codes"], v["hq_sf"], v["gs_h"], weights.w2_codes,
                              weights.w2_scales, weights.w2_gs.view(-1, 1), v["offsets"],
-                             v["padded_offsets"], megamoe.EPI_F32, expected_tokens=expected,
-                             out=v["y"], out_amax=None)
+                             v["padded_offsets"], megamoe.EPI_BFP16, expected_tokens=expected,
+                             out=v["y_buf"], out_amax=None)
 
     def timed(fn, n):
         for _ in range(3):
@@ -486,15 +486,16 @@ def measure_forward(cfg, args, dev, world, rank, local, with_e2e=True, with_cpu=
     a_row1 = cfg.d * (0.5 + 1 / 16)  # one quantised token row of x
     a_row2 = cfg.I * (0.5 + 1 / 16)  # one requantised row of h
     # per launch: the active experts' weights once, each routed row's
-    # activations in and its output row out
+    # activations in and its output row out (L2: BFP16, 2 bytes a value and
+    # one exponent byte per 32)
     l1_bytes = active * 2 * w_el + valid_slots * (a_row1 + cfg.I * 2)
-    l2_bytes = active * w_el + valid_slots * (a_row2 + cfg.d * 4)
+    l2_bytes = active * w_el + valid_slots * (a_row2 + cfg.d * (2 + 1 / 32))
     l1_flops = 4 * cfg.d * cfg.I * valid_slots
     l2_flops = 2 * cfg.d * cfg.I * valid_slots
     rl1 = gemm_roofline("k_grouped_gemm (L1 gate+up, SiLU*up epilogue)", l1_bytes, l1_flops,
                         l1_ms, hbm_gbs, fp4_tf, peak_kind,
                         _profile_traffic(f"l1_gemm_{cfg.name}.json"))
-    rl2 = gemm_roofline("k_grouped_gemm (L2 down, fp32 epilogue)", l2_bytes, l2_flops, l2_ms,
+    rl2 = gemm_roofline("k_grouped_gemm (L2 down, BFP16 epilogue)", l2_bytes, l2_flops, l2_ms,
                         hbm_gbs, fp4_tf, peak_kind,
                         _profile_traffic(f"l2_gemm_{cfg.name}.json"))
     t_floor = max(alg_bytes / (hbm_gbs * 1e9), flops / (fp4_tf * 1e12))

@@ -81,6 +81,29 @@ typedef enum megamoe_status {
 #define MEGAMOE_EPI_F32 0      /* out[r, n] = fp32 accumulator * alpha            */
 #define MEGAMOE_EPI_SILU_MUL 1 /* out[r, i] = bf16(silu(gate) * up), amax of it   */
 #define MEGAMOE_EPI_BF16 2     /* out[r, n] = bf16(fp32 accumulator * alpha)      */
+#define MEGAMOE_EPI_BFP16 3    /* out = BFP16 matrix of fp32 accumulator * alpha */
+
+/*
+ * BFP16 (16-bit block floating point): the storage of the forward's L2
+ * output y between the down GEMM and the combine (the pages fix no type for
+ * it; fp32 would double its round trip through HBM).  A [rows, ld] BFP16
+ * matrix holds one power-of-two exponent per group of 16 rows x 1 column
+ * (rows 16g .. 16g + 15 of column c).  It is one buffer of
+ * MEGAMOE_BFP16_BYTES(rows, ld) bytes:
+ *   bytes [0, 2*rows*ld)                        int16 values q[r*ld + c]
+ *   bytes [2*rows*ld, + ceil(rows/16)*ld)       int8 exponents s[(r/16)*ld + c]
+ *   element (r, c) = q * 2^s            (s <= 113)
+ *                  = fp16 value of the bits of q   (s = 127)
+ * Writing the fp32 values v of a group's written rows: with m = max |v| and
+ * E = floor(log2 m), s = max(E - 14, -126) and q = clamp(rint(v * 2^-s),
+ * -32767, 32767), so the group's largest values keep 15 significant bits
+ * (v * 2^-s is exact; the only rounding is to the integer); s = 0 and q = 0
+ * when all are zero.  A group holding Inf or NaN gets s = 127 and the fp16
+ * encoding of each value, so non-finite values pass through.  Rows that are
+ * not written (padding rows) take no part in their group's exponent.
+ */
+#define MEGAMOE_BFP16_BYTES(rows, ld) \
+  ((size_t)(rows) * (size_t)(ld) * 2 + ((size_t)(rows) + 15) / 16 * (size_t)(ld))
 
 /* Limits. */
 #define MEGAMOE_MAX_EXPERTS 1024
@@ -231,6 +254,10 @@ megamoe_status megamoe_pack_weight_codes(const uint8_t* src, int64_t rows, int K
  *   MEGAMOE_EPI_F32:      out float [act_rows, ld_out], out[r, n] = acc * alpha,
  *                         alpha = 1 / (act_gs * w_gs[e]).
  *   MEGAMOE_EPI_BF16:     out bf16 [act_rows, ld_out], out[r, n] = bf16(acc * alpha).
+ *   MEGAMOE_EPI_BFP16:    out BFP16 [act_rows, ld_out] of acc * alpha (the
+ *                         format above; ld_out a multiple of 32; a group is
+ *                         16 padded rows of one expert; weights-on-M tiles
+ *                         only: tile_n 256 runs as 128).
  *   MEGAMOE_EPI_SILU_MUL: N = 2I; out bf16 [act_rows, ld_out],
  *                         out[r, i] = bf16(silu(acc[r, i] * alpha_gate) *
  *                                          (acc[r, I + i] * alpha_up)),
@@ -344,6 +371,18 @@ megamoe_status megamoe_combine(const float* y, int64_t ld_y, const int32_t* slot
                                megamoe_stream_t stream);
 
 /*
+ * megamoe_combine_bfp16 -- the same combine over a BFP16 y of y_rows rows and
+ * leading dimension ld_y (the forward's own form of y): each element is
+ * decoded exactly into fp32, then summed in fp32 in ascending j and rounded
+ * once to bf16.  Requires d and ld_y multiples of 32, y 16-byte and out
+ * 8-byte aligned (else MEGAMOE_ERR_UNSUPPORTED_SHAPE); slot_dst entries must
+ * be below y_rows.
+ */
+megamoe_status megamoe_combine_bfp16(const void* y, int64_t ld_y, int64_t y_rows,
+                                     const int32_t* slot_dst, const float* topk_weights, int T,
+                                     int k, int d, uint16_t* out, megamoe_stream_t stream);
+
+/*
  * Workspace bytes megamoe_forward needs for these sizes (host-only).
  */
 size_t megamoe_workspace_size(int T, int k, int E, int d, int I, int pad);
@@ -352,7 +391,8 @@ size_t megamoe_workspace_size(int T, int k, int E, int d, int I, int pad);
  * megamoe_forward -- the whole routed-expert forward on one stream:
  * route -> amax(x) -> quantise x into routed rows -> L1 grouped GEMM with
  * SiLU(gate)*up and amax(h) in its epilogue -> requantise h -> L2 grouped
- * GEMM -> top-k weighted combine.
+ * GEMM into a BFP16 y -> top-k weighted combine (y decoded exactly, fp32
+ * sums, one bf16 rounding).
  *   x             [T, d] bf16 hidden_states
  *   topk_ids      [T, k] int32 (ids < 0 skipped)
  *   topk_weights  [T, k] float (used as given)
@@ -463,7 +503,8 @@ megamoe_status megamoe_round_bf16(const float* in, int64_t n, uint16_t* out,
  *   MEGAMOE_STAGE_XQ_SCALE  a block scale of the quantised x is an E4M3 NaN byte
  *   MEGAMOE_STAGE_H         h = bf16(SiLU(gate) * up) holds Inf or NaN
  *   MEGAMOE_STAGE_HQ_SCALE  a block scale of the requantised h is an E4M3 NaN byte
- *   MEGAMOE_STAGE_Y         the L2 output y (fp32) holds Inf or NaN
+ *   MEGAMOE_STAGE_Y         the L2 output y holds Inf or NaN (a BFP16 group
+ *                           of valid rows with exponent 127)
  *   MEGAMOE_STAGE_OUT       the combined output holds Inf or NaN
  * Reads every intermediate once (~3.7 GB at 16384 tokens): for diagnosis,
  * not the forward's path.  Asynchronous on `stream`.

@@ -50,8 +50,9 @@ struct Workspace {
   uint16_t* h;
   uint8_t* hq_codes;
   uint8_t* hq_sf;
-  float* y;
-  float* partial;  // split-K planes, shared by L1 and L2 (they run in turn)
+  uint16_t* y;     // the L2 output: a BFP16 [rows, d] matrix (int16 values ...
+  int8_t* y_exp;   // ... then the exponents [rows, d / 32])
+  float* partial;  // split-K planes of L1
   int32_t* r_ids;  // router outputs of megamoe_forward_from_logits [T, k]
   float* r_w;
   int32_t* route_hist;  // per-block expert histograms of the multi-block routing
@@ -99,7 +100,8 @@ void forward_splits(int T, int k, int E, int d, int I, int* ks1, int* ks2) {
   if (slots == 0 || forced < 2) return;
   const int tile_n = tile_n_setting(static_cast<double>(slots) / E);
   *ks1 = ksplit_setting(0.0, d / 256, tile_n);
-  *ks2 = ksplit_setting(0.0, I / 256, tile_n);
+  // L2 writes the BFP16 y, whose exponent groups need whole-K sums: not split
+  *ks2 = 1;
 }
 
 Workspace carve(void* base, int T, int k, int E, int d, int I, int pad) {
@@ -131,12 +133,13 @@ Workspace carve(void* base, int T, int k, int E, int d, int I, int pad) {
   w.h = reinterpret_cast<uint16_t*>(take(static_cast<size_t>(rows) * I * 2));
   w.hq_codes = take(static_cast<size_t>(rows) * (I / 2));
   w.hq_sf = take(static_cast<size_t>(rows) * (I / 16));
-  w.y = reinterpret_cast<float*>(take(static_cast<size_t>(rows) * d * 4));
+  uint8_t* y = take(MEGAMOE_BFP16_BYTES(rows, d));
+  w.y = reinterpret_cast<uint16_t*>(y);
+  w.y_exp = y ? reinterpret_cast<int8_t*>(y + static_cast<size_t>(rows) * d * 2) : nullptr;
   forward_splits(T, k, E, d, I, &w.ks1, &w.ks2);
   const size_t slots = static_cast<size_t>(T) * k;
   const size_t p1 = w.ks1 > 1 ? w.ks1 * slots * 2 * I : 0;
-  const size_t p2 = w.ks2 > 1 ? w.ks2 * slots * d : 0;
-  w.partial = reinterpret_cast<float*>(take(std::max(p1, p2) * 4));
+  w.partial = reinterpret_cast<float*>(take(p1 * 4));
   w.r_ids = reinterpret_cast<int32_t*>(take(4 * slots));
   w.r_w = reinterpret_cast<float*>(take(4 * slots));
   w.route_hist = reinterpret_cast<int32_t*>(
@@ -150,8 +153,8 @@ Workspace carve(void* base, int T, int k, int E, int d, int I, int pad) {
 // The L1 GEMM's tiles: where 128-token tiles are chosen, token-major tiles
 // (128 tokens x the gate and up rows of 128 features in one MMA) instead;
 // measured on the 4096- and 16384-token MegaMoE batches they take 5-6 % off
-// the L1 GEMM, while for the L2 GEMM (fp32 epilogue, 8 K steps per tile)
-// token-major tiles were slower, so L2 keeps the tile of tile_n_setting.
+// the L1 GEMM, while for the L2 GEMM (8 K steps per tile) token-major tiles
+// were slower, so L2 keeps the tile of tile_n_setting.
 int l1_tile(int tile_n) { return tile_n == 128 ? 256 : tile_n; }
 
 megamoe_status check_route_args(int T, int k, int E, int pad) {
@@ -297,7 +300,7 @@ megamoe_status megamoe_grouped_gemm(const uint8_t* act_codes, const uint8_t* act
                                     megamoe_stream_t stream) {
   if (act_rows < 0 || E < 1 || N <= 0 || K <= 0) return MEGAMOE_ERR_INVALID_ARG;
   if (epilogue != MEGAMOE_EPI_F32 && epilogue != MEGAMOE_EPI_SILU_MUL &&
-      epilogue != MEGAMOE_EPI_BF16)
+      epilogue != MEGAMOE_EPI_BF16 && epilogue != MEGAMOE_EPI_BFP16)
     return MEGAMOE_ERR_INVALID_ARG;
   if (E > MEGAMOE_MAX_EXPERTS || K % 256 != 0 || N % (epilogue == MEGAMOE_EPI_SILU_MUL ? 256 : 128))
     return MEGAMOE_ERR_UNSUPPORTED_SHAPE;
@@ -311,7 +314,9 @@ megamoe_status megamoe_grouped_gemm(const uint8_t* act_codes, const uint8_t* act
   const int width = epilogue == MEGAMOE_EPI_SILU_MUL ? N / 2 : N;
   if (ld_out < width) return MEGAMOE_ERR_INVALID_ARG;
   // output rows start on 16-byte boundaries: the epilogue stores 16-byte vectors
-  if (ld_out % (epilogue == MEGAMOE_EPI_F32 ? 4 : 8) != 0) return MEGAMOE_ERR_UNSUPPORTED_SHAPE;
+  // (BFP16: whole 32-column exponent groups)
+  if (ld_out % (epilogue == MEGAMOE_EPI_F32 ? 4 : epilogue == MEGAMOE_EPI_BFP16 ? 32 : 8) != 0)
+    return MEGAMOE_ERR_UNSUPPORTED_SHAPE;
   if (!w_codes || !w_scales || !w_gs || !offsets || !padded_offsets ||
       (act_rows > 0 && (!act_codes || !act_scales || !act_gs || !out)))
     return MEGAMOE_ERR_INVALID_ARG;
@@ -353,8 +358,21 @@ megamoe_status megamoe_combine(const float* y, int64_t ld_y, const int32_t* slot
   if (T > 0 && (!y || !slot_dst || !topk_weights || !out)) return MEGAMOE_ERR_INVALID_ARG;
   if (T > 0 && (!aligned(y, 16) || !aligned(out, 8))) return MEGAMOE_ERR_UNSUPPORTED_SHAPE;
   return cuda_status(
-      launch_combine(y, ld_y, slot_dst, topk_weights, T, k, d, out, false,
+      launch_combine(y, nullptr, ld_y, slot_dst, topk_weights, T, k, d, out, false,
                      reinterpret_cast<cudaStream_t>(stream)));
+}
+
+megamoe_status megamoe_combine_bfp16(const void* y, int64_t ld_y, int64_t y_rows,
+                                     const int32_t* slot_dst, const float* topk_weights, int T,
+                                     int k, int d, uint16_t* out, megamoe_stream_t stream) {
+  if (T < 0 || k < 1 || k > MEGAMOE_MAX_TOPK || d <= 0 || ld_y < d || y_rows < 0)
+    return MEGAMOE_ERR_INVALID_ARG;
+  if (d % 32 != 0 || ld_y % 32 != 0) return MEGAMOE_ERR_UNSUPPORTED_SHAPE;
+  if (T > 0 && (!y || !slot_dst || !topk_weights || !out)) return MEGAMOE_ERR_INVALID_ARG;
+  if (T > 0 && (!aligned(y, 16) || !aligned(out, 8))) return MEGAMOE_ERR_UNSUPPORTED_SHAPE;
+  const int8_t* y_exp = static_cast<const int8_t*>(y) + y_rows * ld_y * 2;
+  return cuda_status(launch_combine(y, y_exp, ld_y, slot_dst, topk_weights, T, k, d, out, false,
+                                    reinterpret_cast<cudaStream_t>(stream)));
 }
 
 size_t megamoe_workspace_size(int T, int k, int E, int d, int I, int pad) {
@@ -458,7 +476,7 @@ bool g_fused_requant = false;
 bool requant_fused(const Workspace& wk) { return g_fused_requant && wk.ks1 <= 1; }
 
 // Steps 5-7: requantise h with gs from the amax(h) held in the workspace, L2
-// down grouped GEMM -> fp32 y, top-k weighted combine (bf16 out, or the fp32
+// down grouped GEMM -> BFP16 y, top-k weighted combine (bf16 out, or the fp32
 // sum before its rounding with out_f32).
 cudaError_t forward_l2(const megamoe_weights* w, const float* topk_weights, int T, int k,
                        void* out, bool out_f32, const Workspace& wk, cudaStream_t s,
@@ -474,7 +492,7 @@ cudaError_t forward_l2(const megamoe_weights* w, const float* topk_weights, int 
                      MEGAMOE_SCALES_ROWMAJOR, s, /*slot_rows=*/true);
     if (e != cudaSuccess) return e;
   }
-  // 6. L2 down grouped GEMM -> fp32 y
+  // 6. L2 down grouped GEMM -> BFP16 y
   GemmLaunch g{};
   g.act_codes = wk.hq_codes;
   g.act_scales = wk.hq_sf;
@@ -488,16 +506,13 @@ cudaError_t forward_l2(const megamoe_weights* w, const float* topk_weights, int 
   g.K = I;
   g.offsets = wk.offsets;
   g.padded_offsets = wk.padded_offsets;
-  g.epilogue = MEGAMOE_EPI_F32;
+  g.epilogue = MEGAMOE_EPI_BFP16;
   g.out = wk.y;
   g.ld_out = d;
   g.out_amax = nullptr;
   g.tile_n = tile_n;
   g.status = wk.status;
   g.early_weights = true;
-  g.ksplit = wk.ks2;
-  g.partial = wk.partial;
-  g.partial_plane = static_cast<int64_t>(T) * k * d;
   {
     StageRange r("megamoe.l2_gemm");
     e = launch_grouped_gemm(g, s);
@@ -505,7 +520,7 @@ cudaError_t forward_l2(const megamoe_weights* w, const float* topk_weights, int 
   if (e != cudaSuccess) return e;
   // 7. top-k weighted combine
   StageRange r("megamoe.combine");
-  return launch_combine(wk.y, d, wk.slot_dst, topk_weights, T, k, d, out, out_f32, s);
+  return launch_combine(wk.y, wk.y_exp, d, wk.slot_dst, topk_weights, T, k, d, out, out_f32, s);
 }
 
 // The forward; with `router` the ids and weights are computed here from the
@@ -621,7 +636,7 @@ megamoe_status megamoe_forward_scan_stages(const megamoe_weights* w, int T, int 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (T == 0) return cuda_status(cudaMemsetAsync(flags, 0, sizeof(uint32_t), s));
   return cuda_status(launch_stage_scan(wk.row_src, wk.padded_offsets + w->num_experts, wk.xq_sf,
-                                       wk.h, wk.hq_sf, wk.y, out, T, w->hidden, w->intermediate,
+                                       wk.h, wk.hq_sf, wk.y_exp, out, T, w->hidden, w->intermediate,
                                        flags, s));
 }
 

@@ -3,9 +3,10 @@
 // "Test Plan -- Finding the NaN", Phase 1).  One thread per 4 consecutive
 // features of one token: 128-bit loads of each routed row of y (up to eight
 // slots' loads in flight at once), fp32 sums in ascending j, one bf16
-// rounding, 64-bit stores.  An expert-parallel shard writes the fp32 sum of
-// its own slots instead, and the shards' sums are added and rounded once
-// after the exchange (k_round_bf16).
+// rounding, 64-bit stores.  y is fp32, or (the forward) BFP16, then one
+// thread per 8 features (k_combine_bfp16).  An expert-parallel
+// shard writes the fp32 sum of its own slots instead, and the shards' sums
+// are added and rounded once after the exchange (k_round_bf16).
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -84,6 +85,93 @@ __global__ void __launch_bounds__(256) k_round_bf16(const float4* __restrict__ i
   }
 }
 
+// The combine over a BFP16 y: one thread per 8 consecutive features of one
+// token.  Per slot one 16-byte load of int16 values and one 8-byte load of
+// their exponents (16-row group r / 16, the same 8 columns), up to eight
+// slots in flight; each value decoded exactly, fp32 sums in ascending j, one
+// bf16 rounding, two 8-byte stores (or the fp32 sum of a shard's slots).
+template <bool F32_OUT>
+__global__ void __launch_bounds__(256) k_combine_bfp16(const uint16_t* __restrict__ y,
+                                                       const int8_t* __restrict__ y_exp,
+                                                       int64_t ld_y,
+                                                       const int32_t* __restrict__ slot_dst,
+                                                       const float* __restrict__ w, int T, int k,
+                                                       int d, void* __restrict__ out) {
+  pdl_wait();
+  pdl_trigger();
+  const int vecs = d / 8;
+  const int64_t total = static_cast<int64_t>(T) * vecs;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int t = (i >> 32) == 0 ? static_cast<int>(static_cast<uint32_t>(i) / static_cast<uint32_t>(vecs))
+                                 : static_cast<int>(i / vecs);
+    const int v = static_cast<int>(i - static_cast<int64_t>(t) * vecs);
+    float acc[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+    for (int j0 = 0; j0 < k; j0 += 8) {
+      int r[8];
+      float wt[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        r[j] = j0 + j < k ? __ldg(slot_dst + static_cast<int64_t>(t) * k + j0 + j) : -1;
+        wt[j] = j0 + j < k ? __ldg(w + static_cast<int64_t>(t) * k + j0 + j) : 0.f;
+      }
+      uint4 qv[8];
+      uint2 sv[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        if (r[j] >= 0) {
+          qv[j] = __ldg(reinterpret_cast<const uint4*>(y + r[j] * ld_y) + v);
+          sv[j] = __ldg(reinterpret_cast<const uint2*>(y_exp + (r[j] >> 4) * ld_y) + v);
+        } else {
+          qv[j] = make_uint4(0u, 0u, 0u, 0u);
+          sv[j] = make_uint2(0u, 0u);
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        if (r[j] < 0) continue;
+        const uint32_t qw[4] = {qv[j].x, qv[j].y, qv[j].z, qv[j].w};
+        // exponents of 100 and above (huge values, or 127: a group holding
+        // Inf or NaN) take the general decode
+        if (__vcmpges4(sv[j].x, 0x64646464u) | __vcmpges4(sv[j].y, 0x64646464u)) {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const int se = static_cast<int8_t>((e < 4 ? sv[j].x : sv[j].y) >> (8 * (e & 3)));
+            const float val = bfp16_decode(static_cast<uint16_t>(qw[e >> 1] >> (16 * (e & 1))), se);
+            acc[e] = fmaf(wt[j], val, acc[e]);
+          }
+          continue;
+        }
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const int se = static_cast<int8_t>((e < 4 ? sv[j].x : sv[j].y) >> (8 * (e & 3)));
+          // the int16 value, sign-extended from its half of the word
+          const int qi = e & 1 ? static_cast<int>(qw[e >> 1]) >> 16
+                               : static_cast<int>(qw[e >> 1] << 16) >> 16;
+          acc[e] = fmaf(wt[j], bfp16_value(qi, bfp16_pow2(se)), acc[e]);
+        }
+      }
+    }
+    if (F32_OUT) {  // the sum before its rounding (one shard's share of the output)
+      float4* o = reinterpret_cast<float4*>(static_cast<float*>(out) + static_cast<int64_t>(t) * d + 8 * v);
+      __stcs(o, make_float4(acc[0], acc[1], acc[2], acc[3]));
+      __stcs(o + 1, make_float4(acc[4], acc[5], acc[6], acc[7]));
+    } else {
+      uint32_t pk[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const __nv_bfloat162 b2 = __floats2bfloat162_rn(acc[2 * e], acc[2 * e + 1]);
+        pk[e] = *reinterpret_cast<const uint32_t*>(&b2);
+      }
+      uint2* o = reinterpret_cast<uint2*>(static_cast<uint16_t*>(out) + static_cast<int64_t>(t) * d + 8 * v);
+      o[0] = make_uint2(pk[0], pk[1]);
+      o[1] = make_uint2(pk[2], pk[3]);
+    }
+  }
+}
+
 // Up to 16 resident blocks of 256 threads per SM, grid-stride beyond that.
 static unsigned stream_blocks(int64_t tasks) {
   int64_t blocks = (tasks + 255) / 256;
@@ -91,16 +179,29 @@ static unsigned stream_blocks(int64_t tasks) {
   return static_cast<unsigned>(blocks > cap ? cap : blocks);
 }
 
-cudaError_t launch_combine(const float* y, int64_t ld_y, const int32_t* slot_dst, const float* w,
-                           int T, int k, int d, void* out, bool out_f32, cudaStream_t stream) {
+cudaError_t launch_combine(const void* y, const int8_t* y_exp, int64_t ld_y,
+                           const int32_t* slot_dst, const float* w, int T, int k, int d,
+                           void* out, bool out_f32, cudaStream_t stream) {
+  if (y_exp) {
+    const int64_t tasks = static_cast<int64_t>(T) * (d / 8);
+    if (tasks == 0) return cudaSuccess;
+    const dim3 grid(stream_blocks(tasks));
+    const uint16_t* yq = static_cast<const uint16_t*>(y);
+    if (out_f32)
+      return launch_pdl(k_combine_bfp16<true>, grid, dim3(256), 0, stream, yq, y_exp, ld_y,
+                        slot_dst, w, T, k, d, out);
+    return launch_pdl(k_combine_bfp16<false>, grid, dim3(256), 0, stream, yq, y_exp, ld_y,
+                      slot_dst, w, T, k, d, out);
+  }
   const int64_t tasks = static_cast<int64_t>(T) * (d / 4);
   if (tasks == 0) return cudaSuccess;
   const dim3 grid(stream_blocks(tasks));
+  const float* yf = static_cast<const float*>(y);
   if (out_f32)
-    return launch_pdl(k_combine<true>, grid, dim3(256), 0, stream, y, ld_y, slot_dst, w, T, k, d,
-                      out);
-  return launch_pdl(k_combine<false>, grid, dim3(256), 0, stream, y, ld_y, slot_dst, w, T, k, d,
-                    out);
+    return launch_pdl(k_combine<true>, grid, dim3(256), 0, stream, yf, ld_y, slot_dst, w, T, k,
+                      d, out);
+  return launch_pdl(k_combine<false>, grid, dim3(256), 0, stream, yf, ld_y, slot_dst, w, T, k,
+                    d, out);
 }
 
 cudaError_t launch_round_bf16(const float* in, int64_t n, uint16_t* out, cudaStream_t stream) {

@@ -10,6 +10,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_fp8.h>
 #include <stdint.h>
 
@@ -240,6 +241,51 @@ __host__ __device__ constexpr uint32_t idesc_nvf4(int M, int N) {
          | (1u << 10)                               // B format: E2M1
          | (static_cast<uint32_t>(N >> 3) << 17)    // N / 8
          | (static_cast<uint32_t>(M >> 4) << 24);   // M / 16 (scale format bit 23 = E4M3)
+}
+
+// ---------------------------------------------------------------------------
+// BFP16 (int16 values with one power-of-two exponent per 32 columns): the
+// storage of the forward's L2 output between the down GEMM and the combine
+// ---------------------------------------------------------------------------
+constexpr int kBfp16NonFinite = 127;  // exponent of a group holding Inf or NaN
+// 2^s for |s| <= 126: a normal float, so scaling by it is exact.
+__device__ __forceinline__ float bfp16_pow2(int s) {
+  return __uint_as_float(static_cast<uint32_t>(127 + s) << 23);
+}
+// Exponent of a group from the bits of its max |v| (sign bit clear):
+// s = max(floor(log2 m) - 14, -126), so that m * 2^-s < 2^15; 0 for an
+// all-zero group, kBfp16NonFinite when the group holds Inf or NaN.
+__device__ __forceinline__ int bfp16_exponent(uint32_t mbits) {
+  if (mbits >= 0x7f800000u) return kBfp16NonFinite;
+  if (mbits == 0u) return 0;
+  const int be = static_cast<int>(mbits >> 23);
+  return max(-126, (be == 0 ? -127 : be - 127) - 14);  // a subnormal m lies below 2^-126
+}
+// x (already scaled by 2^-s, so |x| < 2^15) -> int16 bits, clamped to
+// +-32767 and rounded to the nearest integer (ties to even): adding
+// 1.5 * 2^23 in round-to-nearest mode leaves the integer in the low mantissa
+// bits (valid for |x| < 2^22), and since 1.5 * 2^23 has no bits in the low
+// half, the low 16 bits of the sum are the integer's two's complement.  ALU
+// work only, no conversion unit.
+__device__ __forceinline__ uint16_t bfp16_round_int(float x) {
+  const float r = __fadd_rn(fminf(fmaxf(x, -32767.f), 32767.f), 12582912.f);
+  return static_cast<uint16_t>(__float_as_uint(r));
+}
+__device__ __forceinline__ uint16_t bfp16_encode(float v, int s) {
+  if (s == kBfp16NonFinite) return __half_as_ushort(__float2half_rn(v));
+  return bfp16_round_int(v * bfp16_pow2(-s));  // v * 2^-s is exact
+}
+// q * 2^s for |s| < 100, exactly: 1.5 * 2^23 + q has the bits 0x4B400000 +
+// q, and (A - 1.5 * 2^23) * P = A * P - 1.5 * 2^23 * P is one fused
+// multiply-add whose exact result q * P needs no rounding (for s >= 105 the
+// term 1.5 * 2^23 * P would overflow).
+__device__ __forceinline__ float bfp16_value(int q, float p) {
+  return __fmaf_rn(__uint_as_float(0x4B400000u + static_cast<uint32_t>(q)), p, -12582912.f * p);
+}
+// Any exponent: the int16 value converted, then scaled by 2^s (exact).
+__device__ __forceinline__ float bfp16_decode(uint16_t q, int s) {
+  if (s == kBfp16NonFinite) return __half2float(__ushort_as_half(q));
+  return static_cast<float>(static_cast<int16_t>(q)) * bfp16_pow2(s);
 }
 
 // ---------------------------------------------------------------------------

@@ -85,9 +85,11 @@ struct GemmCfg {
   // that global stores are 16-byte vectors along the feature axis (512 bytes
   // for bf16, 2 KB for float)
   static constexpr bool BF16_OUT = EPI == MEGAMOE_EPI_SILU_MUL || EPI == MEGAMOE_EPI_BF16;
-  // (the fp32 epilogue stores straight from registers: for each token a
-  // warp's 32 lanes hold 32 consecutive features, one 128-byte run, so it
-  // needs no staging and its shared memory goes to pipeline stages)
+  static constexpr bool BFP16 = EPI == MEGAMOE_EPI_BFP16;
+  // (the fp32 and BFP16 epilogues store straight from registers: for each
+  // token a warp's 32 lanes hold 32 consecutive features, one 128- or 64-byte
+  // run, so they need no staging and their shared memory goes to pipeline
+  // stages; a lane's 16 tokens of one feature are one BFP16 exponent group)
   static constexpr bool STAGED = BF16_OUT || PARTIAL;
   static constexpr int STG_ROWS = BF16_OUT ? 8 : 16;
   static constexpr int STG_BYTES = STAGED ? STG_ROWS * 32 * (BF16_OUT ? 2 : 4) : 0;
@@ -467,6 +469,33 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                   reinterpret_cast<const uint4*>(stg)[lane];
             __syncwarp();
           }
+        } else if (C::BFP16) {
+          tmem_ld_wait();
+          // rows row0 + n0 .. + 15 (16-aligned: pads and tiles are multiples
+          // of 16) of feature f0 + lane are one exponent group, all in this
+          // lane's registers: the max |v| of its written rows, then per token
+          // one 64-byte run of int16 values across the warp, and the warp's
+          // 32 exponents as one 32-byte run
+          float v[16];
+          uint32_t mbits = 0u;
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            v[j] = __uint_as_float(g[j]) * alpha0;
+            if (j < rows) mbits = max(mbits, __float_as_uint(v[j]) & 0x7fffffffu);
+          }
+          const int sg = bfp16_exponent(mbits);
+          uint16_t* q = reinterpret_cast<uint16_t*>(p.out) + (row0 + n0) * p.ld_out + f0 + lane;
+          if (sg != kBfp16NonFinite) {
+            const float sc = bfp16_pow2(-sg);
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              if (j < rows) q[j * p.ld_out] = bfp16_round_int(v[j] * sc);
+          } else {  // a group holding Inf or NaN: fp16 bits
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              if (j < rows) q[j * p.ld_out] = __half_as_ushort(__float2half_rn(v[j]));
+          }
+          p.out_exp[((row0 + n0) >> 4) * p.ld_out + f0 + lane] = static_cast<int8_t>(sg);
         } else {
           tmem_ld_wait();
           // token n0 + j: lanes write features f0 .. f0 + 31, one 128-byte run
@@ -668,7 +697,10 @@ int pick_tile_n(double expected) {
 
 cudaError_t launch_grouped_gemm(const GemmLaunch& g, cudaStream_t stream) {
   if (g.act_rows == 0 || g.E == 0) return cudaSuccess;
-  const int bn = g.tile_n;
+  const bool bfp16 = g.epilogue == MEGAMOE_EPI_BFP16;
+  // BFP16 runs on weights-on-M tiles, whole K
+  const int bn = bfp16 && g.tile_n == 256 ? 128 : g.tile_n;
+  if (bfp16 && (g.ksplit > 1 || g.ld_out % 32 != 0)) return cudaErrorInvalidValue;
   // token-major tiles (256): 128-row boxes; otherwise BN-row boxes
   TokenMaps maps;
   const uint32_t box = bn == 256 ? 128u : static_cast<uint32_t>(bn);
@@ -690,6 +722,8 @@ cudaError_t launch_grouped_gemm(const GemmLaunch& g, cudaStream_t stream) {
              g.padded_offsets, g.out,      g.ld_out,   g.out_amax, g.status,
              wait_limit_ns(),  g.E,        g.N,        g.K,          g.early_weights ? 1 : 0,
              g.ksplit,         g.partial,  g.partial_plane};
+  if (bfp16)
+    a.out_exp = reinterpret_cast<int8_t*>(g.out) + g.act_rows * g.ld_out * 2;
   if (g.epilogue == MEGAMOE_EPI_SILU_MUL && g.ksplit <= 1 && g.rq_arrivals) {
     if (!g.rq_codes || !g.rq_scales || !g.rq_gs || !g.out_amax) return cudaErrorInvalidValue;
     a.rq_arrivals = g.rq_arrivals;
@@ -753,6 +787,12 @@ cudaError_t launch_grouped_gemm(const GemmLaunch& g, cudaStream_t stream) {
       case 32: return launch_cfg<32, MEGAMOE_EPI_BF16, 8>(maps, a, stream);
       case 64: return launch_cfg<64, MEGAMOE_EPI_BF16, 7>(maps, a, stream);
       case 128: return launch_cfg<128, MEGAMOE_EPI_BF16, 5>(maps, a, stream);
+    }
+  } else if (bfp16) {
+    switch (bn) {
+      case 32: return launch_cfg<32, MEGAMOE_EPI_BFP16, 9>(maps, a, stream);
+      case 64: return launch_cfg<64, MEGAMOE_EPI_BFP16, 8>(maps, a, stream);
+      case 128: return launch_cfg<128, MEGAMOE_EPI_BFP16, 6>(maps, a, stream);
     }
   } else {
     switch (bn) {

@@ -50,6 +50,9 @@ struct GemmArgs {
   uint8_t* rq_codes;
   uint8_t* rq_scales;
   float* rq_gs;
+  // MEGAMOE_EPI_BFP16: the int8 exponents [rows / 16, ld_out] after the
+  // int16 values at `out`
+  int8_t* out_exp;
 };
 
 // Tensor maps of the token tile: codes (128-byte swizzle) and row-major

@@ -147,14 +147,16 @@ int num_sms();
 
 // out: bf16 [T, d] (one rounding of the fp32 sum), or with out_f32 the fp32
 // sum itself.
-cudaError_t launch_combine(const float* y, int64_t ld_y, const int32_t* slot_dst,
-                           const float* w, int T, int k, int d, void* out, bool out_f32,
-                           cudaStream_t stream);
+// y fp32 [*, ld_y] (y_exp null) or BFP16 (int16 values at y, exponents
+// [rows / 16, ld_y] at y_exp)
+cudaError_t launch_combine(const void* y, const int8_t* y_exp, int64_t ld_y,
+                           const int32_t* slot_dst, const float* w, int T, int k, int d,
+                           void* out, bool out_f32, cudaStream_t stream);
 // Non-finite scan of a forward's stage outputs (MEGAMOE_STAGE_* bits in
 // *flags, cleared first); valid rows only, every output row.
 cudaError_t launch_stage_scan(const int32_t* row_src, const int32_t* padded_total,
                               const uint8_t* xq_sf, const uint16_t* h, const uint8_t* hq_sf,
-                              const float* y, const uint16_t* out, int T, int d, int I,
+                              const int8_t* y_exp, const uint16_t* out, int T, int d, int I,
                               uint32_t* flags, cudaStream_t stream);
 // out[i] = bf16_rne(in[i]), n a multiple of 4.
 cudaError_t launch_round_bf16(const float* in, int64_t n, uint16_t* out, cudaStream_t stream);

@@ -28,6 +28,7 @@ SCALES_MMA = 1
 EPI_F32 = 0
 EPI_SILU_MUL = 1
 EPI_BF16 = 2
+EPI_BFP16 = 3  # BFP16: int16 values, then one int8 exponent per 16 rows x 1 column
 
 #: every function the header declares, with (restype, argtypes)
 _P = ctypes.c_void_p
@@ -45,6 +46,7 @@ SIGNATURES = {
     "megamoe_grouped_gemm": (_I, [_P, _P, _P, _I64, _P, _P, _P, _I, _I, _I, _P, _P, _I, _P, _I64,
                                   _P, _I, ctypes.c_double, _P, _P]),
     "megamoe_combine": (_I, [_P, _I64, _P, _P, _I, _I, _I, _P, _P]),
+    "megamoe_combine_bfp16": (_I, [_P, _I64, _I64, _P, _P, _I, _I, _I, _P, _P]),
     "megamoe_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I]),
     "megamoe_forward": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P, _SZ, _P]),
     "megamoe_read_status": (_I, [_P, _P, _P]),
@@ -243,26 +245,45 @@ def pack_weight_codes(codes: torch.Tensor, half_rows: int = 0) -> torch.Tensor:
     return dst
 
 
+def bfp16_bytes(rows: int, ld: int) -> int:
+    """Bytes of a BFP16 [rows, ld] matrix: int16 values, then int8 exponents
+    (one per 16 rows x 1 column)."""
+    return rows * ld * 2 + (rows + 15) // 16 * ld
+
+
 def grouped_gemm(act_codes, act_scales, act_gs, w_codes_packed, w_scales_mma, w_gs, offsets,
                  padded_offsets, epilogue=EPI_F32, tile_n=0, expected_tokens=0.0, out=None,
                  out_amax=None, status=None):
     """Grouped block-scaled GEMM; returns (out, out_amax).  ``w_codes_packed``
-    is [E, N, K/2]-shaped in the tile-major layout of pack_weight_codes."""
+    is [E, N, K/2]-shaped in the tile-major layout of pack_weight_codes.  For
+    EPI_BFP16 ``out`` is the uint8 buffer of a BFP16 [act_rows, N] matrix
+    (bfp16_bytes(act_rows, N) bytes)."""
     act_rows, half_k = act_codes.shape
     E, N, _ = w_codes_packed.shape
     w_codes = w_codes_packed
     K = half_k * 2
     dev = act_codes.device
     width = N // 2 if epilogue == EPI_SILU_MUL else N
-    if out is None:
-        dt = torch.float32 if epilogue == EPI_F32 else torch.bfloat16
-        out = torch.full((max(act_rows, 1), width), float("nan"), dtype=dt, device=dev)
+    if epilogue == EPI_BFP16:
+        if out is None:  # all-ones bytes wherever nothing is written
+            out = torch.full((bfp16_bytes(max(act_rows, 1), width),), 255, dtype=torch.uint8,
+                             device=dev)
+        if out.dtype != torch.uint8 or out.numel() < bfp16_bytes(act_rows, width):
+            raise ValueError("out must be a uint8 buffer of bfp16_bytes(act_rows, N) bytes")
+        ld_out = width
+    else:
+        if out is None:
+            dt = torch.float32 if epilogue == EPI_F32 else torch.bfloat16
+            out = torch.full((max(act_rows, 1), width), float("nan"), dtype=dt, device=dev)
+        ld_out = out.shape[1]
     if out_amax is None and epilogue == EPI_SILU_MUL:
         out_amax = torch.empty(1, dtype=torch.float32, device=dev)
     _check("megamoe_grouped_gemm", load().megamoe_grouped_gemm(
         _p(act_codes), _p(act_scales), _p(act_gs), act_rows, _p(w_codes), _p(w_scales_mma),
-        _p(w_gs), E, N, K, _p(offsets), _p(padded_offsets), epilogue, _p(out), out.shape[1],
+        _p(w_gs), E, N, K, _p(offsets), _p(padded_offsets), epilogue, _p(out), ld_out,
         _p(out_amax), tile_n, float(expected_tokens), _p(status), _stream()))
+    if epilogue == EPI_BFP16:
+        return out, out_amax
     return out[:act_rows], out_amax
 
 
@@ -320,6 +341,18 @@ def combine(y, slot_dst, topk_weights, out=None):
         out = torch.empty(T, d, dtype=torch.bfloat16, device=y.device)
     _check("megamoe_combine", load().megamoe_combine(
         _p(y), y.stride(0), _p(slot_dst), _p(topk_weights), T, k, d, _p(out), _stream()))
+    return out
+
+
+def combine_bfp16(y_buf, y_rows: int, d: int, slot_dst, topk_weights, out=None):
+    """The combine over a BFP16 y [y_rows, d] held in the uint8 buffer y_buf."""
+    T, k = topk_weights.shape
+    if y_buf.dtype != torch.uint8 or y_buf.numel() < bfp16_bytes(y_rows, d):
+        raise ValueError("y_buf must be a uint8 buffer of bfp16_bytes(y_rows, d) bytes")
+    if out is None:
+        out = torch.empty(T, d, dtype=torch.bfloat16, device=y_buf.device)
+    _check("megamoe_combine_bfp16", load().megamoe_combine_bfp16(
+        _p(y_buf), d, y_rows, _p(slot_dst), _p(topk_weights), T, k, d, _p(out), _stream()))
     return out
 
 
@@ -547,7 +580,7 @@ def _carve_views(ws, off, T, k, E, d, I, pad):
     take("h", rows * I * 2)
     take("hq_codes", rows * (I // 2))
     take("hq_sf", rows * (I // 16))
-    take("y", rows * d * 4)
+    take("y", bfp16_bytes(rows, d))  # BFP16: int16 values, then exponents
     hdr = views.pop("hdr")
     v = {
         "status": hdr[0:4].view(torch.int32),
@@ -565,7 +598,9 @@ def _carve_views(ws, off, T, k, E, d, I, pad):
         "h": views["h"].view(torch.bfloat16).view(rows, I),
         "hq_codes": views["hq_codes"].view(rows, I // 2),
         "hq_sf": views["hq_sf"].view(rows, I // 16),
-        "y": views["y"].view(torch.float32).view(rows, d),
+        "y": views["y"][:rows * d * 2].view(torch.int16).view(rows, d),
+        "y_exp": views["y"][rows * d * 2:].view(torch.int8).view((rows + 15) // 16, d),
+        "y_buf": views["y"],
         "rows": rows,
     }
     return v

@@ -87,8 +87,10 @@ def test_argument_errors_return_before_any_device_work(lib):
                                     fake, 0, fake, 256, P, 0, 0.0, P, P) == 2
     assert lib.megamoe_grouped_gemm(fake, fake, fake, 8, fake, fake, fake, 2, 256, 256, fake,
                                     fake, 0, fake, 256, P, 48, 0.0, P, P) == 1
-    # combine: d not a multiple of 4
+    # combine: d not a multiple of 4; BFP16 combine: d not a multiple of 32, y_rows < 0
     assert lib.megamoe_combine(fake, 6, fake, fake, 2, 2, 6, fake, P) == 2
+    assert lib.megamoe_combine_bfp16(fake, 48, 8, fake, fake, 2, 2, 48, fake, P) == 2
+    assert lib.megamoe_combine_bfp16(fake, 64, -1, fake, fake, 2, 2, 64, fake, P) == 1
     # forward: no weights; pad not a multiple of 32; workspace too small
     assert lib.megamoe_forward(P, fake, fake, fake, 1, 1, 32, fake, fake, 1 << 30, P) == 1
     w = megamoe.CWeights(8, 256, 512, 256, 256, 256, 256, 256, 256)
@@ -213,13 +215,18 @@ def test_stage_views_mirror_the_workspace_layout(lib, T, k, E, d, I, pad):
     regions = [("counts", 4 * E), ("offsets", 4 * (E + 1)), ("padded_offsets", 4 * (E + 1)),
                ("slot_dst", 4 * T * k), ("row_src", 4 * rows), ("xq_codes", rows * d // 2),
                ("xq_sf", rows * d // 16), ("h", rows * I * 2), ("hq_codes", rows * I // 2),
-               ("hq_sf", rows * I // 16), ("y", rows * d * 4)]
+               ("hq_sf", rows * I // 16), ("y_buf", rows * d * 2 + (rows + 15) // 16 * d)]
     a256 = lambda n: -(-n // 256) * 256
     off = 256  # the status word and the scalars
     for name, nbytes in regions:
         t = v[name]
         assert t.storage_offset() * t.element_size() == off, name
         assert t.numel() * t.element_size() == nbytes, name
+        if name == "y_buf":  # BFP16: the int16 values, then one exponent per 16 x 1
+            y, ye = v["y"], v["y_exp"]
+            assert y.storage_offset() * 2 == off and tuple(y.shape) == (rows, d)
+            assert ye.storage_offset() == off + rows * d * 2
+            assert tuple(ye.shape) == ((rows + 15) // 16, d)
         off = a256(off + nbytes)
     hist = 4 * 256 * E if T * k >= 16384 else 0
     assert size == off + 2 * a256(4 * T * k) + a256(hist)
@@ -287,9 +294,14 @@ def test_alignment_errors_return_before_any_device_work(lib):
                                       0, P, P) == 2
     # combine: y misaligned
     assert lib.megamoe_combine(odd, 8, a16, a16, 2, 2, 8, a16, P) == 2
-    # grouped GEMM: output rows not on 16-byte boundaries (bf16 ld of 4)
+    # grouped GEMM: output rows not on 16-byte boundaries (bf16 ld of 4); a
+    # BFP16 ld that does not hold whole 32-column exponent groups
     assert lib.megamoe_grouped_gemm(a16, a16, a16, 8, a16, a16, a16, 1, 256, 256, a16, a16, 2,
                                     a16, 260, P, 0, 0.0, P, P) == 2
+    assert lib.megamoe_grouped_gemm(a16, a16, a16, 8, a16, a16, a16, 1, 256, 256, a16, a16, 3,
+                                    a16, 272, P, 0, 0.0, P, P) == 2
+    # BFP16 combine: y misaligned
+    assert lib.megamoe_combine_bfp16(odd, 64, 8, a16, a16, 2, 2, 64, a16, P) == 2
     # forward: x misaligned; workspace not 256-byte aligned
     w = megamoe.CWeights(8, 256, 512, 4096, 4096, 4096, 4096, 4096, 4096)
     assert lib.megamoe_forward(ctypes.byref(w), odd, a16, a16, 4, 2, 32, a16, a16, 1 << 30,

@@ -1,7 +1,10 @@
 """megamoe_grouped_gemm (tcgen05 block-scaled NVFP4) against the oracle's
-float64 grouped GEMM on identical NVFP4 operands: the fp32 epilogue and the
-fused SiLU(gate)*up -> bf16 + amax epilogue, over every token tile, with
-ragged per-expert counts, zero-token experts and several tiles per expert."""
+float64 grouped GEMM on identical NVFP4 operands: the fp32 epilogue, the
+BFP16 epilogue (the forward's storage of y; bit-exact against the model of
+tests/helpers.py applied to the fp32 epilogue's output) and the fused
+SiLU(gate)*up -> bf16 + amax epilogue, over every token tile, with ragged
+per-expert counts, zero-token experts and several tiles per expert; the
+combine over fp32 and over BFP16 y."""
 
 import numpy as np
 import pytest
@@ -9,7 +12,8 @@ import torch
 
 import oracle
 from oracle import nvfp4 as q
-from helpers import assert_close, assert_close_bf16, bf16_tensor, random_experts
+from helpers import (assert_close, assert_close_bf16, bf16_tensor, bfp16_decode, bfp16_encode,
+                     bfp16_split, random_experts)
 
 pytestmark = pytest.mark.gpu
 
@@ -77,6 +81,47 @@ def test_grouped_gemm_f32_epilogue(cuda_lib, tile_n):
     assert np.all(np.isnan(got[~v]))  # padding rows untouched
 
 
+def _gemm(megamoe, ac, asc, ag, wcodes, wsc, wgs, rt, epi, tile_n):
+    out, amax = megamoe.grouped_gemm(
+        torch.from_numpy(ac).cuda(), torch.from_numpy(np.ascontiguousarray(asc)).cuda(),
+        torch.tensor([float(ag)], dtype=torch.float32).cuda(), wcodes, wsc, wgs,
+        torch.from_numpy(rt.offsets.astype(np.int32)).cuda(),
+        torch.from_numpy(rt.padded_offsets.astype(np.int32)).cuda(), epi, tile_n=tile_n)
+    torch.cuda.synchronize()
+    return out, amax
+
+
+def _check_bfp16(buf, f32_out, rt, R, n, want64, what):
+    """A BFP16 output against the model's encoding of the fp32 epilogue's
+    output on the same operands (bit-exact), untouched padding rows, and the
+    decoded values against the oracle."""
+    qv, sv = bfp16_split(buf, R, n)
+    v = rt.row_src >= 0
+    g = v[::16]  # 16-row groups holding valid rows (they come first in an expert)
+    q_want, s_want = bfp16_encode(f32_out, v)
+    assert np.array_equal(sv[g], s_want[g]), what
+    assert np.array_equal(qv[v], q_want[v]), what
+    assert np.all(qv[~v] == -1) and np.all(sv[~g] == -1), what  # 0xFF fill untouched
+    assert_close(bfp16_decode(qv, sv)[v], want64[v], what=what)
+
+
+@pytest.mark.parametrize("tile_n", [32, 64, 128, 256])
+def test_grouped_gemm_bfp16_epilogue(cuda_lib, tile_n):
+    """EPI_BFP16: the bytes are the BFP16 encoding of the fp32 epilogue's
+    values (the same fp32 accumulators times alpha) at the same weights-on-M
+    tile (tile 256 runs as 128)."""
+    from nvfp4_block_scaled_topk_gb300 import megamoe
+
+    E, d, I = len(COUNTS), 512, 256
+    rng, ex, stacked, rt, R = _setup(130 + tile_n, E, d, I, COUNTS)
+    a, ac, asc, ag = _quantised_rows(rng, rt, R, I, 0.5)
+    wcodes, wsc, wgs = _dev_weights(stacked, "w2", megamoe)
+    f32, _ = _gemm(megamoe, ac, asc, ag, wcodes, wsc, wgs, rt, megamoe.EPI_F32, min(tile_n, 128))
+    buf, _ = _gemm(megamoe, ac, asc, ag, wcodes, wsc, wgs, rt, megamoe.EPI_BFP16, tile_n)
+    want = oracle.grouped_gemm(ac, asc, ag, ex, "w2", rt, "f32")
+    _check_bfp16(buf, f32.cpu().numpy(), rt, R, d, want, f"bfp16 tile {tile_n}")
+
+
 @pytest.mark.parametrize("tile_n", [32, 64, 128, 256])
 def test_grouped_gemm_silu_mul_epilogue(cuda_lib, tile_n):
     from nvfp4_block_scaled_topk_gb300 import megamoe
@@ -141,6 +186,54 @@ def test_combine_matches_oracle(cuda_lib, T, k, d):
     torch.cuda.synchronize()
     want64 = oracle.combine(y.astype(np.float64), w, slot_dst, round_bf16=False)
     assert_close_bf16(out.float().cpu().numpy(), want64, what="combine")
+
+
+@pytest.mark.parametrize("T,k,d", [(64, 2, 256), (8, 6, 7168), (333, 6, 1024)])
+def test_combine_bfp16_matches_oracle(cuda_lib, T, k, d):
+    """The combine over a BFP16 y: each element decoded exactly, so against
+    the oracle's combine of the decoded values; a group holding NaN or Inf
+    (exponent 127) passes its values through to the output."""
+    from nvfp4_block_scaled_topk_gb300 import megamoe
+
+    rng = np.random.default_rng(160 + T)
+    rows = (T * k + 40 + 15) // 16 * 16
+    y = (rng.standard_normal((rows, d)) * np.exp(rng.uniform(-8, 8, (rows, 1)))).astype(np.float32)
+    slot_dst = rng.permutation(rows)[:T * k].astype(np.int32)
+    slot_dst[rng.random(T * k) < 0.1] = -1  # skipped slots
+    w = rng.random((T, k)).astype(np.float32)
+    qv, sv = bfp16_encode(y)
+    buf = np.concatenate([qv.reshape(-1).view(np.uint8), sv.reshape(-1).view(np.uint8)])
+    out = megamoe.combine_bfp16(torch.from_numpy(buf).cuda(), rows, d,
+                                torch.from_numpy(slot_dst).cuda(), torch.from_numpy(w).cuda())
+    torch.cuda.synchronize()
+    assert (sv != 0).any() and (np.diff(sv, axis=0) != 0).any()  # exponents vary by group
+    want64 = oracle.combine(bfp16_decode(qv, sv), w, slot_dst, round_bf16=False)
+    assert_close_bf16(out.float().cpu().numpy(), want64, what="combine bfp16")
+    # groups of huge values (exponents 100 and above take the general decode)
+    yh = y.copy()
+    yh[:16] = (rng.standard_normal((16, d)) * 2.0 ** 115).astype(np.float32)
+    qh, sh = bfp16_encode(yh)
+    assert sh[0].min() >= 100
+    buf = np.concatenate([qh.reshape(-1).view(np.uint8), sh.reshape(-1).view(np.uint8)])
+    out = megamoe.combine_bfp16(torch.from_numpy(buf).cuda(), rows, d,
+                                torch.from_numpy(slot_dst).cuda(), torch.from_numpy(w).cuda())
+    want64 = oracle.combine(bfp16_decode(qh, sh), w, slot_dst, round_bf16=False)
+    huge = np.isin(slot_dst.reshape(T, k), np.arange(16)).any(axis=1)
+    assert huge.any()
+    assert_close_bf16(out.float().cpu().numpy()[huge], want64[huge], what="combine bfp16 huge")
+    # a NaN in one group of one routed row reaches exactly that token's group
+    t = int(np.nonzero((slot_dst.reshape(T, k) >= 0).any(axis=1))[0][0])
+    j = int(np.nonzero(slot_dst.reshape(T, k)[t] >= 0)[0][0])
+    r = int(slot_dst[t * k + j])
+    y[r, 33] = np.nan
+    qv, sv = bfp16_encode(y)
+    assert sv[r // 16, 33] == 127
+    buf = np.concatenate([qv.reshape(-1).view(np.uint8), sv.reshape(-1).view(np.uint8)])
+    out = megamoe.combine_bfp16(torch.from_numpy(buf).cuda(), rows, d,
+                                torch.from_numpy(slot_dst).cuda(),
+                                torch.from_numpy(w).cuda()).float().cpu().numpy()
+    bad = np.isnan(out)
+    assert bad[t, 33] and bad.sum() == 1
 
 
 def test_pack_weight_codes_layout(cuda_lib):
@@ -269,3 +362,6 @@ def test_grouped_gemm_real_shape_prefill_tiles(cuda_lib, which, tile_n):
         err, _ = assert_close(got[v], want[v], what=f"L2 tile {tile_n}")
         assert err < 1e-5  # identical operands: only fp32 accumulation differs
         assert np.all(np.isnan(got[~v]))  # padding rows untouched
+        if tile_n == 128:  # the forward's L2: BFP16 of the same values
+            buf, _ = _gemm(megamoe, ac, asc, ag, wcodes, wsc, wgs, rt, megamoe.EPI_BFP16, 128)
+            _check_bfp16(buf, out.cpu().numpy(), rt, R, d, want, "L2 bfp16 tile 128")

@@ -311,13 +311,15 @@ def test_stage_scan_finds_the_stage_that_holds_a_nan(cuda_lib, name):
     assert (v["row_src"][:R] < 0).any() or R == valid.numel()
     r = int(valid[valid.numel() // 2].item())
     cases = [("xq_sf", megamoe.STAGE_XQ_SCALE, 0x7F), ("h", megamoe.STAGE_H, float("nan")),
-             ("hq_sf", megamoe.STAGE_HQ_SCALE, 0xFF), ("y", megamoe.STAGE_Y, float("inf"))]
+             ("hq_sf", megamoe.STAGE_HQ_SCALE, 0xFF),
+             ("y_exp", megamoe.STAGE_Y, 127)]  # a BFP16 group holding Inf or NaN
     for key, bit, bad in cases:
         t = v[key]
-        keep = t[r, 3].clone()
-        t[r, 3] = bad
+        i = r // 16 if key == "y_exp" else r  # one exponent row per 16 rows
+        keep = t[i, 3].clone()
+        t[i, 3] = bad
         assert fwd.scan_stages() == bit, key
-        t[r, 3] = keep
+        t[i, 3] = keep
     assert fwd.scan_stages() == 0
     keep = out[1, 5].clone()
     out[1, 5] = float("nan")
