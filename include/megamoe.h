@@ -95,9 +95,10 @@ typedef enum megamoe_status {
  *   element (r, c) = q * 2^s            (s <= 113)
  *                  = fp16 value of the bits of q   (s = 127)
  * Writing the fp32 values v of a group's written rows: with m = max |v| and
- * E = floor(log2 m), s = max(E - 14, -126) and q = clamp(rint(v * 2^-s),
- * -32767, 32767), so the group's largest values keep 15 significant bits
- * (v * 2^-s is exact; the only rounding is to the integer); s = 0 and q = 0
+ * E = floor(log2 m), s = max(E - 14, -126), plus one when m * 2^-s >=
+ * 32767.5 (so that no value rounds to 2^15), and q = rint(v * 2^-s) (ties to
+ * even); the group's largest values keep 15 significant bits (v * 2^-s is
+ * exact; the only rounding is to the integer, |q| <= 32767); s = 0 and q = 0
  * when all are zero.  A group holding Inf or NaN gets s = 127 and the fp16
  * encoding of each value, so non-finite values pass through.  Rows that are
  * not written (padding rows) take no part in their group's exponent.

@@ -261,19 +261,18 @@ __device__ __forceinline__ int bfp16_exponent(uint32_t mbits) {
   const int be = static_cast<int>(mbits >> 23);
   return max(-126, (be == 0 ? -127 : be - 127) - 14);  // a subnormal m lies below 2^-126
 }
-// x (already scaled by 2^-s, so |x| < 2^15) -> int16 bits, clamped to
-// +-32767 and rounded to the nearest integer (ties to even): adding
-// 1.5 * 2^23 in round-to-nearest mode leaves the integer in the low mantissa
-// bits (valid for |x| < 2^22), and since 1.5 * 2^23 has no bits in the low
-// half, the low 16 bits of the sum are the integer's two's complement.  ALU
-// work only, no conversion unit.
-__device__ __forceinline__ uint16_t bfp16_round_int(float x) {
-  const float r = __fadd_rn(fminf(fmaxf(x, -32767.f), 32767.f), 12582912.f);
-  return static_cast<uint16_t>(__float_as_uint(r));
+// The group exponent given the group max m (finite, nonzero): s from
+// bfp16_exponent, plus one when m * 2^-s would round to 2^15.
+__device__ __forceinline__ int bfp16_exponent_fit(float m, int s) {
+  return m * bfp16_pow2(-s) >= 32767.5f ? s + 1 : s;
 }
-__device__ __forceinline__ uint16_t bfp16_encode(float v, int s) {
-  if (s == kBfp16NonFinite) return __half_as_ushort(__float2half_rn(v));
-  return bfp16_round_int(v * bfp16_pow2(-s));  // v * 2^-s is exact
+// x (already scaled by 2^-s, |x| < 32767.5) -> int16 bits, rounded to the
+// nearest integer (ties to even): adding 1.5 * 2^23 in round-to-nearest mode
+// leaves the integer in the low mantissa bits (valid for |x| < 2^22), and
+// since 1.5 * 2^23 has no bits in the low half, the low 16 bits of the sum
+// are the integer's two's complement.  ALU work only, no conversion unit.
+__device__ __forceinline__ uint16_t bfp16_round_int(float x) {
+  return static_cast<uint16_t>(__float_as_uint(__fadd_rn(x, 12582912.f)));
 }
 // q * 2^s for |s| < 100, exactly: 1.5 * 2^23 + q has the bits 0x4B400000 +
 // q, and (A - 1.5 * 2^23) * P = A * P - 1.5 * 2^23 * P is one fused

@@ -483,9 +483,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             v[j] = __uint_as_float(g[j]) * alpha0;
             if (j < rows) mbits = max(mbits, __float_as_uint(v[j]) & 0x7fffffffu);
           }
-          const int sg = bfp16_exponent(mbits);
+          int sg = bfp16_exponent(mbits);
           uint16_t* q = reinterpret_cast<uint16_t*>(p.out) + (row0 + n0) * p.ld_out + f0 + lane;
           if (sg != kBfp16NonFinite) {
+            sg = bfp16_exponent_fit(__uint_as_float(mbits), sg);
             const float sc = bfp16_pow2(-sg);
 #pragma unroll
             for (int j = 0; j < 16; ++j)

@@ -272,10 +272,15 @@ def grouped_gemm(act_codes, act_scales, act_gs, w_codes_packed, w_scales_mma, w_
             raise ValueError("out must be a uint8 buffer of bfp16_bytes(act_rows, N) bytes")
         ld_out = width
     else:
+        dt = torch.float32 if epilogue == EPI_F32 else torch.bfloat16
         if out is None:
-            dt = torch.float32 if epilogue == EPI_F32 else torch.bfloat16
             out = torch.full((max(act_rows, 1), width), float("nan"), dtype=dt, device=dev)
-        ld_out = out.shape[1]
+        # the library writes act_rows rows of ld_out elements of this type
+        if (out.dtype != dt or out.dim() != 2 or out.shape[0] < act_rows or out.shape[1] < width
+                or out.stride(1) != 1 or out.device != dev):
+            raise ValueError(f"out must be a {dt} tensor of at least [{act_rows}, {width}] "
+                             "with unit column stride on the activations' device")
+        ld_out = out.stride(0)
     if out_amax is None and epilogue == EPI_SILU_MUL:
         out_amax = torch.empty(1, dtype=torch.float32, device=dev)
     _check("megamoe_grouped_gemm", load().megamoe_grouped_gemm(

@@ -250,8 +250,8 @@ BFP16_NONFINITE = 127
 def bfp16_exponents(v32, valid=None):
     """Per group of 16 rows x 1 column of a float32 [rows, n] array (rows a
     multiple of 16), over the group's written rows (``valid``, default all):
-    s = max(floor(log2 max|v|) - 14, -126); 0 when they are all zero, 127
-    when they hold Inf or NaN."""
+    s = max(floor(log2 max|v|) - 14, -126), plus one when max|v| * 2^-s >=
+    32767.5; 0 when they are all zero, 127 when they hold Inf or NaN."""
     v32 = np.asarray(v32, dtype=np.float32)
     rows, n = v32.shape
     bits = v32.view(np.uint32) & np.uint32(0x7FFFFFFF)
@@ -260,6 +260,8 @@ def bfp16_exponents(v32, valid=None):
     bits = bits.reshape(rows // 16, 16, n).max(axis=1)
     be = (bits >> 23).astype(np.int64)
     s = np.maximum(np.where(be == 0, -127, be - 127) - 14, -126)
+    m = bits.view(np.float32).astype(np.float64)
+    s = np.where(np.ldexp(m, -s) >= 32767.5, s + 1, s)
     s = np.where(bits == 0, 0, s)
     return np.where(bits >= 0x7F800000, BFP16_NONFINITE, s).astype(np.int8)
 
@@ -274,7 +276,10 @@ def bfp16_encode(v32, valid=None):
     nonfin = se == BFP16_NONFINITE
     scaled = np.ldexp(v32.astype(np.float64), np.where(nonfin, 0, -se))  # exact
     with np.errstate(invalid="ignore", over="ignore"):
-        q = np.clip(np.rint(np.where(nonfin, 0.0, scaled)), -32767, 32767).astype(np.int16)
+        q = np.rint(np.where(nonfin, 0.0, scaled))
+        rows_ok = np.ones(q.shape[0], bool) if valid is None else np.asarray(valid)
+        assert np.all(np.abs(q[rows_ok]) <= 32767)  # by the choice of s
+        q = np.clip(q, -32768, 32767).astype(np.int16)  # rows outside `valid`: any bits
         half = v32.astype(np.float16).view(np.int16)  # used only in non-finite groups
     return np.where(nonfin, half, q).astype(np.int16), s
 

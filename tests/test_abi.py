@@ -308,3 +308,27 @@ def test_alignment_errors_return_before_any_device_work(lib):
                                P) == 2
     assert lib.megamoe_forward(ctypes.byref(w), a16, a16, a16, 4, 2, 32, a16, odd, 1 << 30,
                                P) == 1
+
+
+def test_binding_refuses_an_output_buffer_that_does_not_fit_the_epilogue():
+    """megamoe.grouped_gemm checks the output's type and size against the
+    epilogue before anything is launched: an fp32 epilogue into a narrower
+    buffer (the BFP16 y's int16 view) or a too-short one is an error, not a
+    write past the buffer."""
+    import pytest
+    import torch
+
+    E, N, K, rows = 2, 256, 256, 64
+    act = torch.zeros(rows, K // 2, dtype=torch.uint8)
+    sf = torch.zeros(rows, K // 16, dtype=torch.uint8)
+    w = torch.zeros(E, N, K // 2, dtype=torch.uint8)
+    ws = torch.zeros(E * N, K // 16, dtype=torch.uint8)
+    gs = torch.ones(E)
+    offs = torch.zeros(E + 1, dtype=torch.int32)
+    for bad in (torch.zeros(rows, N, dtype=torch.int16), torch.zeros(rows - 1, N),
+                torch.zeros(rows, N - 4)):
+        with pytest.raises(ValueError):
+            megamoe.grouped_gemm(act, sf, gs[:1], w, ws, gs, offs, offs, megamoe.EPI_F32, out=bad)
+    with pytest.raises(ValueError):  # BFP16 wants the byte buffer of bfp16_bytes(rows, N)
+        megamoe.grouped_gemm(act, sf, gs[:1], w, ws, gs, offs, offs, megamoe.EPI_BFP16,
+                             out=torch.zeros(megamoe.bfp16_bytes(rows, N) - 1, dtype=torch.uint8))

@@ -26,9 +26,13 @@ def test_exponent_puts_the_group_max_just_below_2_to_15():
     # max 3.0 (floor(log2) = 1): s = -13, q = 3 * 2^13 = 24576
     q, s = bfp16_encode(_group([3.0, 1.0]))
     assert s[0, 0] == -13 and q[0, 0] == 24576 and q[1, 0] == 8192
-    # just below the next power of two: 2^15 - 2^-9 rounds to 32768, clamped
+    # a max whose scaled value would round to 2^15 takes the next exponent
     q, s = bfp16_encode(_group([np.nextafter(np.float32(2.0), np.float32(0)), -2.0 + 2 ** -23]))
-    assert s[0, 0] == -14 and q[0, 0] == 32767 and q[1, 0] == -32767
+    assert s[0, 0] == -13 and q[0, 0] == 16384 and q[1, 0] == -16384
+    q, s = bfp16_encode(_group([1.99996]))  # fl32(1.99996) * 2^14 = 32767.34
+    assert s[0, 0] == -14 and q[0, 0] == 32767
+    q, s = bfp16_encode(_group([1.99997]))  # fl32(1.99997) * 2^14 = 32767.51
+    assert s[0, 0] == -13 and q[0, 0] == 16384
     # ties go to even: v * 2^14 = 8192.5 -> 8192, 8193.5 -> 8194
     q, s = bfp16_encode(_group([1.0, 0.5 + 2.0 ** -15, 0.5 + 3 * 2.0 ** -15]))
     assert q[1, 0] == 8192 and q[2, 0] == 8194
@@ -50,7 +54,7 @@ def test_zero_group_huge_and_tiny_values():
     # the largest float32 keeps 15 bits: s = 127 - 14 = 113
     big = np.finfo(np.float32).max
     q, s = bfp16_encode(_group([big, -big / 2]))
-    assert s[0, 0] == 113 and q[0, 0] == 32767 and q[1, 0] == -16384
+    assert s[0, 0] == 114 and q[0, 0] == 16384 and q[1, 0] == -8192
     assert abs(bfp16_decode(q, s)[0, 0] - float(big)) <= float(big) * 2.0 ** -15
     # tiny groups clamp at -126 (q = v * 2^126)
     q, s = bfp16_encode(_group([1e-37, 3e-38]))
@@ -78,13 +82,10 @@ def test_round_trip_error_is_half_a_unit_of_the_group():
     back = bfp16_decode(q, s)
     unit = np.ldexp(1.0, np.repeat(s.astype(np.int64), 16, axis=0))
     err = np.abs(back - v.astype(np.float64))
-    # half a unit, or a whole unit where the clamp at 32767 applied
-    clamped = np.abs(v.astype(np.float64)) / unit > 32767
-    assert np.all(err[~clamped] <= unit[~clamped] / 2)
-    assert np.all(err[clamped] <= unit[clamped])
+    assert np.all(err <= unit / 2)  # half a unit of the group
     # each group's max keeps 15 significant bits
     m = np.abs(v).reshape(4, 16, 256).max(axis=1)
-    assert np.all(m.astype(np.float64) / unit[::16] >= 2.0 ** 14)
+    assert np.all(m.astype(np.float64) / unit[::16] >= 16383.75)
 
 
 def test_bfp16_y_leaves_the_forward_well_inside_the_stated_tolerance():
