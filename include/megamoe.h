@@ -87,24 +87,25 @@ typedef enum megamoe_status {
  * BFP16 (16-bit block floating point): the storage of the forward's L2
  * output y between the down GEMM and the combine (the pages fix no type for
  * it; fp32 would double its round trip through HBM).  A [rows, ld] BFP16
- * matrix holds one power-of-two exponent per group of 16 rows x 1 column
- * (rows 16g .. 16g + 15 of column c).  It is one buffer of
- * MEGAMOE_BFP16_BYTES(rows, ld) bytes:
- *   bytes [0, 2*rows*ld)                        int16 values q[r*ld + c]
- *   bytes [2*rows*ld, + ceil(rows/16)*ld)       int8 exponents s[(r/16)*ld + c]
- *   element (r, c) = q * 2^s            (s <= 113)
- *                  = fp16 value of the bits of q   (s = 127)
+ * matrix (ld a multiple of 32) holds one power-of-two exponent per group of
+ * 16 rows x 8 columns (rows 16g .. 16g + 15, columns 8c .. 8c + 7).  It is one
+ * buffer of MEGAMOE_BFP16_BYTES(rows, ld) bytes:
+ *   bytes [0, 2*rows*ld)                          uint16 values u[r*ld + c]
+ *   bytes [2*rows*ld, + ceil(rows/16)*(ld/8))     int8 exponents s[(r/16)*(ld/8) + c/8]
+ *   element (r, c) = (u - 32768) * 2^s              (s <= 114)
+ *                  = fp16 value of the bits of u    (s = 127)
  * Writing the fp32 values v of a group's written rows: with m = max |v| and
- * E = floor(log2 m), s = max(E - 14, -126), plus one when m * 2^-s >=
- * 32767.5 (so that no value rounds to 2^15), and q = rint(v * 2^-s) (ties to
- * even); the group's largest values keep 15 significant bits (v * 2^-s is
- * exact; the only rounding is to the integer, |q| <= 32767); s = 0 and q = 0
- * when all are zero.  A group holding Inf or NaN gets s = 127 and the fp16
- * encoding of each value, so non-finite values pass through.  Rows that are
- * not written (padding rows) take no part in their group's exponent.
+ * E = floor(log2 m), s = max(E - 14, -126), plus one when m * 2^-s >= 32767.5,
+ * and u = rint(v * 2^-s) + 32768 (ties to even; |rint| <= 32767), so the
+ * group's largest values keep 15 significant bits (v * 2^-s is exact; the
+ * only rounding is to the integer); s = 0 and u = 32768 when all are zero.
+ * A group holding Inf or NaN gets s = 127 and the fp16 encoding of each
+ * value, so non-finite values pass through.  Rows that are not written
+ * (padding rows) take no part in their group's exponent.  (A value within
+ * 2^-16 of the largest float decodes to Inf.)
  */
 #define MEGAMOE_BFP16_BYTES(rows, ld) \
-  ((size_t)(rows) * (size_t)(ld) * 2 + ((size_t)(rows) + 15) / 16 * (size_t)(ld))
+  ((size_t)(rows) * (size_t)(ld) * 2 + ((size_t)(rows) + 15) / 16 * ((size_t)(ld) / 8))
 
 /* Limits. */
 #define MEGAMOE_MAX_EXPERTS 1024
@@ -256,9 +257,9 @@ megamoe_status megamoe_pack_weight_codes(const uint8_t* src, int64_t rows, int K
  *                         alpha = 1 / (act_gs * w_gs[e]).
  *   MEGAMOE_EPI_BF16:     out bf16 [act_rows, ld_out], out[r, n] = bf16(acc * alpha).
  *   MEGAMOE_EPI_BFP16:    out BFP16 [act_rows, ld_out] of acc * alpha (the
- *                         format above; ld_out a multiple of 32; a group is
- *                         16 padded rows of one expert; weights-on-M tiles
- *                         only: tile_n 256 runs as 128).
+ *                         format above; ld_out a multiple of 32; a group's
+ *                         rows are 16 padded rows of one expert; weights-on-M
+ *                         tiles only: tile_n 256 runs as 128).
  *   MEGAMOE_EPI_SILU_MUL: N = 2I; out bf16 [act_rows, ld_out],
  *                         out[r, i] = bf16(silu(acc[r, i] * alpha_gate) *
  *                                          (acc[r, I + i] * alpha_up)),

@@ -86,10 +86,13 @@ __global__ void __launch_bounds__(256) k_round_bf16(const float4* __restrict__ i
 }
 
 // The combine over a BFP16 y: one thread per 8 consecutive features of one
-// token.  Per slot one 16-byte load of int16 values and one 8-byte load of
-// their exponents (16-row group r / 16, the same 8 columns), up to eight
-// slots in flight; each value decoded exactly, fp32 sums in ascending j, one
-// bf16 rounding, two 8-byte stores (or the fp32 sum of a shard's slots).
+// token, which are one exponent group of each routed row.  Per slot one
+// 16-byte load of values and one exponent byte, up to eight slots in flight;
+// the slot's power of two is folded into its weight (w * 2^s is exact), so
+// each element costs a byte permute, an exact subtraction and one fused
+// multiply-add into the fp32 sum (the same sum as decoding first), in
+// ascending j; one bf16 rounding, two 8-byte stores (or the fp32 sum of a
+// shard's slots).
 template <bool F32_OUT>
 __global__ void __launch_bounds__(256) k_combine_bfp16(const uint16_t* __restrict__ y,
                                                        const int8_t* __restrict__ y_exp,
@@ -118,40 +121,30 @@ __global__ void __launch_bounds__(256) k_combine_bfp16(const uint16_t* __restric
         wt[j] = j0 + j < k ? __ldg(w + static_cast<int64_t>(t) * k + j0 + j) : 0.f;
       }
       uint4 qv[8];
-      uint2 sv[8];
+      int sv[8];
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
         if (r[j] >= 0) {
           qv[j] = __ldg(reinterpret_cast<const uint4*>(y + r[j] * ld_y) + v);
-          sv[j] = __ldg(reinterpret_cast<const uint2*>(y_exp + (r[j] >> 4) * ld_y) + v);
+          sv[j] = __ldg(y_exp + (r[j] >> 4) * (ld_y / 8) + v);
         } else {
           qv[j] = make_uint4(0u, 0u, 0u, 0u);
-          sv[j] = make_uint2(0u, 0u);
+          sv[j] = 0;
         }
       }
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
         if (r[j] < 0) continue;
         const uint32_t qw[4] = {qv[j].x, qv[j].y, qv[j].z, qv[j].w};
-        // exponents of 100 and above (huge values, or 127: a group holding
-        // Inf or NaN) take the general decode
-        if (__vcmpges4(sv[j].x, 0x64646464u) | __vcmpges4(sv[j].y, 0x64646464u)) {
+        if (sv[j] == kBfp16NonFinite) {  // a group holding Inf or NaN: fp16 values
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const int se = static_cast<int8_t>((e < 4 ? sv[j].x : sv[j].y) >> (8 * (e & 3)));
-            const float val = bfp16_decode(static_cast<uint16_t>(qw[e >> 1] >> (16 * (e & 1))), se);
-            acc[e] = fmaf(wt[j], val, acc[e]);
-          }
+          for (int e = 0; e < 8; ++e)
+            acc[e] = fmaf(wt[j], bfp16_decode(qw[e >> 1], e & 1, sv[j]), acc[e]);
           continue;
         }
+        const float wp = wt[j] * bfp16_pow2(sv[j]);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const int se = static_cast<int8_t>((e < 4 ? sv[j].x : sv[j].y) >> (8 * (e & 3)));
-          // the int16 value, sign-extended from its half of the word
-          const int qi = e & 1 ? static_cast<int>(qw[e >> 1]) >> 16
-                               : static_cast<int>(qw[e >> 1] << 16) >> 16;
-          acc[e] = fmaf(wt[j], bfp16_value(qi, bfp16_pow2(se)), acc[e]);
-        }
+        for (int e = 0; e < 8; ++e) acc[e] = fmaf(wp, bfp16_offset_value(qw[e >> 1], e & 1), acc[e]);
       }
     }
     if (F32_OUT) {  // the sum before its rounding (one shard's share of the output)

@@ -244,8 +244,9 @@ __host__ __device__ constexpr uint32_t idesc_nvf4(int M, int N) {
 }
 
 // ---------------------------------------------------------------------------
-// BFP16 (int16 values with one power-of-two exponent per 32 columns): the
-// storage of the forward's L2 output between the down GEMM and the combine
+// BFP16 (uint16 values offset by 32768, one power-of-two exponent per 16 rows
+// x 8 columns): the storage of the forward's L2 output between the down GEMM
+// and the combine
 // ---------------------------------------------------------------------------
 constexpr int kBfp16NonFinite = 127;  // exponent of a group holding Inf or NaN
 // 2^s for |s| <= 126: a normal float, so scaling by it is exact.
@@ -253,38 +254,35 @@ __device__ __forceinline__ float bfp16_pow2(int s) {
   return __uint_as_float(static_cast<uint32_t>(127 + s) << 23);
 }
 // Exponent of a group from the bits of its max |v| (sign bit clear):
-// s = max(floor(log2 m) - 14, -126), so that m * 2^-s < 2^15; 0 for an
-// all-zero group, kBfp16NonFinite when the group holds Inf or NaN.
+// s = max(floor(log2 m) - 14, -126), plus one when m * 2^-s >= 32767.5, so
+// that every value rounds to at most 32767 units; 0 for an all-zero group,
+// kBfp16NonFinite when the group holds Inf or NaN.
 __device__ __forceinline__ int bfp16_exponent(uint32_t mbits) {
   if (mbits >= 0x7f800000u) return kBfp16NonFinite;
   if (mbits == 0u) return 0;
   const int be = static_cast<int>(mbits >> 23);
-  return max(-126, (be == 0 ? -127 : be - 127) - 14);  // a subnormal m lies below 2^-126
+  const int s = max(-126, (be == 0 ? -127 : be - 127) - 14);  // subnormal m: below 2^-126
+  return __uint_as_float(mbits) * bfp16_pow2(-s) >= 32767.5f ? s + 1 : s;
 }
-// The group exponent given the group max m (finite, nonzero): s from
-// bfp16_exponent, plus one when m * 2^-s would round to 2^15.
-__device__ __forceinline__ int bfp16_exponent_fit(float m, int s) {
-  return m * bfp16_pow2(-s) >= 32767.5f ? s + 1 : s;
-}
-// x (already scaled by 2^-s, |x| < 32767.5) -> int16 bits, rounded to the
-// nearest integer (ties to even): adding 1.5 * 2^23 in round-to-nearest mode
-// leaves the integer in the low mantissa bits (valid for |x| < 2^22), and
-// since 1.5 * 2^23 has no bits in the low half, the low 16 bits of the sum
-// are the integer's two's complement.  ALU work only, no conversion unit.
+// x (already scaled by 2^-s, |x| < 32767.5) -> the stored value
+// rint(x) + 32768 (ties to even): adding 1.5 * 2^23 + 2^15 in round-to-
+// nearest mode leaves 0x4B400000 + 32768 + rint(x) as the sum's bits (valid
+// for |x| < 2^22), whose low 16 bits are the stored value.  ALU work only.
 __device__ __forceinline__ uint16_t bfp16_round_int(float x) {
-  return static_cast<uint16_t>(__float_as_uint(__fadd_rn(x, 12582912.f)));
+  return static_cast<uint16_t>(__float_as_uint(__fadd_rn(x, 12615680.f)));
 }
-// q * 2^s for |s| < 100, exactly: 1.5 * 2^23 + q has the bits 0x4B400000 +
-// q, and (A - 1.5 * 2^23) * P = A * P - 1.5 * 2^23 * P is one fused
-// multiply-add whose exact result q * P needs no rounding (for s >= 105 the
-// term 1.5 * 2^23 * P would overflow).
-__device__ __forceinline__ float bfp16_value(int q, float p) {
-  return __fmaf_rn(__uint_as_float(0x4B400000u + static_cast<uint32_t>(q)), p, -12582912.f * p);
+// A 32-bit word's low (hi = false) or high stored value -> u - 32768 as a
+// float, exactly: one byte permute builds the bits 0x4B40:u of 1.5 * 2^23 +
+// u, and subtracting 1.5 * 2^23 + 2^15 is exact.
+__device__ __forceinline__ float bfp16_offset_value(uint32_t word, bool hi) {
+  return __fsub_rn(__uint_as_float(__byte_perm(word, 0x4B40u, hi ? 0x5432u : 0x5410u)),
+                   12615680.f);
 }
-// Any exponent: the int16 value converted, then scaled by 2^s (exact).
-__device__ __forceinline__ float bfp16_decode(uint16_t q, int s) {
-  if (s == kBfp16NonFinite) return __half2float(__ushort_as_half(q));
-  return static_cast<float>(static_cast<int16_t>(q)) * bfp16_pow2(s);
+// Any group: the element's value (fp16 bits when s = kBfp16NonFinite).
+__device__ __forceinline__ float bfp16_decode(uint32_t word, bool hi, int s) {
+  if (s == kBfp16NonFinite)
+    return __half2float(__ushort_as_half(static_cast<uint16_t>(hi ? word >> 16 : word)));
+  return bfp16_offset_value(word, hi) * bfp16_pow2(s);
 }
 
 // ---------------------------------------------------------------------------

@@ -89,7 +89,8 @@ struct GemmCfg {
   // (the fp32 and BFP16 epilogues store straight from registers: for each
   // token a warp's 32 lanes hold 32 consecutive features, one 128- or 64-byte
   // run, so they need no staging and their shared memory goes to pipeline
-  // stages; a lane's 16 tokens of one feature are one BFP16 exponent group)
+  // stages; a lane's 16 tokens of one feature share a BFP16 exponent group
+  // with those of 7 neighbouring lanes)
   static constexpr bool STAGED = BF16_OUT || PARTIAL;
   static constexpr int STG_ROWS = BF16_OUT ? 8 : 16;
   static constexpr int STG_BYTES = STAGED ? STG_ROWS * 32 * (BF16_OUT ? 2 : 4) : 0;
@@ -472,10 +473,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         } else if (C::BFP16) {
           tmem_ld_wait();
           // rows row0 + n0 .. + 15 (16-aligned: pads and tiles are multiples
-          // of 16) of feature f0 + lane are one exponent group, all in this
-          // lane's registers: the max |v| of its written rows, then per token
-          // one 64-byte run of int16 values across the warp, and the warp's
-          // 32 exponents as one 32-byte run
+          // of 16) of features 8c .. 8c + 7 (8 consecutive lanes) are one
+          // exponent group: the max |v| of this lane's written rows, then of
+          // the 8 lanes; per token one 64-byte run of values across the warp,
+          // and one exponent byte per 8 lanes
           float v[16];
           uint32_t mbits = 0u;
 #pragma unroll
@@ -483,10 +484,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             v[j] = __uint_as_float(g[j]) * alpha0;
             if (j < rows) mbits = max(mbits, __float_as_uint(v[j]) & 0x7fffffffu);
           }
-          int sg = bfp16_exponent(mbits);
+#pragma unroll
+          for (int o = 1; o < 8; o <<= 1) mbits = max(mbits, __shfl_xor_sync(0xffffffffu, mbits, o));
+          const int sg = bfp16_exponent(mbits);
           uint16_t* q = reinterpret_cast<uint16_t*>(p.out) + (row0 + n0) * p.ld_out + f0 + lane;
           if (sg != kBfp16NonFinite) {
-            sg = bfp16_exponent_fit(__uint_as_float(mbits), sg);
             const float sc = bfp16_pow2(-sg);
 #pragma unroll
             for (int j = 0; j < 16; ++j)
@@ -496,7 +498,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             for (int j = 0; j < 16; ++j)
               if (j < rows) q[j * p.ld_out] = __half_as_ushort(__float2half_rn(v[j]));
           }
-          p.out_exp[((row0 + n0) >> 4) * p.ld_out + f0 + lane] = static_cast<int8_t>(sg);
+          if ((lane & 7) == 0)
+            p.out_exp[((row0 + n0) >> 4) * (p.ld_out / 8) + ((f0 + lane) >> 3)] = static_cast<int8_t>(sg);
         } else {
           tmem_ld_wait();
           // token n0 + j: lanes write features f0 .. f0 + 31, one 128-byte run

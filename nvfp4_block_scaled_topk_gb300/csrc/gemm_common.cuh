@@ -50,8 +50,8 @@ struct GemmArgs {
   uint8_t* rq_codes;
   uint8_t* rq_scales;
   float* rq_gs;
-  // MEGAMOE_EPI_BFP16: the int8 exponents [rows / 16, ld_out] after the
-  // int16 values at `out`
+  // MEGAMOE_EPI_BFP16: the int8 exponents [rows / 16, ld_out / 8] after the
+  // uint16 values at `out`
   int8_t* out_exp;
 };
 

@@ -147,8 +147,8 @@ int num_sms();
 
 // out: bf16 [T, d] (one rounding of the fp32 sum), or with out_f32 the fp32
 // sum itself.
-// y fp32 [*, ld_y] (y_exp null) or BFP16 (int16 values at y, exponents
-// [rows / 16, ld_y] at y_exp)
+// y fp32 [*, ld_y] (y_exp null) or BFP16 (uint16 values at y, exponents
+// [rows / 16, ld_y / 8] at y_exp)
 cudaError_t launch_combine(const void* y, const int8_t* y_exp, int64_t ld_y,
                            const int32_t* slot_dst, const float* w, int T, int k, int d,
                            void* out, bool out_f32, cudaStream_t stream);

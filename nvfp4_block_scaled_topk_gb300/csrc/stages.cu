@@ -27,7 +27,7 @@ struct StageScan {
   const uint8_t* xq_sf;           // [rows, d/16]
   const uint16_t* h;              // [rows, I]
   const uint8_t* hq_sf;           // [rows, I/16]
-  const int8_t* y_exp;           // exponents of the BFP16 y [rows/16, d]
+  const int8_t* y_exp;           // exponents of the BFP16 y [rows/16, d/8]
   const uint16_t* out;            // [T, d]
   int T, d, I;
   uint32_t* flags;
@@ -77,11 +77,11 @@ __global__ void __launch_bounds__(256) k_stage_scan(const StageScan a) {
       continue;
     }
   }
-  const int w_y = a.d / 16;  // 16-byte words of exponents per 16-row group
+  const int w_y = a.d / 128;  // 16-byte words of exponents per 16-row group (d/8 bytes)
   for (int64_t i = tid; i < (R / 16) * w_y; i += stride) {
     const int64_t grp = i / w_y;
     if (__ldg(a.row_src + 16 * grp) < 0) continue;
-    const uint4 v = __ldg(reinterpret_cast<const uint4*>(a.y_exp + grp * a.d) + (i - grp * w_y));
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(a.y_exp + grp * (a.d / 8)) + (i - grp * w_y));
     const uint32_t m[4] = {v.x, v.y, v.z, v.w};
     for (int j = 0; j < 4; ++j)
       for (int b = 0; b < 4; ++b)

@@ -28,7 +28,7 @@ SCALES_MMA = 1
 EPI_F32 = 0
 EPI_SILU_MUL = 1
 EPI_BF16 = 2
-EPI_BFP16 = 3  # BFP16: int16 values, then one int8 exponent per 16 rows x 1 column
+EPI_BFP16 = 3  # BFP16: uint16 values, then one int8 exponent per 16 rows x 8 columns
 
 #: every function the header declares, with (restype, argtypes)
 _P = ctypes.c_void_p
@@ -246,9 +246,9 @@ def pack_weight_codes(codes: torch.Tensor, half_rows: int = 0) -> torch.Tensor:
 
 
 def bfp16_bytes(rows: int, ld: int) -> int:
-    """Bytes of a BFP16 [rows, ld] matrix: int16 values, then int8 exponents
-    (one per 16 rows x 1 column)."""
-    return rows * ld * 2 + (rows + 15) // 16 * ld
+    """Bytes of a BFP16 [rows, ld] matrix: uint16 values, then int8 exponents
+    (one per 16 rows x 8 columns)."""
+    return rows * ld * 2 + (rows + 15) // 16 * (ld // 8)
 
 
 def grouped_gemm(act_codes, act_scales, act_gs, w_codes_packed, w_scales_mma, w_gs, offsets,
@@ -585,7 +585,7 @@ def _carve_views(ws, off, T, k, E, d, I, pad):
     take("h", rows * I * 2)
     take("hq_codes", rows * (I // 2))
     take("hq_sf", rows * (I // 16))
-    take("y", bfp16_bytes(rows, d))  # BFP16: int16 values, then exponents
+    take("y", bfp16_bytes(rows, d))  # BFP16: uint16 values, then exponents
     hdr = views.pop("hdr")
     v = {
         "status": hdr[0:4].view(torch.int32),
@@ -603,8 +603,8 @@ def _carve_views(ws, off, T, k, E, d, I, pad):
         "h": views["h"].view(torch.bfloat16).view(rows, I),
         "hq_codes": views["hq_codes"].view(rows, I // 2),
         "hq_sf": views["hq_sf"].view(rows, I // 16),
-        "y": views["y"][:rows * d * 2].view(torch.int16).view(rows, d),
-        "y_exp": views["y"][rows * d * 2:].view(torch.int8).view((rows + 15) // 16, d),
+        "y": views["y"][:rows * d * 2].view(torch.int16).view(rows, d),  # uint16 bits
+        "y_exp": views["y"][rows * d * 2:].view(torch.int8).view((rows + 15) // 16, d // 8),
         "y_buf": views["y"],
         "rows": rows,
     }

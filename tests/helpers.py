@@ -242,22 +242,24 @@ def check_sampled_tokens(experts, ids, topk_weights, slot_dst, h, hq_codes, hq_s
 # ---------------------------------------------------------------------------
 # BFP16 (the forward's storage of y): a NumPy model of the encoding, in the
 # float32 decisions the epilogue takes, to check the GPU bytes and to bound
-# the error the format adds
+# the error the format adds.  Groups are 16 rows x 8 columns; values are
+# stored as u = rint(v * 2^-s) + 32768.
 # ---------------------------------------------------------------------------
 BFP16_NONFINITE = 127
 
 
 def bfp16_exponents(v32, valid=None):
-    """Per group of 16 rows x 1 column of a float32 [rows, n] array (rows a
-    multiple of 16), over the group's written rows (``valid``, default all):
-    s = max(floor(log2 max|v|) - 14, -126), plus one when max|v| * 2^-s >=
-    32767.5; 0 when they are all zero, 127 when they hold Inf or NaN."""
+    """Per group of 16 rows x 8 columns of a float32 [rows, n] array (rows a
+    multiple of 16, n of 8), over the group's written rows (``valid``,
+    default all): s = max(floor(log2 max|v|) - 14, -126), plus one when
+    max|v| * 2^-s >= 32767.5; 0 when they are all zero, 127 when they hold
+    Inf or NaN."""
     v32 = np.asarray(v32, dtype=np.float32)
     rows, n = v32.shape
     bits = v32.view(np.uint32) & np.uint32(0x7FFFFFFF)
     if valid is not None:
         bits = np.where(np.asarray(valid)[:, None], bits, np.uint32(0))
-    bits = bits.reshape(rows // 16, 16, n).max(axis=1)
+    bits = bits.reshape(rows // 16, 16, n // 8, 8).max(axis=(1, 3))
     be = (bits >> 23).astype(np.int64)
     s = np.maximum(np.where(be == 0, -127, be - 127) - 14, -126)
     m = bits.view(np.float32).astype(np.float64)
@@ -266,39 +268,44 @@ def bfp16_exponents(v32, valid=None):
     return np.where(bits >= 0x7F800000, BFP16_NONFINITE, s).astype(np.int8)
 
 
+def _expand(s, rows):
+    """Exponents [rows/16, n/8] -> per element [rows, n]."""
+    return np.repeat(np.repeat(np.asarray(s, dtype=np.int64), 16, axis=0), 8, axis=1)[:rows]
+
+
 def bfp16_encode(v32, valid=None):
-    """(int16 values q [rows, n], int8 exponents s [rows/16, n]) of a float32
-    array; rows outside ``valid`` are encoded with their group's exponent but
-    take no part in choosing it."""
+    """(stored uint16 values u [rows, n], int8 exponents s [rows/16, n/8]) of
+    a float32 array; rows outside ``valid`` are encoded with their group's
+    exponent but take no part in choosing it."""
     v32 = np.asarray(v32, dtype=np.float32)
     s = bfp16_exponents(v32, valid)
-    se = np.repeat(s.astype(np.int64), 16, axis=0)
+    se = _expand(s, v32.shape[0])
     nonfin = se == BFP16_NONFINITE
     scaled = np.ldexp(v32.astype(np.float64), np.where(nonfin, 0, -se))  # exact
     with np.errstate(invalid="ignore", over="ignore"):
         q = np.rint(np.where(nonfin, 0.0, scaled))
         rows_ok = np.ones(q.shape[0], bool) if valid is None else np.asarray(valid)
         assert np.all(np.abs(q[rows_ok]) <= 32767)  # by the choice of s
-        q = np.clip(q, -32768, 32767).astype(np.int16)  # rows outside `valid`: any bits
-        half = v32.astype(np.float16).view(np.int16)  # used only in non-finite groups
-    return np.where(nonfin, half, q).astype(np.int16), s
+        u = (np.clip(q, -32768, 32767) + 32768).astype(np.uint16)  # rows outside `valid`: any bits
+        half = v32.astype(np.float16).view(np.uint16)  # used only in non-finite groups
+    return np.where(nonfin, half, u).astype(np.uint16), s
 
 
-def bfp16_decode(q, s):
-    """float64 values of a BFP16 matrix (q [rows, n], s [rows/16, n])."""
-    q = np.asarray(q, dtype=np.int16)
-    se = np.repeat(np.asarray(s, dtype=np.int64), 16, axis=0)[:q.shape[0]]
+def bfp16_decode(u, s):
+    """float64 values of a BFP16 matrix (u [rows, n], s [rows/16, n/8])."""
+    u = np.asarray(u, dtype=np.uint16)
+    se = _expand(s, u.shape[0])
     nonfin = se == BFP16_NONFINITE
-    val = np.ldexp(q.astype(np.float64), np.where(nonfin, 0, se))
+    val = np.ldexp(u.astype(np.float64) - 32768.0, np.where(nonfin, 0, se))
     with np.errstate(invalid="ignore"):
-        return np.where(nonfin, q.view(np.float16).astype(np.float64), val)
+        return np.where(nonfin, u.view(np.float16).astype(np.float64), val)
 
 
 def bfp16_split(buf, rows, ld):
-    """(q [rows, ld], s [ceil(rows/16), ld]) NumPy views of a BFP16 matrix held
-    in a uint8 buffer."""
+    """(u [rows, ld], s [ceil(rows/16), ld/8]) NumPy views of a BFP16 matrix
+    held in a uint8 buffer."""
     b = np.asarray(buf.cpu().numpy() if isinstance(buf, torch.Tensor) else buf, dtype=np.uint8)
     g = (rows + 15) // 16
-    q = b[:rows * ld * 2].view(np.int16).reshape(rows, ld)
-    s = b[rows * ld * 2:rows * ld * 2 + g * ld].view(np.int8).reshape(g, ld)
-    return q, s
+    u = b[:rows * ld * 2].view(np.uint16).reshape(rows, ld)
+    s = b[rows * ld * 2:rows * ld * 2 + g * (ld // 8)].view(np.int8).reshape(g, ld // 8)
+    return u, s

@@ -215,18 +215,18 @@ def test_stage_views_mirror_the_workspace_layout(lib, T, k, E, d, I, pad):
     regions = [("counts", 4 * E), ("offsets", 4 * (E + 1)), ("padded_offsets", 4 * (E + 1)),
                ("slot_dst", 4 * T * k), ("row_src", 4 * rows), ("xq_codes", rows * d // 2),
                ("xq_sf", rows * d // 16), ("h", rows * I * 2), ("hq_codes", rows * I // 2),
-               ("hq_sf", rows * I // 16), ("y_buf", rows * d * 2 + (rows + 15) // 16 * d)]
+               ("hq_sf", rows * I // 16), ("y_buf", rows * d * 2 + (rows + 15) // 16 * (d // 8))]
     a256 = lambda n: -(-n // 256) * 256
     off = 256  # the status word and the scalars
     for name, nbytes in regions:
         t = v[name]
         assert t.storage_offset() * t.element_size() == off, name
         assert t.numel() * t.element_size() == nbytes, name
-        if name == "y_buf":  # BFP16: the int16 values, then one exponent per 16 x 1
+        if name == "y_buf":  # BFP16: the uint16 values, then one exponent per 16 x 8
             y, ye = v["y"], v["y_exp"]
             assert y.storage_offset() * 2 == off and tuple(y.shape) == (rows, d)
             assert ye.storage_offset() == off + rows * d * 2
-            assert tuple(ye.shape) == ((rows + 15) // 16, d)
+            assert tuple(ye.shape) == ((rows + 15) // 16, d // 8)
         off = a256(off + nbytes)
     hist = 4 * 256 * E if T * k >= 16384 else 0
     assert size == off + 2 * a256(4 * T * k) + a256(hist)
