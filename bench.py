@@ -487,9 +487,9 @@ def measure_forward(cfg, args, dev, world, rank, local, with_e2e=True, with_cpu=
     a_row2 = cfg.I * (0.5 + 1 / 16)  # one requantised row of h
     # per launch: the active experts' weights once, each routed row's
     # activations in and its output row out (L2: BFP16, 2 bytes a value and
-    # one exponent byte per 32)
+    # one exponent byte per 16 rows x 8 columns)
     l1_bytes = active * 2 * w_el + valid_slots * (a_row1 + cfg.I * 2)
-    l2_bytes = active * w_el + valid_slots * (a_row2 + cfg.d * (2 + 1 / 32))
+    l2_bytes = active * w_el + valid_slots * (a_row2 + cfg.d * (2 + 1 / 128))
     l1_flops = 4 * cfg.d * cfg.I * valid_slots
     l2_flops = 2 * cfg.d * cfg.I * valid_slots
     rl1 = gemm_roofline("k_grouped_gemm (L1 gate+up, SiLU*up epilogue)", l1_bytes, l1_flops,
