@@ -427,9 +427,9 @@ void megamoe_set_wait_limit_ns(uint64_t ns);
 
 /*
  * megamoe_set_fused_requant -- where megamoe_forward / _from_logits /
- * _static requantise h (north_star's "requant fused into the L1 epilogue";
- * host setting of this library, all devices, for forwards launched
- * afterwards):
+ * _static requantise h (the requantisation fused into the L1 GEMM's
+ * epilogue, or after it; host setting of this library, all devices, for
+ * forwards launched afterwards):
  *   0 (default)  a separate kernel after the L1 GEMM reads h once and encodes
  *                it with the global scale of amax(h);
  *   1            the L1 GEMM kernel does it: after its last tile each CTA
