@@ -377,8 +377,8 @@ megamoe_status megamoe_combine(const float* y, int64_t ld_y, const int32_t* slot
  * leading dimension ld_y (the forward's own form of y): each element is
  * decoded exactly into fp32, then summed in fp32 in ascending j and rounded
  * once to bf16.  Requires d and ld_y multiples of 32, y 16-byte and out
- * 8-byte aligned (else MEGAMOE_ERR_UNSUPPORTED_SHAPE); slot_dst entries must
- * be below y_rows.
+ * 8-byte aligned (else MEGAMOE_ERR_UNSUPPORTED_SHAPE); a slot_dst entry at or
+ * past y_rows is skipped like a negative one.
  */
 megamoe_status megamoe_combine_bfp16(const void* y, int64_t ld_y, int64_t y_rows,
                                      const int32_t* slot_dst, const float* topk_weights, int T,

@@ -358,7 +358,7 @@ megamoe_status megamoe_combine(const float* y, int64_t ld_y, const int32_t* slot
   if (T > 0 && (!y || !slot_dst || !topk_weights || !out)) return MEGAMOE_ERR_INVALID_ARG;
   if (T > 0 && (!aligned(y, 16) || !aligned(out, 8))) return MEGAMOE_ERR_UNSUPPORTED_SHAPE;
   return cuda_status(
-      launch_combine(y, nullptr, ld_y, slot_dst, topk_weights, T, k, d, out, false,
+      launch_combine(y, nullptr, ld_y, 0, slot_dst, topk_weights, T, k, d, out, false,
                      reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -371,8 +371,8 @@ megamoe_status megamoe_combine_bfp16(const void* y, int64_t ld_y, int64_t y_rows
   if (T > 0 && (!y || !slot_dst || !topk_weights || !out)) return MEGAMOE_ERR_INVALID_ARG;
   if (T > 0 && (!aligned(y, 16) || !aligned(out, 8))) return MEGAMOE_ERR_UNSUPPORTED_SHAPE;
   const int8_t* y_exp = static_cast<const int8_t*>(y) + y_rows * ld_y * 2;
-  return cuda_status(launch_combine(y, y_exp, ld_y, slot_dst, topk_weights, T, k, d, out, false,
-                                    reinterpret_cast<cudaStream_t>(stream)));
+  return cuda_status(launch_combine(y, y_exp, ld_y, y_rows, slot_dst, topk_weights, T, k, d, out,
+                                    false, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 size_t megamoe_workspace_size(int T, int k, int E, int d, int I, int pad) {
@@ -520,7 +520,8 @@ cudaError_t forward_l2(const megamoe_weights* w, const float* topk_weights, int 
   if (e != cudaSuccess) return e;
   // 7. top-k weighted combine
   StageRange r("megamoe.combine");
-  return launch_combine(wk.y, wk.y_exp, d, wk.slot_dst, topk_weights, T, k, d, out, out_f32, s);
+  return launch_combine(wk.y, wk.y_exp, d, wk.rows, wk.slot_dst, topk_weights, T, k, d, out,
+                        out_f32, s);
 }
 
 // The forward; with `router` the ids and weights are computed here from the

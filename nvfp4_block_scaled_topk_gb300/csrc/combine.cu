@@ -96,7 +96,7 @@ __global__ void __launch_bounds__(256) k_round_bf16(const float4* __restrict__ i
 template <bool F32_OUT>
 __global__ void __launch_bounds__(256) k_combine_bfp16(const uint16_t* __restrict__ y,
                                                        const int8_t* __restrict__ y_exp,
-                                                       int64_t ld_y,
+                                                       int64_t ld_y, int64_t y_rows,
                                                        const int32_t* __restrict__ slot_dst,
                                                        const float* __restrict__ w, int T, int k,
                                                        int d, void* __restrict__ out) {
@@ -118,6 +118,7 @@ __global__ void __launch_bounds__(256) k_combine_bfp16(const uint16_t* __restric
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
         r[j] = j0 + j < k ? __ldg(slot_dst + static_cast<int64_t>(t) * k + j0 + j) : -1;
+        if (r[j] >= y_rows) r[j] = -1;  // outside y: skipped like a -1 slot
         wt[j] = j0 + j < k ? __ldg(w + static_cast<int64_t>(t) * k + j0 + j) : 0.f;
       }
       uint4 qv[8];
@@ -172,7 +173,7 @@ static unsigned stream_blocks(int64_t tasks) {
   return static_cast<unsigned>(blocks > cap ? cap : blocks);
 }
 
-cudaError_t launch_combine(const void* y, const int8_t* y_exp, int64_t ld_y,
+cudaError_t launch_combine(const void* y, const int8_t* y_exp, int64_t ld_y, int64_t y_rows,
                            const int32_t* slot_dst, const float* w, int T, int k, int d,
                            void* out, bool out_f32, cudaStream_t stream) {
   if (y_exp) {
@@ -182,9 +183,9 @@ cudaError_t launch_combine(const void* y, const int8_t* y_exp, int64_t ld_y,
     const uint16_t* yq = static_cast<const uint16_t*>(y);
     if (out_f32)
       return launch_pdl(k_combine_bfp16<true>, grid, dim3(256), 0, stream, yq, y_exp, ld_y,
-                        slot_dst, w, T, k, d, out);
+                        y_rows, slot_dst, w, T, k, d, out);
     return launch_pdl(k_combine_bfp16<false>, grid, dim3(256), 0, stream, yq, y_exp, ld_y,
-                      slot_dst, w, T, k, d, out);
+                      y_rows, slot_dst, w, T, k, d, out);
   }
   const int64_t tasks = static_cast<int64_t>(T) * (d / 4);
   if (tasks == 0) return cudaSuccess;

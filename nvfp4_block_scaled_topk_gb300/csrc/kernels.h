@@ -149,7 +149,8 @@ int num_sms();
 // sum itself.
 // y fp32 [*, ld_y] (y_exp null) or BFP16 (uint16 values at y, exponents
 // [rows / 16, ld_y / 8] at y_exp)
-cudaError_t launch_combine(const void* y, const int8_t* y_exp, int64_t ld_y,
+// (y_rows: rows of a BFP16 y; slots at or past it are skipped)
+cudaError_t launch_combine(const void* y, const int8_t* y_exp, int64_t ld_y, int64_t y_rows,
                            const int32_t* slot_dst, const float* w, int T, int k, int d,
                            void* out, bool out_f32, cudaStream_t stream);
 // Non-finite scan of a forward's stage outputs (MEGAMOE_STAGE_* bits in

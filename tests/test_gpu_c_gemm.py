@@ -221,6 +221,15 @@ def test_combine_bfp16_matches_oracle(cuda_lib, T, k, d):
     huge = np.isin(slot_dst.reshape(T, k), np.arange(16)).any(axis=1)
     assert huge.any()
     assert_close_bf16(out.float().cpu().numpy()[huge], want64[huge], what="combine bfp16 huge")
+    # slot indices at or past y_rows are skipped like -1 (not read)
+    far = slot_dst.copy()
+    far[::3] = np.where(far[::3] >= 0, rows + far[::3], far[::3])
+    near = np.where(far >= rows, -1, far).astype(np.int32)
+    out = megamoe.combine_bfp16(torch.from_numpy(buf).cuda(), rows, d,
+                                torch.from_numpy(far).cuda(), torch.from_numpy(w).cuda())
+    want64 = oracle.combine(bfp16_decode(qh, sh), w, near, round_bf16=False)
+    small = ~np.isin(near.reshape(T, k), np.arange(16)).any(axis=1)
+    assert_close_bf16(out.float().cpu().numpy()[small], want64[small], what="combine bfp16 far")
     # a NaN in one group of one routed row reaches exactly that token's group
     t = int(np.nonzero((slot_dst.reshape(T, k) >= 0).any(axis=1))[0][0])
     j = int(np.nonzero(slot_dst.reshape(T, k)[t] >= 0)[0][0])
