@@ -371,8 +371,8 @@ def measure_forward(cfg, args, dev, world, rank, local, with_e2e=True, with_cpu=
         return a.elapsed_time(b) / n
 
     # a GEMM whose weights fit in L2 (decode sizes) would read them from L2
-    # when replayed back to back: those are timed with a 512 MB write between
-    # launches, its own time subtracted
+    # when replayed back to back: those are timed after a 512 MB write (the
+    # median (write, GEMM) window minus the median write)
     w_el0 = cfg.d * cfg.I * (0.5 + 1.0 / 16)
     small = active * 2 * w_el0 < 2 * 126e6
     if small:
@@ -538,8 +538,8 @@ def measure_forward(cfg, args, dev, world, rank, local, with_e2e=True, with_cpu=
             "loop": e2e["loop"]},
         "gpu_launches": kernels_per_step(cfg) * args.steps,
         "clocks": clk,
-        "stage_timing": ("each GEMM alone with a 512 MB write between launches (its weights "
-                         "fit in L2), the writes' time subtracted") if small else
+        "stage_timing": ("each GEMM alone after a 512 MB write (its weights fit in L2): median "
+                         "(write, GEMM) window minus median write") if small else
                         "each GEMM alone, back to back (its weights exceed L2)",
     }
     del fwd, weights, raw, x, ids, w, v, l1_out
@@ -610,31 +610,37 @@ def run_ours(args):
 
 
 def _time_with_flush(step, steps, dev, stream):
-    """Device time of one `step` whose inputs fit in L2: `steps` back-to-back
-    pairs (write a 512 MB buffer, then the step) minus the same number of
-    buffer writes alone, both between CUDA events on the launching stream, so
-    neither the host's launch latency nor L2-resident inputs enter it."""
+    """Device time of one `step` whose inputs fit in L2: windows of (write a
+    512 MB buffer, then the step) and windows of the write alone, interleaved,
+    each between two CUDA events on the launching stream; the median pair
+    minus the median write.  The step follows the write back to back as it
+    would follow other work (queued while the write runs, so the host's launch
+    latency stays hidden), the events' own cost cancels, and the medians keep
+    a stray slow window (a power-capped clock) out of the difference."""
     import torch
 
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
-
-    def run(with_step):
-        a = torch.cuda.Event(enable_timing=True)
-        b = torch.cuda.Event(enable_timing=True)
-        torch.cuda.synchronize()
+    n = max(steps, 9)
+    for _ in range(2):
+        flush.fill_(1)
+        step()
+    torch.cuda.synchronize()
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+    pairs = [(ev(), ev()) for _ in range(n)]
+    alone = [(ev(), ev()) for _ in range(n)]
+    for (a, b), (c, e) in zip(pairs, alone):
         a.record(stream)
-        for _ in range(steps):
-            flush.fill_(1)
-            if with_step:
-                step()
+        flush.fill_(1)
+        step()
         b.record(stream)
-        torch.cuda.synchronize()
-        return a.elapsed_time(b)
-
-    run(True)
-    t_pairs = run(True)
-    t_flush = run(False)
-    return max(t_pairs - t_flush, 1e-6) / steps
+        c.record(stream)
+        flush.fill_(1)
+        e.record(stream)
+    torch.cuda.synchronize()
+    med = lambda xs: sorted(xs)[len(xs) // 2]
+    t_pair = med([a.elapsed_time(b) for a, b in pairs])
+    t_write = med([c.elapsed_time(e) for c, e in alone])
+    return max(t_pair - t_write, 1e-6)
 
 
 def run_linear(args):
@@ -660,8 +666,8 @@ def run_linear(args):
     torch.cuda.synchronize()
     clocks = ClockSampler(0)
     clocks.start()
-    # weights and x are smaller than L2 for the decode shape: time with a
-    # 512 MB write between steps, subtracted (see _time_with_flush)
+    # weights and x are smaller than L2 for the decode shape: each step timed
+    # after a 512 MB write, the write's median time subtracted (_time_with_flush)
     ms = _time_with_flush(lambda: megamoe.linear_nvfp4(x, w, out=out, ws=ws), args.steps, dev,
                           stream)
     clk = clocks.stop()
@@ -681,8 +687,8 @@ def run_linear(args):
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "dtype": "nvfp4 (e2m1 x e4m3 scales, fp32 acc), bf16 out", "data": "synthetic",
         "config": {"workload": f"{cfg.name}: x [{cfg.T}, {cfg.K}] bf16 @ W [{cfg.N}, {cfg.K}] "
-                               "NVFP4", "l2": "512 MB written before every step; the writes' "
-                                              "own time subtracted"},
+                               "NVFP4", "l2": "512 MB written before every step; median "
+                                              "(write, step) minus median write"},
         "tflops": flops / (ms * 1e-3) / 1e12,
         "hbm_gbs": alg_bytes / (ms * 1e-3) / 1e9,
         "roofline": {"bound": bound, "achieved": achieved, "peak": peak,
@@ -734,7 +740,7 @@ def run_layer(args, router_only=False):
     clocks.start()
     if router_only:
         # the router's inputs are small: a 512 MB write before every step,
-        # its own time subtracted
+        # the write's median time subtracted
         ms = _time_with_flush(step, args.steps, dev, stream)
     else:
         # the layer reads more expert weights per step than L2 holds: steps
@@ -770,8 +776,8 @@ def run_layer(args, router_only=False):
         "config": {"workload": f"{base.name}: logits [{base.T}, {base.E}] fp32, top-{base.k} "
                                "+ 1 shared expert" + ("" if router_only else
                                                       f", d={base.d} I={base.I}"),
-                   "l2": ("512 MB written before every step; the writes' own time "
-                          "subtracted") if router_only else
+                   "l2": ("512 MB written before every step; median (write, step) minus "
+                          "median write") if router_only else
                          "expert weights read per step larger than L2"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_gbs, "unit": "GB/s",
                      "frac": achieved / hbm_gbs, "traffic": None, "kernel": kernel,
