@@ -216,9 +216,13 @@ def run_reference(args):
     rank, world, _ = _dist()
     if rank != 0:
         return
+    import numpy as np
+
     cfg = inputs.CONFIGS[args.config]
     x = inputs.make_activations(cfg)
     ids, w = inputs.make_routing(cfg)
+    flat = ids.numpy().reshape(-1)
+    counts = np.bincount(flat[(flat >= 0) & (flat < cfg.E)], minlength=cfg.E)
     tokens = max(1, min(cfg.T, args.ref_tokens))
     ex = inputs.ExpertSet(cfg, None)  # experts drawn on the CPU once, on first use
     times = []
@@ -233,15 +237,38 @@ def run_reference(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / len(times),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": f"{cfg.name}: E={cfg.E} top-{cfg.k} d={cfg.d} I={cfg.I} "
-                               f"T={cfg.T} (oracle on the first {tokens} tokens per step)",
-                   "global_batch": cfg.T, "parallelism": "replicas"},
+        "config": workload_config(cfg, counts, args.gpus),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": _cores(), "kind": "oracle",
-                         "sample": f"first {tokens} of {cfg.T} tokens of the {cfg.name} batch, "
-                                   "weights of the experts they touch, full forward"},
+                         "sample": f"each step: the first {tokens} of {cfg.T} tokens of the "
+                                   f"{cfg.name} batch, full float64 forward over the experts "
+                                   "they touch; weights fetched before timing"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
+
+
+def workload_config(cfg, counts, world):
+    """The `config` object of a forward workload, the same for both arms:
+    its name and sizes and the routing's per-expert row counts (`counts`, from
+    the library's routing or, for the reference arm, counted on the host from
+    the same seeded ids)."""
+    import numpy as np
+
+    counts = np.asarray(counts)
+    active = int((counts > 0).sum())
+    w_el = cfg.d * cfg.I * (0.5 + 1.0 / 16)
+    return {
+        "workload": f"{cfg.name}: MegaMoE routed-expert forward, E={cfg.E} top-{cfg.k} "
+                    f"d={cfg.d} I={cfg.I} T={cfg.T}, NVFP4 weights resident",
+        "global_batch": cfg.T * world,
+        "parallelism": f"replicas x{world}",
+        "l2": (f"inputs larger than L2 (~{active * 3 * w_el / 1e9:.2f} GB of expert weights "
+               "read per step, L2 is 0.13 GB)") if active * 3 * w_el > 126e6 else
+              (f"expert weights (~{active * 3 * w_el / 1e6:.0f} MB) smaller than L2: steps "
+               "replay them from L2"),
+        "active_experts": active, "valid_slots": int(counts.sum()),
+        "max_expert_load": int(counts.max()), "zero_token_experts": int((counts == 0).sum()),
+    }
 
 
 # --------------------------------------------------------------------------
@@ -302,8 +329,9 @@ def measure_forward(cfg, args, dev, world, rank, local, with_e2e=True, with_cpu=
         del raw
         raw = None
     torch.cuda.empty_cache()
-    x = inputs.make_activations(cfg, device=dev)
-    ids, w = inputs.make_routing(cfg, device=dev)
+    # the batch is drawn on the host (the reference arm draws the same one)
+    x = inputs.make_activations(cfg).to(dev)
+    ids, w = (t.to(dev) for t in inputs.make_routing(cfg))
     fwd = megamoe.Forward(weights, cfg.T, cfg.k, pad=cfg.pad)
     stream = torch.cuda.current_stream()
 
@@ -516,13 +544,7 @@ def measure_forward(cfg, args, dev, world, rank, local, with_e2e=True, with_cpu=
                          f"({total:.1f} s); weights fetched before timing"}
     rec = {
         "value": tokens_total / (ms * 1e-3), "ms_per_step": ms,
-        "workload": f"{cfg.name}: MegaMoE routed-expert forward, E={cfg.E} top-{cfg.k} "
-                    f"d={cfg.d} I={cfg.I} T={cfg.T}, NVFP4 weights resident",
-        "global_batch": cfg.T * world,
-        "l2": f"inputs larger than L2 (~{active * 3 * w_el / 1e9:.2f} GB of expert weights "
-              "read per step, L2 is 0.13 GB)",
-        "active_experts": active, "valid_slots": valid_slots,
-        "max_expert_load": int(counts.max()), "zero_token_experts": int((counts == 0).sum()),
+        "config": workload_config(cfg, counts, world),
         "tflops": flops / (ms * 1e-3) / 1e12,
         "hbm_gbs": alg_bytes / (ms * 1e-3) / 1e9,
         "hbm_frac_of_measured": alg_bytes / (ms * 1e-3) / 1e9 / hbm_gbs,
@@ -572,22 +594,19 @@ def run_ours(args):
             r = measure_forward(inputs.CONFIGS[name], args, dev, world, rank, local,
                                 with_e2e=True, with_cpu=False)
             subs[name] = {key: r[key] for key in (
-                "value", "ms_per_step", "workload", "active_experts", "valid_slots",
-                "max_expert_load", "zero_token_experts", "tflops", "hbm_gbs",
+                "value", "ms_per_step", "tflops", "hbm_gbs",
                 "hbm_frac_of_measured", "fp4_frac_of_measured", "attainable_frac", "stage_ms",
                 "stage_timing", "roofline", "roofline_other_gemm", "e2e", "clocks")}
+            subs[name].update({key: r["config"][key] for key in (
+                "workload", "active_experts", "valid_slots", "max_expert_load",
+                "zero_token_experts")})
     if rank == 0:
         line = {
             "metric": METRIC, "value": main["value"], "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": main["ms_per_step"],
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "nvfp4 (e2m1 x e4m3 scales, fp32 acc)", "data": "synthetic",
-            "config": {"workload": main["workload"], "global_batch": main["global_batch"],
-                       "parallelism": f"replicas x{world}", "l2": main["l2"],
-                       "active_experts": main["active_experts"],
-                       "valid_slots": main["valid_slots"],
-                       "max_expert_load": main["max_expert_load"],
-                       "zero_token_experts": main["zero_token_experts"]},
+            "config": main["config"],
             "tflops": main["tflops"], "hbm_gbs": main["hbm_gbs"],
             "hbm_frac_of_measured": main["hbm_frac_of_measured"],
             "fp4_frac_of_measured": main["fp4_frac_of_measured"],
