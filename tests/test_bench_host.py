@@ -100,3 +100,30 @@ def test_linear_launch_count_follows_the_workspace_layout():
     big = 256 + 4096 * 3584 + 4096 * 448
     assert bench.linear_kernels_per_call(4096, 7168, big) == 4
     assert bench.linear_kernels_per_call(4096, 7168, big + 256) == 5
+
+
+def test_workload_config_counts_the_routing_and_matches_the_reference_arm():
+    """workload_config: active experts, valid slots, the largest load and the
+    zero-token experts from per-expert counts; the reference arm's line (run
+    on CPU here) carries the config the forward's arm builds from the same
+    seeded batch."""
+    import numpy as np
+
+    sys.path.insert(0, ROOT)
+    import bench
+    from nvfp4_block_scaled_topk_gb300 import inputs
+
+    cfg = inputs.CONFIGS["tiny"]
+    c = bench.workload_config(cfg, np.array([3, 0, 5, 0, 1, 0, 0, 7]), world=2)
+    assert (c["active_experts"], c["valid_slots"], c["max_expert_load"], c["zero_token_experts"]) \
+        == (4, 16, 7, 4)
+    assert c["global_batch"] == 2 * cfg.T and c["parallelism"] == "replicas x2"
+    ids, _ = inputs.make_routing(cfg)
+    flat = ids.numpy().reshape(-1)
+    want = bench.workload_config(cfg, np.bincount(flat, minlength=cfg.E), world=1)
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--config", "tiny", "--steps", "1", "--warmup", "0"],
+                       capture_output=True, text=True, timeout=600, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    line = json.loads([l for l in r.stdout.splitlines() if l.startswith("{")][-1])
+    assert line["config"] == want
