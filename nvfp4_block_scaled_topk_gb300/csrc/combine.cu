@@ -3,8 +3,8 @@
 // "Test Plan -- Finding the NaN", Phase 1).  One thread per 4 consecutive
 // features of one token: 128-bit loads of each routed row of y (up to eight
 // slots' loads in flight at once), fp32 sums in ascending j, one bf16
-// rounding, 64-bit stores.  y is fp32, or (the forward) BFP16, then one
-// thread per 8 features (k_combine_bfp16).  An expert-parallel
+// rounding, 64-bit stores.  y is fp32 (megamoe_combine), or (the forward)
+// BFP16, then one thread per 8 features (k_combine_bfp16).  An expert-parallel
 // shard writes the fp32 sum of its own slots instead, and the shards' sums
 // are added and rounded once after the exchange (k_round_bf16).
 #include <cuda_bf16.h>
@@ -15,7 +15,6 @@
 
 namespace megamoe {
 
-template <bool F32_OUT>
 __global__ void __launch_bounds__(256) k_combine(const float* __restrict__ y, int64_t ld_y,
                                                  const int32_t* __restrict__ slot_dst,
                                                  const float* __restrict__ w, int T, int k, int d,
@@ -54,17 +53,12 @@ __global__ void __launch_bounds__(256) k_combine(const float* __restrict__ y, in
         acc.w = fmaf(wt[j], yv[j].w, acc.w);
       }
     }
-    if (F32_OUT) {  // the sum before its rounding (one shard's share of the output)
-      float* o = static_cast<float*>(out) + static_cast<int64_t>(t) * d + 4 * v;
-      __stcs(reinterpret_cast<float4*>(o), acc);
-    } else {
-      const __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
-      const __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
-      uint2 pk;
-      pk.x = *reinterpret_cast<const uint32_t*>(&lo);
-      pk.y = *reinterpret_cast<const uint32_t*>(&hi);
-      reinterpret_cast<uint2*>(static_cast<uint16_t*>(out) + static_cast<int64_t>(t) * d)[v] = pk;
-    }
+    const __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
+    const __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
+    uint2 pk;
+    pk.x = *reinterpret_cast<const uint32_t*>(&lo);
+    pk.y = *reinterpret_cast<const uint32_t*>(&hi);
+    reinterpret_cast<uint2*>(static_cast<uint16_t*>(out) + static_cast<int64_t>(t) * d)[v] = pk;
   }
 }
 
@@ -187,15 +181,13 @@ cudaError_t launch_combine(const void* y, const int8_t* y_exp, int64_t ld_y, int
     return launch_pdl(k_combine_bfp16<false>, grid, dim3(256), 0, stream, yq, y_exp, ld_y,
                       y_rows, slot_dst, w, T, k, d, out);
   }
+  // an fp32 y (megamoe_combine) always gives the bf16 output
+  if (out_f32) return cudaErrorInvalidValue;
   const int64_t tasks = static_cast<int64_t>(T) * (d / 4);
   if (tasks == 0) return cudaSuccess;
   const dim3 grid(stream_blocks(tasks));
-  const float* yf = static_cast<const float*>(y);
-  if (out_f32)
-    return launch_pdl(k_combine<true>, grid, dim3(256), 0, stream, yf, ld_y, slot_dst, w, T, k,
-                      d, out);
-  return launch_pdl(k_combine<false>, grid, dim3(256), 0, stream, yf, ld_y, slot_dst, w, T, k,
-                    d, out);
+  return launch_pdl(k_combine, grid, dim3(256), 0, stream, static_cast<const float*>(y), ld_y,
+                    slot_dst, w, T, k, d, out);
 }
 
 cudaError_t launch_round_bf16(const float* in, int64_t n, uint16_t* out, cudaStream_t stream) {
