@@ -449,7 +449,12 @@ cudaError_t forward_l1(const megamoe_weights* w, const uint16_t* x, const int32_
   g.tile_n = tile_n;
   g.status = wk.status;
   g.zero_amax = false;
-  // routing finished before the quantiser (and the requantiser) ran
+  // The kernel reads the routing offsets before its grid-dependency wait
+  // (its tile schedule and first weight stages start early).  Sound only with
+  // a kernel in between: the quantiser lets this kernel launch after its own
+  // wait, which returns once the routing kernel has completed and its writes
+  // are visible.  Launched straight after the routing, it could read offsets
+  // still being written.
   g.early_weights = true;
   g.ksplit = wk.ks1;
   g.partial = wk.partial;

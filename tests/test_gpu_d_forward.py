@@ -49,10 +49,27 @@ def test_forward_matches_oracle(cuda_lib, name, pad):
     cfg = inputs.CONFIGS[name]
     raw, fwd, x, ids, w, out, bits = _run(cfg, pad)
     assert bits == 0
+    _stage_checks(cfg, fwd, x, ids, pad)
     ex = inputs.ExpertSet(cfg, raw)
     _, inter = oracle.forward(x.float().numpy(), ids.numpy(), w.numpy(), ex, pad=pad,
                               return_intermediates=True)
     check_forward(fwd, out, inter, ex, ids.numpy(), w.numpy(), what=name)
+
+
+@pytest.mark.parametrize("T", [36, 37])
+def test_forward_around_the_prologue_limit(cuda_lib, T):
+    """The two sides of the one-block prologue's limit at d = 7168: 36 tokens
+    (the largest batch whose routing and amax(x) one thread block takes) and
+    37 (the routing and amax kernels).  Every stage bit-exact, then the
+    whole forward against the oracle."""
+    cfg = inputs.MoEConfig("decode_mid", 16, 6, 7168, 512, T, "uniform", seed=900 + T)
+    raw, fwd, x, ids, w, out, bits = _run(cfg, 32)
+    assert bits == 0
+    _stage_checks(cfg, fwd, x, ids)
+    ex = inputs.ExpertSet(cfg, raw)
+    _, inter = oracle.forward(x.float().numpy(), ids.numpy(), w.numpy(), ex, pad=32,
+                              return_intermediates=True)
+    check_forward(fwd, out, inter, ex, ids.numpy(), w.numpy(), what=f"decode_mid T={T}")
 
 
 def test_forward_prefill_shaped_mid_size(cuda_lib):
@@ -68,12 +85,12 @@ def test_forward_prefill_shaped_mid_size(cuda_lib):
     check_forward(fwd, out, inter, ex, ids.numpy(), w.numpy(), what="prefill_mid")
 
 
-def _full_size_stage_checks(cfg, fwd, x, ids):
+def _stage_checks(cfg, fwd, x, ids, pad=32):
     """Routing and the quantised x bit-exact, amax(h) = max |h| over the
     forward's own valid rows, and the requantisation of the forward's own h
     bit-exact (all rows)."""
     v = fwd.intermediates()
-    rt = oracle.route(ids.numpy(), cfg.E, 32)
+    rt = oracle.route(ids.numpy(), cfg.E, pad)
     R = int(rt.padded_offsets[-1])
     assert np.array_equal(v["padded_offsets"].cpu().numpy(), rt.padded_offsets)
     assert np.array_equal(v["row_src"].cpu().numpy()[:R], rt.row_src)
@@ -102,7 +119,7 @@ def test_forward_full_size_prefill_against_the_full_oracle(cuda_lib):
     cfg = inputs.CONFIGS["prefill"]
     raw, fwd, x, ids, w, out, bits = _run(cfg, 32)
     assert bits == 0
-    _full_size_stage_checks(cfg, fwd, x, ids)
+    _stage_checks(cfg, fwd, x, ids)
     ex = inputs.ExpertSet(cfg, raw)
     _, inter = oracle.forward(x.float().numpy(), ids.numpy(), w.numpy(), ex, pad=32,
                               return_intermediates=True)
@@ -118,7 +135,7 @@ def test_forward_full_size_large_on_a_token_sample(cuda_lib):
     cfg = inputs.CONFIGS["large"]
     raw, fwd, x, ids, w, out, bits = _run(cfg, 32)
     assert bits == 0
-    amax_x, amax_h = _full_size_stage_checks(cfg, fwd, x, ids)
+    amax_x, amax_h = _stage_checks(cfg, fwd, x, ids)
     sample = np.sort(np.random.default_rng(5).choice(cfg.T, size=256, replace=False))
     ex = inputs.ExpertSet(cfg, raw)
     xs = x.float().numpy()[sample]
