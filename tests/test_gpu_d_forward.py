@@ -72,6 +72,25 @@ def test_forward_around_the_prologue_limit(cuda_lib, T):
     check_forward(fwd, out, inter, ex, ids.numpy(), w.numpy(), what=f"decode_mid T={T}")
 
 
+@pytest.mark.parametrize("T,routing", [(80, "uniform"), (160, "uniform"), (2000, "zipf")])
+def test_forward_at_shapes_off_the_powers_of_two(cuda_lib, T, routing):
+    """d = 1280 and I = 768, multiples of 256 that are not powers of two: the
+    gate+up GEMM has 5 K steps and 6 feature tiles of 256 (12 of 128), the
+    down GEMM 3 K steps (fewer than any stage count, so every tile's loads
+    run on into the next tile's) and 10 feature tiles.  12 experts, top-3:
+    T = 80, 160 and 2000 give 32- and 64-token tiles and, at 2000 with a
+    Zipf-skewed load, 128-token tiles (token-major for L1).  Every stage
+    bit-exact, then the whole forward against the oracle."""
+    cfg = inputs.MoEConfig("off_pow2", 12, 3, 1280, 768, T, routing, seed=1300 + T)
+    raw, fwd, x, ids, w, out, bits = _run(cfg, 32)
+    assert bits == 0
+    _stage_checks(cfg, fwd, x, ids)
+    ex = inputs.ExpertSet(cfg, raw)
+    _, inter = oracle.forward(x.float().numpy(), ids.numpy(), w.numpy(), ex, pad=32,
+                              return_intermediates=True)
+    check_forward(fwd, out, inter, ex, ids.numpy(), w.numpy(), what=f"off_pow2 T={T}")
+
+
 def test_forward_prefill_shaped_mid_size(cuda_lib):
     """Zipf-skewed routing with hot and empty experts, outliers, several
     token tiles per expert; small enough for the full oracle."""
