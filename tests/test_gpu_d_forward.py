@@ -176,8 +176,12 @@ def test_forward_ignores_poisoned_workspace(cuda_lib):
 
 
 @pytest.mark.parametrize("case", ["all_one_expert", "one_nonempty", "skipped_slots",
-                                  "bad_ids", "no_tokens"])
+                                  "bad_ids", "no_tokens", "all_skipped", "zero_x"])
 def test_forward_stress_routings(cuda_lib, case):
+    """Degenerate routings and inputs against the oracle.  all_skipped: every
+    id is -1, so no expert has a row and every output is exactly 0.  zero_x:
+    amax(x) = 0 gives gs = 1 and all-zero blocks (scale 0, codes 0), then
+    h = 0, amax(h) = 0 and again gs = 1: the output is exactly 0."""
     cfg = inputs.CONFIGS["tiny"]
     raw, weights = _weights(cfg)
     x = inputs.make_activations(cfg)
@@ -196,6 +200,10 @@ def test_forward_stress_routings(cuda_lib, case):
         ids[9, 1] = 100
     elif case == "no_tokens":
         x, ids, w = x[:0], ids[:0], w[:0]
+    elif case == "all_skipped":
+        ids[:] = -1
+    elif case == "zero_x":
+        x = torch.zeros_like(x)
     raw, fwd, x, ids, w, out, bits = _run(cfg, 32, x=x, ids=ids, w=w)
     if case == "bad_ids":
         assert bits & megamoe.DEV_BAD_EXPERT_ID
@@ -207,6 +215,14 @@ def test_forward_stress_routings(cuda_lib, case):
     _, inter = oracle.forward(x.float().numpy(), ids_ok.numpy(), w.numpy(), ex, pad=32,
                               return_intermediates=True)
     check_forward(fwd, out, inter, ex, ids_ok.numpy(), w.numpy(), what=case)
+    if case in ("all_skipped", "zero_x"):
+        assert not out.any()
+        v = fwd.intermediates()
+        if case == "zero_x":
+            assert v["amax_x"].item() == 0 and v["gs_x"].item() == 1
+            assert v["amax_h"].item() == 0 and v["gs_h"].item() == 1
+        else:
+            assert v["padded_offsets"][-1].item() == 0
 
 
 def test_forward_captures_in_a_cuda_graph(cuda_lib):
