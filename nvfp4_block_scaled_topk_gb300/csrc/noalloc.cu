@@ -64,11 +64,16 @@ CtxGetCurrent ctx_get_current() {
 void* static_workspace() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-  // makes the device's primary context current when no context is
-  if (cudaFree(nullptr) != cudaSuccess) return nullptr;
   CtxGetCurrent get = ctx_get_current();
+  if (!get) return nullptr;
   CUcontext ctx = nullptr;
-  if (!get || get(&ctx) != CUDA_SUCCESS || !ctx) return nullptr;
+  if (get(&ctx) != CUDA_SUCCESS || !ctx) {
+    // no context is current on this thread: the device's primary context
+    // (a context the caller made current is kept as it is)
+    if (cudaSetDevice(dev) != cudaSuccess) return nullptr;
+    ctx = nullptr;
+    if (get(&ctx) != CUDA_SUCCESS || !ctx) return nullptr;
+  }
   std::lock_guard<std::mutex> lock(g_ws_mutex);
   if (!g_ws[dev].ptr || g_ws[dev].ctx != ctx) {
     void* p = nullptr;

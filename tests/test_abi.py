@@ -332,3 +332,23 @@ def test_binding_refuses_an_output_buffer_that_does_not_fit_the_epilogue():
     with pytest.raises(ValueError):  # BFP16 wants the byte buffer of bfp16_bytes(rows, N)
         megamoe.grouped_gemm(act, sf, gs[:1], w, ws, gs, offs, offs, megamoe.EPI_BFP16,
                              out=torch.zeros(megamoe.bfp16_bytes(rows, N) - 1, dtype=torch.uint8))
+
+
+def test_library_sources_call_no_device_allocator():
+    """The library allocates and frees no device memory: every buffer,
+    workspace included, is the caller's (megamoe_forward_static uses a
+    file-scope device array).  No allocator or free call appears in the
+    code of any library source (comments stripped)."""
+    import glob
+    csrc = os.path.join(ROOT, "nvfp4_block_scaled_topk_gb300", "csrc")
+    calls = re.compile(r"\b(cudaMalloc\w*|cudaFree\w*|cudaHostAlloc|cuMemAlloc\w*|cuMemFree\w*|"
+                       r"cuMemCreate|cuMemHostAlloc|cudaMemPoolCreate|cuMemPoolCreate)\s*\(")
+    files = sorted(glob.glob(os.path.join(csrc, "*.cu")) + glob.glob(os.path.join(csrc, "*.cuh"))
+                   + glob.glob(os.path.join(csrc, "*.h")))
+    assert files
+    for f in files:
+        with open(f) as fh:
+            code = re.sub(r"/\*.*?\*/", "", fh.read(), flags=re.S)
+        code = re.sub(r"//[^\n]*", "", code)
+        found = calls.findall(code)
+        assert not found, f"{os.path.basename(f)} calls {sorted(set(found))}"
