@@ -747,6 +747,118 @@ def run_linear(args):
     print(json.dumps(line), flush=True)
 
 
+# --op gemm_sweep: the grouped GEMM alone, the same tiles at several K
+SWEEP_CFGS = {
+    "l2_bfp16_128": ("weights-on-M, 128-token tiles, BFP16 out (the L2 GEMM's tile)", "EPI_BFP16", 128),
+    "l1_tm_silu": ("token-major 128 tokens x 256 weight rows, SiLU*up (the L1 GEMM's tile at "
+                   "prefill sizes)", "EPI_SILU_MUL", 256),
+    "f32_128": ("weights-on-M, 128-token tiles, fp32 out", "EPI_F32", 128),
+    "bf16_128": ("weights-on-M, 128-token tiles, bf16 out (staged stores)", "EPI_BF16", 128),
+    "bfp16_64": ("weights-on-M, 64-token tiles, BFP16 out", "EPI_BFP16", 64),
+    "silu_64": ("weights-on-M, 64-token tiles, SiLU*up", "EPI_SILU_MUL", 64),
+}
+
+
+def sweep_tiles(silu: bool, bfp16: bool, tile_n: int, E: int, rows_per_expert: int, N: int) -> int:
+    """Tiles of one grouped-GEMM launch with E experts of rows_per_expert rows
+    each (a multiple of the token tile) and N weight rows per expert.
+    Token-major tiles (tile_n 256; BFP16 runs those as 128-token tiles) are
+    128 tokens x 256 weight rows; weights-on-M tiles are tile_n tokens x 128
+    output features (for SiLU*up the gate and up rows of 128 features)."""
+    if tile_n == 256 and bfp16:
+        tile_n = 128
+    if tile_n == 256:
+        return E * (rows_per_expert // 128) * (N // 256)
+    return E * (rows_per_expert // tile_n) * (N // 256 if silu else N // 128)
+
+
+def run_gemm_sweep(args):
+    """The grouped GEMM alone on synthetic NVFP4 operands: 128 experts of 256
+    token rows, N = 4096 weight rows per expert, uniform random E2M1 code bytes
+    and E4M3 block scales 0x30-0x47, weights above L2 at every K.  The same
+    tiles are timed at each K (CUDA events, median over --steps launches);
+    the time per wave of tiles fits a + b * (K / 256): a is what a tile costs
+    beyond its K steps, b what one K step costs."""
+    import math
+
+    import numpy as np
+    import torch
+
+    from nvfp4_block_scaled_topk_gb300 import megamoe
+
+    megamoe.load()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    E, rpe, N = 128, 256, 4096
+    ks = [int(v) for v in args.sweep_k.split(",")]
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    gen = torch.Generator(device=dev).manual_seed(2024)
+    rows = E * rpe
+    offs = torch.arange(0, E + 1, dtype=torch.int32, device=dev) * rpe
+    one = torch.ones(1, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+    clocks = ClockSampler(0)
+    clocks.start()
+    result = {}
+    for name in args.sweep_cfg.split(","):
+        desc, epi_name, tile_n = SWEEP_CFGS[name]
+        epi = getattr(megamoe, epi_name)
+        silu, bfp16 = epi == megamoe.EPI_SILU_MUL, epi == megamoe.EPI_BFP16
+        pts = []
+        for K in ks:
+            def codes(n):
+                return torch.randint(0, 256, (n, K // 2), dtype=torch.uint8, device=dev, generator=gen)
+
+            def scales(n):
+                return torch.randint(0x30, 0x48, (n, K // 16), dtype=torch.uint8, device=dev,
+                                     generator=gen)
+
+            ac, asf = codes(rows), scales(rows)
+            wc = megamoe.pack_weight_codes(codes(E * N), N // 2 if silu else 0).view(E, N, K // 2)
+            wsc = megamoe.swizzle_scales(scales(E * N))
+            wgs = torch.ones(E, 2 if silu else 1, device=dev)
+            amax = torch.empty(1, dtype=torch.float32, device=dev) if silu else None
+            if bfp16:
+                out = torch.empty(megamoe.bfp16_bytes(rows, N), dtype=torch.uint8, device=dev)
+            else:
+                dt = torch.float32 if epi == megamoe.EPI_F32 else torch.bfloat16
+                out = torch.empty(rows, N // 2 if silu else N, dtype=dt, device=dev)
+
+            def step():
+                megamoe.grouped_gemm(ac, asf, one, wc, wsc, wgs, offs, offs, epi, tile_n=tile_n,
+                                     out=out, out_amax=amax)
+
+            for _ in range(max(3, args.warmup)):
+                step()
+            torch.cuda.synchronize()
+            times = []
+            for _ in range(args.steps):
+                a = torch.cuda.Event(enable_timing=True)
+                b = torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                step()
+                b.record(stream)
+                torch.cuda.synchronize()
+                times.append(a.elapsed_time(b))
+            ms = float(np.median(times))
+            waves = math.ceil(sweep_tiles(silu, bfp16, tile_n, E, rpe, N) / sms)
+            pts.append([K // 256, ms, ms * 1e3 / waves])
+            del ac, asf, wc, wsc, out
+            torch.cuda.empty_cache()
+        rec = {"tile": desc, "tiles": sweep_tiles(silu, bfp16, tile_n, E, rpe, N),
+               "points": [{"k_steps": kt, "ms": ms, "us_per_wave": us} for kt, ms, us in pts]}
+        if len(pts) >= 2:
+            slope, icept = np.polyfit([p[0] for p in pts], [p[2] for p in pts], 1)
+            rec.update(per_tile_us=float(icept), per_k_step_us=float(slope))
+        result[name] = rec
+    line = {"op": "gemm_sweep", "metric": "grouped GEMM time per wave of tiles against K",
+            "unit": "us", "data": "synthetic", "steps": args.steps, "warmup": args.warmup,
+            "config": {"workload": f"{E} experts x {rpe} token rows, N = {N}, K in {ks}",
+                       "fit": "us per wave = per_tile_us + per_k_step_us * K / 256"},
+            "configs": result, "clocks": clocks.stop()}
+    print(json.dumps(line), flush=True)
+
+
 def run_layer(args, router_only=False):
     """The MoE layer from router logits on one GPU: megamoe_router_topk (k
     routed experts + the shared expert as expert E) then megamoe_forward over
@@ -844,12 +956,20 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--ref-tokens", type=int, default=1)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--op", default="forward", choices=["forward", "linear", "router", "layer"],
+    ap.add_argument("--op", default="forward",
+                    choices=["forward", "linear", "router", "layer", "gemm_sweep"],
                     help="forward: the routed-expert forward (default); linear: the dense "
                          "NVFP4 linear (--config one of the linear_* workloads); router: the "
-                         "router top-k alone; layer: router + forward with a shared expert")
+                         "router top-k alone; layer: router + forward with a shared expert; "
+                         "gemm_sweep: the grouped GEMM alone at several K (--sweep-k, "
+                         "--sweep-cfg)")
+    ap.add_argument("--sweep-k", default="1024,2048,3584,7168")
+    ap.add_argument("--sweep-cfg", default="l2_bfp16_128,l1_tm_silu",
+                    help="comma-separated: " + ", ".join(SWEEP_CFGS))
     args = ap.parse_args()
-    if args.op == "linear":
+    if args.op == "gemm_sweep":
+        run_gemm_sweep(args)
+    elif args.op == "linear":
         if args.config == "large":
             args.config = "linear_qa_decode"
         run_linear(args)

@@ -127,3 +127,20 @@ def test_workload_config_counts_the_routing_and_matches_the_reference_arm():
     assert r.returncode == 0, r.stderr[-2000:]
     line = json.loads([l for l in r.stdout.splitlines() if l.startswith("{")][-1])
     assert line["config"] == want
+
+
+def test_gemm_sweep_tile_counts():
+    """The K sweep's waves come from these tile counts (128 experts x 256 token
+    rows, N = 4096): token-major tiles are 128 tokens x 256 weight rows, BFP16
+    runs tile 256 as 128-token tiles, weights-on-M tiles cover 128 output
+    features (SiLU*up: the gate and up rows of 128 features)."""
+    import bench
+
+    E, rpe, N = 128, 256, 4096
+    assert bench.sweep_tiles(True, False, 256, E, rpe, N) == 128 * 2 * 16
+    assert bench.sweep_tiles(True, False, 64, E, rpe, N) == 128 * 4 * 16
+    assert bench.sweep_tiles(False, True, 256, E, rpe, N) == 128 * 2 * 32
+    assert bench.sweep_tiles(False, True, 128, E, rpe, N) == 128 * 2 * 32
+    assert bench.sweep_tiles(False, False, 256, E, rpe, N) == 128 * 2 * 16
+    assert bench.sweep_tiles(False, True, 64, E, rpe, N) == 128 * 4 * 32
+    assert set(bench.SWEEP_CFGS) >= {"l2_bfp16_128", "l1_tm_silu"}
